@@ -1,0 +1,226 @@
+"""CPU oracle for sparse flash attention -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its binding) never calls it, and shares no code with it.
+
+The arithmetic lives in ``sfa_oracle.c`` (plain C, IEEE double, OpenMP over
+query rows).  This module compiles it with gcc, loads it with ctypes and
+marshals CPU tensors into it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sfa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+LAYOUTS = {"BSND": 0, "BNSD": 1}
+DTYPES = {"f16": 0, "bf16": 1}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into liboracle.so."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """ctypes handle of an oracle shared object with its signatures set."""
+    lib = ctypes.CDLL(path)
+    vp, i64, ci, cd = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    sfa_common = [vp, vp, vp, i64, vp] + [ci] * 8 + [cd, ci, ci, ci]
+    lib.oracle_sfa.argtypes = sfa_common + [vp, vp]
+    lib.oracle_sfa.restype = ci
+    lib.oracle_sfa_rows.argtypes = sfa_common + [vp, i64, vp, vp]
+    lib.oracle_sfa_rows.restype = ci
+    bsr_common = [vp, vp, vp, vp, vp] + [ci] * 7 + [cd, ci]
+    lib.oracle_bsr.argtypes = bsr_common + [vp, vp]
+    lib.oracle_bsr.restype = ci
+    lib.oracle_bsr_rows.argtypes = bsr_common + [vp, i64, vp, vp]
+    lib.oracle_bsr_rows.restype = ci
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def threads() -> int:
+    """OpenMP threads the oracle runs with."""
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def _dtype_of(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise TypeError(f"oracle takes fp16/bf16 tensors, got {t.dtype}")
+
+
+def _ptr(t: torch.Tensor) -> int:
+    if t.device.type != "cpu":
+        raise TypeError("oracle takes CPU tensors")
+    return t.data_ptr()
+
+
+def _value_ld(v: torch.Tensor) -> int:
+    """Element distance between consecutive value rows; v must be rows of
+    `ld` elements (contiguous, or the prefix view key[..., :Dv])."""
+    d0, d1, d2, dv = v.shape
+    ld = v.stride(2)
+    if v.stride(3) != 1 or v.stride(1) != d2 * ld or v.stride(0) != d1 * d2 * ld or ld < dv:
+        raise ValueError("value must be contiguous rows (or a prefix view of key)")
+    return ld
+
+
+def _check(rc: int, what: str):
+    if rc == -2:
+        raise OracleError(f"{what}: index out of range")
+    if rc != 0:
+        raise OracleError(f"{what}: invalid arguments ({rc})")
+
+
+def sfa_dims(q, k, v, idx, layout):
+    if layout == "BSND":
+        B, S1, N1, Dk = q.shape
+        _, S2, N2, _ = k.shape
+    else:
+        B, N1, S1, Dk = q.shape
+        _, N2, S2, _ = k.shape
+    return B, S1, S2, N1, N2, Dk, v.shape[-1], idx.shape[-1]
+
+
+def sfa(q, k, v, idx, scale, layout="BSND", causal=False):
+    """Top-K sparse attention on CPU tensors.  Returns (y, lse) as float64
+    numpy arrays; y in the input layout, lse [B,S1,N1] (BSND) / [B,N1,S1]."""
+    B, S1, S2, N1, N2, Dk, Dv, topK = sfa_dims(q, k, v, idx, layout)
+    for t in (q, k, idx):
+        assert t.is_contiguous()
+    assert idx.dtype == torch.int32
+    if layout == "BSND":
+        y = np.empty((B, S1, N1, Dv))
+        lse = np.empty((B, S1, N1))
+    else:
+        y = np.empty((B, N1, S1, Dv))
+        lse = np.empty((B, N1, S1))
+    rc = _load().oracle_sfa(_ptr(q), _ptr(k), _ptr(v), _value_ld(v), _ptr(idx), B, S1, S2, N1,
+                            N2, Dk, Dv, topK, float(scale), LAYOUTS[layout], int(bool(causal)),
+                            _dtype_of(q), y.ctypes.data, lse.ctypes.data)
+    _check(rc, "oracle_sfa")
+    return y, lse
+
+
+def sfa_rows(q, k, v, idx, scale, rows, layout="BSND", causal=False):
+    """Selected output rows: rows is an (n, 3) int array of (b, n1, s1).
+    Returns (y_rows (n, Dv), lse_rows (n,))."""
+    B, S1, S2, N1, N2, Dk, Dv, topK = sfa_dims(q, k, v, idx, layout)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.shape[0]
+    y = np.empty((n, Dv))
+    lse = np.empty(n)
+    rc = _load().oracle_sfa_rows(_ptr(q), _ptr(k), _ptr(v), _value_ld(v), _ptr(idx), B, S1, S2,
+                                 N1, N2, Dk, Dv, topK, float(scale), LAYOUTS[layout],
+                                 int(bool(causal)), _dtype_of(q), rows.ctypes.data, n,
+                                 y.ctypes.data, lse.ctypes.data)
+    _check(rc, "oracle_sfa_rows")
+    return y, lse
+
+
+def bsr(q, k, v, indptr, indices, M, N, R, C, scale):
+    """Block-sparse attention, NHD tensors.  Returns (y (M,Hq,d), lse (M,Hq))."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    indptr = indptr.to(torch.int32).contiguous()
+    indices = indices.to(torch.int32).contiguous()
+    y = np.empty((M, Hq, d))
+    lse = np.empty((M, Hq))
+    ind_ptr = _ptr(indices) if indices.numel() else 0
+    rc = _load().oracle_bsr(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, M, N, R, C, Hq,
+                            Hkv, d, float(scale), _dtype_of(q), y.ctypes.data, lse.ctypes.data)
+    _check(rc, "oracle_bsr")
+    return y, lse
+
+
+def bsr_rows(q, k, v, indptr, indices, M, N, R, C, scale, rows):
+    """Selected rows: rows is (n, 2) of (query row i, qo head h)."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    indptr = indptr.to(torch.int32).contiguous()
+    indices = indices.to(torch.int32).contiguous()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.shape[0]
+    y = np.empty((n, d))
+    lse = np.empty(n)
+    ind_ptr = _ptr(indices) if indices.numel() else 0
+    rc = _load().oracle_bsr_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, M, N, R, C,
+                                 Hq, Hkv, d, float(scale), _dtype_of(q), rows.ctypes.data, n,
+                                 y.ctypes.data, lse.ctypes.data)
+    _check(rc, "oracle_bsr_rows")
+    return y, lse
+
+
+# ---------------------------------------------------------------------------
+# Precision standard ("SparseFlashAttention 算子 API 描述", §4 精度要求):
+# relative error re = |actual - golden| / (|golden| + 1e-7) over the compared
+# points; MERE = mean(re), MARE = max(re); pass iff MERE < Thr and
+# MARE < 10 * Thr, with Thr = 2^-10 (fp16) or 2^-7 (bf16).  Near-zero golden
+# values: an element also passes the MARE test when |actual - golden| <= cap
+# (1e-2 fp16, 4e-2 bf16).
+
+THRESHOLD = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}
+ABS_CAP = {"f16": 1e-2, "bf16": 4e-2}
+
+
+def round_to(x, dtype: str) -> np.ndarray:
+    """Round float64 values to fp16 / bf16 (nearest-even) and back."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64))
+    return t.to({"f16": torch.float16, "bf16": torch.bfloat16}[dtype]).to(torch.float64).numpy()
+
+
+def precision_report(actual, golden, dtype: str, round_golden: bool = True) -> dict:
+    """MERE / MARE of `actual` against `golden`.  The golden of the operator
+    spec returns its output in the input dtype, so by default the float64
+    oracle values are rounded to `dtype` before comparing."""
+    a = np.asarray(actual, dtype=np.float64).ravel()
+    g = np.asarray(golden, dtype=np.float64).ravel()
+    if round_golden:
+        g = round_to(g, dtype)
+    if a.shape != g.shape:
+        raise ValueError("shape mismatch")
+    thr = THRESHOLD[dtype]
+    if a.size == 0:
+        return {"n": 0, "mere": 0.0, "mare": 0.0, "mare_capped": 0.0, "max_abs": 0.0,
+                "threshold": thr, "passed": True, "finite": True}
+    diff = np.abs(a - g)
+    re = diff / (np.abs(g) + 1e-7)
+    capped = np.where(diff <= ABS_CAP[dtype], 0.0, re)
+    big = np.abs(g) >= 1e-3
+    mere = float(re.mean())
+    mare_c = float(capped.max())
+    finite = bool(np.isfinite(a).all())
+    return {"n": int(a.size), "mere": mere, "mere_big": float(re[big].mean()) if big.any() else 0.0,
+            "mare": float(re.max()), "mare_capped": mare_c, "max_abs": float(diff.max()),
+            "threshold": thr, "finite": finite,
+            "passed": finite and mere < thr and mare_c < 10 * thr}

@@ -1,0 +1,364 @@
+/*
+ * CPU oracle for sparse flash attention (top-K index form and block-sparse
+ * BSR form).  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
+ * CPU-baseline leg of the benchmark call it; the product path never does.
+ * It shares no code, header or constant with the CUDA library.
+ *
+ * Arithmetic is IEEE double throughout.  Inputs are the same fp16 / bf16
+ * buffers the GPU reads, widened exactly to double; outputs are double.
+ * The steps follow the pages' definitions in their order, one query row at a
+ * time, with a plain two-pass softmax (no online rescaling, no blocking):
+ *
+ *   Top-K form -- "SparseFlashAttention 算子 API 描述":
+ *     §2 算子定义 / 稀疏机制: each (b, n2, s1) owns topK int32 positions in
+ *         [0, S2), shared by the N1/N2 query heads of that KV head.
+ *     §2 具体子步骤: sparse gather of K and V rows, GQA expansion (query head
+ *         n1 reads KV head n1 / (N1/N2), as the golden's unsqueeze/expand/
+ *         reshape does), scaled dot product (scores = (q . k_sel) * scale),
+ *         optional causal mask, softmax over the topK slots, weighted sum.
+ *     §2 因果掩码 and §3 规则与约束: with is_causal, slot i of query row s1
+ *         is masked when idx > s1 + (S2 - S1) (bottom-right aligned
+ *         diagonal; idx equal to the diagonal stays visible).
+ *     §3 规则与约束 and §5 (nan_to_num): a row whose slots are all masked
+ *         outputs 0.
+ *     §2 布局说明: BSND and BNSD layouts for every tensor, sparseIndices
+ *         included.
+ *     §3 语义约束: value may be the prefix view key[..., :Dv]; `ldv` is the
+ *         element distance between consecutive value rows (Dv for a separate
+ *         contiguous value tensor, Dk for the prefix view).
+ *   Block-sparse form -- "flashinfer.sparse", BlockSparseAttentionWrapper:
+ *     the class description (scipy bsr_matrix convention, any block R x C)
+ *     and plan(): indptr has MB + 1 = ceil(M / R) + 1 entries, indices hold
+ *     block columns < NB = N / C; query row i may attend key column j iff
+ *     block (i / R, j / C) is stored.  num_qo_heads is a multiple of
+ *     num_kv_heads (grouped-query attention, qo head h reads kv head
+ *     h / (Hq / Hkv)).
+ *   LSE -- run() / run_return_lse(): "log-sum-exp of attention logits".
+ *     Read as the natural logarithm of sum_j exp(scaled logit j) over the
+ *     unmasked positions; -inf for a fully masked row.
+ *
+ * Return codes: 0 ok, -1 bad argument, -2 an index outside [0, S2) (the
+ * operator spec makes in-range indices a precondition).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG (-1)
+#define ORACLE_BAD_INDEX (-2)
+
+/* IEEE binary16 -> double, exact. */
+static double oracle_f16(uint16_t h) {
+    int sign = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)m, -24);
+    else if (e == 31) v = m ? NAN : INFINITY;
+    else v = ldexp((double)(m + 1024), e - 25);
+    return sign ? -v : v;
+}
+
+/* bfloat16 -> double, exact (bf16 is the top half of a binary32). */
+static double oracle_bf16(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double oracle_load(const uint16_t* p, int64_t i, int dtype) {
+    return dtype == 1 ? oracle_bf16(p[i]) : oracle_f16(p[i]);
+}
+
+typedef struct {
+    int B, S1, S2, N1, N2, Dk, Dv, topK, layout, causal, dtype;
+    int64_t ldv;
+    double scale;
+} oracle_sfa_shape;
+
+/* Element offsets of one head-row in each tensor (§2 布局说明). */
+static int64_t off_q(const oracle_sfa_shape* s, int b, int n1, int s1) {
+    return s->layout == 0 ? (((int64_t)b * s->S1 + s1) * s->N1 + n1) * s->Dk
+                          : (((int64_t)b * s->N1 + n1) * s->S1 + s1) * s->Dk;
+}
+static int64_t row_kv(const oracle_sfa_shape* s, int b, int n2, int s2) {
+    return s->layout == 0 ? ((int64_t)b * s->S2 + s2) * s->N2 + n2
+                          : ((int64_t)b * s->N2 + n2) * s->S2 + s2;
+}
+static int64_t off_idx(const oracle_sfa_shape* s, int b, int n2, int s1) {
+    return s->layout == 0 ? (((int64_t)b * s->S1 + s1) * s->N2 + n2) * s->topK
+                          : (((int64_t)b * s->N2 + n2) * s->S1 + s1) * s->topK;
+}
+static int64_t row_out(const oracle_sfa_shape* s, int b, int n1, int s1) {
+    return s->layout == 0 ? ((int64_t)b * s->S1 + s1) * s->N1 + n1
+                          : ((int64_t)b * s->N1 + n1) * s->S1 + s1;
+}
+
+/*
+ * One output row (b, n1, s1) of the top-K form, written to y_row[0..Dv) and
+ * *lse_row.  `scores` and `weights` are caller scratch of topK doubles.
+ */
+static int oracle_sfa_row(const oracle_sfa_shape* s, const uint16_t* q, const uint16_t* k,
+                          const uint16_t* v, const int32_t* idx, int b, int n1, int s1,
+                          double* scores, double* weights, double* y_row, double* lse_row) {
+    const int G = s->N1 / s->N2;
+    const int n2 = n1 / G;                       /* GQA expansion */
+    const int32_t* si = idx + off_idx(s, b, n2, s1);
+    const int64_t qo = off_q(s, b, n1, s1);
+    const int diag = s1 + (s->S2 - s->S1);       /* bottom-right diagonal */
+    int any_visible = 0;
+
+    /* Sparse gather + scaled dot product + causal mask. */
+    for (int i = 0; i < s->topK; ++i) {
+        int32_t id = si[i];
+        if (id < 0 || id >= s->S2) return ORACLE_BAD_INDEX;
+        const int64_t ko = row_kv(s, b, n2, id) * s->Dk;
+        double dot = 0.0;
+        for (int d = 0; d < s->Dk; ++d)
+            dot += oracle_load(q, qo + d, s->dtype) * oracle_load(k, ko + d, s->dtype);
+        scores[i] = dot * s->scale;
+        if (s->causal && id > diag) scores[i] = -INFINITY;
+        else any_visible = 1;
+    }
+
+    /* Softmax over the topK slots.  All slots masked: softmax is 0/0 = NaN in
+     * every slot, which nan_to_num turns into 0, so the row's output is 0. */
+    if (!any_visible) {
+        for (int e = 0; e < s->Dv; ++e) y_row[e] = 0.0;
+        if (lse_row) *lse_row = -INFINITY;
+        return ORACLE_OK;
+    }
+    double mx = -INFINITY;
+    for (int i = 0; i < s->topK; ++i) if (scores[i] > mx) mx = scores[i];
+    double sum = 0.0;
+    for (int i = 0; i < s->topK; ++i) {
+        weights[i] = exp(scores[i] - mx);        /* exp(-inf) = 0 for masked */
+        sum += weights[i];
+    }
+    for (int i = 0; i < s->topK; ++i) weights[i] /= sum;
+    if (lse_row) *lse_row = mx + log(sum);
+
+    /* Weighted sum of the gathered value rows. */
+    for (int e = 0; e < s->Dv; ++e) y_row[e] = 0.0;
+    for (int i = 0; i < s->topK; ++i) {
+        const int64_t vo = row_kv(s, b, n2, si[i]) * s->ldv;
+        for (int e = 0; e < s->Dv; ++e)
+            y_row[e] += weights[i] * oracle_load(v, vo + e, s->dtype);
+    }
+    return ORACLE_OK;
+}
+
+static int oracle_sfa_check(const oracle_sfa_shape* s) {
+    if (s->B < 1 || s->S1 < 1 || s->S2 < 1 || s->N1 < 1 || s->N2 < 1 || s->Dk < 1 ||
+        s->Dv < 1 || s->topK < 1)
+        return ORACLE_BAD_ARG;
+    if (s->N1 % s->N2 != 0 || s->Dv > s->Dk || s->ldv < s->Dv) return ORACLE_BAD_ARG;
+    if (s->layout != 0 && s->layout != 1) return ORACLE_BAD_ARG;
+    if (s->dtype != 0 && s->dtype != 1) return ORACLE_BAD_ARG;
+    if (s->causal && s->S1 > s->S2) return ORACLE_BAD_ARG;
+    return ORACLE_OK;
+}
+
+/*
+ * Full top-K sparse attention.  y has the output's shape in `layout`
+ * ([B,S1,N1,Dv] for BSND, [B,N1,S1,Dv] for BNSD); lse (nullable) is
+ * [B,S1,N1] or [B,N1,S1].
+ */
+int oracle_sfa(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t ldv,
+               const int32_t* idx, int B, int S1, int S2, int N1, int N2, int Dk, int Dv,
+               int topK, double scale, int layout, int causal, int dtype, double* y,
+               double* lse) {
+    oracle_sfa_shape s = {B, S1, S2, N1, N2, Dk, Dv, topK, layout, causal, dtype, ldv, scale};
+    int rc = oracle_sfa_check(&s);
+    if (rc) return rc;
+    const int64_t rows = (int64_t)B * N1 * S1;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double* scores = (double*)malloc(sizeof(double) * (size_t)topK);
+        double* weights = (double*)malloc(sizeof(double) * (size_t)topK);
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
+            int b = (int)(r / ((int64_t)N1 * S1));
+            int n1 = (int)((r / S1) % N1);
+            int s1 = (int)(r % S1);
+            int64_t o = row_out(&s, b, n1, s1);
+            int e = (scores && weights)
+                        ? oracle_sfa_row(&s, q, k, v, idx, b, n1, s1, scores, weights,
+                                         y + o * Dv, lse ? lse + o : NULL)
+                        : ORACLE_BAD_ARG;
+            if (e) {
+#pragma omp atomic write
+                err = e;
+            }
+        }
+        free(scores);
+        free(weights);
+    }
+    return err;
+}
+
+/*
+ * Selected rows only: rows[3*r .. 3*r+2] = (b, n1, s1).  y_rows is
+ * nrows x Dv, lse_rows (nullable) nrows.
+ */
+int oracle_sfa_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t ldv,
+                    const int32_t* idx, int B, int S1, int S2, int N1, int N2, int Dk, int Dv,
+                    int topK, double scale, int layout, int causal, int dtype,
+                    const int64_t* rows, int64_t nrows, double* y_rows, double* lse_rows) {
+    oracle_sfa_shape s = {B, S1, S2, N1, N2, Dk, Dv, topK, layout, causal, dtype, ldv, scale};
+    int rc = oracle_sfa_check(&s);
+    if (rc) return rc;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double* scores = (double*)malloc(sizeof(double) * (size_t)topK);
+        double* weights = (double*)malloc(sizeof(double) * (size_t)topK);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            int b = (int)rows[3 * r], n1 = (int)rows[3 * r + 1], s1 = (int)rows[3 * r + 2];
+            int e;
+            if (b < 0 || b >= B || n1 < 0 || n1 >= N1 || s1 < 0 || s1 >= S1 || !scores || !weights)
+                e = ORACLE_BAD_ARG;
+            else
+                e = oracle_sfa_row(&s, q, k, v, idx, b, n1, s1, scores, weights,
+                                   y_rows + r * Dv, lse_rows ? lse_rows + r : NULL);
+            if (e) {
+#pragma omp atomic write
+                err = e;
+            }
+        }
+        free(scores);
+        free(weights);
+    }
+    return err;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Block-sparse (BSR) form.  q: (M, Hq, d), k/v: (N, Hkv, d), NHD; y: (M, Hq, d);
+ * lse: (M, Hq). */
+
+typedef struct {
+    int M, N, R, C, Hq, Hkv, d, dtype;
+    double scale;
+} oracle_bsr_shape;
+
+static int oracle_bsr_check(const oracle_bsr_shape* s, const int32_t* indptr,
+                            const int32_t* indices) {
+    if (s->M < 1 || s->N < 1 || s->R < 1 || s->C < 1 || s->Hq < 1 || s->Hkv < 1 || s->d < 1)
+        return ORACLE_BAD_ARG;
+    if (s->N % s->C != 0 || s->Hq % s->Hkv != 0) return ORACLE_BAD_ARG;
+    if (s->dtype != 0 && s->dtype != 1) return ORACLE_BAD_ARG;
+    const int MB = (s->M + s->R - 1) / s->R, NB = s->N / s->C;
+    if (indptr[0] != 0) return ORACLE_BAD_ARG;
+    for (int i = 0; i < MB; ++i) {
+        if (indptr[i + 1] < indptr[i]) return ORACLE_BAD_ARG;
+        for (int j = indptr[i]; j < indptr[i + 1]; ++j)
+            if (indices[j] < 0 || indices[j] >= NB) return ORACLE_BAD_INDEX;
+    }
+    return ORACLE_OK;
+}
+
+/* One output row (query row i, qo head h).  `allowed` is caller scratch of N
+ * bytes, `scores` of N doubles. */
+static void oracle_bsr_row(const oracle_bsr_shape* s, const uint16_t* q, const uint16_t* k,
+                           const uint16_t* v, const int32_t* indptr, const int32_t* indices,
+                           int i, int h, unsigned char* allowed, double* scores, double* y_row,
+                           double* lse_row) {
+    const int kvh = h / (s->Hq / s->Hkv);
+    const int br = i / s->R;
+    /* The dense mask row: column j allowed iff its block (br, j / C) is stored. */
+    memset(allowed, 0, (size_t)s->N);
+    for (int jj = indptr[br]; jj < indptr[br + 1]; ++jj)
+        for (int c = 0; c < s->C; ++c) allowed[(int64_t)indices[jj] * s->C + c] = 1;
+
+    const int64_t qo = ((int64_t)i * s->Hq + h) * s->d;
+    double mx = -INFINITY;
+    for (int j = 0; j < s->N; ++j) {
+        if (!allowed[j]) continue;
+        const int64_t ko = ((int64_t)j * s->Hkv + kvh) * s->d;
+        double dot = 0.0;
+        for (int e = 0; e < s->d; ++e)
+            dot += oracle_load(q, qo + e, s->dtype) * oracle_load(k, ko + e, s->dtype);
+        scores[j] = dot * s->scale;
+        if (scores[j] > mx) mx = scores[j];
+    }
+    for (int e = 0; e < s->d; ++e) y_row[e] = 0.0;
+    if (mx == -INFINITY) {               /* no stored block in this row: output 0 */
+        if (lse_row) *lse_row = -INFINITY;
+        return;
+    }
+    double sum = 0.0;
+    for (int j = 0; j < s->N; ++j) {
+        if (!allowed[j]) continue;
+        scores[j] = exp(scores[j] - mx);
+        sum += scores[j];
+    }
+    for (int j = 0; j < s->N; ++j) {
+        if (!allowed[j]) continue;
+        const double w = scores[j] / sum;
+        const int64_t vo = ((int64_t)j * s->Hkv + kvh) * s->d;
+        for (int e = 0; e < s->d; ++e) y_row[e] += w * oracle_load(v, vo + e, s->dtype);
+    }
+    if (lse_row) *lse_row = mx + log(sum);
+}
+
+int oracle_bsr(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* indptr,
+               const int32_t* indices, int M, int N, int R, int C, int Hq, int Hkv, int d,
+               double scale, int dtype, double* y, double* lse) {
+    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale};
+    int rc = oracle_bsr_check(&s, indptr, indices);
+    if (rc) return rc;
+    const int64_t rows = (int64_t)M * Hq;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        unsigned char* allowed = (unsigned char*)malloc((size_t)N);
+        double* scores = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
+            if (!allowed || !scores) {
+#pragma omp atomic write
+                err = ORACLE_BAD_ARG;
+                continue;
+            }
+            int i = (int)(r / Hq), h = (int)(r % Hq);
+            oracle_bsr_row(&s, q, k, v, indptr, indices, i, h, allowed, scores, y + r * d,
+                           lse ? lse + r : NULL);
+        }
+        free(allowed);
+        free(scores);
+    }
+    return err;
+}
+
+/* Selected rows only: rows[2*r], rows[2*r+1] = (query row i, qo head h). */
+int oracle_bsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    const int32_t* indptr, const int32_t* indices, int M, int N, int R, int C,
+                    int Hq, int Hkv, int d, double scale, int dtype, const int64_t* rows,
+                    int64_t nrows, double* y_rows, double* lse_rows) {
+    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale};
+    int rc = oracle_bsr_check(&s, indptr, indices);
+    if (rc) return rc;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        unsigned char* allowed = (unsigned char*)malloc((size_t)N);
+        double* scores = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            int i = (int)rows[2 * r], h = (int)rows[2 * r + 1];
+            if (!allowed || !scores || i < 0 || i >= M || h < 0 || h >= Hq) {
+#pragma omp atomic write
+                err = ORACLE_BAD_ARG;
+                continue;
+            }
+            oracle_bsr_row(&s, q, k, v, indptr, indices, i, h, allowed, scores, y_rows + r * d,
+                           lse_rows ? lse_rows + r : NULL);
+        }
+        free(allowed);
+        free(scores);
+    }
+    return err;
+}

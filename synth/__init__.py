@@ -1,0 +1,261 @@
+"""Seeded synthetic inputs for the sparse-attention workloads.
+
+Holds random numbers, index lists and workload shapes only -- none of the
+attention arithmetic.  The CPU oracle and the CUDA path both consume the
+buffers made here (the float32 normals are rounded to fp16/bf16 once, and the
+same rounded tensors go to both sides).
+
+Index lists and tensors are always generated in the canonical BSND order
+([B, S1, N2, topK] for indices, [B, S, N, D] for q/k/v) and permuted for BNSD,
+so one seed describes one problem in either layout.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_LIB_PATH = os.path.join(_HERE, "libsynth.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile synth.c into libsynth.so (plain C, OpenMP)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, u64, i32, f64 = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int32, ctypes.c_double
+            vp = ctypes.c_void_p
+            lib.syn_normal_f32.argtypes = [u64, u64, i64, vp]
+            lib.syn_normal_f32.restype = None
+            lib.syn_index_uniform.argtypes = [u64, i64, i32, i32, ctypes.c_int, vp]
+            lib.syn_index_uniform.restype = ctypes.c_int
+            lib.syn_index_causal_mix.argtypes = [u64, i32, i32, i32, i32, i32, f64, i32, vp]
+            lib.syn_index_causal_mix.restype = ctypes.c_int
+            lib.syn_bsr_pattern.argtypes = [u64, i32, i32, f64, vp, vp]
+            lib.syn_bsr_pattern.restype = i64
+            _lib = lib
+    return _lib
+
+
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def normal(seed: int, stream: int, shape, dtype: str) -> torch.Tensor:
+    """N(0,1) samples of `shape`, rounded (nearest-even) to fp16 or bf16."""
+    n = int(np.prod(shape))
+    buf = np.empty(n, dtype=np.float32)
+    if n:
+        _load().syn_normal_f32(seed, stream, n, buf.ctypes.data)
+    return torch.from_numpy(buf).reshape(shape).to(_TORCH_DTYPE[dtype])
+
+
+def index_uniform(seed: int, rows: int, rng: int, topk: int, sorted_: bool) -> np.ndarray:
+    """rows x topk distinct draws from [0, rng), random order or ascending."""
+    out = np.empty((rows, topk), dtype=np.int32)
+    rc = _load().syn_index_uniform(seed, rows, rng, topk, int(sorted_), out.ctypes.data)
+    if rc:
+        raise ValueError(f"syn_index_uniform failed ({rc})")
+    return out
+
+
+def index_causal_mix(seed, B, S1, N2, S2, topk, masked_frac, full_masked_rows) -> np.ndarray:
+    """[B, S1, N2, topk] lists: ~masked_frac of each row above the bottom-right
+    diagonal, the rest visible; rows (b=0, s1 < full_masked_rows) entirely above
+    it (drawn with replacement)."""
+    out = np.empty((B, S1, N2, topk), dtype=np.int32)
+    rc = _load().syn_index_causal_mix(seed, B, S1, N2, S2, topk, masked_frac, full_masked_rows,
+                                      out.ctypes.data)
+    if rc:
+        raise ValueError(f"syn_index_causal_mix failed ({rc})")
+    return out
+
+
+def bsr_pattern(seed: int, MB: int, NB: int, p: float):
+    """(indptr, indices) of an MB x NB block pattern: diagonal always set,
+    other blocks independently with probability p, columns ascending."""
+    lib = _load()
+    indptr = np.empty(MB + 1, dtype=np.int32)
+    nnz = lib.syn_bsr_pattern(seed, MB, NB, p, indptr.ctypes.data, None)
+    indices = np.empty(max(int(nnz), 1), dtype=np.int32)
+    lib.syn_bsr_pattern(seed, MB, NB, p, indptr.ctypes.data, indices.ctypes.data)
+    return indptr, indices[: int(nnz)]
+
+
+# ---------------------------------------------------------------------------
+# Workload descriptions
+
+
+@dataclasses.dataclass(frozen=True)
+class SfaCase:
+    """One top-K sparse attention problem and its input recipe."""
+
+    name: str
+    B: int
+    S1: int
+    S2: int
+    N1: int
+    N2: int
+    Dk: int
+    Dv: int
+    topK: int
+    dtype: str              # "f16" | "bf16"
+    layout: str             # "BSND" | "BNSD"
+    causal: bool
+    scale: float
+    value_is_key_prefix: bool = False
+    index_kind: str = "uniform"     # "uniform" | "sorted" | "causal_mix"
+    masked_frac: float = 0.0        # causal_mix only
+    full_masked_rows: int = 0       # causal_mix only
+    seed: int = 1234
+
+    @property
+    def G(self) -> int:
+        return self.N1 // self.N2
+
+    def replace(self, **kw) -> "SfaCase":
+        return dataclasses.replace(self, **kw)
+
+
+@dataclasses.dataclass(frozen=True)
+class BsrCase:
+    """One block-sparse attention problem and its input recipe."""
+
+    name: str
+    M: int
+    N: int
+    R: int
+    C: int
+    Hq: int
+    Hkv: int
+    d: int
+    dtype: str
+    p: float
+    sm_scale: float
+    seed: int = 1238
+
+    @property
+    def MB(self) -> int:
+        return (self.M + self.R - 1) // self.R
+
+    @property
+    def NB(self) -> int:
+        return self.N // self.C
+
+    def replace(self, **kw) -> "BsrCase":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads (data seed = 1234 + workload number - 1).
+TINY = SfaCase("tiny", B=1, S1=4, S2=64, N1=4, N2=1, Dk=64, Dv=64, topK=16, dtype="f16",
+               layout="BSND", causal=False, scale=1.0 / math.sqrt(64), seed=1234)
+GQA_DECODE = SfaCase("gqa_decode", B=16, S1=1, S2=8192, N1=32, N2=8, Dk=128, Dv=128, topK=1024,
+                     dtype="bf16", layout="BNSD", causal=True, scale=0.08839,
+                     index_kind="sorted", seed=1235)
+MLA_DECODE = SfaCase("mla_decode", B=32, S1=1, S2=8192, N1=128, N2=1, Dk=576, Dv=512, topK=2048,
+                     dtype="bf16", layout="BSND", causal=True, scale=0.04167,
+                     value_is_key_prefix=True, seed=1236)
+MLA_MTP = MLA_DECODE.replace(name="mla_mtp", S1=4)
+PREFILL = SfaCase("sparse_prefill", B=2, S1=2048, S2=16384, N1=64, N2=8, Dk=192, Dv=128, topK=2048,
+                  dtype="f16", layout="BSND", causal=True, scale=0.07217, value_is_key_prefix=True,
+                  index_kind="causal_mix", masked_frac=0.10, full_masked_rows=8, seed=1237)
+BSR = BsrCase("bsr", M=16384, N=16384, R=64, C=64, Hq=32, Hkv=8, d=128, dtype="f16", p=0.10,
+              sm_scale=1.0 / math.sqrt(128), seed=1238)
+
+SFA_WORKLOADS = {c.name: c for c in (TINY, GQA_DECODE, MLA_DECODE, MLA_MTP, PREFILL)}
+BSR_WORKLOADS = {BSR.name: BSR}
+
+
+def _to_layout(t: torch.Tensor, layout: str) -> torch.Tensor:
+    """Canonical [B, S, N, D] -> the requested layout (contiguous)."""
+    return t if layout == "BSND" else t.permute(0, 2, 1, 3).contiguous()
+
+
+def make_sfa_inputs(case: SfaCase) -> dict:
+    """CPU tensors q, k, v, idx for `case` in its layout.
+
+    Streams: q = 0, k = 1, v = 2 of the data seed; indices use seed + 1.  With
+    value_is_key_prefix, v is the strided view k[..., :Dv] (no copy)."""
+    c = case
+    q = normal(c.seed, 0, (c.B, c.S1, c.N1, c.Dk), c.dtype)
+    k = normal(c.seed, 1, (c.B, c.S2, c.N2, c.Dk), c.dtype)
+    if c.index_kind == "causal_mix":
+        idx = index_causal_mix(c.seed + 1, c.B, c.S1, c.N2, c.S2, c.topK, c.masked_frac,
+                               c.full_masked_rows)
+    else:
+        idx = index_uniform(c.seed + 1, c.B * c.S1 * c.N2, c.S2, c.topK, c.index_kind == "sorted")
+        idx = idx.reshape(c.B, c.S1, c.N2, c.topK)
+    q = _to_layout(q, c.layout)
+    k = _to_layout(k, c.layout)
+    idx = _to_layout(torch.from_numpy(idx), c.layout)
+    if c.value_is_key_prefix:
+        v = k[..., : c.Dv]
+    else:
+        v = _to_layout(normal(c.seed, 2, (c.B, c.S2, c.N2, c.Dv), c.dtype), c.layout)
+    return {"q": q, "k": k, "v": v, "idx": idx}
+
+
+def make_bsr_inputs(case: BsrCase) -> dict:
+    """CPU tensors q (M,Hq,d), k/v (N,Hkv,d) in NHD order, and int32 indptr/indices."""
+    c = case
+    q = normal(c.seed, 0, (c.M, c.Hq, c.d), c.dtype)
+    k = normal(c.seed, 1, (c.N, c.Hkv, c.d), c.dtype)
+    v = normal(c.seed, 2, (c.N, c.Hkv, c.d), c.dtype)
+    indptr, indices = bsr_pattern(c.seed + 1, c.MB, c.NB, c.p)
+    return {"q": q, "k": k, "v": v, "indptr": torch.from_numpy(indptr),
+            "indices": torch.from_numpy(indices.copy())}
+
+
+def sfa_counts(case: SfaCase, idx: torch.Tensor | None = None) -> dict:
+    """Algorithmic work of one call: useful FLOPs (2*(Dk+Dv) per unmasked
+    (query head, slot) pair), gathered K/V bytes (per selected slot per KV
+    group; V counted separately unless it is the key prefix), and the bytes of
+    q, indices and output."""
+    c = case
+    E = 2
+    slots = c.B * c.N2 * c.S1 * c.topK
+    if idx is not None and c.causal:
+        t = idx if c.layout == "BSND" else idx.permute(0, 2, 1, 3)
+        s1 = torch.arange(c.S1, dtype=torch.int64).view(1, c.S1, 1, 1)
+        unmasked = int((t.to(torch.int64) <= s1 + (c.S2 - c.S1)).sum())
+    else:
+        unmasked = slots
+    flops = 2 * (c.Dk + c.Dv) * unmasked * c.G
+    row_bytes = c.Dk * E + (0 if c.value_is_key_prefix else c.Dv * E)
+    gathered = slots * row_bytes
+    other = (c.B * c.S1 * c.N1 * c.Dk * E + slots * 4 + c.B * c.S1 * c.N1 * c.Dv * E)
+    return {"flops": flops, "gathered_bytes": gathered, "other_bytes": other,
+            "slots": slots, "unmasked_slots": unmasked}
+
+
+def bsr_counts(case: BsrCase, indptr: torch.Tensor) -> dict:
+    """Useful FLOPs (2*2*d per allowed (row, column, qo head)) and the K/V bytes
+    each (row block, kv head) work item reads (64x64 blocks of K and V)."""
+    c = case
+    ip = indptr.to(torch.int64)
+    rows_in_block = torch.full((c.MB,), c.R, dtype=torch.int64)
+    rows_in_block[-1] = c.M - (c.MB - 1) * c.R
+    blocks_per_row = ip[1:] - ip[:-1]
+    allowed = int((blocks_per_row * rows_in_block).sum()) * c.C
+    nnz = int(ip[-1])
+    flops = 4 * c.d * allowed * c.Hq
+    gathered = nnz * c.C * c.Hkv * c.d * 2 * 2
+    return {"flops": flops, "gathered_bytes": gathered, "nnz": nnz, "allowed": allowed}

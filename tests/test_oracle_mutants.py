@@ -1,0 +1,87 @@
+"""Planted mistakes: each test compiles a copy of the oracle with one
+plausible error (a wrong index, sign, operand or constant) and checks that
+the pins in test_oracle_pins catch it.  Runs on the CPU only.  Every planted
+error keeps all memory accesses inside the buffers the pins pass."""
+import contextlib
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "sfa_oracle.c")
+
+# (name, original text, planted text)
+MUTANTS = [
+    ("gqa_head_map", "const int n2 = n1 / G;", "const int n2 = n1 % s->N2;"),
+    ("causal_off_by_one", "if (s->causal && id > diag)", "if (s->causal && id >= diag)"),
+    ("causal_top_left", "const int diag = s1 + (s->S2 - s->S1);", "const int diag = s1;"),
+    ("scale_dropped", "scores[i] = dot * s->scale;", "scores[i] = dot;"),
+    ("softmax_unnormalised", "weights[i] /= sum;", "weights[i] /= 1.0;"),
+    ("lse_base2", "weights[i] /= sum;\n    if (lse_row) *lse_row = mx + log(sum);",
+     "weights[i] /= sum;\n    if (lse_row) *lse_row = mx + log2(sum);"),
+    ("bsr_lse_base2", "if (lse_row) *lse_row = mx + log(sum);\n}", "if (lse_row) *lse_row = mx + log2(sum);\n}"),
+    ("bnsd_index_as_bsnd", ": (((int64_t)b * s->N2 + n2) * s->S1 + s1) * s->topK;",
+     ": (((int64_t)b * s->S1 + s1) * s->N2 + n2) * s->topK;"),
+    ("value_stride_dv", "const int64_t vo = row_kv(s, b, n2, si[i]) * s->ldv;",
+     "const int64_t vo = row_kv(s, b, n2, si[i]) * s->Dv;"),
+    ("value_row_from_slot", "const int64_t vo = row_kv(s, b, n2, si[i]) * s->ldv;",
+     "const int64_t vo = row_kv(s, b, n2, i) * s->ldv;"),
+    ("masked_row_not_zero", "for (int e = 0; e < s->Dv; ++e) y_row[e] = 0.0;\n        if (lse_row) *lse_row = -INFINITY;",
+     "for (int e = 0; e < s->Dv; ++e) y_row[e] = 1.0;\n        if (lse_row) *lse_row = -INFINITY;"),
+    ("bsr_kv_head_map", "const int kvh = h / (s->Hq / s->Hkv);", "const int kvh = h % s->Hkv;"),
+    ("bsr_block_col_unscaled", "allowed[(int64_t)indices[jj] * s->C + c] = 1;",
+     "allowed[(int64_t)indices[jj] + c] = 1;"),
+    ("bsr_row_block_reversed", "const int br = i / s->R;", "const int br = (s->M - 1 - i) / s->R;"),
+    ("bsr_scale_dropped", "scores[j] = dot * s->scale;", "scores[j] = dot;"),
+    ("bf16_as_f16", "return dtype == 1 ? oracle_bf16(p[i]) : oracle_f16(p[i]);",
+     "return oracle_f16(p[i]);"),
+]
+
+
+def all_pins():
+    """Every pin with its parameters, as zero-argument callables."""
+    out = []
+    for layout in ("BSND", "BNSD"):
+        for causal in (False, True):
+            for dtype in ("f16", "bf16"):
+                out.append(lambda l=layout, c=causal, d=dtype: pins.test_brute_force_multiset(l, c, d))
+            out.append(lambda l=layout, c=causal: pins.test_identity_indices_equal_dense_sdpa(l, c))
+        out.append(lambda l=layout: pins.test_value_prefix_view_equals_copy(l))
+    out += [pins.test_causal_mask_matches_printed_rule, pins.test_fully_masked_rows_are_zero,
+            pins.test_single_slot_closed_form, pins.test_uniform_scores_give_mean,
+            pins.test_bsr_worked_example, pins.test_bsr_empty_block_row_is_zero]
+    for args in ((3, 2, 10, 8), (4, 4, 12, 16), (1, 3, 5, 9)):
+        out.append(lambda a=args: pins.test_bsr_equals_block_expanded_mask(*a))
+    return out
+
+
+@contextlib.contextmanager
+def mutant_oracle(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    path_c = tmp_path / f"{name}.c"
+    path_c.write_text(src.replace(old, new))
+    path_so = tmp_path / f"{name}.so"
+    subprocess.check_call(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-o", str(path_so),
+                           str(path_c), "-lm"])
+    saved = oracle._load()
+    oracle._lib = oracle.load_library(str(path_so))
+    try:
+        yield
+    finally:
+        oracle._lib = saved
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    caught = 0
+    with mutant_oracle(tmp_path, name, old, new):
+        for pin in all_pins():
+            try:
+                pin()
+            except (AssertionError, oracle.OracleError):
+                caught += 1
+    assert caught > 0, f"no pin caught the planted mistake '{name}'"
