@@ -1,0 +1,380 @@
+"""Benchmark of the sparse-attention hot path on GB300.
+
+One step = one call of the top-K sparse flash attention entry point over the
+GQA-decode workload (B=16, S1=1, S2=8192, N1=32, N2=8, Dk=Dv=128, topK=1024,
+bf16, BNSD, causal), inputs resident in HBM, L2 flushed between steps.
+Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores
+on a bounded sample of the same workload.  Under torchrun every rank runs an
+independent replica of the workload (weak scaling, no collective on the data
+path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "sparse-attn effective TFLOP/s & gathered-KV GB/s, fraction of GB300 roofline"
+UNIT = "GB/s"   # gathered-KV bytes per second (the decode workload is HBM-bound)
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_decode", choices=sorted(synth.SFA_WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dtype_name(case):
+    return {"f16": "f16", "bf16": "bf16"}[case.dtype]
+
+
+def config_of(case, world):
+    return {"workload": case.name, "B": case.B, "S1": case.S1, "S2": case.S2, "N1": case.N1,
+            "N2": case.N2, "Dk": case.Dk, "Dv": case.Dv, "topK": case.topK,
+            "layout": case.layout, "causal": case.causal,
+            "value_is_key_prefix": case.value_is_key_prefix, "index": case.index_kind,
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampling during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# traffic figure from a committed ncu summary (only while the kernel source
+# it was taken on is unchanged)
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_serving_sfa_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def committed_traffic(workload):
+    path = os.path.join(ROOT, "profiles", f"{workload}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    sha = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not sha or not val or sha.group(1) != kernel_source_sha():
+        return None
+    return float(val.group(1))
+
+
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local):
+    import sparse_attention_serving_sfa_gb300 as sfa
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    sfa.build()
+    sfa.load()
+    case = synth.SFA_WORKLOADS[args.workload]
+    host = synth.make_sfa_inputs(case)
+    counts = synth.sfa_counts(case, host["idx"])
+    dev = {"q": host["q"].cuda(), "k": host["k"].cuda(), "idx": host["idx"].cuda()}
+    prefix = case.value_is_key_prefix
+    dev["v"] = dev["k"] if prefix else host["v"].cuda()
+    if case.layout == "BSND":
+        out_shape, lse_shape = (case.B, case.S1, case.N1, case.Dv), (case.B, case.S1, case.N1)
+    else:
+        out_shape, lse_shape = (case.B, case.N1, case.S1, case.Dv), (case.B, case.N1, case.S1)
+    tdt = dev["q"].dtype
+    out = torch.empty(out_shape, dtype=tdt, device="cuda")
+    lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    ws_bytes = sfa.sfa_workspace_size(case.B, case.S1, case.N1, case.N2, case.Dk, case.Dv,
+                                      case.topK)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def step(q=dev["q"], idx=dev["idx"], o=out, l=lse):
+        sfa.sfa_run_ex(q, dev["k"], dev["v"], idx, case.B, case.S1, case.S2, case.N1, case.N2,
+                       case.Dk, case.Dv, case.topK, case.scale, case.layout, case.causal,
+                       case.dtype, o, l, stream, workspace=ws, value_is_key_prefix=prefix)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = sfa.sfa_kernel_launches()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                     # L2 flush outside the timed interval
+        starts[i].record(stream)
+        step()
+        stops[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = sfa.sfa_kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, stops)]
+    ms = float(np.mean(step_ms))
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the same entry point with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq = host["q"].pin_memory()
+        hidx = host["idx"].pin_memory()
+        hout = torch.empty(out_shape, dtype=tdt).pin_memory()
+        hlse = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
+        dq = torch.empty_like(dev["q"])
+        didx = torch.empty_like(dev["idx"])
+        n_e2e = max(args.steps // 4, 10)
+        e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+        e_stops = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+        for i in range(n_e2e + 3):
+            flush.zero_()
+            if i >= 3:
+                e_starts[i - 3].record(stream)
+            dq.copy_(hq, non_blocking=True)
+            didx.copy_(hidx, non_blocking=True)
+            step(q=dq, idx=didx)
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            if i >= 3:
+                e_stops[i - 3].record(stream)
+        torch.cuda.synchronize()
+        e_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(e_starts, e_stops)]))
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = hq.numel() * hq.element_size() + hidx.numel() * 4
+        d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
+        e2e = {"value": world * counts["gathered_bytes"] / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peaks, peak_src = load_peaks()
+    gbs = counts["gathered_bytes"] / (ms * 1e-3) / 1e9
+    tflops = counts["flops"] / (ms * 1e-3) / 1e12
+    roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "traffic": committed_traffic(args.workload),
+                "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                "kernel": "whole call (every kernel of one sfa_run_ex)"}
+    t_roof = max(counts["gathered_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                 counts["flops"] / (peaks["bf16_tflops"] * 1e12))
+    res = {"metric": METRIC, "value": world * gbs, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": dtype_name(case), "data": "synthetic (seeded generator, shapes of the workload)",
+           "config": config_of(case, world),
+           "tflops": world * tflops, "us_per_call": ms * 1e3,
+           "roofline_time_frac": t_roof / (ms * 1e-3),
+           "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+           "clocks": clocks, "wall_s_timed_loop": wall,
+           "work": {"flops": counts["flops"], "gathered_bytes": counts["gathered_bytes"],
+                    "unmasked_slots": counts["unmasked_slots"]}}
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(case, host, counts)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return res
+
+
+def cpu_baseline(case, host, counts, target_s=10.0):
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload (whole calls while they fit in ~target_s, else sampled rows
+    scaled to a whole call)."""
+    import oracle
+    rows_total = case.B * case.N1 * case.S1
+    t0 = time.perf_counter()
+    probe = np.array([[0, 0, 0]])
+    oracle.sfa_rows(host["q"], host["k"], host["v"], host["idx"], case.scale, probe, case.layout,
+                    case.causal)
+    per_row = max(time.perf_counter() - t0, 1e-6)
+    est_full = per_row * rows_total / max(oracle.threads(), 1)
+    if est_full < target_s / 2:
+        reps = 0
+        t0 = time.perf_counter()
+        while True:
+            oracle.sfa(host["q"], host["k"], host["v"], host["idx"], case.scale, case.layout,
+                       case.causal)
+            reps += 1
+            if time.perf_counter() - t0 > target_s / 2 or reps >= 20:
+                break
+        sec = (time.perf_counter() - t0) / reps
+        sample = f"{reps} whole calls ({rows_total} output rows each)"
+    else:
+        n = max(int(target_s / per_row * max(oracle.threads(), 1) / 2), 16)
+        n = min(n, rows_total)
+        rng = np.random.default_rng(0)
+        flat = rng.choice(rows_total, size=n, replace=False)
+        rows = np.stack([flat // (case.N1 * case.S1), (flat // case.S1) % case.N1,
+                         flat % case.S1], axis=1)
+        t0 = time.perf_counter()
+        oracle.sfa_rows(host["q"], host["k"], host["v"], host["idx"], case.scale, rows,
+                        case.layout, case.causal)
+        sec = (time.perf_counter() - t0) * rows_total / n
+        sample = f"{n} of {rows_total} output rows, time scaled to a whole call"
+    return {"value": counts["gathered_bytes"] / sec / 1e9, "unit": UNIT,
+            "cores": oracle.threads(), "kind": "oracle", "sample": sample,
+            "seconds_per_call": sec}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    case = synth.SFA_WORKLOADS[args.workload]
+    host = synth.make_sfa_inputs(case)
+    counts = synth.sfa_counts(case, host["idx"])
+    oracle.build()
+    cb = cpu_baseline(case, host, counts, target_s=4.0)
+    # steps: each step is one bounded sample of the workload
+    secs = []
+    for _ in range(max(args.warmup, 0)):
+        cpu_baseline(case, host, counts, target_s=1.0)
+    n_steps = min(args.steps, 5)
+    for _ in range(n_steps):
+        secs.append(cpu_baseline(case, host, counts, target_s=2.0)["seconds_per_call"])
+    sec = float(np.mean(secs))
+    val = counts["gathered_bytes"] / sec / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+            "steps": n_steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded generator, shapes of the workload)",
+            "config": config_of(case, world),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.threads(),
+                             "kind": "oracle", "sample": cb["sample"]},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)))
+        return 0
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,198 @@
+/*
+ * sfa.h -- C ABI of the GB300 sparse flash attention library (libsfa_gb300.so).
+ *
+ * Two forms of sparse attention, both computed entirely by the library's own
+ * sm_103a CUDA kernels:
+ *
+ *   1. Top-K index form ("SparseFlashAttention 算子 API 描述", §2 算子定义 and
+ *      §3 接口规范): every (b, n2, s1) owns topK int32 key positions; the
+ *      N1/N2 query heads of KV head n2 attend only to those rows of K and V.
+ *   2. Block-sparse form ("flashinfer.sparse", BlockSparseAttentionWrapper):
+ *      query row i attends to key column j iff block (i / R, j / C) is stored
+ *      in a BSR matrix (indptr / indices), with a plan() / run() split.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named q, k, v, out, lse, sparse_idx and the workspaces are
+ *     DEVICE pointers owned by the caller; the library never frees them.
+ *     Pointers named *_host are host memory, read during the call only.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream) and returns without synchronising, except sfa_get_last_error.
+ *   - Host-detectable argument errors return a status before anything is
+ *     launched; no kernel traps, asserts or spins on the device.
+ *   - All device pointers must be 16-byte aligned.
+ */
+#ifndef SFA_GB300_H
+#define SFA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* sfa_stream_t;
+
+typedef enum {
+    SFA_OK = 0,
+    SFA_ERR_INVALID_ARG = 1,  /* shape, enum, pointer or alignment rule broken */
+    SFA_ERR_UNSUPPORTED = 2,  /* legal per the spec but outside this build's limits */
+    SFA_ERR_WORKSPACE = 3,    /* caller workspace missing or too small */
+    SFA_ERR_INDEX_RANGE = 4,  /* a sparse index outside [0, S2) was seen (validate mode) */
+    SFA_ERR_CUDA = 5          /* a CUDA runtime call or launch failed */
+} sfa_status;
+
+/* Tensor layouts ("SparseFlashAttention 算子 API 描述", §2 布局说明):
+ *   BSND: q [B,S1,N1,Dk]  k [B,S2,N2,Dk]  v [B,S2,N2,Dv]
+ *         sparse_idx [B,S1,N2,topK]  out [B,S1,N1,Dv]  lse [B,S1,N1]
+ *   BNSD: q [B,N1,S1,Dk]  k [B,N2,S2,Dk]  v [B,N2,S2,Dv]
+ *         sparse_idx [B,N2,S1,topK]  out [B,N1,S1,Dv]  lse [B,N1,S1]
+ * All row-major and contiguous, except v in key-prefix mode (below). */
+typedef enum { SFA_LAYOUT_BSND = 0, SFA_LAYOUT_BNSD = 1 } sfa_layout;
+
+/* q, k, v and out share one element type (§3 数据类型). */
+typedef enum { SFA_DTYPE_F16 = 0, SFA_DTYPE_BF16 = 1 } sfa_dtype;
+
+/*
+ * sfa_run -- top-K sparse flash attention.
+ *
+ * Computes, for every batch b, query head n1 (KV head n2 = n1 / (N1/N2)) and
+ * query position s1, with the topK positions idx_i = sparse_idx[b, n2, s1, i]
+ * (layout-mapped):
+ *     s_i   = scale * <q[b,n1,s1,:Dk], k[b,n2,idx_i,:Dk]>
+ *     s_i   = -inf  if causal and idx_i > s1 + (S2 - S1)      (bottom-right)
+ *     out   = sum_i softmax(s)_i * v[b,n2,idx_i,:Dv]
+ *     lse   = ln(sum_i exp(s_i))
+ * (§2 具体子步骤 and 因果掩码).  A row whose slots are all masked writes
+ * out = +0 and lse = -inf (§3 规则与约束: "softmax 输出按全 0 处理").
+ * Duplicate positions in a row count once per slot, as in the spec's golden.
+ *
+ * Arguments
+ *   q, k, v       device, dtype elements, layout above.  If v == k and
+ *                 Dv <= Dk, v is read as the prefix view k[..., :Dv] (rows of
+ *                 Dk elements; §3 语义约束, the MLA latent cache).
+ *   sparse_idx    device int32 in [0, S2).  Out-of-range positions are never
+ *                 dereferenced: their slot is treated as masked.
+ *   B,S1,S2,N1,N2 sizes; N1 % N2 == 0; causal requires S1 <= S2.
+ *   Dk, Dv        multiples of 64, Dv <= Dk; this build: Dk <= 1024, Dv <= 512.
+ *   topK          1 <= topK <= S2.
+ *   scale         softmax scale (usually 1/sqrt(Dk)); any finite value.
+ *   out           device, dtype, layout above.
+ *   lse           device float32 or NULL.
+ *   stream        CUDA stream for every launch of the call.
+ * Workspace: a library-owned device workspace is allocated (and grown) on
+ * first use per device; the growing call synchronises the device once.  Use
+ * sfa_run_ex to pass your own.
+ * Errors: SFA_ERR_INVALID_ARG / SFA_ERR_UNSUPPORTED before any launch;
+ * SFA_ERR_CUDA if a launch fails.
+ */
+sfa_status sfa_run(const void* q, const void* k, const void* v, const int32_t* sparse_idx,
+                   int B, int S1, int S2, int N1, int N2, int Dk, int Dv, int topK, float scale,
+                   sfa_layout layout, int causal, sfa_dtype dtype, void* out, float* lse,
+                   sfa_stream_t stream);
+
+/* Options of sfa_run_ex.  Zero-initialise and set what you need. */
+typedef struct {
+    /* Caller-owned device float workspace for split-topK partial results
+     * ("flashinfer.sparse", BlockSparseAttentionWrapper.__init__: the float
+     * workspace that holds split-k intermediates).  NULL = library-owned.
+     * Size: sfa_workspace_size().  Must not be used by another call that
+     * overlaps this one on the GPU. */
+    void* workspace;
+    size_t workspace_bytes;
+    /* 1: v is the prefix view k[..., :Dv] (v must equal k).  0: inferred from
+     * v == k. */
+    int value_is_key_prefix;
+    /* 1: an out-of-range index also sets the library's device error word,
+     * read (and cleared) by sfa_get_last_error. */
+    int validate_indices;
+    /* Number of topK splits; 0 = chosen from the SM count. */
+    int num_splits;
+} sfa_options;
+
+sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t* sparse_idx,
+                      int B, int S1, int S2, int N1, int N2, int Dk, int Dv, int topK,
+                      float scale, sfa_layout layout, int causal, sfa_dtype dtype, void* out,
+                      float* lse, sfa_stream_t stream, const sfa_options* opt);
+
+/* Bytes of float workspace sfa_run_ex may need for these sizes with any
+ * split count it would choose (or with num_splits, if > 0).  Host only. */
+sfa_status sfa_workspace_size(int B, int S1, int N1, int N2, int Dk, int Dv, int topK,
+                              int num_splits, size_t* bytes);
+
+/* Synchronises `stream`, then returns SFA_ERR_INDEX_RANGE if a call with
+ * validate_indices saw an index outside [0, S2) since the last check
+ * (clearing the flag), SFA_ERR_CUDA on a CUDA error, else SFA_OK. */
+sfa_status sfa_get_last_error(sfa_stream_t stream);
+
+/* Static text for a status code. */
+const char* sfa_status_string(sfa_status status);
+
+/* Number of CUDA kernels this library has launched in this process, over
+ * all entry points (a diagnostic for launch accounting; no paper
+ * counterpart). */
+uint64_t sfa_kernel_launches(void);
+
+/* ------------------------------------------------------------------------ */
+/* Block-sparse (BSR) attention ("flashinfer.sparse",
+ * BlockSparseAttentionWrapper: plan() builds cached auxiliary structures,
+ * run() may then be called many times). */
+
+typedef struct bsr_plan_s* bsr_plan_t;
+
+/*
+ * bsr_plan -- validate a BSR pattern and build the device work list.
+ *
+ *   indptr_host   host int32[MB + 1], MB = ceil(M / R); indptr[0] == 0,
+ *                 non-decreasing.
+ *   indices_host  host int32[nnz] (nnz = indptr[MB]) block columns, each in
+ *                 [0, NB), NB = N / C; no repeats within a block row (a mask
+ *                 holds a block once).  Any order.
+ *   M, N, R, C    rows / columns of the mask and block size; N % C == 0.
+ *   num_qo_heads, num_kv_heads   num_qo_heads % num_kv_heads == 0; qo head h
+ *                 reads kv head h / (num_qo_heads / num_kv_heads).
+ *   head_dim      multiple of 64, <= 256 in this build.
+ *   causal        must be 0 in this build (SFA_ERR_UNSUPPORTED otherwise).
+ *   sm_scale      softmax scale; <= 0 selects 1/sqrt(head_dim).
+ *   dtype         element type of q, k, v and out.
+ *   int_ws        device buffer the work list is copied into (on `stream`);
+ *                 size from bsr_plan_int_workspace_size().
+ *   float_ws      device float workspace for split partial results, or
+ *                 NULL.  This build's BSR kernels keep every row block's
+ *                 keys in one CTA and never touch it.
+ *   plan_out      receives a handle, valid until bsr_plan_destroy(); the
+ *                 workspaces must stay allocated as long as it is used.
+ */
+sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int M, int N,
+                    int R, int C, int num_qo_heads, int num_kv_heads, int head_dim, int causal,
+                    float sm_scale, sfa_dtype dtype, void* int_ws, size_t int_ws_bytes,
+                    void* float_ws, size_t float_ws_bytes, sfa_stream_t stream,
+                    bsr_plan_t* plan_out);
+
+/* Bytes of int workspace bsr_plan needs for this pattern. Host only. */
+sfa_status bsr_plan_int_workspace_size(const int32_t* indptr_host, int M, int N, int R, int C,
+                                       int num_qo_heads, int num_kv_heads, int head_dim,
+                                       size_t* bytes);
+
+/*
+ * bsr_run -- block-sparse attention with a plan.
+ *   q    device (M, num_qo_heads, head_dim), NHD, dtype.
+ *   k, v device (N, num_kv_heads, head_dim), NHD, dtype.
+ *   out  device (M, num_qo_heads, head_dim), dtype.
+ *   lse  device float32 (M, num_qo_heads) or NULL: natural-log log-sum-exp
+ *        of the scaled logits of the row's allowed columns.
+ * Rows with no stored block write out = +0 and lse = -inf.
+ */
+sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v, void* out,
+                   float* lse, sfa_stream_t stream);
+
+/* Frees the plan's host state.  Safe on NULL.  Does not touch the
+ * caller's workspaces. */
+void bsr_plan_destroy(bsr_plan_t plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFA_GB300_H */

@@ -1,0 +1,248 @@
+"""Python binding of libsfa_gb300.so (sparse flash attention for GB300).
+
+Argument marshalling only: every function here forwards to the C entry point
+of the same name declared in include/sfa.h; all computation runs in the
+library's CUDA kernels.  Tensors are passed as device pointers (torch is used
+for device memory and streams only).  If the shared library has not been
+built, loading raises -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+LIB_PATH = _build.LIB_PATH
+
+SFA_OK = 0
+SFA_ERR_INVALID_ARG = 1
+SFA_ERR_UNSUPPORTED = 2
+SFA_ERR_WORKSPACE = 3
+SFA_ERR_INDEX_RANGE = 4
+SFA_ERR_CUDA = 5
+
+LAYOUTS = {"BSND": 0, "BNSD": 1}
+DTYPES = {"f16": 0, "bf16": 1}
+
+# Every entry point of include/sfa.h.
+EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
+           "sfa_status_string", "sfa_kernel_launches", "bsr_plan", "bsr_plan_int_workspace_size", "bsr_run",
+           "bsr_plan_destroy")
+
+
+class SfaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class SfaOptions(ctypes.Structure):
+    _fields_ = [("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("value_is_key_prefix", ctypes.c_int), ("validate_indices", ctypes.c_int),
+                ("num_splits", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library (nvcc, sm_103a)."""
+    return _build.build(force=force)
+
+
+def load():
+    """ctypes handle of the built library (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is not built; call build() first")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            sfa_args = [vp, vp, vp, vp] + [ci] * 8 + [cf, ci, ci, ci, vp, vp, vp]
+            lib.sfa_run.argtypes = sfa_args
+            lib.sfa_run.restype = ci
+            lib.sfa_run_ex.argtypes = sfa_args + [ctypes.POINTER(SfaOptions)]
+            lib.sfa_run_ex.restype = ci
+            lib.sfa_workspace_size.argtypes = [ci] * 8 + [ctypes.POINTER(sz)]
+            lib.sfa_workspace_size.restype = ci
+            lib.sfa_get_last_error.argtypes = [vp]
+            lib.sfa_get_last_error.restype = ci
+            lib.sfa_status_string.argtypes = [ci]
+            lib.sfa_status_string.restype = ctypes.c_char_p
+            lib.sfa_kernel_launches.argtypes = []
+            lib.sfa_kernel_launches.restype = ctypes.c_uint64
+            lib.bsr_plan.argtypes = [vp, vp] + [ci] * 8 + [cf, ci, vp, sz, vp, sz, vp,
+                                                          ctypes.POINTER(vp)]
+            lib.bsr_plan.restype = ci
+            lib.bsr_plan_int_workspace_size.argtypes = [vp] + [ci] * 7 + [ctypes.POINTER(sz)]
+            lib.bsr_plan_int_workspace_size.restype = ci
+            lib.bsr_run.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+            lib.bsr_run.restype = ci
+            lib.bsr_plan_destroy.argtypes = [vp]
+            lib.bsr_plan_destroy.restype = None
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().sfa_status_string(int(status)).decode()
+
+
+def _ptr(x) -> int | None:
+    """Device/host address of a tensor, or an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != SFA_OK:
+        raise SfaError(status, what)
+
+
+def _enum(v, table):
+    return table[v] if isinstance(v, str) else int(v)
+
+
+def sfa_run(q, k, v, sparse_idx, B, S1, S2, N1, N2, Dk, Dv, topK, scale, layout, causal, dtype,
+            out, lse=None, stream=None, check=True) -> int:
+    """Forwards to sfa_run(); returns the status (raises unless check=False)."""
+    st = load().sfa_run(_ptr(q), _ptr(k), _ptr(v), _ptr(sparse_idx), B, S1, S2, N1, N2, Dk, Dv,
+                        topK, float(scale), _enum(layout, LAYOUTS), int(bool(causal)),
+                        _enum(dtype, DTYPES), _ptr(out), _ptr(lse), _stream(stream))
+    if check:
+        _check(st, "sfa_run")
+    return st
+
+
+def sfa_run_ex(q, k, v, sparse_idx, B, S1, S2, N1, N2, Dk, Dv, topK, scale, layout, causal, dtype,
+               out, lse=None, stream=None, workspace=None, workspace_bytes=0,
+               value_is_key_prefix=False, validate_indices=False, num_splits=0,
+               check=True) -> int:
+    """Forwards to sfa_run_ex() with an sfa_options built from the keywords."""
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    opt = SfaOptions(_ptr(workspace), int(workspace_bytes), int(bool(value_is_key_prefix)),
+                     int(bool(validate_indices)), int(num_splits))
+    st = load().sfa_run_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(sparse_idx), B, S1, S2, N1, N2, Dk, Dv,
+                           topK, float(scale), _enum(layout, LAYOUTS), int(bool(causal)),
+                           _enum(dtype, DTYPES), _ptr(out), _ptr(lse), _stream(stream),
+                           ctypes.byref(opt))
+    if check:
+        _check(st, "sfa_run_ex")
+    return st
+
+
+def sfa_workspace_size(B, S1, N1, N2, Dk, Dv, topK, num_splits=0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().sfa_workspace_size(B, S1, N1, N2, Dk, Dv, topK, num_splits, ctypes.byref(out)),
+           "sfa_workspace_size")
+    return out.value
+
+
+def sfa_kernel_launches() -> int:
+    """Kernels the library has launched in this process."""
+    return int(load().sfa_kernel_launches())
+
+
+def sfa_get_last_error(stream=None) -> int:
+    """Status of the device error word (synchronises the stream)."""
+    return load().sfa_get_last_error(_stream(stream))
+
+
+class BsrPlan:
+    """Owner of a bsr_plan_t handle (destroyed with the object)."""
+
+    def __init__(self, handle: int, int_ws, M, N, Hq, d):
+        self.handle = handle
+        self.int_ws = int_ws          # keeps the device work list alive
+        self.M, self.N, self.Hq, self.d = M, N, Hq, d
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.bsr_plan_destroy(self.handle)
+            self.handle = None
+
+
+def bsr_plan_int_workspace_size(indptr_host, M, N, R, C, num_qo_heads, num_kv_heads,
+                                head_dim) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().bsr_plan_int_workspace_size(_ptr(indptr_host), M, N, R, C, num_qo_heads,
+                                              num_kv_heads, head_dim, ctypes.byref(out)),
+           "bsr_plan_int_workspace_size")
+    return out.value
+
+
+def bsr_plan(indptr_host, indices_host, M, N, R, C, num_qo_heads, num_kv_heads, head_dim,
+             causal=False, sm_scale=0.0, dtype="f16", int_ws=None, float_ws=None,
+             stream=None) -> BsrPlan:
+    """Forwards to bsr_plan().  indptr/indices are host int32 tensors; int_ws a
+    device uint8 tensor (allocated here with torch if None)."""
+    import torch
+    if int_ws is None:
+        need = bsr_plan_int_workspace_size(indptr_host, M, N, R, C, num_qo_heads, num_kv_heads,
+                                           head_dim)
+        int_ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    fws_bytes = 0 if float_ws is None else float_ws.numel() * float_ws.element_size()
+    handle = ctypes.c_void_p(0)
+    st = load().bsr_plan(_ptr(indptr_host), _ptr(indices_host) if indices_host.numel() else None,
+                         M, N, R, C, num_qo_heads, num_kv_heads, head_dim, int(bool(causal)),
+                         float(sm_scale), _enum(dtype, DTYPES), _ptr(int_ws),
+                         int_ws.numel() * int_ws.element_size(), _ptr(float_ws), fws_bytes,
+                         _stream(stream), ctypes.byref(handle))
+    _check(st, "bsr_plan")
+    return BsrPlan(handle.value, int_ws, M, N, num_qo_heads, head_dim)
+
+
+def bsr_run(plan: BsrPlan, q, k, v, out, lse=None, stream=None):
+    _check(load().bsr_run(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                          _stream(stream)), "bsr_run")
+
+
+def bsr_plan_destroy(plan: BsrPlan):
+    if plan.handle:
+        load().bsr_plan_destroy(plan.handle)
+        plan.handle = None
+
+
+# ---------------------------------------------------------------------------
+# Convenience: allocate outputs with torch and call the entry points above.
+
+def sparse_flash_attention(query, key, value, sparse_indices, scale, layout="BSND",
+                           causal=False, return_lse=False, stream=None, **opts):
+    """Shapes as in the operator spec; value may be key[..., :Dv] (prefix view)."""
+    import torch
+    if layout == "BSND":
+        B, S1, N1, Dk = query.shape
+        _, S2, N2, _ = key.shape
+        out_shape, lse_shape = (B, S1, N1, value.shape[-1]), (B, S1, N1)
+    else:
+        B, N1, S1, Dk = query.shape
+        _, N2, S2, _ = key.shape
+        out_shape, lse_shape = (B, N1, S1, value.shape[-1]), (B, N1, S1)
+    Dv = value.shape[-1]
+    topK = sparse_indices.shape[-1]
+    dtype = {torch.float16: "f16", torch.bfloat16: "bf16"}[query.dtype]
+    prefix = value.data_ptr() == key.data_ptr()
+    if not prefix:
+        value = value.contiguous()
+    out = torch.empty(out_shape, dtype=query.dtype, device=query.device)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=query.device) if return_lse else None
+    v_arg = key if prefix else value
+    sfa_run_ex(query, key, v_arg, sparse_indices, B, S1, S2, N1, N2, Dk, Dv, topK, scale, layout,
+               causal, dtype, out, lse, stream, value_is_key_prefix=prefix, **opts)
+    return (out, lse) if return_lse else out

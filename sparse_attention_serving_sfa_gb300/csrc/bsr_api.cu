@@ -1,0 +1,171 @@
+// C ABI of the block-sparse path ("flashinfer.sparse",
+// BlockSparseAttentionWrapper): plan() validates the BSR pattern on the host
+// and uploads it with a row-tile work list into the caller's int workspace;
+// run() launches the kernels with that plan.
+#include <math.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+struct bsr_plan_s {
+    int M, N, R, C, Hq, Hkv, d;
+    sfa_dtype dtype;
+    float scale;
+    int MB, NB, nnz, ntiles;
+    const int32_t* d_indptr;
+    const int32_t* d_indices;
+    const sfa::BsrTile* d_tiles;
+    std::vector<int32_t> staging;   // host copy kept alive for the async upload
+};
+
+namespace {
+
+constexpr int kTileRows = 64;
+
+size_t round4(size_t n) { return (n + 3) & ~size_t(3); }
+
+int count_tiles(int M, int R) {
+    const int MB = (M + R - 1) / R;
+    int n = 0;
+    for (int rb = 0; rb < MB; ++rb) {
+        const int rows = std::min(R, M - rb * R);
+        n += (rows + kTileRows - 1) / kTileRows;
+    }
+    return n;
+}
+
+sfa_status check_shape(int M, int N, int R, int C, int Hq, int Hkv, int d) {
+    if (M < 1 || N < 1 || R < 1 || C < 1 || Hq < 1 || Hkv < 1 || d < 1) return SFA_ERR_INVALID_ARG;
+    if (N % C != 0) return SFA_ERR_INVALID_ARG;        // NB = N / C, N divisible by C
+    if (Hq % Hkv != 0) return SFA_ERR_INVALID_ARG;     // qo heads a multiple of kv heads
+    if (d % 64 != 0) return SFA_ERR_INVALID_ARG;
+    if (d > 256) return SFA_ERR_UNSUPPORTED;
+    return SFA_OK;
+}
+
+size_t int_ws_bytes(int MB, int nnz, int ntiles) {
+    return 4 * (round4((size_t)MB + 1) + round4((size_t)nnz) + 4 * (size_t)ntiles);
+}
+
+}  // namespace
+
+extern "C" {
+
+sfa_status bsr_plan_int_workspace_size(const int32_t* indptr_host, int M, int N, int R, int C,
+                                       int num_qo_heads, int num_kv_heads, int head_dim,
+                                       size_t* bytes) {
+    if (!indptr_host || !bytes) return SFA_ERR_INVALID_ARG;
+    sfa_status st = check_shape(M, N, R, C, num_qo_heads, num_kv_heads, head_dim);
+    if (st != SFA_OK) return st;
+    const int MB = (M + R - 1) / R;
+    const int nnz = indptr_host[MB];
+    if (nnz < 0) return SFA_ERR_INVALID_ARG;
+    *bytes = int_ws_bytes(MB, nnz, count_tiles(M, R));
+    return SFA_OK;
+}
+
+sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int M, int N,
+                    int R, int C, int num_qo_heads, int num_kv_heads, int head_dim, int causal,
+                    float sm_scale, sfa_dtype dtype, void* int_ws, size_t int_ws_bytes_given,
+                    void* float_ws, size_t float_ws_bytes, sfa_stream_t stream,
+                    bsr_plan_t* plan_out) {
+    (void)float_ws;
+    (void)float_ws_bytes;
+    if (!plan_out || !indptr_host) return SFA_ERR_INVALID_ARG;
+    *plan_out = nullptr;
+    sfa_status st = check_shape(M, N, R, C, num_qo_heads, num_kv_heads, head_dim);
+    if (st != SFA_OK) return st;
+    if (dtype != SFA_DTYPE_F16 && dtype != SFA_DTYPE_BF16) return SFA_ERR_INVALID_ARG;
+    if (!isfinite(sm_scale)) return SFA_ERR_INVALID_ARG;
+    if (causal) return SFA_ERR_UNSUPPORTED;
+    const int MB = (M + R - 1) / R, NB = N / C;
+    // indptr: starts at 0, non-decreasing
+    if (indptr_host[0] != 0) return SFA_ERR_INVALID_ARG;
+    for (int i = 0; i < MB; ++i)
+        if (indptr_host[i + 1] < indptr_host[i]) return SFA_ERR_INVALID_ARG;
+    const int nnz = indptr_host[MB];
+    if (nnz > 0 && !indices_host) return SFA_ERR_INVALID_ARG;
+    // indices: each block column in [0, NB), at most once per block row
+    {
+        std::vector<unsigned char> seen((size_t)NB, 0);
+        for (int i = 0; i < MB; ++i) {
+            for (int j = indptr_host[i]; j < indptr_host[i + 1]; ++j) {
+                const int c = indices_host[j];
+                if (c < 0 || c >= NB || seen[(size_t)c]) return SFA_ERR_INVALID_ARG;
+                seen[(size_t)c] = 1;
+            }
+            for (int j = indptr_host[i]; j < indptr_host[i + 1]; ++j) seen[(size_t)indices_host[j]] = 0;
+        }
+    }
+    const int ntiles = count_tiles(M, R);
+    const size_t need = int_ws_bytes(MB, nnz, ntiles);
+    if (!int_ws || int_ws_bytes_given < need) return SFA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(int_ws) & 15u) return SFA_ERR_INVALID_ARG;
+
+    bsr_plan_s* plan = new (std::nothrow) bsr_plan_s();
+    if (!plan) return SFA_ERR_INVALID_ARG;
+    plan->M = M; plan->N = N; plan->R = R; plan->C = C;
+    plan->Hq = num_qo_heads; plan->Hkv = num_kv_heads; plan->d = head_dim;
+    plan->dtype = dtype;
+    plan->scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)head_dim);
+    plan->MB = MB; plan->NB = NB; plan->nnz = nnz; plan->ntiles = ntiles;
+
+    // Work list: row tiles of <= 64 rows, heaviest block rows first.
+    std::vector<sfa::BsrTile> tiles;
+    tiles.reserve((size_t)ntiles);
+    for (int rb = 0; rb < MB; ++rb) {
+        const int rows = std::min(R, M - rb * R);
+        for (int r0 = 0; r0 < rows; r0 += kTileRows)
+            tiles.push_back({rb, rb * R + r0, std::min(kTileRows, rows - r0), 0});
+    }
+    std::stable_sort(tiles.begin(), tiles.end(), [&](const sfa::BsrTile& a, const sfa::BsrTile& b) {
+        return (indptr_host[a.rb + 1] - indptr_host[a.rb]) > (indptr_host[b.rb + 1] - indptr_host[b.rb]);
+    });
+
+    const size_t n_indptr = round4((size_t)MB + 1), n_indices = round4((size_t)nnz);
+    plan->staging.assign(need / 4, 0);
+    std::copy(indptr_host, indptr_host + MB + 1, plan->staging.begin());
+    if (nnz) std::copy(indices_host, indices_host + nnz, plan->staging.begin() + n_indptr);
+    std::copy(reinterpret_cast<const int32_t*>(tiles.data()),
+              reinterpret_cast<const int32_t*>(tiles.data()) + 4 * tiles.size(),
+              plan->staging.begin() + n_indptr + n_indices);
+    int32_t* base = static_cast<int32_t*>(int_ws);
+    plan->d_indptr = base;
+    plan->d_indices = base + n_indptr;
+    plan->d_tiles = reinterpret_cast<const sfa::BsrTile*>(base + n_indptr + n_indices);
+    cudaError_t err = cudaMemcpyAsync(int_ws, plan->staging.data(), need, cudaMemcpyHostToDevice,
+                                      reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) {
+        delete plan;
+        return SFA_ERR_CUDA;
+    }
+    *plan_out = plan;
+    return SFA_OK;
+}
+
+sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v, void* out,
+                   float* lse, sfa_stream_t stream) {
+    if (!plan || !q || !k || !v || !out) return SFA_ERR_INVALID_ARG;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!a16(q) || !a16(k) || !a16(v) || !a16(out)) return SFA_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SFA_ERR_INVALID_ARG;
+    sfa::BsrParams p{};
+    p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse;
+    p.indptr = plan->d_indptr;
+    p.indices = plan->d_indices;
+    p.tiles = plan->d_tiles;
+    p.ntiles = plan->ntiles;
+    p.M = plan->M; p.N = plan->N; p.R = plan->R; p.C = plan->C;
+    p.Hq = plan->Hq; p.Hkv = plan->Hkv; p.d = plan->d;
+    p.scale_log2 = plan->scale * sfa::kLog2e;
+    cudaError_t err = sfa::launch_bsr_generic(p, plan->dtype, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+void bsr_plan_destroy(bsr_plan_t plan) { delete plan; }
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Path selection for a top-K sparse attention call.
+#include "dispatch.h"
+
+namespace sfa {
+
+namespace {
+constexpr int kMaxSplits = 32;
+constexpr int kGenericChunk = 32;
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Splits of whole chunks so that no split is empty.
+void set_splits(Plan& pl, int topK, int want, int chunk) {
+    if (want < 1) want = 1;
+    int per = ceil_div(topK, want);
+    per = ceil_div(per, chunk) * chunk;
+    pl.slots_per_split = per;
+    pl.splits = ceil_div(topK, per);
+}
+}  // namespace
+
+int max_splits_for(int topK) {
+    int s = ceil_div(topK, 64);
+    return s < kMaxSplits ? s : kMaxSplits;
+}
+
+size_t plan_extra_ws_bytes(int, int, int, int, int, int, int) { return 0; }
+
+Plan choose_plan(const SfaParams& p, sfa_dtype, int num_sms, int forced_splits) {
+    Plan pl;
+    pl.kind = PATH_GENERIC;
+    const int hb = p.G > 4 ? 8 : 4;
+    const int64_t ctas = (int64_t)p.B * p.N2 * p.S1 * ceil_div(p.G, hb);
+    int want = forced_splits > 0 ? forced_splits
+                                 : (int)((2LL * num_sms + ctas - 1) / ctas);
+    if (forced_splits <= 0 && want > max_splits_for(p.topK)) want = max_splits_for(p.topK);
+    set_splits(pl, p.topK, want, kGenericChunk);
+    return pl;
+}
+
+cudaError_t run_plan(const Plan& plan, SfaParams& p, sfa_dtype dtype, void*, cudaStream_t stream) {
+    p.splits = plan.splits;
+    p.slots_per_split = plan.slots_per_split;
+    cudaError_t err = launch_sfa_generic(p, dtype, stream);
+    if (err != cudaSuccess) return err;
+    if (p.splits > 1) err = launch_sfa_combine(p, dtype, stream);
+    return err;
+}
+
+}  // namespace sfa

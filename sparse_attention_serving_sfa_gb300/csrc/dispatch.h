@@ -1,0 +1,32 @@
+// Path selection for a top-K sparse attention call.
+#pragma once
+
+#include "internal.h"
+
+namespace sfa {
+
+enum PathKind {
+    PATH_GENERIC = 0,  // warp-FMA kernel, any supported shape
+};
+
+struct Plan {
+    int kind = PATH_GENERIC;
+    int splits = 1;            // topK splits (partials merged by the combine kernel)
+    int slots_per_split = 0;   // multiple of the path's chunk size
+    size_t extra_ws_bytes = 0; // workspace beyond the split partials
+};
+
+// Picks the kernel path and split count for `p` (sizes and strides filled).
+Plan choose_plan(const SfaParams& p, sfa_dtype dtype, int num_sms, int forced_splits);
+
+// Launches the plan's kernels on `stream`.
+cudaError_t run_plan(const Plan& plan, SfaParams& p, sfa_dtype dtype, void* extra_ws,
+                     cudaStream_t stream);
+
+// Upper bound of Plan::extra_ws_bytes over every plan these sizes can get.
+size_t plan_extra_ws_bytes(int B, int S1, int N1, int N2, int Dk, int Dv, int topK);
+
+// Largest split count any plan uses for this topK.
+int max_splits_for(int topK);
+
+}  // namespace sfa

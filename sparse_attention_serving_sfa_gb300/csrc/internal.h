@@ -1,0 +1,67 @@
+// Internal launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sfa.h"
+
+namespace sfa {
+
+// Library-wide count of kernel launches (see sfa_kernel_launches()).
+void count_launches(int n);
+
+// One top-K sparse attention call, resolved to element strides.  A "row" of
+// q / out is one (b, n1, s1) head vector; a row of k / v is one (b, n2, s2)
+// key; a row of idx is the topK list of one (b, n2, s1).
+struct SfaParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* idx;
+    void* out;
+    float* lse;
+    float* ws_o;   // [rows][splits][Dv] unnormalised partial outputs
+    float* ws_ml;  // [rows][splits][2]  (running max in log2 units, sum)
+    int* err_word; // bit 0 set when validation sees an index outside [0, S2)
+    int B, S1, S2, N1, N2, G, Dk, Dv, topK;
+    int causal, validate, splits, slots_per_split;
+    float scale_log2;  // scale * log2(e)
+    int64_t q_sb, q_ss, q_sh;
+    int64_t k_sb, k_ss, k_sh;
+    int64_t v_sb, v_ss, v_sh;
+    int64_t i_sb, i_ss, i_sh;
+    int64_t o_sb, o_ss, o_sh;
+    int64_t l_sb, l_ss, l_sh;
+};
+
+// Bytes of split workspace for `splits` splits.
+size_t sfa_split_ws_bytes(int64_t rows, int splits, int Dv);
+
+// Generic warp-FMA path (any supported shape) and its split combine.
+cudaError_t launch_sfa_generic(const SfaParams& p, sfa_dtype dtype, cudaStream_t stream);
+cudaError_t launch_sfa_combine(const SfaParams& p, sfa_dtype dtype, cudaStream_t stream);
+
+// One row tile of the block-sparse work list: `nrows` query rows starting at
+// `row0`, all inside block row `rb`.
+struct BsrTile {
+    int rb, row0, nrows, pad;
+};
+
+struct BsrParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    float* lse;
+    const int32_t* indptr;   // device copy, MB + 1
+    const int32_t* indices;  // device copy, nnz
+    const BsrTile* tiles;    // device work list
+    int ntiles;
+    int M, N, R, C, Hq, Hkv, d;
+    float scale_log2;
+};
+
+cudaError_t launch_bsr_generic(const BsrParams& p, sfa_dtype dtype, cudaStream_t stream);
+
+}  // namespace sfa

@@ -1,0 +1,138 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry
+point declared in include/*.h, and rejects bad arguments on the host before
+any launch."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+import sparse_attention_serving_sfa_gb300 as sfa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sfa.build()
+    return sfa.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"sfa_run", "sfa_run_ex", "bsr_plan", "bsr_run", "bsr_plan_destroy"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(sfa.EXPORTS) <= names
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert sfa.status_string(st)
+
+
+FAKE = 1 << 20     # aligned non-null address; never dereferenced by rejected calls
+
+
+def call_run(**over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE + 4096, idx=FAKE, B=1, S1=4, S2=64, N1=4, N2=1, Dk=64, Dv=64,
+             topK=16, scale=0.125, layout=0, causal=0, dtype=0, out=FAKE, lse=None)
+    a.update(over)
+    return sfa.sfa_run(a["q"], a["k"], a["v"], a["idx"], a["B"], a["S1"], a["S2"], a["N1"],
+                       a["N2"], a["Dk"], a["Dv"], a["topK"], a["scale"], a["layout"], a["causal"],
+                       a["dtype"], a["out"], a["lse"], None, check=False)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(N1=6, N2=4), sfa.SFA_ERR_INVALID_ARG),            # N1 % N2 != 0
+    (dict(Dv=128, Dk=64), sfa.SFA_ERR_INVALID_ARG),         # Dv > Dk
+    (dict(Dk=96, Dv=64), sfa.SFA_ERR_INVALID_ARG),          # Dk not 64-aligned
+    (dict(Dv=32), sfa.SFA_ERR_INVALID_ARG),                 # Dv not 64-aligned
+    (dict(topK=65), sfa.SFA_ERR_INVALID_ARG),               # topK > S2
+    (dict(topK=0), sfa.SFA_ERR_INVALID_ARG),
+    (dict(causal=1, S1=65), sfa.SFA_ERR_INVALID_ARG),       # causal needs S1 <= S2
+    (dict(layout=2), sfa.SFA_ERR_INVALID_ARG),
+    (dict(dtype=7), sfa.SFA_ERR_INVALID_ARG),
+    (dict(q=None), sfa.SFA_ERR_INVALID_ARG),
+    (dict(idx=None), sfa.SFA_ERR_INVALID_ARG),
+    (dict(out=None), sfa.SFA_ERR_INVALID_ARG),
+    (dict(k=FAKE + 2), sfa.SFA_ERR_INVALID_ARG),            # misaligned
+    (dict(lse=FAKE + 1), sfa.SFA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), sfa.SFA_ERR_INVALID_ARG),
+    (dict(B=0), sfa.SFA_ERR_INVALID_ARG),
+    (dict(Dk=640, Dv=64), sfa.SFA_ERR_UNSUPPORTED),         # beyond this build's limits
+    (dict(Dk=640, Dv=576), sfa.SFA_ERR_UNSUPPORTED),
+])
+def test_sfa_run_rejects(lib, over, status):
+    assert call_run(**over) == status
+
+
+def test_prefix_flag_requires_alias(lib):
+    st = sfa.sfa_run_ex(FAKE, FAKE, FAKE + 4096, FAKE, 1, 4, 64, 4, 1, 128, 64, 16, 0.1, 0, 0, 0,
+                        FAKE, None, None, value_is_key_prefix=True, check=False)
+    assert st == sfa.SFA_ERR_INVALID_ARG
+
+
+def test_workspace_size(lib):
+    n = sfa.sfa_workspace_size(16, 1, 32, 8, 128, 128, 1024)
+    assert n >= 16 * 32 * 2 * (128 + 2) * 4
+    assert sfa.sfa_workspace_size(1, 1, 1, 1, 64, 64, 16, num_splits=1) == 0
+    assert sfa.sfa_workspace_size(2, 3, 4, 2, 64, 64, 64, num_splits=4) == 2 * 3 * 4 * 4 * 66 * 4
+    with pytest.raises(sfa.SfaError):
+        sfa.sfa_workspace_size(0, 1, 1, 1, 64, 64, 16)
+
+
+def bsr_call(indptr, indices, M, N, R, C, Hq=4, Hkv=2, d=64, causal=0, ws_bytes=1 << 20):
+    handle = ctypes.c_void_p(0)
+    ip = torch.tensor(indptr, dtype=torch.int32)
+    ix = torch.tensor(indices if indices else [0], dtype=torch.int32)
+    st = sfa.load().bsr_plan(ip.data_ptr(), ix.data_ptr(), M, N, R, C, Hq, Hkv, d, causal, 0.0, 0,
+                             FAKE, ws_bytes, None, 0, None, ctypes.byref(handle))
+    assert not handle.value
+    return st
+
+
+@pytest.mark.parametrize("args,status", [
+    (([0, 1, 2], [0, 1], 4, 5, 2, 2), sfa.SFA_ERR_INVALID_ARG),        # N % C != 0
+    (([1, 1, 2], [0, 1], 4, 4, 2, 2), sfa.SFA_ERR_INVALID_ARG),        # indptr[0] != 0
+    (([0, 2, 1], [0, 1], 4, 4, 2, 2), sfa.SFA_ERR_INVALID_ARG),        # decreasing indptr
+    (([0, 1, 2], [0, 2], 4, 4, 2, 2), sfa.SFA_ERR_INVALID_ARG),        # block column >= NB
+    (([0, 2, 2], [1, 1], 4, 4, 2, 2), sfa.SFA_ERR_INVALID_ARG),        # repeated block
+    (([0, 1, 2], [0, 1], 4, 4, 2, 2, 3, 2), sfa.SFA_ERR_INVALID_ARG),  # Hq % Hkv != 0
+    (([0, 1, 2], [0, 1], 4, 4, 2, 2, 4, 2, 96), sfa.SFA_ERR_INVALID_ARG),   # head_dim % 64
+    (([0, 1, 2], [0, 1], 4, 4, 2, 2, 4, 2, 320), sfa.SFA_ERR_UNSUPPORTED),  # head_dim > 256
+    (([0, 1, 2], [0, 1], 4, 4, 2, 2, 4, 2, 64, 1), sfa.SFA_ERR_UNSUPPORTED),  # causal
+])
+def test_bsr_plan_rejects(lib, args, status):
+    assert bsr_call(*args) == status
+
+
+def test_bsr_plan_workspace_too_small(lib):
+    assert bsr_call([0, 1, 2], [0, 1], 4, 4, 2, 2, ws_bytes=8) == sfa.SFA_ERR_WORKSPACE
+
+
+def test_bsr_int_workspace_size(lib):
+    ip = torch.tensor([0, 1, 3, 5], dtype=torch.int32)
+    n = sfa.bsr_plan_int_workspace_size(ip, 3, 3, 1, 1, 32, 8, 128)
+    # indptr (4) + indices (5 -> 8) + 3 tiles x 4 ints
+    assert n == 4 * (4 + 8 + 12)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(sfa, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(sfa, "_lib", None)
+    with pytest.raises(RuntimeError):
+        sfa.load()

@@ -1,0 +1,199 @@
+"""GPU parity of the top-K path: the CUDA library (through the C ABI) against
+the CPU oracle on the same seeded inputs, element by element at small sizes
+and on sampled rows at the full workload sizes."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_serving_sfa_gb300 as sfa
+import synth
+from tests import sfa_testlib as T
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    sfa.build()
+    sfa.load()
+
+
+def small(**kw):
+    base = dict(name="s", B=2, S1=3, S2=300, N1=8, N2=2, Dk=128, Dv=128, topK=100, dtype="bf16",
+                layout="BSND", causal=False, scale=0.09, seed=4321)
+    base.update(kw)
+    return synth.SfaCase(**base)
+
+
+def run_and_check(case, **opts):
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    out, lse = T.run_gpu(case, dev, **opts)
+    return T.check_full(case, d, out, lse)
+
+
+def test_tiny_workload():
+    run_and_check(synth.TINY)
+
+
+@pytest.mark.parametrize("layout", ["BSND", "BNSD"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_layouts_dtypes_causal(layout, dtype, causal):
+    run_and_check(small(layout=layout, dtype=dtype, causal=causal, S2=120 if causal else 300))
+
+
+@pytest.mark.parametrize("G,N2", [(1, 3), (4, 2), (8, 1), (16, 1), (128, 1)])
+def test_gqa_groups(G, N2):
+    run_and_check(small(N1=G * N2, N2=N2, S1=2, topK=70))
+
+
+@pytest.mark.parametrize("Dk,Dv,prefix", [(64, 64, False), (192, 128, True), (256, 64, False),
+                                          (576, 512, True), (512, 512, False)])
+def test_head_dims(Dk, Dv, prefix):
+    run_and_check(small(Dk=Dk, Dv=Dv, value_is_key_prefix=prefix, N1=4, N2=1, topK=77, S1=2))
+
+
+@pytest.mark.parametrize("topK", [1, 2, 31, 32, 33, 64, 65, 257])
+def test_ragged_topk(topK):
+    run_and_check(small(topK=topK, S2=max(topK, 300)))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_forced_splits_agree(splits):
+    case = small(topK=224, causal=True, S2=240)
+    run_and_check(case, num_splits=splits)
+
+
+def test_fully_masked_rows_exact_zero():
+    """causal, indices of some rows entirely above the diagonal; those rows
+    must be exactly +0 with lse = -inf, also when the row is split."""
+    case = small(causal=True, S1=16, S2=64, topK=20, index_kind="causal_mix", masked_frac=0.1,
+                 full_masked_rows=5)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    for splits in (1, 3):
+        out, lse = T.run_gpu(case, dev, num_splits=splits)
+        T.check_full(case, d, out, lse)
+        assert torch.all(out[0, :5] == 0) and torch.all(torch.isneginf(lse[0, :5]))
+
+
+def test_identity_indices_equal_dense_attention():
+    """topK = S2 with identity indices is dense attention (also checked by the
+    oracle pins); here against the oracle on the GPU path."""
+    case = small(S1=5, S2=96, topK=96, causal=True)
+    d = synth.make_sfa_inputs(case)
+    ident = torch.arange(case.S2, dtype=torch.int32).expand(case.B, case.S1, case.N2, case.S2)
+    d["idx"] = ident.contiguous()
+    out, lse = T.run_gpu(case, T.to_dev(d))
+    T.check_full(case, d, out, lse)
+
+
+def test_duplicate_indices_count_per_slot():
+    case = small(topK=40, S2=50)
+    d = synth.make_sfa_inputs(case)
+    g = torch.Generator().manual_seed(3)
+    d["idx"] = torch.randint(0, 10, d["idx"].shape, generator=g, dtype=torch.int32)
+    out, lse = T.run_gpu(case, T.to_dev(d))
+    T.check_full(case, d, out, lse)
+
+
+def test_prefix_view_equals_separate_value():
+    case = small(Dk=192, Dv=128, value_is_key_prefix=True)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    out1, lse1 = T.run_gpu(case, dev)
+    dev2 = dict(dev, v=dev["v"].contiguous())
+    out2, lse2 = T.run_gpu(case.replace(value_is_key_prefix=False), dev2)
+    T.check_full(case, d, out1, lse1)
+    assert torch.allclose(out1.float(), out2.float(), atol=1e-2, rtol=0)
+
+
+def test_caller_workspace_and_too_small():
+    case = small(topK=256, S2=300)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    need = sfa.sfa_workspace_size(case.B, case.S1, case.N1, case.N2, case.Dk, case.Dv, case.topK,
+                                  num_splits=4)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out, lse = T.run_gpu(case, dev, workspace=ws, num_splits=4)
+    T.check_full(case, d, out, lse)
+    small_ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sfa.SfaError) as e:
+        T.run_gpu(case, dev, workspace=small_ws, num_splits=4)
+    assert e.value.status == sfa.SFA_ERR_WORKSPACE
+
+
+def test_out_of_range_indices_masked_and_reported():
+    case = small(topK=16, S2=64)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    assert sfa.sfa_get_last_error() == sfa.SFA_OK
+    bad = dev["idx"].clone()
+    bad[0, 0, 0, :4] = torch.tensor([-1, 64, 1 << 30, -(1 << 30)], dtype=torch.int32)
+    out, lse = T.run_gpu(case, dict(dev, idx=bad), validate_indices=True)
+    assert sfa.sfa_get_last_error() == sfa.SFA_ERR_INDEX_RANGE
+    assert sfa.sfa_get_last_error() == sfa.SFA_OK        # cleared by the read
+    # the bad slots behave as masked: equal to the oracle with those slots dropped
+    keep = d["idx"][0, 0, 0, 4:].clone()
+    G = case.G
+    ds = {"q": d["q"][:1, :1, :G].contiguous(), "k": d["k"][:1, :, :1].contiguous(),
+          "v": d["v"][:1, :, :1].contiguous(), "idx": keep.reshape(1, 1, 1, 12).contiguous()}
+    y, l = oracle.sfa(ds["q"], ds["k"], ds["v"], ds["idx"], case.scale, "BSND", False)
+    got = out[0, 0, :case.G].float().cpu().numpy()
+    assert oracle.precision_report(got, y[0, 0, :case.G], case.dtype)["passed"]
+
+
+def test_guard_bytes_untouched():
+    """Writes stay inside out / lse: canaries around both survive."""
+    case = small(topK=64, S2=100)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    n_out = case.B * case.S1 * case.N1 * case.Dv
+    n_lse = case.B * case.S1 * case.N1
+    big = torch.full((n_out + 2048,), 7.0, dtype=torch.bfloat16, device="cuda")
+    lbig = torch.full((n_lse + 256,), 7.0, dtype=torch.float32, device="cuda")
+    out = big[1024:1024 + n_out]
+    lse = lbig[128:128 + n_lse]
+    sfa.sfa_run(dev["q"], dev["k"], dev["v"], dev["idx"], case.B, case.S1, case.S2, case.N1,
+                case.N2, case.Dk, case.Dv, case.topK, case.scale, case.layout, case.causal,
+                case.dtype, out, lse)
+    torch.cuda.synchronize()
+    assert torch.all(big[:1024] == 7.0) and torch.all(big[1024 + n_out:] == 7.0)
+    assert torch.all(lbig[:128] == 7.0) and torch.all(lbig[128 + n_lse:] == 7.0)
+
+
+def test_stream_argument():
+    case = small()
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, lse = sfa.sparse_flash_attention(dev["q"], dev["k"], dev["v"], dev["idx"], case.scale,
+                                              case.layout, case.causal, return_lse=True, stream=s)
+    s.synchronize()
+    T.check_full(case, d, out, lse)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled rows
+
+@pytest.mark.parametrize("name", ["gqa_decode", "mla_decode", "mla_mtp", "sparse_prefill"])
+def test_full_workload_sampled(name):
+    case = synth.SFA_WORKLOADS[name]
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    out, lse = T.run_gpu(case, dev)
+    rows = T.sample_rows(case, 96 if name != "sparse_prefill" else 64)
+    if name == "sparse_prefill":
+        # include fully masked rows (b = 0, s1 < 8) and the last rows
+        extra = np.array([[0, n1, s1] for n1 in (0, 63) for s1 in (0, 7, 8)] +
+                         [[1, 5, 2047], [1, 63, 2046]])
+        rows = np.unique(np.concatenate([rows, extra]), axis=0)
+    T.check_rows(case, d, out, lse, rows)
+    assert torch.isfinite(out.float()).all()
+    if name == "sparse_prefill":
+        assert torch.all(out[0, :8] == 0)
