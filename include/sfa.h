@@ -134,6 +134,45 @@ const char* sfa_status_string(sfa_status status);
  * counterpart). */
 uint64_t sfa_kernel_launches(void);
 
+/* Size of the device scratch array behind sfa_run_noalloc (8 MiB). */
+#define SFA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * sfa_run_noalloc -- sfa_run for callers that cannot allocate device memory.
+ * (No counterpart in the operator spec or the FlashInfer pages: this is a
+ * deployment variant of the same computation.)
+ *
+ * Some callers may not call cudaMalloc at all: a serving engine that has
+ * reserved nearly all of HBM up front for its KV cache and owns every later
+ * allocation, a plugin host that forbids libraries from allocating behind its
+ * back, or a latency-critical loop that cannot take the device-wide
+ * synchronisation cudaFree can cause.  sfa_run, by contrast, may allocate (and
+ * grow) its library-owned workspace.  This entry point computes the same result
+ * as sfa_run with the generic kernel and its split combine, and keeps the split
+ * partials in a fixed device array of SFA_NOALLOC_SCRATCH_BYTES that is part of
+ * the library image: every GPU that loads the library holds those bytes until
+ * the process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *
+ * Arguments, layouts and results are those of sfa_run (value-prefix mode is
+ * inferred from v == k; no index validation).
+ * Limits: a shape whose sfa_workspace_size(..., num_splits = 0) exceeds
+ * SFA_NOALLOC_SCRATCH_BYTES is rejected with SFA_ERR_WORKSPACE before
+ * anything is launched; other argument errors as in sfa_run.
+ * Set-up: the first call on each device looks up the device address of the
+ * array (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.
+ * Sharing: all calls on a device share the one array and it keeps the last
+ * call's contents.  Nothing in it needs clearing (every split partial is
+ * written before it is read), but calls whose kernels overlap on the GPU --
+ * concurrent streams, or several host threads -- race on it and must be
+ * serialised by the caller.
+ */
+sfa_status sfa_run_noalloc(const void* q, const void* k, const void* v,
+                           const int32_t* sparse_idx, int B, int S1, int S2, int N1, int N2,
+                           int Dk, int Dv, int topK, float scale, sfa_layout layout, int causal,
+                           sfa_dtype dtype, void* out, float* lse, sfa_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Block-sparse (BSR) attention ("flashinfer.sparse",
  * BlockSparseAttentionWrapper: plan() builds cached auxiliary structures,

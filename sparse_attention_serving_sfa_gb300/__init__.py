@@ -28,7 +28,7 @@ DTYPES = {"f16": 0, "bf16": 1}
 
 # Every entry point of include/sfa.h.
 EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
-           "sfa_status_string", "sfa_kernel_launches", "bsr_plan", "bsr_plan_int_workspace_size", "bsr_run",
+           "sfa_status_string", "sfa_kernel_launches", "sfa_run_noalloc", "bsr_plan", "bsr_plan_int_workspace_size", "bsr_run",
            "bsr_plan_destroy")
 
 
@@ -65,6 +65,8 @@ def load():
             sfa_args = [vp, vp, vp, vp] + [ci] * 8 + [cf, ci, ci, ci, vp, vp, vp]
             lib.sfa_run.argtypes = sfa_args
             lib.sfa_run.restype = ci
+            lib.sfa_run_noalloc.argtypes = sfa_args
+            lib.sfa_run_noalloc.restype = ci
             lib.sfa_run_ex.argtypes = sfa_args + [ctypes.POINTER(SfaOptions)]
             lib.sfa_run_ex.restype = ci
             lib.sfa_workspace_size.argtypes = [ci] * 8 + [ctypes.POINTER(sz)]
@@ -145,6 +147,23 @@ def sfa_run_ex(q, k, v, sparse_idx, B, S1, S2, N1, N2, Dk, Dv, topK, scale, layo
     if check:
         _check(st, "sfa_run_ex")
     return st
+
+
+def sfa_run_noalloc(q, k, v, sparse_idx, B, S1, S2, N1, N2, Dk, Dv, topK, scale, layout, causal,
+                    dtype, out, lse=None, stream=None, check=True) -> int:
+    """Forwards to sfa_run_noalloc(): same arguments as sfa_run, for callers
+    that cannot allocate device memory (the library keeps the split partials
+    in a fixed device array of SFA_NOALLOC_SCRATCH_BYTES)."""
+    st = load().sfa_run_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(sparse_idx), B, S1, S2, N1, N2,
+                                Dk, Dv, topK, float(scale), _enum(layout, LAYOUTS),
+                                int(bool(causal)), _enum(dtype, DTYPES), _ptr(out), _ptr(lse),
+                                _stream(stream))
+    if check:
+        _check(st, "sfa_run_noalloc")
+    return st
+
+
+SFA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def sfa_workspace_size(B, S1, N1, N2, Dk, Dv, topK, num_splits=0) -> int:

@@ -35,6 +35,19 @@ struct SfaParams {
     int64_t l_sb, l_ss, l_sh;
 };
 
+// Host-side argument rules of the top-K entry points (status before launch).
+sfa_status check_args(const void* q, const void* k, const void* v, const int32_t* idx, int B,
+                      int S1, int S2, int N1, int N2, int Dk, int Dv, int topK, float scale,
+                      int layout, int causal, int dtype, const void* out, const float* lse,
+                      const sfa_options* opt);
+
+// Fills the element strides of `p` (sizes already set) for `layout`; with
+// `prefix`, value rows use the key's row length.
+void resolve_strides(SfaParams& p, int layout, bool prefix);
+
+// SM count of the current device (cached).
+int num_sms();
+
 // Bytes of split workspace for `splits` splits.
 size_t sfa_split_ws_bytes(int64_t rows, int splits, int Dv);
 

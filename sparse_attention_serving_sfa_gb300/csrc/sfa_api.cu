@@ -62,6 +62,8 @@ cudaError_t owned_workspace(size_t need, void** out) {
     return cudaSuccess;
 }
 
+}  // namespace
+
 int num_sms() {
     static int cached[64] = {};
     int dev = 0;
@@ -122,7 +124,6 @@ void resolve_strides(SfaParams& p, int layout, bool prefix) {
     }
 }
 
-}  // namespace
 }  // namespace sfa
 
 using namespace sfa;
