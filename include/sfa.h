@@ -40,7 +40,9 @@ typedef enum {
     SFA_ERR_UNSUPPORTED = 2,  /* legal per the spec but outside this build's limits */
     SFA_ERR_WORKSPACE = 3,    /* caller workspace missing or too small */
     SFA_ERR_INDEX_RANGE = 4,  /* a sparse index outside [0, S2) was seen (validate mode) */
-    SFA_ERR_CUDA = 5          /* a CUDA runtime call or launch failed */
+    SFA_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+    SFA_ERR_DEVICE_TIMEOUT = 6 /* a kernel's bounded wait gave up (reported by
+                                  sfa_get_last_error); that call's output is invalid */
 } sfa_status;
 
 /* Tensor layouts ("SparseFlashAttention 算子 API 描述", §2 布局说明):
@@ -107,8 +109,14 @@ typedef struct {
     /* 1: an out-of-range index also sets the library's device error word,
      * read (and cleared) by sfa_get_last_error. */
     int validate_indices;
-    /* Number of topK splits; 0 = chosen from the SM count. */
+    /* Number of topK splits of the generic path; 0 = chosen from the SM
+     * count. */
     int num_splits;
+    /* Launch tuning of the small-group path (G <= 8): persistent CTAs per SM
+     * (1 = deep shared-memory ring, 2 = two CTAs with shallow rings) and the
+     * total number of CTAs (chunk ranges).  0 = automatic. */
+    int ctas_per_sm;
+    int num_ctas;
 } sfa_options;
 
 sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t* sparse_idx,
@@ -121,9 +129,10 @@ sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t
 sfa_status sfa_workspace_size(int B, int S1, int N1, int N2, int Dk, int Dv, int topK,
                               int num_splits, size_t* bytes);
 
-/* Synchronises `stream`, then returns SFA_ERR_INDEX_RANGE if a call with
- * validate_indices saw an index outside [0, S2) since the last check
- * (clearing the flag), SFA_ERR_CUDA on a CUDA error, else SFA_OK. */
+/* Synchronises `stream`, then reads (and clears) the library's device error
+ * word: SFA_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up since the
+ * last check, else SFA_ERR_INDEX_RANGE if a call with validate_indices saw an
+ * index outside [0, S2); SFA_ERR_CUDA on a CUDA error; else SFA_OK. */
 sfa_status sfa_get_last_error(sfa_stream_t stream);
 
 /* Static text for a status code. */

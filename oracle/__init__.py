@@ -87,10 +87,22 @@ def _ptr(t: torch.Tensor) -> int:
 
 def _value_ld(v: torch.Tensor) -> int:
     """Element distance between consecutive value rows; v must be rows of
-    `ld` elements (contiguous, or the prefix view key[..., :Dv])."""
-    d0, d1, d2, dv = v.shape
-    ld = v.stride(2)
-    if v.stride(3) != 1 or v.stride(1) != d2 * ld or v.stride(0) != d1 * d2 * ld or ld < dv:
+    `ld` elements (contiguous, or the prefix view key[..., :Dv]).  Strides of
+    size-1 dimensions are ignored."""
+    if v.is_contiguous():
+        return v.shape[-1]
+    d, st = list(v.shape), list(v.stride())
+    ld = v.shape[-1]
+    for ax in (2, 1, 0):
+        if d[ax] > 1:
+            inner = int(np.prod(d[ax + 1:3]))
+            ld = st[ax] // inner
+            break
+    ok = st[3] == 1 and ld >= d[3]
+    for ax in (0, 1, 2):
+        if d[ax] > 1 and st[ax] != ld * int(np.prod(d[ax + 1:3])):
+            ok = False
+    if not ok:
         raise ValueError("value must be contiguous rows (or a prefix view of key)")
     return ld
 

@@ -24,10 +24,23 @@ int max_splits_for(int topK) {
     return s < kMaxSplits ? s : kMaxSplits;
 }
 
-size_t plan_extra_ws_bytes(int, int, int, int, int, int, int) { return 0; }
+size_t plan_extra_ws_bytes(int B, int S1, int N1, int N2, int Dk, int Dv, int topK) {
+    SfaParams p{};
+    p.B = B; p.S1 = S1; p.N1 = N1; p.N2 = N2; p.G = N1 / N2;
+    p.Dk = Dk; p.Dv = Dv; p.topK = topK;
+    return decode_supported(p) ? decode_ws_bytes(p) : 0;
+}
 
 Plan choose_plan(const SfaParams& p, sfa_dtype, int num_sms, int forced_splits) {
     Plan pl;
+    if (decode_supported(p)) {
+        // persistent stream-K kernel: its own schedule, partials in extra_ws
+        pl.kind = PATH_DECODE;
+        pl.splits = 1;
+        pl.slots_per_split = p.topK;
+        pl.extra_ws_bytes = decode_ws_bytes(p);
+        return pl;
+    }
     pl.kind = PATH_GENERIC;
     const int hb = p.G > 4 ? 8 : 4;
     const int64_t ctas = (int64_t)p.B * p.N2 * p.S1 * ceil_div(p.G, hb);
@@ -38,9 +51,12 @@ Plan choose_plan(const SfaParams& p, sfa_dtype, int num_sms, int forced_splits) 
     return pl;
 }
 
-cudaError_t run_plan(const Plan& plan, SfaParams& p, sfa_dtype dtype, void*, cudaStream_t stream) {
+cudaError_t run_plan(const Plan& plan, SfaParams& p, sfa_dtype dtype, void* extra_ws,
+                     int num_sms, cudaStream_t stream) {
     p.splits = plan.splits;
     p.slots_per_split = plan.slots_per_split;
+    if (plan.kind == PATH_DECODE)
+        return launch_sfa_decode(p, dtype, num_sms, extra_ws, plan.extra_ws_bytes, stream);
     cudaError_t err = launch_sfa_generic(p, dtype, stream);
     if (err != cudaSuccess) return err;
     if (p.splits > 1) err = launch_sfa_combine(p, dtype, stream);

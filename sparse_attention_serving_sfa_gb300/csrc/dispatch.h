@@ -7,6 +7,7 @@ namespace sfa {
 
 enum PathKind {
     PATH_GENERIC = 0,  // warp-FMA kernel, any supported shape
+    PATH_DECODE = 1,   // small-group persistent gather kernel (sfa_decode.cu)
 };
 
 struct Plan {
@@ -19,9 +20,10 @@ struct Plan {
 // Picks the kernel path and split count for `p` (sizes and strides filled).
 Plan choose_plan(const SfaParams& p, sfa_dtype dtype, int num_sms, int forced_splits);
 
-// Launches the plan's kernels on `stream`.
+// Launches the plan's kernels on `stream`; `extra_ws` holds
+// plan.extra_ws_bytes bytes.
 cudaError_t run_plan(const Plan& plan, SfaParams& p, sfa_dtype dtype, void* extra_ws,
-                     cudaStream_t stream);
+                     int num_sms, cudaStream_t stream);
 
 // Upper bound of Plan::extra_ws_bytes over every plan these sizes can get.
 size_t plan_extra_ws_bytes(int B, int S1, int N1, int N2, int Dk, int Dv, int topK);

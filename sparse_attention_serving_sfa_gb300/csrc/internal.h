@@ -26,6 +26,7 @@ struct SfaParams {
     int* err_word; // bit 0 set when validation sees an index outside [0, S2)
     int B, S1, S2, N1, N2, G, Dk, Dv, topK;
     int causal, validate, splits, slots_per_split;
+    int ctas_per_sm, num_ctas;   // launch tuning of the small-group path (0 = auto)
     float scale_log2;  // scale * log2(e)
     int64_t q_sb, q_ss, q_sh;
     int64_t k_sb, k_ss, k_sh;
@@ -50,6 +51,14 @@ int num_sms();
 
 // Bytes of split workspace for `splits` splits.
 size_t sfa_split_ws_bytes(int64_t rows, int splits, int Dv);
+
+// Small-group decode path (G <= 8, Dk == Dv in {64, 128, 256}, G * Dk <= 512):
+// persistent stream-K kernel plus a combine of the ranges that share an index
+// list.  decode_ws_bytes bounds the workspace it needs.
+bool decode_supported(const SfaParams& p);
+size_t decode_ws_bytes(const SfaParams& p);
+cudaError_t launch_sfa_decode(const SfaParams& p, sfa_dtype dtype, int num_sms, void* ws,
+                              size_t ws_bytes, cudaStream_t stream);
 
 // Generic warp-FMA path (any supported shape) and its split combine.
 cudaError_t launch_sfa_generic(const SfaParams& p, sfa_dtype dtype, cudaStream_t stream);

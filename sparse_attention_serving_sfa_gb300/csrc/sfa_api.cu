@@ -8,6 +8,7 @@
 #include "common.cuh"
 #include "dispatch.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace sfa {
 
@@ -20,10 +21,19 @@ void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order
 
 namespace {
 
+// Device address of g_error_word on the current device (looked up once).
 int* error_word_ptr() {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
-    return static_cast<int*>(ptr);
+    static std::mutex mu;
+    static void* cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+        cached[dev] = ptr;
+    }
+    return static_cast<int*>(cached[dev]);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -95,7 +105,9 @@ sfa_status check_args(const void* q, const void* k, const void* v, const int32_t
         return SFA_ERR_INVALID_ARG;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SFA_ERR_INVALID_ARG;
     if (opt && opt->value_is_key_prefix && v != k) return SFA_ERR_INVALID_ARG;
-    if (opt && opt->num_splits < 0) return SFA_ERR_INVALID_ARG;
+    if (opt && (opt->num_splits < 0 || opt->ctas_per_sm < 0 || opt->ctas_per_sm > 2 ||
+                opt->num_ctas < 0))
+        return SFA_ERR_INVALID_ARG;
     if (opt && opt->workspace && !aligned16(opt->workspace)) return SFA_ERR_INVALID_ARG;
     if (Dk > 576 || Dv > 512) return SFA_ERR_UNSUPPORTED;
     // element offsets must fit int64 comfortably and grid.x must fit
@@ -138,6 +150,7 @@ const char* sfa_status_string(sfa_status s) {
         case SFA_ERR_WORKSPACE: return "workspace missing or too small";
         case SFA_ERR_INDEX_RANGE: return "sparse index outside [0, S2)";
         case SFA_ERR_CUDA: return "CUDA error";
+        case SFA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
     }
     return "unknown status";
 }
@@ -150,7 +163,10 @@ sfa_status sfa_workspace_size(int B, int S1, int N1, int N2, int Dk, int Dv, int
         Dk < Dv)
         return SFA_ERR_INVALID_ARG;
     const int splits = num_splits > 0 ? num_splits : max_splits_for(topK);
-    *bytes = sfa_split_ws_bytes((int64_t)B * S1 * N1, splits, Dv) + plan_extra_ws_bytes(B, S1, N1, N2, Dk, Dv, topK);
+    // a plan uses either split partials or its own extra workspace
+    const size_t split = sfa_split_ws_bytes((int64_t)B * S1 * N1, splits, Dv);
+    const size_t extra = plan_extra_ws_bytes(B, S1, N1, N2, Dk, Dv, topK);
+    *bytes = split > extra ? split : extra;
     return SFA_OK;
 }
 
@@ -169,10 +185,10 @@ sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t
     p.Dk = Dk; p.Dv = Dv; p.topK = topK;
     p.causal = causal ? 1 : 0;
     p.validate = (opt && opt->validate_indices) ? 1 : 0;
-    if (p.validate) {
-        p.err_word = error_word_ptr();
-        if (!p.err_word) return SFA_ERR_CUDA;
-    }
+    p.ctas_per_sm = opt ? opt->ctas_per_sm : 0;
+    p.num_ctas = opt ? opt->num_ctas : 0;
+    p.err_word = error_word_ptr();     // index checks (if validating) and wait timeouts
+    if (!p.err_word) return SFA_ERR_CUDA;
     p.scale_log2 = scale * kLog2e;
     resolve_strides(p, (int)layout, prefix);
 
@@ -197,7 +213,7 @@ sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t
     }
     void* extra = ws ? static_cast<char*>(ws) + sfa_split_ws_bytes((int64_t)B * S1 * N1, p.splits, Dv)
                      : nullptr;
-    cudaError_t err = run_plan(plan, p, dtype, extra, s);
+    cudaError_t err = run_plan(plan, p, dtype, extra, num_sms(), s);
     return err == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }
 
@@ -217,7 +233,7 @@ sfa_status sfa_get_last_error(sfa_stream_t stream) {
     if (word) {
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return SFA_ERR_CUDA;
-        return SFA_ERR_INDEX_RANGE;
+        return (word & kErrWaitTimeout) ? SFA_ERR_DEVICE_TIMEOUT : SFA_ERR_INDEX_RANGE;
     }
     return SFA_OK;
 }

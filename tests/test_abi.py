@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for st in range(6):
+    for st in range(7):
         assert sfa.status_string(st)
 
 

@@ -197,3 +197,46 @@ def test_full_workload_sampled(name):
     assert torch.isfinite(out.float()).all()
     if name == "sparse_prefill":
         assert torch.all(out[0, :8] == 0)
+
+
+# ---------------------------------------------------------------------------
+# small-group decode path (G <= 8, Dk == Dv, G * Dk <= 512)
+
+@pytest.mark.parametrize("D,G,N2", [(64, 1, 2), (64, 2, 2), (64, 4, 1), (64, 8, 2), (128, 1, 3),
+                                    (128, 2, 2), (128, 4, 2), (256, 1, 1), (256, 2, 2)])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_decode_path_shapes(D, G, N2, dtype):
+    run_and_check(small(Dk=D, Dv=D, N1=G * N2, N2=N2, S1=2, topK=150, S2=400, dtype=dtype,
+                        causal=True, layout="BNSD"))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 16])
+def test_decode_multi_chunk_online_softmax(splits):
+    """Several 64-slot chunks per CTA (online rescaling across chunks)."""
+    case = small(Dk=128, Dv=128, N1=16, N2=4, S1=1, topK=1000, S2=3000, causal=True,
+                 index_kind="sorted")
+    run_and_check(case, num_splits=splits)
+
+
+def test_decode_fully_masked_rows():
+    case = small(Dk=128, Dv=128, N1=8, N2=2, S1=12, S2=64, topK=40, causal=True,
+                 index_kind="causal_mix", masked_frac=0.2, full_masked_rows=6)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    for splits in (1, 2):
+        out, lse = T.run_gpu(case, dev, num_splits=splits)
+        T.check_full(case, d, out, lse)
+        assert torch.all(out[0, :6] == 0) and torch.all(torch.isneginf(lse[0, :6]))
+
+
+@pytest.mark.parametrize("B,S1,N2,topK,S2", [(8, 64, 4, 64, 256),     # one chunk per index list
+                                             (4, 50, 4, 150, 400),    # ranges span several lists
+                                             (1, 1, 1, 1000, 3000),   # one list over many CTAs
+                                             (3, 7, 2, 1, 9)])        # topK = 1
+def test_decode_stream_k_partitions(B, S1, N2, topK, S2):
+    """The persistent decode kernel's contiguous chunk ranges: lists written
+    directly by one CTA, lists split across CTAs (merged by the combine), and
+    CTAs whose ranges cross list boundaries."""
+    case = small(B=B, S1=S1, N1=4 * N2, N2=N2, Dk=128, Dv=128, topK=topK, S2=S2, causal=True,
+                 layout="BSND", dtype="f16")
+    run_and_check(case)
