@@ -99,8 +99,11 @@ typedef struct {
     /* Caller-owned device float workspace for split-topK partial results
      * ("flashinfer.sparse", BlockSparseAttentionWrapper.__init__: the float
      * workspace that holds split-k intermediates).  NULL = library-owned.
-     * Size: sfa_workspace_size().  Must not be used by another call that
-     * overlaps this one on the GPU. */
+     * Size: sfa_workspace_size().  Its head holds per-index-list arrival
+     * counters: zero-fill the buffer once before its first use; every call
+     * that completes leaves the head zero again (after an
+     * SFA_ERR_DEVICE_TIMEOUT, zero it again).  Must not be used by another
+     * call that overlaps this one on the GPU. */
     void* workspace;
     size_t workspace_bytes;
     /* 1: v is the prefix view k[..., :Dv] (v must equal k).  0: inferred from

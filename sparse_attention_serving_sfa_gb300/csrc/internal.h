@@ -24,6 +24,7 @@ struct SfaParams {
     float* ws_o;   // [rows][splits][Dv] unnormalised partial outputs
     float* ws_ml;  // [rows][splits][2]  (running max in log2 units, sum)
     int* err_word; // bit 0 set when validation sees an index outside [0, S2)
+    unsigned* counters;  // per index list, zero between calls (reserved workspace head)
     int B, S1, S2, N1, N2, G, Dk, Dv, topK;
     int causal, validate, splits, slots_per_split;
     int ctas_per_sm, num_ctas;   // launch tuning of the small-group path (0 = auto)
@@ -48,6 +49,11 @@ void resolve_strides(SfaParams& p, int layout, bool prefix);
 
 // SM count of the current device (cached).
 int num_sms();
+
+// Every workspace starts with a fixed head of per-index-list arrival
+// counters, kept zero between calls and never used for anything else.
+constexpr int64_t kMaxCounters = 16384;
+size_t counter_region_bytes(int64_t units);
 
 // Bytes of split workspace for `splits` splits.
 size_t sfa_split_ws_bytes(int64_t rows, int splits, int Dv);

@@ -66,6 +66,9 @@ cudaError_t owned_workspace(size_t need, void** out) {
             g_ws.ptr[dev] = nullptr;
             return err;
         }
+        // the counter region must start at zero (kernels leave it zero)
+        err = cudaMemset(g_ws.ptr[dev], 0, sz);
+        if (err != cudaSuccess) return err;
         g_ws.bytes[dev] = sz;
     }
     *out = g_ws.ptr[dev];
@@ -163,10 +166,11 @@ sfa_status sfa_workspace_size(int B, int S1, int N1, int N2, int Dk, int Dv, int
         Dk < Dv)
         return SFA_ERR_INVALID_ARG;
     const int splits = num_splits > 0 ? num_splits : max_splits_for(topK);
-    // a plan uses either split partials or its own extra workspace
+    // counter head + either split partials or the plan's own extra workspace
     const size_t split = sfa_split_ws_bytes((int64_t)B * S1 * N1, splits, Dv);
     const size_t extra = plan_extra_ws_bytes(B, S1, N1, N2, Dk, Dv, topK);
-    *bytes = split > extra ? split : extra;
+    const size_t region = split > extra ? split : extra;
+    *bytes = region ? counter_region_bytes((int64_t)B * S1 * N2) + region : 0;
     return SFA_OK;
 }
 
@@ -197,7 +201,11 @@ sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t
     p.splits = plan.splits;
     p.slots_per_split = plan.slots_per_split;
 
-    const size_t need = sfa_split_ws_bytes((int64_t)B * S1 * N1, p.splits, Dv) + plan.extra_ws_bytes;
+    // workspace: [counter head][split partials | plan's extra region]
+    const size_t split_bytes = sfa_split_ws_bytes((int64_t)B * S1 * N1, p.splits, Dv);
+    const size_t region = split_bytes + plan.extra_ws_bytes;
+    const size_t head = counter_region_bytes((int64_t)B * S1 * N2);
+    const size_t need = region ? head + region : 0;
     void* ws = nullptr;
     if (need > 0) {
         if (opt && opt->workspace) {
@@ -206,13 +214,14 @@ sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t
         } else {
             if (owned_workspace(need, &ws) != cudaSuccess) return SFA_ERR_CUDA;
         }
+        p.counters = static_cast<unsigned*>(ws);
     }
+    char* region_base = ws ? static_cast<char*>(ws) + head : nullptr;
     if (p.splits > 1) {
-        p.ws_o = static_cast<float*>(ws);
+        p.ws_o = reinterpret_cast<float*>(region_base);
         p.ws_ml = p.ws_o + (int64_t)B * S1 * N1 * p.splits * Dv;
     }
-    void* extra = ws ? static_cast<char*>(ws) + sfa_split_ws_bytes((int64_t)B * S1 * N1, p.splits, Dv)
-                     : nullptr;
+    void* extra = region_base ? region_base + split_bytes : nullptr;
     cudaError_t err = run_plan(plan, p, dtype, extra, num_sms(), s);
     return err == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }

@@ -30,7 +30,9 @@
 //   - at the end of an index list the four warps' states are merged through
 //     shared memory; a range that holds the whole list writes the output,
 //     otherwise its partial (O, running max, sum) goes to the workspace and
-//     sfa_decode_combine_kernel (programmatic dependent launch) merges them.
+//     the last CTA to finish the list (a per-list arrival counter in the
+//     workspace head, reset by that CTA) merges the L2-resident partials and
+//     writes the output -- one launch, no separate combine kernel.
 #include <limits.h>
 
 #include <type_traits>
@@ -53,19 +55,25 @@ constexpr int kRowPad = 16;                   // bytes of padding per smem row
 constexpr int kHeads = 8;                     // G <= 8: the N = 8 side of the MMAs
 constexpr int kLookahead = 8;                 // chunks of indices prefetched
 
+// Chunk ranges of the persistent CTAs.  Stream-K: equal contiguous ranges of
+// the flat chunk sequence (an index list may be split across CTAs, which then
+// merge through the workspace).  Aligned: each CTA takes whole index lists
+// (used when there are many more lists than CTAs; nothing to merge).
 struct DecodeSched {
     int64_t total;   // chunks over all index lists
+    int64_t units;   // index lists
     int cpu;         // chunks per index list
     int ctas;        // grid size
     int seg_max;     // most CTAs sharing one index list
+    int aligned;     // 1: ranges hold whole index lists
 };
 
 __host__ __device__ inline int64_t range_begin(int64_t c, const DecodeSched& s) {
-    return c * s.total / s.ctas;
+    return s.aligned ? (c * s.units / s.ctas) * s.cpu : c * s.total / s.ctas;
 }
 // CTA whose range holds chunk x.
 __host__ __device__ inline int64_t cta_of(int64_t x, const DecodeSched& s) {
-    return ((x + 1) * s.ctas - 1) / s.total;
+    return s.aligned ? ((x / s.cpu + 1) * s.ctas - 1) / s.units : ((x + 1) * s.ctas - 1) / s.total;
 }
 
 template <int DK, int DV, bool VK, int NS>
@@ -177,6 +185,7 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
     const int64_t c_end = range_begin((int64_t)blockIdx.x + 1, sch);
     const uint32_t full0 = smem_base + L::bars, empty0 = full0 + NS * 8;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::abort);
+    volatile int* last_flag = abort_flag + 1;     // this CTA merges the list
     const int G = p.G;
 
     // zero the q tiles (rows >= G are never copied) and set up the barriers
@@ -318,7 +327,18 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
         named_sync(1, kConsThreads);
         const int64_t first = u * sch.cpu, last = first + sch.cpu - 1;
         const int64_t c_lo = cta_of(first, sch), c_hi = cta_of(last, sch);
+        const int nseg = (int)(c_hi - c_lo + 1);
         const UnitCoord uc = unit_coord(u, p);
+        auto write_out = [&](int g, int d2, float M, float Ls, float ax, float ay) {
+            const int n1 = uc.n2 * G + g;
+            T* orow = static_cast<T*>(p.out) + uc.b * p.o_sb + n1 * p.o_sh + uc.s1 * p.o_ss;
+            const bool empty = !(Ls > 0.f);
+            const float inv = empty ? 0.f : 1.f / Ls;
+            reinterpret_cast<uint32_t*>(orow)[d2] = empty ? 0u : E::pack2(ax * inv, ay * inv);
+            if (p.lse && d2 == 0)
+                p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] =
+                    empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
+        };
         for (int e = tid; e < G * (DV / 2); e += kConsThreads) {
             const int g = e / (DV / 2), d2 = e % (DV / 2);
             float M = -INFINITY;
@@ -334,15 +354,8 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
                 ax += f * ov.x;
                 ay += f * ov.y;
             }
-            const int n1 = uc.n2 * G + g;
-            if (c_lo == c_hi) {
-                T* orow = static_cast<T*>(p.out) + uc.b * p.o_sb + n1 * p.o_sh + uc.s1 * p.o_ss;
-                const bool empty = !(Ls > 0.f);
-                const float inv = empty ? 0.f : 1.f / Ls;
-                reinterpret_cast<uint32_t*>(orow)[d2] = empty ? 0u : E::pack2(ax * inv, ay * inv);
-                if (p.lse && d2 == 0)
-                    p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] =
-                        empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
+            if (nseg == 1) {
+                write_out(g, d2, M, Ls, ax, ay);
             } else {
                 const int64_t slot = (u * G + g) * sch.seg_max + (blockIdx.x - c_lo);
                 reinterpret_cast<float2*>(p.ws_o + slot * p.Dv)[d2] = make_float2(ax, ay);
@@ -350,6 +363,56 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
                     p.ws_ml[slot * 2] = M;
                     p.ws_ml[slot * 2 + 1] = Ls;
                 }
+            }
+        }
+        if (nseg > 1) {
+            // publish the partial, count arrivals; the last CTA merges
+            __threadfence();
+            named_sync(1, kConsThreads);
+            if (tid == 0) {
+                const unsigned prev = atomicAdd(p.counters + u, 1u);
+                *last_flag = (prev == (unsigned)(nseg - 1)) ? 1 : 0;
+            }
+            named_sync(1, kConsThreads);
+            if (*last_flag) {
+                __threadfence();
+                // all loads of a pair's segments are issued before any use
+                constexpr int KB = 8;
+                for (int e = tid; e < G * (DV / 2); e += kConsThreads) {
+                    const int g = e / (DV / 2), d2 = e % (DV / 2);
+                    const int64_t row = u * G + g;
+                    const float* ml = p.ws_ml + row * sch.seg_max * 2;
+                    const float2* wo = reinterpret_cast<const float2*>(p.ws_o + row * sch.seg_max * p.Dv) + d2;
+                    float M = -INFINITY, Ls = 0.f, ax = 0.f, ay = 0.f;
+                    for (int k0 = 0; k0 < nseg; k0 += KB) {
+                        float2 mv[KB], ov[KB];
+#pragma unroll
+                        for (int k2 = 0; k2 < KB; ++k2) {
+                            const bool ok = k0 + k2 < nseg;
+                            mv[k2] = ok ? __ldcg(reinterpret_cast<const float2*>(ml) + k0 + k2)
+                                        : make_float2(-INFINITY, 0.f);
+                            ov[k2] = ok ? __ldcg(wo + (int64_t)(k0 + k2) * (p.Dv / 2))
+                                        : make_float2(0.f, 0.f);
+                        }
+                        float Mb = M;
+#pragma unroll
+                        for (int k2 = 0; k2 < KB; ++k2) Mb = fmaxf(Mb, mv[k2].x);
+                        const float r = rescale_factor(M, Mb);
+                        Ls *= r;
+                        ax *= r;
+                        ay *= r;
+#pragma unroll
+                        for (int k2 = 0; k2 < KB; ++k2) {
+                            const float f = rescale_factor(mv[k2].x, Mb);
+                            Ls += f * mv[k2].y;
+                            ax += f * ov[k2].x;
+                            ay += f * ov[k2].y;
+                        }
+                        M = Mb;
+                    }
+                    write_out(g, d2, M, Ls, ax, ay);
+                }
+                if (tid == 0) atomicExch(p.counters + u, 0u);   // ready for the next call
             }
         }
         named_sync(1, kConsThreads);
@@ -475,46 +538,6 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
     if (cur >= 0) flush(cur);
-    grid_launch_dependents();
-}
-
-// Merge of the partials of one output row written by the CTAs whose ranges
-// share its index list (same math as sfa_combine_kernel).
-template <class E>
-__global__ void __launch_bounds__(64) sfa_decode_combine_kernel(const SfaParams p, const DecodeSched sch) {
-    using T = typename E::T;
-    grid_dependency_wait();
-    const int64_t row = blockIdx.x;
-    const int64_t u = row / p.G;
-    const int h = (int)(row % p.G);
-    const int64_t c_lo = cta_of(u * sch.cpu, sch), c_hi = cta_of(u * sch.cpu + sch.cpu - 1, sch);
-    if (c_lo == c_hi) return;      // written directly by the kernel
-    const int nseg = (int)(c_hi - c_lo + 1);
-    const float* ml = p.ws_ml + row * sch.seg_max * 2;
-    float M = -INFINITY;
-    for (int k = 0; k < nseg; ++k) M = fmaxf(M, ml[2 * k]);
-    float Lsum = 0.f;
-    for (int k = 0; k < nseg; ++k) Lsum += rescale_factor(ml[2 * k], M) * ml[2 * k + 1];
-    const bool empty = !(Lsum > 0.f);
-    const float inv = empty ? 0.f : 1.f / Lsum;
-    const UnitCoord uc = unit_coord(u, p);
-    const int n1 = uc.n2 * p.G + h;
-    T* orow = static_cast<T*>(p.out) + uc.b * p.o_sb + n1 * p.o_sh + uc.s1 * p.o_ss;
-    const float* wo = p.ws_o + row * sch.seg_max * p.Dv;
-    for (int e2 = threadIdx.x; e2 < p.Dv / 2; e2 += blockDim.x) {
-        float ax = 0.f, ay = 0.f;
-        if (!empty)
-            for (int k = 0; k < nseg; ++k) {
-                const float w = rescale_factor(ml[2 * k], M);
-                const float2 o = reinterpret_cast<const float2*>(wo + (int64_t)k * p.Dv)[e2];
-                ax += w * o.x;
-                ay += w * o.y;
-            }
-        reinterpret_cast<uint32_t*>(orow)[e2] = empty ? 0u : E::pack2(ax * inv, ay * inv);
-    }
-    if (p.lse && threadIdx.x == 0)
-        p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] =
-            empty ? -INFINITY : (M + __log2f(Lsum)) * kLn2;
 }
 
 // Deepest ring that fits in shared memory next to the merge buffers, for
@@ -540,38 +563,31 @@ cudaError_t run_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaStrea
     if (occ < 1) occ = 1;
     DecodeSched s;
     s.cpu = (p.topK + kChunk - 1) / kChunk;
-    s.total = (int64_t)p.B * p.N2 * p.S1 * s.cpu;
+    s.units = (int64_t)p.B * p.N2 * p.S1;
+    s.total = s.units * s.cpu;
     int64_t ctas = p.num_ctas > 0 ? p.num_ctas : (int64_t)num_sms * occ;
-    if (ctas > s.total) ctas = s.total;
+    // many index lists per CTA: whole lists per range balance well enough
+    s.aligned = (s.units >= 8 * ctas || s.units > kMaxCounters) ? 1 : 0;
+    if (ctas > (s.aligned ? s.units : s.total)) ctas = s.aligned ? s.units : s.total;
     s.ctas = (int)ctas;
-    const int64_t lmin = s.total / s.ctas;                 // shortest range
-    int64_t seg = (s.cpu + lmin - 1) / lmin + 1;
-    if (seg > s.cpu) seg = s.cpu;
-    s.seg_max = (int)seg;
+    if (s.aligned) {
+        s.seg_max = 1;
+    } else {
+        const int64_t lmin = s.total / s.ctas;             // shortest range
+        int64_t seg = (s.cpu + lmin - 1) / lmin + 1;
+        if (seg > s.cpu) seg = s.cpu;
+        s.seg_max = (int)seg;
+    }
     if (s.seg_max > 1) {
         const int64_t rows = (int64_t)p.B * p.N2 * p.S1 * p.G;
         const size_t need = (size_t)rows * s.seg_max * ((size_t)p.Dv + 2) * sizeof(float);
-        if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
+        if (!ws || ws_bytes < need || !p.counters) return cudaErrorInvalidValue;
         p.ws_o = static_cast<float*>(ws);
         p.ws_ml = p.ws_o + rows * s.seg_max * p.Dv;
     }
     kern<<<s.ctas, kThreads, L::total, stream>>>(p, s);
     count_launches(1);
-    err = cudaGetLastError();
-    if (err != cudaSuccess || s.seg_max <= 1) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((int64_t)p.B * p.N2 * p.S1 * p.G));
-    cfg.blockDim = dim3(64);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, sfa_decode_combine_kernel<E>, p, s);
-    count_launches(1);
-    return err;
+    return cudaGetLastError();
 }
 
 template <class E, int DK, int DV, bool VK>

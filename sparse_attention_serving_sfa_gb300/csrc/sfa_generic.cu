@@ -296,6 +296,12 @@ cudaError_t launch_generic_t(const SfaParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+size_t counter_region_bytes(int64_t) {
+    // fixed size, so that calls of different shapes sharing a workspace never
+    // place other data where another call keeps its counters
+    return (size_t)kMaxCounters * sizeof(unsigned);
+}
+
 size_t sfa_split_ws_bytes(int64_t rows, int splits, int Dv) {
     if (splits <= 1) return 0;
     return (size_t)rows * splits * ((size_t)Dv + 2) * sizeof(float);

@@ -90,7 +90,8 @@ def test_workspace_size(lib):
     n = sfa.sfa_workspace_size(16, 1, 32, 8, 128, 128, 1024)
     assert n >= 16 * 32 * 2 * (128 + 2) * 4
     assert sfa.sfa_workspace_size(1, 1, 1, 1, 64, 64, 16, num_splits=1) == 0
-    assert sfa.sfa_workspace_size(2, 3, 4, 2, 64, 64, 64, num_splits=4) == 2 * 3 * 4 * 4 * 66 * 4
+    # fixed counter head (16384 ints) + split partials
+    assert sfa.sfa_workspace_size(2, 3, 4, 2, 64, 64, 64, num_splits=4) == 65536 + 2 * 3 * 4 * 4 * 66 * 4
     with pytest.raises(sfa.SfaError):
         sfa.sfa_workspace_size(0, 1, 1, 1, 64, 64, 16)
 

@@ -118,7 +118,7 @@ def test_caller_workspace_and_too_small():
     dev = T.to_dev(d)
     need = sfa.sfa_workspace_size(case.B, case.S1, case.N1, case.N2, case.Dk, case.Dv, case.topK,
                                   num_splits=4)
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     out, lse = T.run_gpu(case, dev, workspace=ws, num_splits=4)
     T.check_full(case, d, out, lse)
     small_ws = torch.empty(16, dtype=torch.uint8, device="cuda")
@@ -232,7 +232,8 @@ def test_decode_fully_masked_rows():
 @pytest.mark.parametrize("B,S1,N2,topK,S2", [(8, 64, 4, 64, 256),     # one chunk per index list
                                              (4, 50, 4, 150, 400),    # ranges span several lists
                                              (1, 1, 1, 1000, 3000),   # one list over many CTAs
-                                             (3, 7, 2, 1, 9)])        # topK = 1
+                                             (3, 7, 2, 1, 9),         # topK = 1
+                                             (8, 400, 2, 128, 512)])  # many lists: whole lists per CTA
 def test_decode_stream_k_partitions(B, S1, N2, topK, S2):
     """The persistent decode kernel's contiguous chunk ranges: lists written
     directly by one CTA, lists split across CTAs (merged by the combine), and
@@ -240,3 +241,16 @@ def test_decode_stream_k_partitions(B, S1, N2, topK, S2):
     case = small(B=B, S1=S1, N1=4 * N2, N2=N2, Dk=128, Dv=128, topK=topK, S2=S2, causal=True,
                  layout="BSND", dtype="f16")
     run_and_check(case)
+
+
+def test_workspace_shared_across_shapes():
+    """Calls of different shapes and paths share the library-owned workspace:
+    split partials of the generic path must never land in the arrival
+    counters of the decode path (and the counters must be left at zero)."""
+    cases = [small(N1=16, N2=1, topK=200, S2=300),                       # generic, splits
+             small(B=4, S1=50, N1=16, N2=4, topK=150, S2=400, causal=True),   # decode, stream-K merge
+             small(N1=32, N2=2, topK=300, S2=300, S1=1),                 # generic again
+             small(B=2, S1=3, N1=8, N2=2, topK=900, S2=1000)]            # decode again
+    for rep in range(2):
+        for case in cases:
+            run_and_check(case)
