@@ -16,9 +16,10 @@ struct bsr_plan_s {
     sfa_dtype dtype;
     float scale;
     int MB, NB, nnz, ntiles;
+    bool tc;                        // tensor-core path (work items) vs generic (row tiles)
     const int32_t* d_indptr;
     const int32_t* d_indices;
-    const sfa::BsrTile* d_tiles;
+    const void* d_work;             // BsrTile list (generic) or 4-int items (tensor cores)
     std::vector<int32_t> staging;   // host copy kept alive for the async upload
 };
 
@@ -28,14 +29,22 @@ constexpr int kTileRows = 64;
 
 size_t round4(size_t n) { return (n + 3) & ~size_t(3); }
 
-int count_tiles(int M, int R) {
+// Row tiles of `rows_per` rows (never crossing a block row).
+int count_tiles(int M, int R, int rows_per = kTileRows) {
     const int MB = (M + R - 1) / R;
     int n = 0;
     for (int rb = 0; rb < MB; ++rb) {
         const int rows = std::min(R, M - rb * R);
-        n += (rows + kTileRows - 1) / kTileRows;
+        n += (rows + rows_per - 1) / rows_per;
     }
     return n;
+}
+
+// Work entries of either path (4 ints each).
+int count_work(int M, int R, int C, int Hq, int Hkv, int d) {
+    if (sfa::bsr_tc_supported(d, C, Hq, Hkv))
+        return count_tiles(M, R, sfa::bsr_tc_rows_per_item(Hq, Hkv)) * Hkv;
+    return count_tiles(M, R);
 }
 
 sfa_status check_shape(int M, int N, int R, int C, int Hq, int Hkv, int d) {
@@ -64,7 +73,7 @@ sfa_status bsr_plan_int_workspace_size(const int32_t* indptr_host, int M, int N,
     const int MB = (M + R - 1) / R;
     const int nnz = indptr_host[MB];
     if (nnz < 0) return SFA_ERR_INVALID_ARG;
-    *bytes = int_ws_bytes(MB, nnz, count_tiles(M, R));
+    *bytes = int_ws_bytes(MB, nnz, count_work(M, R, C, num_qo_heads, num_kv_heads, head_dim));
     return SFA_OK;
 }
 
@@ -101,7 +110,8 @@ sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int
             for (int j = indptr_host[i]; j < indptr_host[i + 1]; ++j) seen[(size_t)indices_host[j]] = 0;
         }
     }
-    const int ntiles = count_tiles(M, R);
+    const bool tc = sfa::bsr_tc_supported(head_dim, C, num_qo_heads, num_kv_heads);
+    const int ntiles = count_work(M, R, C, num_qo_heads, num_kv_heads, head_dim);
     const size_t need = int_ws_bytes(MB, nnz, ntiles);
     if (!int_ws || int_ws_bytes_given < need) return SFA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(int_ws) & 15u) return SFA_ERR_INVALID_ARG;
@@ -113,14 +123,23 @@ sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int
     plan->dtype = dtype;
     plan->scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)head_dim);
     plan->MB = MB; plan->NB = NB; plan->nnz = nnz; plan->ntiles = ntiles;
+    plan->tc = tc;
 
-    // Work list: row tiles of <= 64 rows, heaviest block rows first.
+    // Work list, heaviest block rows first: generic row tiles of <= 64 rows
+    // (the kernel's grid.y spans the qo heads), or tensor-core items of
+    // (block row, first row, kv head).
     std::vector<sfa::BsrTile> tiles;
     tiles.reserve((size_t)ntiles);
+    const int rows_per = tc ? sfa::bsr_tc_rows_per_item(num_qo_heads, num_kv_heads) : kTileRows;
     for (int rb = 0; rb < MB; ++rb) {
         const int rows = std::min(R, M - rb * R);
-        for (int r0 = 0; r0 < rows; r0 += kTileRows)
-            tiles.push_back({rb, rb * R + r0, std::min(kTileRows, rows - r0), 0});
+        for (int r0 = 0; r0 < rows; r0 += rows_per) {
+            if (tc) {
+                for (int h = 0; h < num_kv_heads; ++h) tiles.push_back({rb, rb * R + r0, h, 0});
+            } else {
+                tiles.push_back({rb, rb * R + r0, std::min(kTileRows, rows - r0), 0});
+            }
+        }
     }
     std::stable_sort(tiles.begin(), tiles.end(), [&](const sfa::BsrTile& a, const sfa::BsrTile& b) {
         return (indptr_host[a.rb + 1] - indptr_host[a.rb]) > (indptr_host[b.rb + 1] - indptr_host[b.rb]);
@@ -136,7 +155,7 @@ sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int
     int32_t* base = static_cast<int32_t*>(int_ws);
     plan->d_indptr = base;
     plan->d_indices = base + n_indptr;
-    plan->d_tiles = reinterpret_cast<const sfa::BsrTile*>(base + n_indptr + n_indices);
+    plan->d_work = base + n_indptr + n_indices;
     cudaError_t err = cudaMemcpyAsync(int_ws, plan->staging.data(), need, cudaMemcpyHostToDevice,
                                       reinterpret_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) {
@@ -157,12 +176,20 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
     p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse;
     p.indptr = plan->d_indptr;
     p.indices = plan->d_indices;
-    p.tiles = plan->d_tiles;
+    p.tiles = static_cast<const sfa::BsrTile*>(plan->d_work);
     p.ntiles = plan->ntiles;
     p.M = plan->M; p.N = plan->N; p.R = plan->R; p.C = plan->C;
     p.Hq = plan->Hq; p.Hkv = plan->Hkv; p.d = plan->d;
     p.scale_log2 = plan->scale * sfa::kLog2e;
-    cudaError_t err = sfa::launch_bsr_generic(p, plan->dtype, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    if (plan->tc) {
+        int* ew = sfa::device_error_word();
+        if (!ew) return SFA_ERR_CUDA;
+        err = sfa::launch_bsr_tc(p, plan->d_work, plan->ntiles, ew, plan->dtype, s);
+    } else {
+        err = sfa::launch_bsr_generic(p, plan->dtype, s);
+    }
     return err == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }
 

@@ -92,4 +92,15 @@ struct BsrParams {
 
 cudaError_t launch_bsr_generic(const BsrParams& p, sfa_dtype dtype, cudaStream_t stream);
 
+// Tensor-core BSR path (head_dim 64 or 128, C % 64 == 0, G | 128).  A work
+// item (4 ints: block row, first row, kv head, -) covers
+// bsr_tc_rows_per_item() rows of one block row.
+bool bsr_tc_supported(int head_dim, int C, int Hq, int Hkv);
+int bsr_tc_rows_per_item(int Hq, int Hkv);
+cudaError_t launch_bsr_tc(const BsrParams& p, const void* items, int nitems, int* err_word,
+                          sfa_dtype dtype, cudaStream_t stream);
+
+// Device address of the library's error word on the current device.
+int* device_error_word();
+
 }  // namespace sfa

@@ -36,6 +36,12 @@ int* error_word_ptr() {
     return static_cast<int*>(cached[dev]);
 }
 
+}  // namespace
+
+int* device_error_word() { return error_word_ptr(); }
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Library-owned split workspace, one per device, grown on demand.

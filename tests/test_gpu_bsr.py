@@ -105,3 +105,51 @@ def test_full_workload_sampled():
     gl = torch.stack([lse[i, h] for i, h in rows])
     compare(got, gl, y, l, case.dtype)
     assert torch.isfinite(out.float()).all()
+
+
+# ---------------------------------------------------------------------------
+# tensor-core path (head_dim 64/128, C % 64 == 0, Hq/Hkv divides 128)
+
+@pytest.mark.parametrize("M,N,R,C,Hq,Hkv,d,dtype,p", [
+    (256, 256, 64, 64, 8, 2, 128, "f16", 0.5),      # G = 4, 32 rows per tile
+    (190, 320, 64, 64, 8, 8, 128, "bf16", 0.4),     # G = 1, 128 rows per tile, ragged M
+    (300, 256, 100, 128, 4, 2, 64, "f16", 0.5),     # G = 2, C = 2 x 64, R not a tile multiple
+    (128, 384, 32, 64, 16, 2, 128, "bf16", 0.3),    # G = 8, 16 rows per tile
+    (96, 192, 48, 64, 16, 1, 64, "f16", 0.6),       # G = 16, 8 rows per tile
+])
+def test_tensor_core_shapes(M, N, R, C, Hq, Hkv, d, dtype, p):
+    case = synth.BsrCase("tc", M=M, N=N, R=R, C=C, Hq=Hq, Hkv=Hkv, d=d, dtype=dtype, p=p,
+                         sm_scale=1 / math.sqrt(d), seed=55)
+    x = synth.make_bsr_inputs(case)
+    out, lse = run_bsr(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                       case.sm_scale, dtype)
+    y, l = oracle.bsr(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C, case.sm_scale)
+    compare(out, lse, y, l, dtype)
+
+
+def test_tensor_core_empty_block_rows():
+    M, N, R, C = 256, 256, 64, 64
+    indptr = torch.tensor([0, 3, 3, 4, 4], dtype=torch.int32)   # block rows 1 and 3 empty
+    indices = torch.tensor([0, 2, 3, 1], dtype=torch.int32)
+    q = synth.normal(8, 0, (M, 8, 128), "bf16")
+    k = synth.normal(8, 1, (N, 2, 128), "bf16")
+    v = synth.normal(8, 2, (N, 2, 128), "bf16")
+    out, lse = run_bsr(q, k, v, indptr, indices, M, N, R, C, 0.09, "bf16")
+    y, l = oracle.bsr(q, k, v, indptr, indices, M, N, R, C, 0.09)
+    compare(out, lse, y, l, "bf16")
+    assert torch.all(out[64:128] == 0) and torch.all(torch.isneginf(lse[192:256]))
+    assert sfa.sfa_get_last_error() == sfa.SFA_OK
+
+
+def test_tensor_core_large_scores_rescale():
+    """Scores spanning a wide range exercise the conditional O rescale."""
+    M, N, R, C = 128, 512, 64, 64
+    indptr = torch.tensor([0, 8, 16], dtype=torch.int32)
+    indices = torch.arange(8, dtype=torch.int32).repeat(2)
+    q = (synth.normal(9, 0, (M, 4, 128), "f16").float() * 3).half()
+    k = (synth.normal(9, 1, (N, 1, 128), "f16").float()
+         * torch.linspace(0.2, 4.0, N).view(N, 1, 1)).half()
+    v = synth.normal(9, 2, (N, 1, 128), "f16")
+    out, lse = run_bsr(q, k, v, indptr, indices, M, N, R, C, 0.0884, "f16")
+    y, l = oracle.bsr(q, k, v, indptr, indices, M, N, R, C, 0.0884)
+    compare(out, lse, y, l, "f16")
