@@ -28,11 +28,20 @@ size_t plan_extra_ws_bytes(int B, int S1, int N1, int N2, int Dk, int Dv, int to
     SfaParams p{};
     p.B = B; p.S1 = S1; p.N1 = N1; p.N2 = N2; p.G = N1 / N2;
     p.Dk = Dk; p.Dv = Dv; p.topK = topK;
+    p.v = p.k = &p;   // value is the key prefix (aliasing decides the MLA path)
+    if (mla_supported(p)) return mla_ws_bytes(p);
     return decode_supported(p) ? decode_ws_bytes(p) : 0;
 }
 
 Plan choose_plan(const SfaParams& p, sfa_dtype, int num_sms, int forced_splits) {
     Plan pl;
+    if (mla_supported(p) && forced_splits <= 0) {
+        pl.kind = PATH_MLA;
+        pl.splits = 1;
+        pl.slots_per_split = p.topK;
+        pl.extra_ws_bytes = mla_ws_bytes(p);
+        return pl;
+    }
     if (decode_supported(p)) {
         // persistent stream-K kernel: its own schedule, partials in extra_ws
         pl.kind = PATH_DECODE;
@@ -55,6 +64,8 @@ cudaError_t run_plan(const Plan& plan, SfaParams& p, sfa_dtype dtype, void* extr
                      int num_sms, cudaStream_t stream) {
     p.splits = plan.splits;
     p.slots_per_split = plan.slots_per_split;
+    if (plan.kind == PATH_MLA)
+        return launch_sfa_mla(p, dtype, num_sms, extra_ws, plan.extra_ws_bytes, stream);
     if (plan.kind == PATH_DECODE)
         return launch_sfa_decode(p, dtype, num_sms, extra_ws, plan.extra_ws_bytes, stream);
     cudaError_t err = launch_sfa_generic(p, dtype, stream);

@@ -8,6 +8,7 @@ namespace sfa {
 enum PathKind {
     PATH_GENERIC = 0,  // warp-FMA kernel, any supported shape
     PATH_DECODE = 1,   // small-group persistent gather kernel (sfa_decode.cu)
+    PATH_MLA = 2,      // 128-head MLA tensor-core kernel (sfa_mla.cu)
 };
 
 struct Plan {

@@ -66,6 +66,14 @@ size_t decode_ws_bytes(const SfaParams& p);
 cudaError_t launch_sfa_decode(const SfaParams& p, sfa_dtype dtype, int num_sms, void* ws,
                               size_t ws_bytes, cudaStream_t stream);
 
+// MLA path (G == 128 query heads per index list, Dk == 576, Dv == 512, value
+// = key prefix): 2-CTA cluster tensor-core kernel, stream-K over chunks with
+// an in-kernel merge of split units.  mla_ws_bytes bounds its workspace.
+bool mla_supported(const SfaParams& p);
+size_t mla_ws_bytes(const SfaParams& p);
+cudaError_t launch_sfa_mla(const SfaParams& p, sfa_dtype dtype, int num_sms, void* ws,
+                           size_t ws_bytes, cudaStream_t stream);
+
 // Generic warp-FMA path (any supported shape) and its split combine.
 cudaError_t launch_sfa_generic(const SfaParams& p, sfa_dtype dtype, cudaStream_t stream);
 cudaError_t launch_sfa_combine(const SfaParams& p, sfa_dtype dtype, cudaStream_t stream);

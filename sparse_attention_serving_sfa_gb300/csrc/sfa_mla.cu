@@ -1,0 +1,624 @@
+// Top-K sparse attention for the MLA latent cache (128 query heads share one
+// index list, Dk = 576 = 512 "nope" + 64 "rope" dims, Dv = 512, V = K[..., :512])
+// on the 5th-generation tensor cores.
+//
+// "SparseFlashAttention 算子 API 描述", §1 (MLA: value is the first Dv dims of
+// key), §2 具体子步骤 (gather, scaled dot product, causal mask, softmax over the
+// selected slots, weighted sum), evaluated as an online softmax over 64-slot
+// chunks.
+//
+// O for 128 heads x 512 dims (fp32) fills all 512 columns of one SM's tensor
+// memory and Q (128 x 576) alone is 144 KB of shared memory, so a unit is
+// computed by a 2-CTA cluster that splits the head dimensions:
+//   CTA r owns K/Q dims [256 r, 256 r + 256) (nope) and [512 + 32 r, 544 + 32 r)
+//   (rope), and V / O dims [256 r, 256 r + 256) -- the first 256 of its K dims.
+// Per 64-slot chunk, each CTA gathers only its 576 bytes of every selected K
+// row (no duplicated gather), computes a partial S_r = Q_r K_r^T (tcgen05.mma,
+// M = 128 heads, N = 64 slots, accumulated in tensor memory), and the two
+// partials are exchanged through distributed shared memory: both CTAs then hold
+// the same S = S_0 + S_1, run the same online softmax, and compute
+// O_r += P V_r for their half of Dv (P as a 16-bit high part plus remainder).
+//
+// Roles per CTA (7 warps): 2 producer warps (cp.async gather of the K rows
+// into 128-byte-swizzled panels, index prefetch, visibility masks), 1 MMA warp
+// (TMA load of the unit's Q half, tcgen05.mma issue), 4 softmax warps (thread
+// = head = TMEM lane: S exchange, softmax, P, O rescale, epilogue).  Work is
+// stream-K over (unit, chunk) pairs per cluster; a unit split over clusters is
+// merged by the last cluster to finish it (arrival counters per unit and half).
+#include <cudaTypedefs.h>
+
+#include <limits.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace sfa {
+namespace {
+
+constexpr int kChunk = 64;
+constexpr int kHeads = 128;               // the MMA M dimension
+constexpr int kDk = 576, kDv = 512;
+constexpr int kHalfDv = 256;              // nope dims (and V / O dims) per CTA
+constexpr int kPanels = 5;                // 4 nope + 1 rope (32 dims used, 32 never read)
+constexpr int kQkSteps = 4 * 4 + 2;       // K = 16 steps: 256 nope dims + 32 rope dims
+constexpr int kStages = 2;
+constexpr int kSoftWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kProdWarp0 = 5;
+constexpr int kProdThreads = 64;
+constexpr int kThreads = (kSoftWarps + 1 + 2) * 32;
+constexpr int kTmemCols = 512;
+constexpr int kOCol = 128;                // TMEM: S buffers at [0, 64), [64, 128); O at [128, 384)
+constexpr int kLookahead = 6;
+constexpr int kNoSlot = INT_MIN;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr int kMaxSeg = 8;                // split partials per unit and half
+
+struct MlaSmem {
+    static constexpr int q = 0;                             // 5 panels x 128 rows x 128 B
+    static constexpr int kvStage = kPanels * kChunk * 128;  // 40 KB
+    static constexpr int kv = q + kPanels * kHeads * 128;
+    static constexpr int p = kv + kStages * kvStage;        // hi, lo: 128 rows x 128 B each
+    static constexpr int x = p + 2 * kHeads * 128;          // 128 rows x 64 fp32 (peer partial S)
+    static constexpr int bars = x + kHeads * kChunk * 4;
+    static constexpr int meta = bars + 16 * 8;              // [stage] uint2 visibility mask
+    static constexpr int misc = meta + kStages * 8;         // tmem base, abort, last flag
+    static constexpr int total = misc + 16;
+    static constexpr int alloc = total + 1024;
+};
+
+enum {
+    B_Q_FULL = 0, B_Q_FREE = 1, B_KV_FULL = 2, B_KV_FREE = 4, B_S_FULL = 6, B_P_FULL = 8,
+    B_O_DONE = 9, B_X_FULL = 10, B_X_EMPTY = 11, B_DRAIN = 12
+};
+
+struct MlaSched {
+    int64_t total;      // chunks over all units
+    int64_t units;
+    int cpu;            // chunks per unit
+    int clusters;
+    int seg_max;
+    int q_head_inner;   // q tensor map dims are {d, head, s1, b} (else {d, s1, head, b})
+};
+
+__host__ __device__ inline int64_t mla_range_begin(int64_t c, const MlaSched& s) {
+    return c * s.total / s.clusters;
+}
+__host__ __device__ inline int64_t mla_cluster_of(int64_t x, const MlaSched& s) {
+    return ((x + 1) * s.clusters - 1) / s.total;
+}
+
+struct UCoord {
+    int b, n2, s1;
+};
+__device__ __forceinline__ UCoord ucoord(int64_t u, const SfaParams& p) {
+    UCoord c;
+    c.s1 = (int)(u % p.S1);
+    c.n2 = (int)((u / p.S1) % p.N2);
+    c.b = (int)(u / ((int64_t)p.S1 * p.N2));
+    return c;
+}
+
+template <class E>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const MlaSched sch) {
+    using T = typename E::T;
+    using L = MlaSmem;
+    constexpr bool kBf16 = std::is_same<E, BF16>::value;
+    constexpr uint32_t kIdescQK = idesc_f16(kHeads, kChunk, kBf16, false, false);
+    constexpr uint32_t kIdescPV = idesc_f16(kHeads, kHalfDv, kBf16, false, true);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+    const int64_t cl = blockIdx.x >> 1;
+    const int64_t c_begin = mla_range_begin(cl, sch), c_end = mla_range_begin(cl + 1, sch);
+    const int n = (int)(c_end - c_begin);
+    auto bar = [&](int i) { return sbase + L::bars + 8 * i; };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc + 4);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::misc + 8);
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bar(B_Q_FULL), 1);
+        mbar_init(bar(B_Q_FREE), 1);
+        mbar_init(bar(B_DRAIN), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(B_KV_FULL + s), kProdThreads + 2);
+            mbar_init(bar(B_KV_FREE + s), 1);
+            mbar_init(bar(B_S_FULL + s), 1);
+        }
+        mbar_init(bar(B_P_FULL), kSoftWarps * 32);
+        mbar_init(bar(B_O_DONE), 1);
+        mbar_init(bar(B_X_FULL), kSoftWarps * 32);     // arrived on by the peer's softmax threads
+        mbar_init(bar(B_X_EMPTY), kSoftWarps * 32);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(sbase + L::misc, kTmemCols);
+    tc_fence_before();
+    cluster_sync();      // both CTAs' barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::misc);
+
+    const int cpu = sch.cpu;
+    auto unit_of = [&](int64_t c) { return c / cpu; };
+
+    if (warp >= kProdWarp0) {
+        // ============================ producers ============================
+        // Warp pw gathers slots 32 pw .. 32 pw + 31 of every chunk: one
+        // 512-byte nope run per warp instruction (lane = 16-byte piece), then
+        // the 64-byte rope runs of the 32 rows, 8 rows per instruction.
+        const int pw = warp - kProdWarp0;
+        int64_t fc = c_begin;
+        auto fetch = [&]() {
+            int id = kNoSlot;
+            if (fc < c_end) {
+                const int64_t u = fc / cpu;
+                const int cc = (int)(fc - u * cpu);
+                const UCoord uc = ucoord(u, p);
+                const int32_t* ig = p.idx + uc.b * p.i_sb + uc.n2 * p.i_sh + uc.s1 * p.i_ss;
+                const int j = cc * kChunk + 32 * pw + lane;
+                if (j < p.topK) id = ig[j];
+                ++fc;
+            }
+            return id;
+        };
+        // indices run kLookahead chunks ahead of the gathers
+        int ring[kLookahead];
+#pragma unroll
+        for (int r = 0; r < kLookahead; ++r) ring[r] = fetch();
+        for (int i = 0; i < n; ++i) {
+            const int s = i % kStages;
+            if (!mbar_wait(bar(B_KV_FREE + s), ((i / kStages) & 1) ^ 1, p.err_word, abort_flag)) break;
+            const int myid = ring[0];
+#pragma unroll
+            for (int r = 0; r + 1 < kLookahead; ++r) ring[r] = ring[r + 1];
+            ring[kLookahead - 1] = fetch();
+            const UCoord uc = ucoord(unit_of(c_begin + i), p);
+            const int diag = uc.s1 + (p.S2 - p.S1);
+            const bool in_range = myid >= 0 && myid < p.S2;
+            if (!in_range && myid != kNoSlot && p.validate) atomicOr(p.err_word, kErrIndexRange);
+            const bool vis = in_range && !(p.causal && myid > diag);
+            const int myrow = in_range ? myid : -1;
+            const T* kg = static_cast<const T*>(p.k) + uc.b * p.k_sb + uc.n2 * p.k_sh;
+            unsigned char* st = smem + L::kv + s * L::kvStage;
+            // nope dims [256 rank, +256): panel = lane / 8, 16-byte chunk lane % 8
+            const T* nope = kg + (int)rank * kHalfDv + 8 * lane;
+            const int pn = lane >> 3, c = lane & 7;
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) {
+                const int id = __shfl_sync(0xffffffffu, myrow, r);
+                const int row = 32 * pw + r;
+                cp_async_16_zfill(st + pn * (kChunk * 128) + row * 128 + ((c ^ (row & 7)) << 4),
+                                  nope + (id >= 0 ? (int64_t)id * p.k_ss : 0), id >= 0 ? 16 : 0);
+            }
+            // rope dims [512 + 32 rank, +32) -> panel 4, chunks 0..3
+            const T* rope = kg + 512 + 32 * (int)rank + 8 * (lane & 3);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int r = 8 * t + (lane >> 2);
+                const int id = __shfl_sync(0xffffffffu, myrow, r);
+                const int row = 32 * pw + r;
+                cp_async_16_zfill(st + 4 * (kChunk * 128) + row * 128 + (((lane & 3) ^ (row & 7)) << 4),
+                                  rope + (id >= 0 ? (int64_t)id * p.k_ss : 0), id >= 0 ? 16 : 0);
+            }
+            cp_async_mbar_arrive(bar(B_KV_FULL + s));
+            const uint32_t mask = __ballot_sync(0xffffffffu, vis);
+            if (lane == 0) {
+                reinterpret_cast<uint32_t*>(smem + L::meta)[2 * s + pw] = mask;
+                mbar_arrive(bar(B_KV_FULL + s));
+            }
+        }
+        // no copy may still be in flight when the warp leaves
+        cp_async_wait<0>();
+    } else if (warp == kMmaWarp) {
+        // ============================ MMA issue ============================
+        if (lane == 0 && n > 0) {
+            tma_prefetch_map(&mq);
+            uint32_t qfree_phase = 0, qfull_phase = 0;
+            bool ok = true;
+            auto load_q = [&](int64_t u) {
+                // every MMA that reads the current Q must have completed
+                tc_commit(bar(B_Q_FREE));
+                ok = ok && mbar_wait(bar(B_Q_FREE), qfree_phase, p.err_word, abort_flag);
+                qfree_phase ^= 1;
+                const UCoord uc = ucoord(u, p);
+                mbar_arrive_expect_tx(bar(B_Q_FULL), kPanels * kHeads * 128);
+                const int c1 = sch.q_head_inner ? uc.n2 * kHeads : uc.s1;
+                const int c2 = sch.q_head_inner ? uc.s1 : uc.n2 * kHeads;
+                // 4 nope panels, then the rope panel (its upper 32 dims are never read)
+                for (int pn = 0; pn < kPanels; ++pn)
+                    tma_load_4d(sbase + L::q + pn * (kHeads * 128), &mq,
+                                pn < 4 ? (int)rank * kHalfDv + 64 * pn : 512 + 32 * (int)rank, c1, c2,
+                                uc.b, bar(B_Q_FULL));
+                ok = ok && mbar_wait(bar(B_Q_FULL), qfull_phase, p.err_word, abort_flag);
+                qfull_phase ^= 1;
+            };
+            auto qk = [&](int i) {
+                const int s = i % kStages;
+                ok = ok && mbar_wait(bar(B_KV_FULL + s), (i / kStages) & 1, p.err_word, abort_flag);
+                fence_proxy_async_smem();     // cp.async (generic proxy) data -> tensor core
+                tc_fence_after();
+                const uint32_t kb = sbase + L::kv + s * L::kvStage;
+#pragma unroll 2
+                for (int kk = 0; kk < kQkSteps; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint64_t ad = sdesc_sw128(sbase + L::q + (kk >> 2) * (kHeads * 128) + off, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * (kChunk * 128) + off, 16, 1024);
+                    tc_mma_f16(tmem + (i & 1) * kChunk, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(B_S_FULL + (i & 1)));
+            };
+            load_q(unit_of(c_begin));
+            qk(0);
+            bool first_of_unit = true;
+            for (int i = 0; i < n; ++i) {
+                const int s = i % kStages;
+                const bool has_next = i + 1 < n;
+                const bool next_same = has_next && unit_of(c_begin + i + 1) == unit_of(c_begin + i);
+                if (next_same) qk(i + 1);
+                ok = ok && mbar_wait(bar(B_P_FULL), i & 1, p.err_word, abort_flag);
+                tc_fence_after();
+                const uint32_t kb = sbase + L::kv + s * L::kvStage;
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kChunk / 16; ++kk) {
+                        const uint64_t ad = sdesc_sw128(sbase + L::p + part * (kHeads * 128) + kk * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(kb + kk * 16 * 128, kChunk * 128, 1024);
+                        const uint32_t acc = (first_of_unit && part == 0 && kk == 0) ? 0u : 1u;
+                        tc_mma_f16(tmem + kOCol, ad, bd, kIdescPV, acc);
+                    }
+                tc_commit(bar(B_O_DONE));
+                tc_commit(bar(B_KV_FREE + s));
+                first_of_unit = false;
+                if (has_next && !next_same) {
+                    load_q(unit_of(c_begin + i + 1));
+                    qk(i + 1);
+                    first_of_unit = true;
+                }
+            }
+            if (!ok) {
+                // a wait gave up: let every MMA this thread issued finish
+                // (bounded) before the tensor memory is released
+                tc_commit(bar(B_DRAIN));
+                mbar_wait(bar(B_DRAIN), 0, nullptr, nullptr, 100000000ull);
+            }
+        }
+    } else {
+        // ============================ softmax ============================
+        const int r = tid;                                   // head row = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t x_peer = map_peer(sbase + L::x, peer);
+        const uint32_t xfull_peer = map_peer(bar(B_X_FULL), peer);
+        const uint32_t xempty_peer = map_peer(bar(B_X_EMPTY), peer);
+        unsigned char* p_hi = smem + L::p;
+        unsigned char* p_lo = p_hi + kHeads * 128;
+        float m_used = -INFINITY, l = 0.f;
+        bool first_of_unit = true;
+        for (int i = 0; i < n; ++i) {
+            const int64_t c = c_begin + i;
+            const int64_t u = unit_of(c);
+            const bool last_of_unit = (i + 1 == n) || unit_of(c + 1) != u;
+            mbar_wait(bar(B_KV_FULL + i % kStages), (i / kStages) & 1, p.err_word, abort_flag);
+            mbar_wait(bar(B_S_FULL + (i & 1)), (i / 2) & 1, p.err_word, abort_flag);
+            tc_fence_after();
+            uint32_t sv[64];
+            tmem_ld32(lane_base + (i & 1) * kChunk, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tmem_ld32(lane_base + (i & 1) * kChunk + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            tmem_wait_ld();
+            // ---- exchange the partial scores with the peer CTA ----
+            if (i > 0) mbar_wait_cluster(bar(B_X_EMPTY), (i - 1) & 1, p.err_word, abort_flag);
+#pragma unroll
+            for (int q4 = 0; q4 < 16; ++q4)
+                st_cluster_v4(x_peer + r * 256 + ((q4 ^ (r & 15)) << 4),
+                              make_uint4(sv[4 * q4], sv[4 * q4 + 1], sv[4 * q4 + 2], sv[4 * q4 + 3]));
+            mbar_arrive_remote(xfull_peer);
+            mbar_wait_cluster(bar(B_X_FULL), i & 1, p.err_word, abort_flag);
+            float s[64];
+#pragma unroll
+            for (int q4 = 0; q4 < 16; ++q4) {
+                const uint4 o = *reinterpret_cast<const uint4*>(smem + L::x + r * 256 + ((q4 ^ (r & 15)) << 4));
+                // both CTAs add the two partials in the same (commutative) way
+                s[4 * q4] = __uint_as_float(sv[4 * q4]) + __uint_as_float(o.x);
+                s[4 * q4 + 1] = __uint_as_float(sv[4 * q4 + 1]) + __uint_as_float(o.y);
+                s[4 * q4 + 2] = __uint_as_float(sv[4 * q4 + 2]) + __uint_as_float(o.z);
+                s[4 * q4 + 3] = __uint_as_float(sv[4 * q4 + 3]) + __uint_as_float(o.w);
+            }
+            mbar_arrive_remote(xempty_peer);
+            // ---- online softmax over the chunk (mask shared by all heads) ----
+            const uint2 vis = reinterpret_cast<const uint2*>(smem + L::meta)[i % kStages];
+            float bmax = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const bool v = ((j < 32 ? vis.x >> j : vis.y >> (j - 32)) & 1u) != 0;
+                s[j] = v ? s[j] * p.scale_log2 : -INFINITY;
+                bmax = fmaxf(bmax, s[j]);
+            }
+            const float m_new = fmaxf(m_used, bmax);
+            const bool need = m_new > m_used + kRescaleThreshold;
+            const float f = need ? fast_exp2(m_used - m_new) : 1.f;   // 0 while m_used is -inf
+            if (need) m_used = m_new;
+            // P (high part and remainder) in registers before P.V of the
+            // previous chunk has released the P buffer
+            uint32_t hw[32], lw[32];
+            float lsum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float a = s[2 * e], b = s[2 * e + 1];
+                const float p0 = (a == -INFINITY) ? 0.f : fast_exp2(a - m_used);
+                const float p1 = (b == -INFINITY) ? 0.f : fast_exp2(b - m_used);
+                lsum += p0 + p1;
+                hw[e] = E::pack2(p0, p1);
+                const float2 h = E::unpack2(hw[e]);
+                lw[e] = E::pack2(p0 - h.x, p1 - h.y);
+            }
+            l = l * f + lsum;
+            if (i > 0) {
+                // P.V of the previous chunk must be done before P and O are touched
+                mbar_wait(bar(B_O_DONE), (i - 1) & 1, p.err_word, abort_flag);
+                tc_fence_after();
+                if (!first_of_unit && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                    for (int cb = 0; cb < kHalfDv / 32; ++cb) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_base + kOCol + 32 * cb, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
+                        tmem_st32(lane_base + kOCol + 32 * cb, ov);
+                    }
+                    tmem_wait_st();
+                }
+            }
+#pragma unroll
+            for (int cb = 0; cb < 8; ++cb) {
+                const int pos = r * 128 + ((cb ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4*>(p_hi + pos) =
+                    make_uint4(hw[4 * cb], hw[4 * cb + 1], hw[4 * cb + 2], hw[4 * cb + 3]);
+                *reinterpret_cast<uint4*>(p_lo + pos) =
+                    make_uint4(lw[4 * cb], lw[4 * cb + 1], lw[4 * cb + 2], lw[4 * cb + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_P_FULL));
+            first_of_unit = false;
+            if (!last_of_unit) continue;
+
+            // ---- epilogue of unit u: this CTA's half of Dv ----
+            mbar_wait(bar(B_O_DONE), i & 1, p.err_word, abort_flag);
+            tc_fence_after();
+            const int64_t first = u * cpu, lastc = first + cpu - 1;
+            const int64_t c_lo = mla_cluster_of(first, sch), c_hi = mla_cluster_of(lastc, sch);
+            const int nseg = (int)(c_hi - c_lo + 1);
+            const UCoord uc = ucoord(u, p);
+            const int n1 = uc.n2 * kHeads + r;
+            const int64_t row = u * kHeads + r;
+            const int64_t slot = row * sch.seg_max + (cl - c_lo);
+            const bool empty = !(l > 0.f);
+            const float inv = empty ? 0.f : 1.f / l;
+            T* orow = static_cast<T*>(p.out) + uc.b * p.o_sb + n1 * p.o_sh + uc.s1 * p.o_ss + rank * kHalfDv;
+#pragma unroll 1
+            for (int cb = 0; cb < kHalfDv / 32; ++cb) {
+                uint32_t ov[32];
+                tmem_ld32(lane_base + kOCol + 32 * cb, ov);
+                tmem_wait_ld();
+                if (nseg == 1) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 w;
+                        w.x = empty ? 0u : E::pack2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+                        w.y = empty ? 0u : E::pack2(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+                        w.z = empty ? 0u : E::pack2(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
+                        w.w = empty ? 0u : E::pack2(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + 32 * cb + j) = w;
+                    }
+                } else {
+                    float* wo = p.ws_o + slot * kDv + rank * kHalfDv + 32 * cb;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(wo + j) =
+                            make_float4(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]),
+                                        __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
+                }
+            }
+            if (nseg == 1) {
+                if (rank == 0 && p.lse)
+                    p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] =
+                        empty ? -INFINITY : (m_used + __log2f(l)) * kLn2;
+            } else {
+                p.ws_ml[slot * 2] = m_used;     // both CTAs write the same values
+                p.ws_ml[slot * 2 + 1] = l;
+                __threadfence();
+                named_sync(1, kSoftWarps * 32);
+                if (r == 0) {
+                    const unsigned prev = atomicAdd(p.counters + 2 * u + rank, 1u);
+                    *last_flag = (prev == (unsigned)(nseg - 1)) ? 1 : 0;
+                }
+                named_sync(1, kSoftWarps * 32);
+                if (*last_flag) {
+                    __threadfence();
+                    const float* ml = p.ws_ml + row * sch.seg_max * 2;
+                    float M = -INFINITY;
+                    for (int k2 = 0; k2 < nseg; ++k2) M = fmaxf(M, __ldcg(ml + 2 * k2));
+                    float Ls = 0.f;
+                    float wk[kMaxSeg];
+#pragma unroll
+                    for (int k2 = 0; k2 < kMaxSeg; ++k2) {
+                        wk[k2] = 0.f;
+                        if (k2 < nseg) {
+                            wk[k2] = rescale_factor(__ldcg(ml + 2 * k2), M);
+                            Ls += wk[k2] * __ldcg(ml + 2 * k2 + 1);
+                        }
+                    }
+                    const bool emp = !(Ls > 0.f);
+                    const float iv = emp ? 0.f : 1.f / Ls;
+                    const float* base = p.ws_o + row * sch.seg_max * kDv + rank * kHalfDv;
+#pragma unroll 1
+                    for (int d = 0; d < kHalfDv; d += 8) {
+                        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        for (int k2 = 0; k2 < nseg; ++k2) {
+                            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(base + (int64_t)k2 * kDv + d));
+                            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(base + (int64_t)k2 * kDv + d + 4));
+                            a[0] += wk[k2] * x0.x; a[1] += wk[k2] * x0.y; a[2] += wk[k2] * x0.z; a[3] += wk[k2] * x0.w;
+                            a[4] += wk[k2] * x1.x; a[5] += wk[k2] * x1.y; a[6] += wk[k2] * x1.z; a[7] += wk[k2] * x1.w;
+                        }
+                        uint4 w;
+                        w.x = emp ? 0u : E::pack2(a[0] * iv, a[1] * iv);
+                        w.y = emp ? 0u : E::pack2(a[2] * iv, a[3] * iv);
+                        w.z = emp ? 0u : E::pack2(a[4] * iv, a[5] * iv);
+                        w.w = emp ? 0u : E::pack2(a[6] * iv, a[7] * iv);
+                        *reinterpret_cast<uint4*>(orow + d) = w;
+                    }
+                    if (rank == 0 && p.lse)
+                        p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] =
+                            emp ? -INFINITY : (M + __log2f(Ls)) * kLn2;
+                    if (r == 0) atomicExch(p.counters + 2 * u + rank, 0u);
+                }
+                named_sync(1, kSoftWarps * 32);
+            }
+            m_used = -INFINITY;
+            l = 0.f;
+            first_of_unit = true;
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();      // the peer no longer writes into this CTA's shared memory
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                            &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 4-D map of q ordered by stride: {d, head, s1, b} when heads are adjacent
+// (BSND), else {d, s1, head, b}; box = 64 dims x 128 heads, 128-byte swizzle,
+// zero fill past Dk.
+bool make_q_map(CUtensorMap* map, const SfaParams& p, bool bf16, bool head_inner) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t n_a = head_inner ? p.N1 : p.S1, n_b = head_inner ? p.S1 : p.N1;
+    const int64_t s_a = head_inner ? p.q_sh : p.q_ss, s_b = head_inner ? p.q_ss : p.q_sh;
+    const cuuint64_t gdim[4] = {(cuuint64_t)p.Dk, n_a, n_b, (cuuint64_t)p.B};
+    const cuuint64_t gstride[3] = {(cuuint64_t)s_a * 2, (cuuint64_t)s_b * 2, (cuuint64_t)p.q_sb * 2};
+    const cuuint32_t box[4] = {64, head_inner ? (cuuint32_t)kHeads : 1u,
+                               head_inner ? 1u : (cuuint32_t)kHeads, 1};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+              const_cast<void*>(p.q), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Per-device setup of the MLA kernel (cached): the shared-memory opt-in and
+// the number of clusters that fit on the device at once -- pairs of SMs
+// inside one GPC, so possibly fewer than SMs / 2.  Returns 0 on failure.
+template <class E>
+int prepare_device(int num_sms) {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] > 0) return cache[dev];
+    if (cudaFuncSetAttribute(sfa_mla_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MlaSmem::alloc) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = MlaSmem::alloc;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sfa_mla_kernel<E>, &cfg) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = num_sms / 2;
+    }
+    if (n > num_sms / 2) n = num_sms / 2;
+    if (n < 1) n = 1;
+    cache[dev] = n;
+    return n;
+}
+
+template <class E>
+cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    const int resident = prepare_device<E>(num_sms);
+    if (resident < 1) return cudaErrorInvalidConfiguration;
+    MlaSched s;
+    s.q_head_inner = p.q_sh <= p.q_ss ? 1 : 0;
+    CUtensorMap mq;
+    if (!make_q_map(&mq, p, std::is_same<E, BF16>::value, s.q_head_inner != 0))
+        return cudaErrorInvalidValue;
+    s.cpu = (p.topK + kChunk - 1) / kChunk;
+    s.units = (int64_t)p.B * p.N2 * p.S1;
+    s.total = s.units * s.cpu;
+    int64_t clusters = resident;
+    if (p.num_ctas > 0) clusters = (p.num_ctas + 1) / 2;    // tuning / tests
+    if (clusters > s.total) clusters = s.total;
+    if (clusters < 1) clusters = 1;
+    // keep the number of clusters sharing one unit within kMaxSeg: a unit of
+    // cpu chunks meets at most ceil(cpu / shortest range) + 1 ranges
+    for (;;) {
+        const int64_t lmin = s.total / clusters;
+        int64_t seg = (s.cpu + lmin - 1) / lmin + 1;
+        if (seg > s.cpu) seg = s.cpu;
+        if (seg <= kMaxSeg || clusters == 1) {
+            s.seg_max = (int)seg;
+            break;
+        }
+        clusters = clusters * 3 / 4;
+    }
+    s.clusters = (int)clusters;
+    if (s.seg_max > 1) {
+        const int64_t rows = s.units * kHeads;
+        const size_t need = (size_t)rows * s.seg_max * ((size_t)kDv + 2) * sizeof(float);
+        if (!ws || ws_bytes < need || !p.counters) return cudaErrorInvalidValue;
+        p.ws_o = static_cast<float*>(ws);
+        p.ws_ml = p.ws_o + rows * s.seg_max * kDv;
+    }
+    sfa_mla_kernel<E><<<(unsigned)(2 * s.clusters), kThreads, MlaSmem::alloc, stream>>>(mq, p, s);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mla_supported(const SfaParams& p) {
+    const bool prefix = (p.v == p.k) && (p.v_ss == p.k_ss);
+    return p.G == kHeads && p.Dk == kDk && p.Dv == kDv && prefix &&
+           2 * (int64_t)p.B * p.N2 * p.S1 <= kMaxCounters;
+}
+
+size_t mla_ws_bytes(const SfaParams& p) {
+    const int64_t cpu = (p.topK + kChunk - 1) / kChunk;
+    const int64_t seg = cpu < kMaxSeg ? cpu : kMaxSeg;
+    const int64_t rows = (int64_t)p.B * p.N2 * p.S1 * kHeads;
+    return seg > 1 ? (size_t)rows * seg * ((size_t)kDv + 2) * sizeof(float) : 0;
+}
+
+cudaError_t launch_sfa_mla(const SfaParams& p, sfa_dtype dtype, int num_sms, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+    if (!mla_supported(p)) return cudaErrorInvalidValue;
+    return dtype == SFA_DTYPE_BF16 ? launch_t<BF16>(p, num_sms, ws, ws_bytes, stream)
+                                   : launch_t<F16>(p, num_sms, ws, ws_bytes, stream);
+}
+
+}  // namespace sfa

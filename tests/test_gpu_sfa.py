@@ -254,3 +254,81 @@ def test_workspace_shared_across_shapes():
     for rep in range(2):
         for case in cases:
             run_and_check(case)
+
+
+# ---------------------------------------------------------------------------
+# MLA tensor-core path (128 heads per index list, Dk = 576, Dv = 512, value =
+# key prefix): 2-CTA clusters, stream-K with in-kernel merge
+
+def mla(**kw):
+    base = dict(name="mla", B=2, S1=2, S2=700, N1=128, N2=1, Dk=576, Dv=512, topK=300,
+                dtype="bf16", layout="BSND", causal=False, scale=1 / math.sqrt(576),
+                value_is_key_prefix=True, seed=777)
+    base.update(kw)
+    return synth.SfaCase(**base)
+
+
+@pytest.mark.parametrize("layout", ["BSND", "BNSD"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_mla_path_layouts_dtypes(layout, dtype, causal):
+    run_and_check(mla(layout=layout, dtype=dtype, causal=causal))
+
+
+def test_mla_two_kv_heads():
+    run_and_check(mla(B=3, S1=1, N1=256, N2=2, topK=200, S2=500, causal=True))
+
+
+@pytest.mark.parametrize("topK", [1, 63, 64, 65, 129])
+def test_mla_ragged_topk(topK):
+    run_and_check(mla(topK=topK, S2=max(topK, 150), S1=3, causal=True, index_kind="sorted"))
+
+
+def test_mla_fully_masked_rows():
+    case = mla(B=2, S1=6, S2=90, topK=70, causal=True, index_kind="causal_mix",
+               masked_frac=0.3, full_masked_rows=3)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    out, lse = T.run_gpu(case, dev)
+    T.check_full(case, d, out, lse)
+    assert torch.all(out[0, :3] == 0) and torch.all(torch.isneginf(lse[0, :3]))
+
+
+@pytest.mark.parametrize("num_ctas", [2, 6, 20, 0])
+def test_mla_cluster_schedules(num_ctas):
+    """One cluster walking every unit; a few clusters whose ranges split
+    units (merged in-kernel by the last to finish); the resident-cluster
+    default where most units are split.  Each case runs twice: the merge
+    counters must be back at zero after a call."""
+    case = mla(B=5, S1=3, topK=260, S2=600, causal=True)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    for _ in range(2):
+        out, lse = T.run_gpu(case, dev, num_ctas=num_ctas)
+        T.check_full(case, d, out, lse)
+
+
+def test_mla_out_of_range_indices_masked_and_reported():
+    """Indices outside [0, S2) act as masked slots and set the error word."""
+    case = mla(B=1, S1=2, topK=130, S2=400)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    bad = dev["idx"].clone()
+    bad_slots = {0: [0, 1, 2, 3, 4], 1: [7, 100]}
+    bad[0, 0, 0, :5] = -1
+    bad[0, 1, 0, 7] = 400
+    bad[0, 1, 0, 100] = 1 << 30
+    assert sfa.sfa_get_last_error() == sfa.SFA_OK
+    out, lse = T.run_gpu(case, dict(dev, idx=bad), validate_indices=True)
+    assert sfa.sfa_get_last_error() == sfa.SFA_ERR_INDEX_RANGE
+    for s1, drop in bad_slots.items():
+        keep = np.delete(d["idx"][0, s1, 0].numpy(), drop)
+        sub = {"q": d["q"][:, s1:s1 + 1].contiguous(), "k": d["k"],
+               "idx": torch.from_numpy(keep).reshape(1, 1, 1, -1).contiguous()}
+        sub["v"] = sub["k"][..., :case.Dv]
+        y, l = oracle.sfa(sub["q"], sub["k"], sub["v"], sub["idx"], case.scale, "BSND", False)
+        got = out[0, s1].float().cpu().numpy()
+        rep = oracle.precision_report(got, y[0, 0], case.dtype)
+        assert rep["passed"], rep
+        np.testing.assert_allclose(lse[0, s1].cpu().numpy(), l[0, 0], atol=T.LSE_ATOL,
+                                   rtol=T.LSE_RTOL)
