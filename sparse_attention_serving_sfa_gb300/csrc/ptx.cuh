@@ -161,6 +161,18 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     }
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
+// another CTA's shared memory (cluster addresses for the destination and its
+// mbarrier); completion is counted in bytes on that mbarrier.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                               uint32_t mbar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src), "r"(bytes), "r"(mbar_cluster)
+        : "memory");
+}
+
 // Whole-cluster barrier (all threads of every CTA of the cluster).
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::

@@ -8,23 +8,32 @@
 // chunks.
 //
 // O for 128 heads x 512 dims (fp32) fills all 512 columns of one SM's tensor
-// memory and Q (128 x 576) alone is 144 KB of shared memory, so a unit is
-// computed by a 2-CTA cluster that splits the head dimensions:
+// memory, so a unit (one index list and its 128 heads) is computed by a 2-CTA
+// cluster that splits the head dimensions:
 //   CTA r owns K/Q dims [256 r, 256 r + 256) (nope) and [512 + 32 r, 544 + 32 r)
 //   (rope), and V / O dims [256 r, 256 r + 256) -- the first 256 of its K dims.
 // Per 64-slot chunk, each CTA gathers only its 576 bytes of every selected K
-// row (no duplicated gather), computes a partial S_r = Q_r K_r^T (tcgen05.mma,
-// M = 128 heads, N = 64 slots, accumulated in tensor memory), and the two
-// partials are exchanged through distributed shared memory: both CTAs then hold
-// the same S = S_0 + S_1, run the same online softmax, and compute
-// O_r += P V_r for their half of Dv (P as a 16-bit high part plus remainder).
+// row (no duplicated gather) and computes a partial S_r = Q_r K_r^T; the two
+// partials are exchanged with one bulk shared-memory copy into the peer CTA,
+// so both CTAs hold the same S = S_0 + S_1, run the same online softmax and
+// compute O_r += P V_r for their half of Dv (P as a 16-bit high part plus
+// remainder, ~fp32 accurate).
 //
-// Roles per CTA (7 warps): 2 producer warps (cp.async gather of the K rows
-// into 128-byte-swizzled panels, index prefetch, visibility masks), 1 MMA warp
-// (TMA load of the unit's Q half, tcgen05.mma issue), 4 softmax warps (thread
-// = head = TMEM lane: S exchange, softmax, P, O rescale, epilogue).  Work is
-// stream-K over (unit, chunk) pairs per cluster; a unit split over clusters is
-// merged by the last cluster to finish it (arrival counters per unit and half).
+// The tensor core reads its shared-memory operands at a limited rate, so the
+// A operands live in tensor memory: the unit's Q nope half (written by the
+// softmax threads) and P (written over the S columns it came from).  Only the
+// gathered K/V rows and the small Q rope panel are read from shared memory.
+//
+// TMEM (512 columns): Q nope [0, 128) | S/P buffer 0 [128, 192) | S/P buffer 1
+// [192, 256) | O [256, 512).
+//
+// Roles per CTA (11 warps): 8 softmax warps (two warpgroups, thread = head =
+// TMEM lane; warpgroup w takes slots [32 w, 32 w + 32) of a chunk and O dims
+// [128 w, 128 w + 128) of the CTA's half), 1 MMA warp (rope TMA, tcgen05.mma
+// issue), 2 producer warps (cp.async gather, index prefetch, visibility
+// masks).  Work is stream-K over (unit, chunk) pairs per cluster; the parts of
+// a unit split over clusters are written as fp32 partials and merged by a
+// second kernel.
 #include <cudaTypedefs.h>
 
 #include <limits.h>
@@ -44,37 +53,39 @@ constexpr int kChunk = 64;
 constexpr int kHeads = 128;               // the MMA M dimension
 constexpr int kDk = 576, kDv = 512;
 constexpr int kHalfDv = 256;              // nope dims (and V / O dims) per CTA
-constexpr int kPanels = 5;                // 4 nope + 1 rope (32 dims used, 32 never read)
-constexpr int kQkSteps = 4 * 4 + 2;       // K = 16 steps: 256 nope dims + 32 rope dims
-constexpr int kStages = 2;
-constexpr int kSoftWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kProdWarp0 = 5;
+constexpr int kPanels = 5;                // K stage: 4 nope panels + 1 rope panel (32 dims used)
+constexpr int kStages = 3;
+constexpr int kSoftThreads = 256;
+constexpr int kMmaWarp = 8;
+constexpr int kProdWarp0 = 9;
 constexpr int kProdThreads = 64;
-constexpr int kThreads = (kSoftWarps + 1 + 2) * 32;
+constexpr int kThreads = kSoftThreads + 32 + kProdThreads;
 constexpr int kTmemCols = 512;
-constexpr int kOCol = 128;                // TMEM: S buffers at [0, 64), [64, 128); O at [128, 384)
+constexpr int kQnCol = 0, kSPCol = 128, kOCol = 256;
 constexpr int kLookahead = 6;
 constexpr int kNoSlot = INT_MIN;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kMaxSeg = 8;                // split partials per unit and half
+constexpr int kMaxSeg = 8;                // clusters sharing one unit
+constexpr uint32_t kXBytes = kHeads * kChunk * 4;
 
 struct MlaSmem {
-    static constexpr int q = 0;                             // 5 panels x 128 rows x 128 B
+    static constexpr int qr = 0;                            // Q rope panel: 128 rows x 128 B
     static constexpr int kvStage = kPanels * kChunk * 128;  // 40 KB
-    static constexpr int kv = q + kPanels * kHeads * 128;
-    static constexpr int p = kv + kStages * kvStage;        // hi, lo: 128 rows x 128 B each
-    static constexpr int x = p + 2 * kHeads * 128;          // 128 rows x 64 fp32 (peer partial S)
-    static constexpr int bars = x + kHeads * kChunk * 4;
+    static constexpr int kv = qr + kHeads * 128;
+    static constexpr int stg = kv + kStages * kvStage;      // own partial S (send), 32 KB
+    static constexpr int x = stg + kXBytes;                 // peer partial S (receive), 32 KB
+    static constexpr int red = x + kXBytes;                 // [2][128] row max per warpgroup
+    static constexpr int red2 = red + 2 * kHeads * 4;       // [2][128] row sum per warpgroup
+    static constexpr int bars = red2 + 2 * kHeads * 4;
     static constexpr int meta = bars + 16 * 8;              // [stage] uint2 visibility mask
-    static constexpr int misc = meta + kStages * 8;         // tmem base, abort, last flag
+    static constexpr int misc = meta + 32;                  // tmem base, abort flag
     static constexpr int total = misc + 16;
     static constexpr int alloc = total + 1024;
 };
 
 enum {
-    B_Q_FULL = 0, B_Q_FREE = 1, B_KV_FULL = 2, B_KV_FREE = 4, B_S_FULL = 6, B_P_FULL = 8,
-    B_O_DONE = 9, B_X_FULL = 10, B_X_EMPTY = 11, B_DRAIN = 12
+    B_QR_FULL = 0, B_Q_FREE = 1, B_Q_READY = 2, B_KV_FULL = 3, B_KV_FREE = 6, B_S_FULL = 9,
+    B_P_FULL = 11, B_O_DONE = 12, B_X_FULL = 13, B_X_EMPTY = 14, B_DRAIN = 15
 };
 
 struct MlaSched {
@@ -124,27 +135,28 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
     const int n = (int)(c_end - c_begin);
     auto bar = [&](int i) { return sbase + L::bars + 8 * i; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::misc + 8);
 
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(bar(B_Q_FULL), 1);
+        mbar_init(bar(B_QR_FULL), 1);
         mbar_init(bar(B_Q_FREE), 1);
+        mbar_init(bar(B_Q_READY), kSoftThreads);
         mbar_init(bar(B_DRAIN), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_KV_FULL + s), kProdThreads + 2);
             mbar_init(bar(B_KV_FREE + s), 1);
-            mbar_init(bar(B_S_FULL + s), 1);
         }
-        mbar_init(bar(B_P_FULL), kSoftWarps * 32);
+        mbar_init(bar(B_S_FULL), 1);
+        mbar_init(bar(B_S_FULL + 1), 1);
+        mbar_init(bar(B_P_FULL), kSoftThreads);
         mbar_init(bar(B_O_DONE), 1);
-        mbar_init(bar(B_X_FULL), kSoftWarps * 32);     // arrived on by the peer's softmax threads
-        mbar_init(bar(B_X_EMPTY), kSoftWarps * 32);
+        mbar_init(bar(B_X_FULL), 1);      // own arrive.expect_tx + the peer's bulk copy bytes
+        mbar_init(bar(B_X_EMPTY), 1);     // the peer has read what this CTA sent it
         fence_barrier_init();
     }
     if (warp == kMmaWarp) tmem_alloc(sbase + L::misc, kTmemCols);
     tc_fence_before();
-    cluster_sync();      // both CTAs' barriers exist before any remote arrive
+    cluster_sync();      // both CTAs' barriers exist before any remote access
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::misc);
 
@@ -223,24 +235,20 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         // ============================ MMA issue ============================
         if (lane == 0 && n > 0) {
             tma_prefetch_map(&mq);
-            uint32_t qfree_phase = 0, qfull_phase = 0;
+            uint32_t qfree_phase = 0, q_phase = 0;
             bool ok = true;
-            auto load_q = [&](int64_t u) {
-                // every MMA that reads the current Q must have completed
-                tc_commit(bar(B_Q_FREE));
-                ok = ok && mbar_wait(bar(B_Q_FREE), qfree_phase, p.err_word, abort_flag);
-                qfree_phase ^= 1;
+            // the unit's Q rope panel (TMA) and its Q nope half (written to
+            // tensor memory by the softmax threads)
+            auto unit_q = [&](int64_t u) {
                 const UCoord uc = ucoord(u, p);
-                mbar_arrive_expect_tx(bar(B_Q_FULL), kPanels * kHeads * 128);
+                mbar_arrive_expect_tx(bar(B_QR_FULL), kHeads * 128);
                 const int c1 = sch.q_head_inner ? uc.n2 * kHeads : uc.s1;
                 const int c2 = sch.q_head_inner ? uc.s1 : uc.n2 * kHeads;
-                // 4 nope panels, then the rope panel (its upper 32 dims are never read)
-                for (int pn = 0; pn < kPanels; ++pn)
-                    tma_load_4d(sbase + L::q + pn * (kHeads * 128), &mq,
-                                pn < 4 ? (int)rank * kHalfDv + 64 * pn : 512 + 32 * (int)rank, c1, c2,
-                                uc.b, bar(B_Q_FULL));
-                ok = ok && mbar_wait(bar(B_Q_FULL), qfull_phase, p.err_word, abort_flag);
-                qfull_phase ^= 1;
+                tma_load_4d(sbase + L::qr, &mq, 512 + 32 * (int)rank, c1, c2, uc.b, bar(B_QR_FULL));
+                ok = ok && mbar_wait(bar(B_QR_FULL), q_phase, p.err_word, abort_flag);
+                ok = ok && mbar_wait(bar(B_Q_READY), q_phase, p.err_word, abort_flag);
+                q_phase ^= 1;
+                tc_fence_after();
             };
             auto qk = [&](int i) {
                 const int s = i % kStages;
@@ -248,16 +256,21 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
                 fence_proxy_async_smem();     // cp.async (generic proxy) data -> tensor core
                 tc_fence_after();
                 const uint32_t kb = sbase + L::kv + s * L::kvStage;
-#pragma unroll 2
-                for (int kk = 0; kk < kQkSteps; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t ad = sdesc_sw128(sbase + L::q + (kk >> 2) * (kHeads * 128) + off, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * (kChunk * 128) + off, 16, 1024);
-                    tc_mma_f16(tmem + (i & 1) * kChunk, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                const uint32_t d = tmem + kSPCol + 64 * (i & 1);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * (kChunk * 128) + (kk & 3) * 32, 16, 1024);
+                    tc_mma_f16_ts(d, tmem + kQnCol + 8 * kk, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sbase + L::qr + kk * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kb + 4 * (kChunk * 128) + kk * 32, 16, 1024);
+                    tc_mma_f16(d, ad, bd, kIdescQK, 1u);
                 }
                 tc_commit(bar(B_S_FULL + (i & 1)));
             };
-            load_q(unit_of(c_begin));
+            unit_q(unit_of(c_begin));
             qk(0);
             bool first_of_unit = true;
             for (int i = 0; i < n; ++i) {
@@ -268,19 +281,24 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
                 ok = ok && mbar_wait(bar(B_P_FULL), i & 1, p.err_word, abort_flag);
                 tc_fence_after();
                 const uint32_t kb = sbase + L::kv + s * L::kvStage;
+                const uint32_t pa = tmem + kSPCol + 64 * (i & 1);
+#pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kChunk / 16; ++kk) {
-                        const uint64_t ad = sdesc_sw128(sbase + L::p + part * (kHeads * 128) + kk * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(kb + kk * 16 * 128, kChunk * 128, 1024);
                         const uint32_t acc = (first_of_unit && part == 0 && kk == 0) ? 0u : 1u;
-                        tc_mma_f16(tmem + kOCol, ad, bd, kIdescPV, acc);
+                        tc_mma_f16_ts(tmem + kOCol, pa + 32 * part + 8 * kk, bd, kIdescPV, acc);
                     }
                 tc_commit(bar(B_O_DONE));
                 tc_commit(bar(B_KV_FREE + s));
                 first_of_unit = false;
                 if (has_next && !next_same) {
-                    load_q(unit_of(c_begin + i + 1));
+                    // the rope panel is rewritten once every MMA of the unit is done
+                    tc_commit(bar(B_Q_FREE));
+                    ok = ok && mbar_wait(bar(B_Q_FREE), qfree_phase, p.err_word, abort_flag);
+                    qfree_phase ^= 1;
+                    unit_q(unit_of(c_begin + i + 1));
                     qk(i + 1);
                     first_of_unit = true;
                 }
@@ -294,64 +312,98 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         }
     } else {
         // ============================ softmax ============================
-        const int r = tid;                                   // head row = TMEM lane
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int w = tid >> 7;                              // warpgroup: slot / dim half
+        const int r = tid & (kHeads - 1);                    // head row = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const uint32_t x_peer = map_peer(sbase + L::x, peer);
         const uint32_t xfull_peer = map_peer(bar(B_X_FULL), peer);
         const uint32_t xempty_peer = map_peer(bar(B_X_EMPTY), peer);
-        unsigned char* p_hi = smem + L::p;
-        unsigned char* p_lo = p_hi + kHeads * 128;
+        float* red = reinterpret_cast<float*>(smem + L::red);
+        float* red2 = reinterpret_cast<float*>(smem + L::red2);
+        // Q nope dims [256 rank + 128 w, +128) of head r into TMEM columns
+        // [64 w, 64 w + 64): two 16-bit dims per column
+        auto load_qn = [&](int64_t u) {
+            const UCoord uc = ucoord(u, p);
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const T*>(p.q) + uc.b * p.q_sb + uc.s1 * p.q_ss +
+                (int64_t)(uc.n2 * kHeads + r) * p.q_sh + (int)rank * kHalfDv + 128 * w);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 x = __ldg(src + 8 * half + j);
+                    v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+                }
+                tmem_st32(lane_base + kQnCol + 64 * w + 32 * half, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(B_Q_READY));
+        };
+        if (n > 0) load_qn(unit_of(c_begin));
         float m_used = -INFINITY, l = 0.f;
         bool first_of_unit = true;
         for (int i = 0; i < n; ++i) {
             const int64_t c = c_begin + i;
             const int64_t u = unit_of(c);
             const bool last_of_unit = (i + 1 == n) || unit_of(c + 1) != u;
+            const uint32_t sp = kSPCol + 64 * (i & 1);
             mbar_wait(bar(B_KV_FULL + i % kStages), (i / kStages) & 1, p.err_word, abort_flag);
             mbar_wait(bar(B_S_FULL + (i & 1)), (i / 2) & 1, p.err_word, abort_flag);
             tc_fence_after();
-            uint32_t sv[64];
-            tmem_ld32(lane_base + (i & 1) * kChunk, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tmem_ld32(lane_base + (i & 1) * kChunk + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            uint32_t sv[32];
+            tmem_ld32(lane_base + sp + 32 * w, sv);
             tmem_wait_ld();
             // ---- exchange the partial scores with the peer CTA ----
-            if (i > 0) mbar_wait_cluster(bar(B_X_EMPTY), (i - 1) & 1, p.err_word, abort_flag);
+            // the staging buffer is free once the peer has read the last copy
+            if (tid == 0 && i > 0)
+                mbar_wait_cluster(bar(B_X_EMPTY), (i - 1) & 1, p.err_word, abort_flag);
+            named_sync(1, kSoftThreads);
+            unsigned char* stg = smem + L::stg + r * 256;
 #pragma unroll
-            for (int q4 = 0; q4 < 16; ++q4)
-                st_cluster_v4(x_peer + r * 256 + ((q4 ^ (r & 15)) << 4),
-                              make_uint4(sv[4 * q4], sv[4 * q4 + 1], sv[4 * q4 + 2], sv[4 * q4 + 3]));
-            mbar_arrive_remote(xfull_peer);
-            mbar_wait_cluster(bar(B_X_FULL), i & 1, p.err_word, abort_flag);
-            float s[64];
-#pragma unroll
-            for (int q4 = 0; q4 < 16; ++q4) {
-                const uint4 o = *reinterpret_cast<const uint4*>(smem + L::x + r * 256 + ((q4 ^ (r & 15)) << 4));
-                // both CTAs add the two partials in the same (commutative) way
-                s[4 * q4] = __uint_as_float(sv[4 * q4]) + __uint_as_float(o.x);
-                s[4 * q4 + 1] = __uint_as_float(sv[4 * q4 + 1]) + __uint_as_float(o.y);
-                s[4 * q4 + 2] = __uint_as_float(sv[4 * q4 + 2]) + __uint_as_float(o.z);
-                s[4 * q4 + 3] = __uint_as_float(sv[4 * q4 + 3]) + __uint_as_float(o.w);
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(stg + (((8 * w + j) ^ (r & 15)) << 4)) =
+                    make_uint4(sv[4 * j], sv[4 * j + 1], sv[4 * j + 2], sv[4 * j + 3]);
+            fence_proxy_async_smem();         // generic writes -> bulk copy engine
+            named_sync(1, kSoftThreads);
+            if (tid == 0) {
+                mbar_arrive_expect_tx(bar(B_X_FULL), kXBytes);
+                bulk_s2cluster(x_peer, sbase + L::stg, kXBytes, xfull_peer);
             }
-            mbar_arrive_remote(xempty_peer);
-            // ---- online softmax over the chunk (mask shared by all heads) ----
+            mbar_wait(bar(B_X_FULL), i & 1, p.err_word, abort_flag);
             const uint2 vis = reinterpret_cast<const uint2*>(smem + L::meta)[i % kStages];
+            const uint32_t vw = w ? vis.y : vis.x;
+            const unsigned char* xr = smem + L::x + r * 256;
+            float s[32];
             float bmax = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const bool v = ((j < 32 ? vis.x >> j : vis.y >> (j - 32)) & 1u) != 0;
-                s[j] = v ? s[j] * p.scale_log2 : -INFINITY;
-                bmax = fmaxf(bmax, s[j]);
+            for (int j = 0; j < 8; ++j) {
+                const uint4 o = *reinterpret_cast<const uint4*>(xr + (((8 * w + j) ^ (r & 15)) << 4));
+                const float ov[4] = {__uint_as_float(o.x), __uint_as_float(o.y), __uint_as_float(o.z),
+                                     __uint_as_float(o.w)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int jj = 4 * j + e;
+                    // both CTAs add the two partials in the same (commutative) way
+                    const float v = __uint_as_float(sv[jj]) + ov[e];
+                    s[jj] = ((vw >> jj) & 1u) ? v * p.scale_log2 : -INFINITY;
+                    bmax = fmaxf(bmax, s[jj]);
+                }
             }
+            red[w * kHeads + r] = bmax;
+            named_sync(1, kSoftThreads);      // X read by every thread, row maxima posted
+            if (tid == 0) mbar_arrive_remote(xempty_peer);
+            bmax = fmaxf(red[r], red[kHeads + r]);
+            // ---- online softmax over the chunk (mask shared by all heads) ----
             const float m_new = fmaxf(m_used, bmax);
             const bool need = m_new > m_used + kRescaleThreshold;
             const float f = need ? fast_exp2(m_used - m_new) : 1.f;   // 0 while m_used is -inf
             if (need) m_used = m_new;
-            // P (high part and remainder) in registers before P.V of the
-            // previous chunk has released the P buffer
-            uint32_t hw[32], lw[32];
+            uint32_t hw[16], lw[16];
             float lsum = 0.f;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
+            for (int e = 0; e < 16; ++e) {
                 const float a = s[2 * e], b = s[2 * e + 1];
                 const float p0 = (a == -INFINITY) ? 0.f : fast_exp2(a - m_used);
                 const float p1 = (b == -INFINITY) ? 0.f : fast_exp2(b - m_used);
@@ -360,134 +412,93 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
                 const float2 h = E::unpack2(hw[e]);
                 lw[e] = E::pack2(p0 - h.x, p1 - h.y);
             }
-            l = l * f + lsum;
+            l = l * f + lsum;                 // this warpgroup's share of the row sum
             if (i > 0) {
-                // P.V of the previous chunk must be done before P and O are touched
+                // P.V of the previous chunk is done before O is rescaled (and
+                // before this chunk's P can be consumed)
                 mbar_wait(bar(B_O_DONE), (i - 1) & 1, p.err_word, abort_flag);
                 tc_fence_after();
                 if (!first_of_unit && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                    for (int cb = 0; cb < kHalfDv / 32; ++cb) {
+                    for (int cb = 0; cb < 4; ++cb) {
                         uint32_t ov[32];
-                        tmem_ld32(lane_base + kOCol + 32 * cb, ov);
+                        tmem_ld32(lane_base + kOCol + 128 * w + 32 * cb, ov);
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
-                        tmem_st32(lane_base + kOCol + 32 * cb, ov);
+                        tmem_st32(lane_base + kOCol + 128 * w + 32 * cb, ov);
                     }
-                    tmem_wait_st();
                 }
             }
-#pragma unroll
-            for (int cb = 0; cb < 8; ++cb) {
-                const int pos = r * 128 + ((cb ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(p_hi + pos) =
-                    make_uint4(hw[4 * cb], hw[4 * cb + 1], hw[4 * cb + 2], hw[4 * cb + 3]);
-                *reinterpret_cast<uint4*>(p_lo + pos) =
-                    make_uint4(lw[4 * cb], lw[4 * cb + 1], lw[4 * cb + 2], lw[4 * cb + 3]);
-            }
-            fence_proxy_async_smem();
+            // P over the S columns: high parts in [sp, sp + 32), remainders in
+            // [sp + 32, sp + 64); slot j -> column j / 2
+            tmem_st16(lane_base + sp + 16 * w, hw);
+            tmem_st16(lane_base + sp + 32 + 16 * w, lw);
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(B_P_FULL));
             first_of_unit = false;
             if (!last_of_unit) continue;
 
-            // ---- epilogue of unit u: this CTA's half of Dv ----
+            // ---- epilogue of unit u: dims [256 rank + 128 w, +128) ----
             mbar_wait(bar(B_O_DONE), i & 1, p.err_word, abort_flag);
             tc_fence_after();
+            red2[w * kHeads + r] = l;
+            named_sync(1, kSoftThreads);
+            const float lt = red2[r] + red2[kHeads + r];
             const int64_t first = u * cpu, lastc = first + cpu - 1;
             const int64_t c_lo = mla_cluster_of(first, sch), c_hi = mla_cluster_of(lastc, sch);
-            const int nseg = (int)(c_hi - c_lo + 1);
+            const bool split = c_hi > c_lo;
             const UCoord uc = ucoord(u, p);
             const int n1 = uc.n2 * kHeads + r;
             const int64_t row = u * kHeads + r;
             const int64_t slot = row * sch.seg_max + (cl - c_lo);
-            const bool empty = !(l > 0.f);
-            const float inv = empty ? 0.f : 1.f / l;
-            T* orow = static_cast<T*>(p.out) + uc.b * p.o_sb + n1 * p.o_sh + uc.s1 * p.o_ss + rank * kHalfDv;
+            const bool empty = !(lt > 0.f);
+            const float inv = empty ? 0.f : 1.f / lt;
+            const int d0 = (int)rank * kHalfDv + 128 * w;
+            T* orow = static_cast<T*>(p.out) + uc.b * p.o_sb + n1 * p.o_sh + uc.s1 * p.o_ss + d0;
+            float* wo = split ? p.ws_o + slot * kDv + d0 : nullptr;
 #pragma unroll 1
-            for (int cb = 0; cb < kHalfDv / 32; ++cb) {
+            for (int cb = 0; cb < 4; ++cb) {
                 uint32_t ov[32];
-                tmem_ld32(lane_base + kOCol + 32 * cb, ov);
+                tmem_ld32(lane_base + kOCol + 128 * w + 32 * cb, ov);
                 tmem_wait_ld();
-                if (nseg == 1) {
+                if (!split) {
 #pragma unroll
                     for (int j = 0; j < 32; j += 8) {
-                        uint4 w;
-                        w.x = empty ? 0u : E::pack2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
-                        w.y = empty ? 0u : E::pack2(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
-                        w.z = empty ? 0u : E::pack2(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
-                        w.w = empty ? 0u : E::pack2(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + 32 * cb + j) = w;
+                        uint4 q;
+                        q.x = empty ? 0u : E::pack2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+                        q.y = empty ? 0u : E::pack2(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+                        q.z = empty ? 0u : E::pack2(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
+                        q.w = empty ? 0u : E::pack2(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + 32 * cb + j) = q;
                     }
                 } else {
-                    float* wo = p.ws_o + slot * kDv + rank * kHalfDv + 32 * cb;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(wo + j) =
+                        *reinterpret_cast<float4*>(wo + 32 * cb + j) =
                             make_float4(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]),
                                         __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
                 }
             }
-            if (nseg == 1) {
-                if (rank == 0 && p.lse)
+            if (!split) {
+                if (rank == 0 && w == 0 && p.lse)
                     p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] =
-                        empty ? -INFINITY : (m_used + __log2f(l)) * kLn2;
-            } else {
-                p.ws_ml[slot * 2] = m_used;     // both CTAs write the same values
-                p.ws_ml[slot * 2 + 1] = l;
-                __threadfence();
-                named_sync(1, kSoftWarps * 32);
-                if (r == 0) {
-                    const unsigned prev = atomicAdd(p.counters + 2 * u + rank, 1u);
-                    *last_flag = (prev == (unsigned)(nseg - 1)) ? 1 : 0;
-                }
-                named_sync(1, kSoftWarps * 32);
-                if (*last_flag) {
-                    __threadfence();
-                    const float* ml = p.ws_ml + row * sch.seg_max * 2;
-                    float M = -INFINITY;
-                    for (int k2 = 0; k2 < nseg; ++k2) M = fmaxf(M, __ldcg(ml + 2 * k2));
-                    float Ls = 0.f;
-                    float wk[kMaxSeg];
-#pragma unroll
-                    for (int k2 = 0; k2 < kMaxSeg; ++k2) {
-                        wk[k2] = 0.f;
-                        if (k2 < nseg) {
-                            wk[k2] = rescale_factor(__ldcg(ml + 2 * k2), M);
-                            Ls += wk[k2] * __ldcg(ml + 2 * k2 + 1);
-                        }
-                    }
-                    const bool emp = !(Ls > 0.f);
-                    const float iv = emp ? 0.f : 1.f / Ls;
-                    const float* base = p.ws_o + row * sch.seg_max * kDv + rank * kHalfDv;
-#pragma unroll 1
-                    for (int d = 0; d < kHalfDv; d += 8) {
-                        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        for (int k2 = 0; k2 < nseg; ++k2) {
-                            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(base + (int64_t)k2 * kDv + d));
-                            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(base + (int64_t)k2 * kDv + d + 4));
-                            a[0] += wk[k2] * x0.x; a[1] += wk[k2] * x0.y; a[2] += wk[k2] * x0.z; a[3] += wk[k2] * x0.w;
-                            a[4] += wk[k2] * x1.x; a[5] += wk[k2] * x1.y; a[6] += wk[k2] * x1.z; a[7] += wk[k2] * x1.w;
-                        }
-                        uint4 w;
-                        w.x = emp ? 0u : E::pack2(a[0] * iv, a[1] * iv);
-                        w.y = emp ? 0u : E::pack2(a[2] * iv, a[3] * iv);
-                        w.z = emp ? 0u : E::pack2(a[4] * iv, a[5] * iv);
-                        w.w = emp ? 0u : E::pack2(a[6] * iv, a[7] * iv);
-                        *reinterpret_cast<uint4*>(orow + d) = w;
-                    }
-                    if (rank == 0 && p.lse)
-                        p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] =
-                            emp ? -INFINITY : (M + __log2f(Ls)) * kLn2;
-                    if (r == 0) atomicExch(p.counters + 2 * u + rank, 0u);
-                }
-                named_sync(1, kSoftWarps * 32);
+                        empty ? -INFINITY : (m_used + __log2f(lt)) * kLn2;
+            } else if (w == 0) {
+                // (m, l) of this part; both CTAs of the cluster write the same values
+                p.ws_ml[slot * 2] = m_used;
+                p.ws_ml[slot * 2 + 1] = lt;
             }
             m_used = -INFINITY;
             l = 0.f;
             first_of_unit = true;
+            // tensor memory's Q columns are free (every MMA of the unit is done)
+            if (i + 1 < n) load_qn(u + 1);
         }
+        // the last copy sent to the peer has landed before this CTA can leave
+        if (tid == 0 && n > 0)
+            mbar_wait_cluster(bar(B_X_EMPTY), (n - 1) & 1, p.err_word, nullptr, 100000000ull);
     }
     __syncwarp();
     tc_fence_before();
@@ -496,6 +507,70 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Merge of the parts of split units: one warp per output row (unit, head);
+// lane l combines dims [16 l, 16 l + 16) of every part.  Rows of units that a
+// single cluster finished were written by the main kernel.
+template <class E>
+__global__ void __launch_bounds__(512) sfa_mla_combine(const SfaParams p, const MlaSched sch) {
+    using T = typename E::T;
+    grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (row >= sch.units * kHeads) return;
+    const int64_t u = row / kHeads;
+    const int h = (int)(row % kHeads);
+    const int64_t first = u * sch.cpu;
+    const int64_t c_lo = mla_cluster_of(first, sch), c_hi = mla_cluster_of(first + sch.cpu - 1, sch);
+    const int nseg = (int)(c_hi - c_lo + 1);
+    if (nseg == 1) return;
+    const float* ml = p.ws_ml + row * sch.seg_max * 2;
+    float M = -INFINITY;
+    for (int k = 0; k < nseg; ++k) M = fmaxf(M, ml[2 * k]);
+    float wk[kMaxSeg];
+    float Ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxSeg; ++k) {
+        wk[k] = 0.f;
+        if (k < nseg) {
+            wk[k] = rescale_factor(ml[2 * k], M);
+            Ls += wk[k] * ml[2 * k + 1];
+        }
+    }
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    const float* base = p.ws_o + row * sch.seg_max * kDv + 16 * lane;
+#pragma unroll
+    for (int k = 0; k < kMaxSeg; ++k) {
+        if (k < nseg) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 x = *reinterpret_cast<const float4*>(base + (int64_t)k * kDv + 4 * q);
+                acc[4 * q] += wk[k] * x.x;
+                acc[4 * q + 1] += wk[k] * x.y;
+                acc[4 * q + 2] += wk[k] * x.z;
+                acc[4 * q + 3] += wk[k] * x.w;
+            }
+        }
+    }
+    const bool empty = !(Ls > 0.f);
+    const float inv = empty ? 0.f : 1.f / Ls;
+    const UCoord uc = ucoord(u, p);
+    const int n1 = uc.n2 * kHeads + h;
+    T* orow = static_cast<T*>(p.out) + uc.b * p.o_sb + n1 * p.o_sh + uc.s1 * p.o_ss + 16 * lane;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        uint4 o;
+        o.x = empty ? 0u : E::pack2(acc[8 * q] * inv, acc[8 * q + 1] * inv);
+        o.y = empty ? 0u : E::pack2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv);
+        o.z = empty ? 0u : E::pack2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv);
+        o.w = empty ? 0u : E::pack2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv);
+        *reinterpret_cast<uint4*>(orow + 8 * q) = o;
+    }
+    if (lane == 0 && p.lse)
+        p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] = empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -590,21 +665,36 @@ cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaSt
     if (s.seg_max > 1) {
         const int64_t rows = s.units * kHeads;
         const size_t need = (size_t)rows * s.seg_max * ((size_t)kDv + 2) * sizeof(float);
-        if (!ws || ws_bytes < need || !p.counters) return cudaErrorInvalidValue;
+        if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
         p.ws_o = static_cast<float*>(ws);
         p.ws_ml = p.ws_o + rows * s.seg_max * kDv;
     }
     sfa_mla_kernel<E><<<(unsigned)(2 * s.clusters), kThreads, MlaSmem::alloc, stream>>>(mq, p, s);
     count_launches(1);
-    return cudaGetLastError();
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess || s.seg_max == 1) return err;
+    // merge of split units; launched early (programmatic dependent launch),
+    // it waits for the main kernel's results before reading them
+    cudaLaunchConfig_t cfg = {};
+    const int64_t rows = s.units * kHeads;
+    cfg.gridDim = dim3((unsigned)((rows + 15) / 16));
+    cfg.blockDim = dim3(512);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, sfa_mla_combine<E>, p, s);
+    count_launches(1);
+    return err;
 }
 
 }  // namespace
 
 bool mla_supported(const SfaParams& p) {
     const bool prefix = (p.v == p.k) && (p.v_ss == p.k_ss);
-    return p.G == kHeads && p.Dk == kDk && p.Dv == kDv && prefix &&
-           2 * (int64_t)p.B * p.N2 * p.S1 <= kMaxCounters;
+    return p.G == kHeads && p.Dk == kDk && p.Dv == kDv && prefix;
 }
 
 size_t mla_ws_bytes(const SfaParams& p) {
