@@ -20,19 +20,23 @@
 // remainder, ~fp32 accurate).
 //
 // The tensor core reads its shared-memory operands at a limited rate, so the
-// A operands live in tensor memory: the unit's Q nope half (written by the
-// softmax threads) and P (written over the S columns it came from).  Only the
-// gathered K/V rows and the small Q rope panel are read from shared memory.
+// unit's Q nope half lives in tensor memory (the A operand of QK, written by
+// the softmax threads); only the gathered K/V rows, the small Q rope panel and
+// P are read from shared memory.  P sits in shared memory so that an S buffer
+// is free as soon as its scores are read: QK then runs two chunks ahead of PV
+// and a chunk's scores never wait behind the previous chunk's PV.
 //
-// TMEM (512 columns): Q nope [0, 128) | S/P buffer 0 [128, 192) | S/P buffer 1
+// TMEM (512 columns): Q nope [0, 128) | S buffer 0 [128, 192) | S buffer 1
 // [192, 256) | O [256, 512).
 //
-// Roles per CTA (11 warps): 8 softmax warps (two warpgroups, thread = head =
+// Roles per CTA (13 warps): 8 softmax warps (two warpgroups, thread = head =
 // TMEM lane; warpgroup w takes slots [32 w, 32 w + 32) of a chunk and O dims
 // [128 w, 128 w + 128) of the CTA's half), 1 MMA warp (rope TMA, tcgen05.mma
-// issue), 2 producer warps (cp.async gather, index prefetch, visibility
-// masks).  Work is stream-K over (unit, chunk) pairs per cluster; the parts of
-// a unit split over clusters are written as fp32 partials and merged by a
+// issue), 4 producer warps (cp.async gather, index prefetch, L2 prefetch of
+// later chunks, visibility masks).  The softmax sends chunk i + 1's partial
+// scores before computing chunk i's probabilities, so the copy overlaps that
+// work.  Work is stream-K over (unit, chunk) pairs per cluster; the parts of a
+// unit split over clusters are written as fp32 partials and merged by a
 // second kernel.
 #include <cudaTypedefs.h>
 
@@ -53,39 +57,45 @@ constexpr int kChunk = 64;
 constexpr int kHeads = 128;               // the MMA M dimension
 constexpr int kDk = 576, kDv = 512;
 constexpr int kHalfDv = 256;              // nope dims (and V / O dims) per CTA
-constexpr int kPanels = 5;                // K stage: 4 nope panels + 1 rope panel (32 dims used)
 constexpr int kStages = 3;
+constexpr int kQkAhead = 2;               // QK runs this many chunks ahead of PV
 constexpr int kSoftThreads = 256;
 constexpr int kMmaWarp = 8;
 constexpr int kProdWarp0 = 9;
-constexpr int kProdThreads = 64;
+constexpr int kProdThreads = 128;
 constexpr int kThreads = kSoftThreads + 32 + kProdThreads;
 constexpr int kTmemCols = 512;
-constexpr int kQnCol = 0, kSPCol = 128, kOCol = 256;
+constexpr int kQnCol = 0, kSCol = 128, kOCol = 256;
 constexpr int kLookahead = 6;
+constexpr int kPrefetch = 3;              // chunks ahead that the producers pull into L2
 constexpr int kNoSlot = INT_MIN;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxSeg = 8;                // clusters sharing one unit
 constexpr uint32_t kXBytes = kHeads * kChunk * 4;
 
 struct MlaSmem {
-    static constexpr int qr = 0;                            // Q rope panel: 128 rows x 128 B
-    static constexpr int kvStage = kPanels * kChunk * 128;  // 40 KB
-    static constexpr int kv = qr + kHeads * 128;
-    static constexpr int stg = kv + kStages * kvStage;      // own partial S (send), 32 KB
+    static constexpr int nopePanel = kChunk * 128;          // 64 rows x 128 B (64 dims), 128B swizzle
+    static constexpr int ropePanel = kChunk * 64;           // 64 rows x 64 B (32 dims), 64B swizzle
+    static constexpr int kvStage = 4 * nopePanel + ropePanel;   // 36 KB
+    static constexpr int kv = 0;
+    static constexpr int p = kv + kStages * kvStage;        // P high / remainder: 128 rows x 128 B each
+    static constexpr int stg = p + 2 * kHeads * 128;        // own partial S (send), 32 KB
     static constexpr int x = stg + kXBytes;                 // peer partial S (receive), 32 KB
-    static constexpr int red = x + kXBytes;                 // [2][128] row max per warpgroup
+    static constexpr int qr = x + kXBytes;                  // Q rope: 128 rows x 64 B, 64B swizzle
+    static constexpr int red = qr + kHeads * 64;            // [2][128] row max per warpgroup
     static constexpr int red2 = red + 2 * kHeads * 4;       // [2][128] row sum per warpgroup
     static constexpr int bars = red2 + 2 * kHeads * 4;
-    static constexpr int meta = bars + 16 * 8;              // [stage] uint2 visibility mask
+    static constexpr int meta = bars + 20 * 8;              // [stage][4] uint16 visibility masks
     static constexpr int misc = meta + 32;                  // tmem base, abort flag
     static constexpr int total = misc + 16;
     static constexpr int alloc = total + 1024;
 };
+static_assert(MlaSmem::kvStage % 1024 == 0 && MlaSmem::p % 1024 == 0 && MlaSmem::qr % 512 == 0,
+              "swizzle atoms must stay aligned");
 
 enum {
     B_QR_FULL = 0, B_Q_FREE = 1, B_Q_READY = 2, B_KV_FULL = 3, B_KV_FREE = 6, B_S_FULL = 9,
-    B_P_FULL = 11, B_O_DONE = 12, B_X_FULL = 13, B_X_EMPTY = 14, B_DRAIN = 15
+    B_S_FREE = 11, B_P_FULL = 13, B_O_DONE = 14, B_X_FULL = 15, B_X_EMPTY = 16, B_DRAIN = 17
 };
 
 struct MlaSched {
@@ -131,8 +141,8 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int64_t cl = blockIdx.x >> 1;
-    const int64_t c_begin = mla_range_begin(cl, sch), c_end = mla_range_begin(cl + 1, sch);
-    const int n = (int)(c_end - c_begin);
+    const int c_begin = (int)mla_range_begin(cl, sch), c_end = (int)mla_range_begin(cl + 1, sch);
+    const int n = c_end - c_begin;
     auto bar = [&](int i) { return sbase + L::bars + 8 * i; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc + 4);
 
@@ -143,11 +153,13 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         mbar_init(bar(B_Q_READY), kSoftThreads);
         mbar_init(bar(B_DRAIN), 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(B_KV_FULL + s), kProdThreads + 2);
+            mbar_init(bar(B_KV_FULL + s), kProdThreads + kProdThreads / 32);
             mbar_init(bar(B_KV_FREE + s), 1);
         }
-        mbar_init(bar(B_S_FULL), 1);
-        mbar_init(bar(B_S_FULL + 1), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_S_FULL + b), 1);
+            mbar_init(bar(B_S_FREE + b), kSoftThreads);
+        }
         mbar_init(bar(B_P_FULL), kSoftThreads);
         mbar_init(bar(B_O_DONE), 1);
         mbar_init(bar(B_X_FULL), 1);      // own arrive.expect_tx + the peer's bulk copy bytes
@@ -161,29 +173,61 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::misc);
 
     const int cpu = sch.cpu;
-    auto unit_of = [&](int64_t c) { return c / cpu; };
+    auto unit_of = [&](int c) { return c / cpu; };       // chunk counts fit in int (host check)
 
     if (warp >= kProdWarp0) {
         // ============================ producers ============================
-        // Warp pw gathers slots 32 pw .. 32 pw + 31 of every chunk: one
-        // 512-byte nope run per warp instruction (lane = 16-byte piece), then
-        // the 64-byte rope runs of the 32 rows, 8 rows per instruction.
+        // Warp pw gathers slots 16 pw .. 16 pw + 15 of every chunk: per slot
+        // one 512-byte nope run (lane = 16-byte piece), then the 64-byte rope
+        // runs of its 16 rows, 8 rows per instruction.  Lane l holds the index
+        // of slot 16 pw + l % 16.  Unit coordinates advance incrementally.
         const int pw = warp - kProdWarp0;
-        int64_t fc = c_begin;
+        const int sl = lane & 15;
+        struct Cursor {
+            int cc;
+            UCoord uc;
+            const int32_t* ig;
+            const T* kg;
+        };
+        auto point = [&](Cursor& k) {
+            k.ig = p.idx + k.uc.b * p.i_sb + k.uc.n2 * p.i_sh + k.uc.s1 * p.i_ss;
+            k.kg = static_cast<const T*>(p.k) + k.uc.b * p.k_sb + k.uc.n2 * p.k_sh;
+        };
+        auto cursor_at = [&](int c) {
+            Cursor k;
+            const int u = c / cpu;
+            k.cc = c - u * cpu;
+            k.uc = ucoord(u, p);
+            point(k);
+            return k;
+        };
+        auto advance = [&](Cursor& k) {
+            if (++k.cc < cpu) return;
+            k.cc = 0;
+            if (++k.uc.s1 == p.S1) {
+                k.uc.s1 = 0;
+                if (++k.uc.n2 == p.N2) {
+                    k.uc.n2 = 0;
+                    ++k.uc.b;
+                }
+            }
+            point(k);
+        };
+        Cursor fk = cursor_at(c_begin);                      // index fetch: kLookahead ahead
+        Cursor pk = cursor_at(c_begin);                      // L2 prefetch: kPrefetch ahead
+        Cursor k = cursor_at(c_begin);                       // the chunk being gathered
+        for (int t = 0; t < kPrefetch; ++t) advance(pk);
+        int fc = c_begin;
         auto fetch = [&]() {
             int id = kNoSlot;
             if (fc < c_end) {
-                const int64_t u = fc / cpu;
-                const int cc = (int)(fc - u * cpu);
-                const UCoord uc = ucoord(u, p);
-                const int32_t* ig = p.idx + uc.b * p.i_sb + uc.n2 * p.i_sh + uc.s1 * p.i_ss;
-                const int j = cc * kChunk + 32 * pw + lane;
-                if (j < p.topK) id = ig[j];
+                const int j = fk.cc * kChunk + 16 * pw + sl;
+                if (j < p.topK) id = fk.ig[j];
+                advance(fk);
                 ++fc;
             }
             return id;
         };
-        // indices run kLookahead chunks ahead of the gathers
         int ring[kLookahead];
 #pragma unroll
         for (int r = 0; r < kLookahead; ++r) ring[r] = fetch();
@@ -194,54 +238,69 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
 #pragma unroll
             for (int r = 0; r + 1 < kLookahead; ++r) ring[r] = ring[r + 1];
             ring[kLookahead - 1] = fetch();
-            const UCoord uc = ucoord(unit_of(c_begin + i), p);
-            const int diag = uc.s1 + (p.S2 - p.S1);
+            const int diag = k.uc.s1 + (p.S2 - p.S1);
             const bool in_range = myid >= 0 && myid < p.S2;
-            if (!in_range && myid != kNoSlot && p.validate) atomicOr(p.err_word, kErrIndexRange);
+            if (!in_range && myid != kNoSlot && p.validate && lane < 16) atomicOr(p.err_word, kErrIndexRange);
             const bool vis = in_range && !(p.causal && myid > diag);
             const int myrow = in_range ? myid : -1;
-            const T* kg = static_cast<const T*>(p.k) + uc.b * p.k_sb + uc.n2 * p.k_sh;
             unsigned char* st = smem + L::kv + s * L::kvStage;
             // nope dims [256 rank, +256): panel = lane / 8, 16-byte chunk lane % 8
-            const T* nope = kg + (int)rank * kHalfDv + 8 * lane;
+            const T* nope = k.kg + (int)rank * kHalfDv + 8 * lane;
             const int pn = lane >> 3, c = lane & 7;
 #pragma unroll 8
-            for (int r = 0; r < 32; ++r) {
+            for (int r = 0; r < 16; ++r) {
                 const int id = __shfl_sync(0xffffffffu, myrow, r);
-                const int row = 32 * pw + r;
-                cp_async_16_zfill(st + pn * (kChunk * 128) + row * 128 + ((c ^ (row & 7)) << 4),
+                const int row = 16 * pw + r;
+                cp_async_16_zfill(st + pn * L::nopePanel + row * 128 + ((c ^ (row & 7)) << 4),
                                   nope + (id >= 0 ? (int64_t)id * p.k_ss : 0), id >= 0 ? 16 : 0);
             }
-            // rope dims [512 + 32 rank, +32) -> panel 4, chunks 0..3
-            const T* rope = kg + 512 + 32 * (int)rank + 8 * (lane & 3);
+            // rope dims [512 + 32 rank, +32): 64-byte rows, chunk c at c ^ ((row / 2) % 4)
+            const T* rope = k.kg + 512 + 32 * (int)rank + 8 * (lane & 3);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
+            for (int t = 0; t < 2; ++t) {
                 const int r = 8 * t + (lane >> 2);
                 const int id = __shfl_sync(0xffffffffu, myrow, r);
-                const int row = 32 * pw + r;
-                cp_async_16_zfill(st + 4 * (kChunk * 128) + row * 128 + (((lane & 3) ^ (row & 7)) << 4),
+                const int row = 16 * pw + r;
+                cp_async_16_zfill(st + 4 * L::nopePanel + row * 64 + (((lane & 3) ^ ((row >> 1) & 3)) << 4),
                                   rope + (id >= 0 ? (int64_t)id * p.k_ss : 0), id >= 0 ? 16 : 0);
             }
             cp_async_mbar_arrive(bar(B_KV_FULL + s));
-            const uint32_t mask = __ballot_sync(0xffffffffu, vis);
+            // rows of chunk i + kPrefetch into L2 ahead of their stage being
+            // free: lane l takes slot l % 16, lines l / 16, 2 + l / 16 of its
+            // nope run and (lanes < 16) its rope line
+            if (i + kPrefetch < n) {
+                const int pid = ring[kPrefetch - 1];
+                if (pid >= 0 && pid < p.S2) {
+                    const char* rowp = reinterpret_cast<const char*>(pk.kg + (int64_t)pid * p.k_ss);
+                    prefetch_l2(rowp + 512 * (int)rank + 128 * (lane >> 4));
+                    prefetch_l2(rowp + 512 * (int)rank + 256 + 128 * (lane >> 4));
+                    if (lane < 16) prefetch_l2(rowp + 1024 + 64 * (int)rank);
+                }
+                advance(pk);
+            }
+            const uint32_t mask = __ballot_sync(0xffffffffu, vis) & 0xffffu;
             if (lane == 0) {
-                reinterpret_cast<uint32_t*>(smem + L::meta)[2 * s + pw] = mask;
+                reinterpret_cast<uint16_t*>(smem + L::meta)[4 * s + pw] = (uint16_t)mask;
                 mbar_arrive(bar(B_KV_FULL + s));
             }
+            advance(k);
         }
         // no copy may still be in flight when the warp leaves
         cp_async_wait<0>();
     } else if (warp == kMmaWarp) {
         // ============================ MMA issue ============================
+        // QK runs up to kQkAhead chunks ahead of PV inside a unit: the scores
+        // of a chunk are in tensor memory (two buffers) before the softmax
+        // asks for them, and never queue behind the previous chunk's PV.
         if (lane == 0 && n > 0) {
             tma_prefetch_map(&mq);
             uint32_t qfree_phase = 0, q_phase = 0;
             bool ok = true;
             // the unit's Q rope panel (TMA) and its Q nope half (written to
             // tensor memory by the softmax threads)
-            auto unit_q = [&](int64_t u) {
+            auto unit_q = [&](int u) {
                 const UCoord uc = ucoord(u, p);
-                mbar_arrive_expect_tx(bar(B_QR_FULL), kHeads * 128);
+                mbar_arrive_expect_tx(bar(B_QR_FULL), kHeads * 64);
                 const int c1 = sch.q_head_inner ? uc.n2 * kHeads : uc.s1;
                 const int c2 = sch.q_head_inner ? uc.s1 : uc.n2 * kHeads;
                 tma_load_4d(sbase + L::qr, &mq, 512 + 32 * (int)rank, c1, c2, uc.b, bar(B_QR_FULL));
@@ -250,57 +309,59 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
                 q_phase ^= 1;
                 tc_fence_after();
             };
-            auto qk = [&](int i) {
-                const int s = i % kStages;
-                ok = ok && mbar_wait(bar(B_KV_FULL + s), (i / kStages) & 1, p.err_word, abort_flag);
+            auto qk = [&](int j) {
+                const int s = j % kStages;
+                ok = ok && mbar_wait(bar(B_KV_FULL + s), (j / kStages) & 1, p.err_word, abort_flag);
+                if (j >= 2) ok = ok && mbar_wait(bar(B_S_FREE + (j & 1)), ((j - 2) / 2) & 1, p.err_word, abort_flag);
                 fence_proxy_async_smem();     // cp.async (generic proxy) data -> tensor core
                 tc_fence_after();
                 const uint32_t kb = sbase + L::kv + s * L::kvStage;
-                const uint32_t d = tmem + kSPCol + 64 * (i & 1);
+                const uint32_t d = tmem + kSCol + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * (kChunk * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * L::nopePanel + (kk & 3) * 32, 16, 1024);
                     tc_mma_f16_ts(d, tmem + kQnCol + 8 * kk, bd, kIdescQK, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sbase + L::qr + kk * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(kb + 4 * (kChunk * 128) + kk * 32, 16, 1024);
+                    const uint64_t ad = sdesc_sw64(sbase + L::qr + kk * 32, 512);
+                    const uint64_t bd = sdesc_sw64(kb + 4 * L::nopePanel + kk * 32, 512);
                     tc_mma_f16(d, ad, bd, kIdescQK, 1u);
                 }
-                tc_commit(bar(B_S_FULL + (i & 1)));
+                tc_commit(bar(B_S_FULL + (j & 1)));
             };
-            unit_q(unit_of(c_begin));
-            qk(0);
-            bool first_of_unit = true;
+            int unit_cur = unit_of(c_begin);
+            int unit_end = min(c_end, (unit_cur + 1) * cpu) - c_begin;   // first chunk past this unit
+            unit_q(unit_cur);
+            int next_qk = 0;
             for (int i = 0; i < n; ++i) {
+                while (next_qk < unit_end && next_qk <= i + kQkAhead) qk(next_qk++);
                 const int s = i % kStages;
-                const bool has_next = i + 1 < n;
-                const bool next_same = has_next && unit_of(c_begin + i + 1) == unit_of(c_begin + i);
-                if (next_same) qk(i + 1);
                 ok = ok && mbar_wait(bar(B_P_FULL), i & 1, p.err_word, abort_flag);
+                fence_proxy_async_smem();
                 tc_fence_after();
                 const uint32_t kb = sbase + L::kv + s * L::kvStage;
-                const uint32_t pa = tmem + kSPCol + 64 * (i & 1);
+                const bool first = (i == 0) || (c_begin + i) % cpu == 0;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kChunk / 16; ++kk) {
-                        const uint64_t bd = sdesc_sw128(kb + kk * 16 * 128, kChunk * 128, 1024);
-                        const uint32_t acc = (first_of_unit && part == 0 && kk == 0) ? 0u : 1u;
-                        tc_mma_f16_ts(tmem + kOCol, pa + 32 * part + 8 * kk, bd, kIdescPV, acc);
+                        const uint64_t ad = sdesc_sw128(sbase + L::p + part * (kHeads * 128) + kk * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(kb + kk * 16 * 128, L::nopePanel, 1024);
+                        const uint32_t acc = (first && part == 0 && kk == 0) ? 0u : 1u;
+                        tc_mma_f16(tmem + kOCol, ad, bd, kIdescPV, acc);
                     }
                 tc_commit(bar(B_O_DONE));
                 tc_commit(bar(B_KV_FREE + s));
-                first_of_unit = false;
-                if (has_next && !next_same) {
-                    // the rope panel is rewritten once every MMA of the unit is done
+                if (i + 1 == unit_end && i + 1 < n) {
+                    // the rope panel and Q columns are rewritten once every
+                    // MMA of the unit is done
                     tc_commit(bar(B_Q_FREE));
                     ok = ok && mbar_wait(bar(B_Q_FREE), qfree_phase, p.err_word, abort_flag);
                     qfree_phase ^= 1;
-                    unit_q(unit_of(c_begin + i + 1));
-                    qk(i + 1);
-                    first_of_unit = true;
+                    ++unit_cur;
+                    unit_end = min(c_end, (unit_cur + 1) * cpu) - c_begin;
+                    unit_q(unit_cur);
                 }
             }
             if (!ok) {
@@ -320,9 +381,11 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         const uint32_t xempty_peer = map_peer(bar(B_X_EMPTY), peer);
         float* red = reinterpret_cast<float*>(smem + L::red);
         float* red2 = reinterpret_cast<float*>(smem + L::red2);
+        unsigned char* p_hi = smem + L::p;
+        unsigned char* p_lo = p_hi + kHeads * 128;
         // Q nope dims [256 rank + 128 w, +128) of head r into TMEM columns
         // [64 w, 64 w + 64): two 16-bit dims per column
-        auto load_qn = [&](int64_t u) {
+        auto load_qn = [&](int u) {
             const UCoord uc = ucoord(u, p);
             const uint4* src = reinterpret_cast<const uint4*>(
                 static_cast<const T*>(p.q) + uc.b * p.q_sb + uc.s1 * p.q_ss +
@@ -341,36 +404,45 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             tc_fence_before();
             mbar_arrive(bar(B_Q_READY));
         };
-        if (n > 0) load_qn(unit_of(c_begin));
-        float m_used = -INFINITY, l = 0.f;
-        bool first_of_unit = true;
-        for (int i = 0; i < n; ++i) {
-            const int64_t c = c_begin + i;
-            const int64_t u = unit_of(c);
-            const bool last_of_unit = (i + 1 == n) || unit_of(c + 1) != u;
-            const uint32_t sp = kSPCol + 64 * (i & 1);
-            mbar_wait(bar(B_KV_FULL + i % kStages), (i / kStages) & 1, p.err_word, abort_flag);
-            mbar_wait(bar(B_S_FULL + (i & 1)), (i / 2) & 1, p.err_word, abort_flag);
+        // send(j): this CTA's partial scores of chunk j to the peer (one bulk
+        // copy from the staging buffer into the peer's receive buffer); sv
+        // keeps them for the sum
+        uint32_t sv[32];
+        auto send = [&](int j) {
+            mbar_wait(bar(B_S_FULL + (j & 1)), (j / 2) & 1, p.err_word, abort_flag);
             tc_fence_after();
-            uint32_t sv[32];
-            tmem_ld32(lane_base + sp + 32 * w, sv);
+            tmem_ld32(lane_base + kSCol + 64 * (j & 1) + 32 * w, sv);
             tmem_wait_ld();
-            // ---- exchange the partial scores with the peer CTA ----
+            tc_fence_before();
+            mbar_arrive(bar(B_S_FREE + (j & 1)));
             // the staging buffer is free once the peer has read the last copy
-            if (tid == 0 && i > 0)
-                mbar_wait_cluster(bar(B_X_EMPTY), (i - 1) & 1, p.err_word, abort_flag);
+            if (tid == 0 && j > 0)
+                mbar_wait_cluster(bar(B_X_EMPTY), (j - 1) & 1, p.err_word, abort_flag);
             named_sync(1, kSoftThreads);
             unsigned char* stg = smem + L::stg + r * 256;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4*>(stg + (((8 * w + j) ^ (r & 15)) << 4)) =
-                    make_uint4(sv[4 * j], sv[4 * j + 1], sv[4 * j + 2], sv[4 * j + 3]);
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4*>(stg + (((8 * w + q) ^ (r & 15)) << 4)) =
+                    make_uint4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
             fence_proxy_async_smem();         // generic writes -> bulk copy engine
             named_sync(1, kSoftThreads);
             if (tid == 0) {
                 mbar_arrive_expect_tx(bar(B_X_FULL), kXBytes);
                 bulk_s2cluster(x_peer, sbase + L::stg, kXBytes, xfull_peer);
             }
+        };
+        if (n > 0) {
+            load_qn(unit_of(c_begin));
+            send(0);
+        }
+        float m_used = -INFINITY, l = 0.f;
+        bool first_of_unit = true;
+        for (int i = 0; i < n; ++i) {
+            const int c = c_begin + i;
+            const int u = unit_of(c);
+            const bool last_of_unit = (i + 1 == n) || unit_of(c + 1) != u;
+            // ---- receive the peer's partial scores of chunk i ----
+            mbar_wait(bar(B_KV_FULL + i % kStages), (i / kStages) & 1, p.err_word, abort_flag);
             mbar_wait(bar(B_X_FULL), i & 1, p.err_word, abort_flag);
             const uint2 vis = reinterpret_cast<const uint2*>(smem + L::meta)[i % kStages];
             const uint32_t vw = w ? vis.y : vis.x;
@@ -378,13 +450,13 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             float s[32];
             float bmax = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 o = *reinterpret_cast<const uint4*>(xr + (((8 * w + j) ^ (r & 15)) << 4));
+            for (int q = 0; q < 8; ++q) {
+                const uint4 o = *reinterpret_cast<const uint4*>(xr + (((8 * w + q) ^ (r & 15)) << 4));
                 const float ov[4] = {__uint_as_float(o.x), __uint_as_float(o.y), __uint_as_float(o.z),
                                      __uint_as_float(o.w)};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int jj = 4 * j + e;
+                    const int jj = 4 * q + e;
                     // both CTAs add the two partials in the same (commutative) way
                     const float v = __uint_as_float(sv[jj]) + ov[e];
                     s[jj] = ((vw >> jj) & 1u) ? v * p.scale_log2 : -INFINITY;
@@ -395,6 +467,9 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             named_sync(1, kSoftThreads);      // X read by every thread, row maxima posted
             if (tid == 0) mbar_arrive_remote(xempty_peer);
             bmax = fmaxf(red[r], red[kHeads + r]);
+            // the next chunk's exchange overlaps this chunk's softmax (a new
+            // unit's first chunk waits for that unit's Q, written below)
+            if (!last_of_unit) send(i + 1);
             // ---- online softmax over the chunk (mask shared by all heads) ----
             const float m_new = fmaxf(m_used, bmax);
             const bool need = m_new > m_used + kRescaleThreshold;
@@ -414,8 +489,8 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             }
             l = l * f + lsum;                 // this warpgroup's share of the row sum
             if (i > 0) {
-                // P.V of the previous chunk is done before O is rescaled (and
-                // before this chunk's P can be consumed)
+                // P.V of the previous chunk is done before O is rescaled and
+                // before the P buffer is rewritten
                 mbar_wait(bar(B_O_DONE), (i - 1) & 1, p.err_word, abort_flag);
                 tc_fence_after();
                 if (!first_of_unit && __any_sync(0xffffffffu, need)) {
@@ -428,13 +503,18 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
                         for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
                         tmem_st32(lane_base + kOCol + 128 * w + 32 * cb, ov);
                     }
+                    tmem_wait_st();
                 }
             }
-            // P over the S columns: high parts in [sp, sp + 32), remainders in
-            // [sp + 32, sp + 64); slot j -> column j / 2
-            tmem_st16(lane_base + sp + 16 * w, hw);
-            tmem_st16(lane_base + sp + 32 + 16 * w, lw);
-            tmem_wait_st();
+            // P (K-major, 128-byte swizzle): row r, slots [32 w, 32 w + 32) =
+            // 16-byte chunks 4 w .. 4 w + 3
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int pos = r * 128 + (((4 * w + q) ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4*>(p_hi + pos) = make_uint4(hw[4 * q], hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
+                *reinterpret_cast<uint4*>(p_lo + pos) = make_uint4(lw[4 * q], lw[4 * q + 1], lw[4 * q + 2], lw[4 * q + 3]);
+            }
+            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_P_FULL));
             first_of_unit = false;
@@ -446,12 +526,12 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             red2[w * kHeads + r] = l;
             named_sync(1, kSoftThreads);
             const float lt = red2[r] + red2[kHeads + r];
-            const int64_t first = u * cpu, lastc = first + cpu - 1;
+            const int64_t first = (int64_t)u * cpu, lastc = first + cpu - 1;
             const int64_t c_lo = mla_cluster_of(first, sch), c_hi = mla_cluster_of(lastc, sch);
             const bool split = c_hi > c_lo;
             const UCoord uc = ucoord(u, p);
             const int n1 = uc.n2 * kHeads + r;
-            const int64_t row = u * kHeads + r;
+            const int64_t row = (int64_t)u * kHeads + r;
             const int64_t slot = row * sch.seg_max + (cl - c_lo);
             const bool empty = !(lt > 0.f);
             const float inv = empty ? 0.f : 1.f / lt;
@@ -493,8 +573,12 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             m_used = -INFINITY;
             l = 0.f;
             first_of_unit = true;
-            // tensor memory's Q columns are free (every MMA of the unit is done)
-            if (i + 1 < n) load_qn(u + 1);
+            // tensor memory's Q columns are free (every MMA of the unit is
+            // done): the next unit's Q, then its first chunk's exchange
+            if (i + 1 < n) {
+                load_qn(u + 1);
+                send(i + 1);
+            }
         }
         // the last copy sent to the peer has landed before this CTA can leave
         if (tid == 0 && n > 0)
@@ -588,8 +672,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 4-D map of q ordered by stride: {d, head, s1, b} when heads are adjacent
-// (BSND), else {d, s1, head, b}; box = 64 dims x 128 heads, 128-byte swizzle,
-// zero fill past Dk.
+// (BSND), else {d, s1, head, b}; box = 32 dims x 128 heads (a CTA's rope
+// dims), 64-byte swizzle.
 bool make_q_map(CUtensorMap* map, const SfaParams& p, bool bf16, bool head_inner) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -597,12 +681,12 @@ bool make_q_map(CUtensorMap* map, const SfaParams& p, bool bf16, bool head_inner
     const int64_t s_a = head_inner ? p.q_sh : p.q_ss, s_b = head_inner ? p.q_ss : p.q_sh;
     const cuuint64_t gdim[4] = {(cuuint64_t)p.Dk, n_a, n_b, (cuuint64_t)p.B};
     const cuuint64_t gstride[3] = {(cuuint64_t)s_a * 2, (cuuint64_t)s_b * 2, (cuuint64_t)p.q_sb * 2};
-    const cuuint32_t box[4] = {64, head_inner ? (cuuint32_t)kHeads : 1u,
+    const cuuint32_t box[4] = {32, head_inner ? (cuuint32_t)kHeads : 1u,
                                head_inner ? 1u : (cuuint32_t)kHeads, 1};
     const cuuint32_t estride[4] = {1, 1, 1, 1};
     return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
               const_cast<void*>(p.q), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -694,7 +778,8 @@ cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaSt
 
 bool mla_supported(const SfaParams& p) {
     const bool prefix = (p.v == p.k) && (p.v_ss == p.k_ss);
-    return p.G == kHeads && p.Dk == kDk && p.Dv == kDv && prefix;
+    const int64_t chunks = (int64_t)p.B * p.N2 * p.S1 * ((p.topK + kChunk - 1) / kChunk);
+    return p.G == kHeads && p.Dk == kDk && p.Dv == kDv && prefix && chunks < (int64_t(1) << 31);
 }
 
 size_t mla_ws_bytes(const SfaParams& p) {

@@ -35,6 +35,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// K-major operand with 64-byte swizzle: rows of 64 bytes (32 16-bit elements
+// of K), 8-row / 512-byte atoms (SBO = 512); 16-byte chunk c of row r sits at
+// chunk c ^ ((r / 2) % 4).  A K step of 16 elements advances 32 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;                                  // LBO (unused for K-major swizzled)
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)4 << 61;
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16 (fp32 accumulate):
 //   [4,6) D format (1 = f32), [7,10) A format, [10,13) B format
 //   (0 = f16, 1 = bf16), [15] A MN-major, [16] B MN-major, [17,23) N >> 3,
