@@ -19,25 +19,26 @@
 // compute O_r += P V_r for their half of Dv (P as a 16-bit high part plus
 // remainder, ~fp32 accurate).
 //
-// The tensor core reads its shared-memory operands at a limited rate, so the
-// unit's Q nope half lives in tensor memory (the A operand of QK, written by
-// the softmax threads); only the gathered K/V rows, the small Q rope panel and
-// P are read from shared memory.  P sits in shared memory so that an S buffer
-// is free as soon as its scores are read: QK then runs two chunks ahead of PV
-// and a chunk's scores never wait behind the previous chunk's PV.
+// Tensor memory holds O, three S/P buffers (a chunk's scores, then its
+// probabilities written over them as the A operand of P.V) and half of the
+// unit's Q nope dims (the other half and the rope dims are read from shared
+// memory; an MMA's A operand costs the same from either).  With three buffers
+// QK runs up to two chunks ahead of P.V, so a chunk's scores are ready when
+// the softmax wants to send them, and P(i + 1) can be written while P.V(i)
+// runs.
 //
-// TMEM (512 columns): Q nope [0, 128) | S buffer 0 [128, 192) | S buffer 1
-// [192, 256) | O [256, 512).
+// TMEM (512 columns): Q nope dims [0, 128) in [0, 64) | S/P buffers
+// [64, 128), [128, 192), [192, 256) | O [256, 512).
 //
 // Roles per CTA (13 warps): 8 softmax warps (two warpgroups, thread = head =
 // TMEM lane; warpgroup w takes slots [32 w, 32 w + 32) of a chunk and O dims
-// [128 w, 128 w + 128) of the CTA's half), 1 MMA warp (rope TMA, tcgen05.mma
-// issue), 4 producer warps (cp.async gather, index prefetch, L2 prefetch of
-// later chunks, visibility masks).  The softmax sends chunk i + 1's partial
-// scores before computing chunk i's probabilities, so the copy overlaps that
-// work.  Work is stream-K over (unit, chunk) pairs per cluster; the parts of a
-// unit split over clusters are written as fp32 partials and merged by a
-// second kernel.
+// [128 w, 128 w + 128) of the CTA's half), 1 MMA warp (Q TMA, tcgen05.mma
+// issue from an event loop), 4 producer warps (cp.async gather, index
+// prefetch, L2 prefetch of later chunks, visibility masks).  The softmax sends
+// chunk i + 1's partial scores before computing chunk i's probabilities when
+// they are ready, so the copy overlaps that work.  Work is stream-K over
+// (unit, chunk) pairs per cluster; the parts of a unit split over clusters are
+// written as fp32 partials and merged by a second kernel.
 #include <cudaTypedefs.h>
 
 #include <limits.h>
@@ -58,14 +59,14 @@ constexpr int kHeads = 128;               // the MMA M dimension
 constexpr int kDk = 576, kDv = 512;
 constexpr int kHalfDv = 256;              // nope dims (and V / O dims) per CTA
 constexpr int kStages = 3;
-constexpr int kQkAhead = 2;               // QK runs this many chunks ahead of PV
+constexpr int kBufs = 3;                  // S/P buffers in tensor memory: QK runs up to 2 chunks ahead
 constexpr int kSoftThreads = 256;
 constexpr int kMmaWarp = 8;
 constexpr int kProdWarp0 = 9;
 constexpr int kProdThreads = 128;
 constexpr int kThreads = kSoftThreads + 32 + kProdThreads;
 constexpr int kTmemCols = 512;
-constexpr int kQnCol = 0, kSCol = 128, kOCol = 256;
+constexpr int kQnCol = 0, kSCol = 64, kOCol = 256;   // Q nope dims [0, 128) | 3 S/P buffers | O
 constexpr int kLookahead = 6;
 constexpr int kPrefetch = 3;              // chunks ahead that the producers pull into L2
 constexpr int kNoSlot = INT_MIN;
@@ -78,24 +79,24 @@ struct MlaSmem {
     static constexpr int ropePanel = kChunk * 64;           // 64 rows x 64 B (32 dims), 64B swizzle
     static constexpr int kvStage = 4 * nopePanel + ropePanel;   // 36 KB
     static constexpr int kv = 0;
-    static constexpr int p = kv + kStages * kvStage;        // P high / remainder: 128 rows x 128 B each
-    static constexpr int stg = p + 2 * kHeads * 128;        // own partial S (send), 32 KB
+    static constexpr int stg = kv + kStages * kvStage;      // own partial S (send), 32 KB
     static constexpr int x = stg + kXBytes;                 // peer partial S (receive), 32 KB
-    static constexpr int qr = x + kXBytes;                  // Q rope: 128 rows x 64 B, 64B swizzle
+    static constexpr int qn = x + kXBytes;                  // Q nope dims [128, 256): 2 panels x 128 rows x 128 B
+    static constexpr int qr = qn + 2 * kHeads * 128;        // Q rope: 128 rows x 64 B, 64B swizzle
     static constexpr int red = qr + kHeads * 64;            // [2][128] row max per warpgroup
     static constexpr int red2 = red + 2 * kHeads * 4;       // [2][128] row sum per warpgroup
     static constexpr int bars = red2 + 2 * kHeads * 4;
-    static constexpr int meta = bars + 20 * 8;              // [stage][4] uint16 visibility masks
-    static constexpr int misc = meta + 32;                  // tmem base, abort flag
+    static constexpr int meta = bars + 24 * 8;              // [stage][4] uint16 visibility masks
+    static constexpr int misc = meta + kStages * 8;         // tmem base, abort flag, early-send flag
     static constexpr int total = misc + 16;
     static constexpr int alloc = total + 1024;
 };
-static_assert(MlaSmem::kvStage % 1024 == 0 && MlaSmem::p % 1024 == 0 && MlaSmem::qr % 512 == 0,
+static_assert(MlaSmem::kvStage % 1024 == 0 && MlaSmem::qn % 1024 == 0 && MlaSmem::qr % 1024 == 0,
               "swizzle atoms must stay aligned");
 
 enum {
     B_QR_FULL = 0, B_Q_FREE = 1, B_Q_READY = 2, B_KV_FULL = 3, B_KV_FREE = 6, B_S_FULL = 9,
-    B_S_FREE = 11, B_P_FULL = 13, B_O_DONE = 14, B_X_FULL = 15, B_X_EMPTY = 16, B_DRAIN = 17
+    B_P_FULL = 12, B_O_DONE = 15, B_UNIT_DONE = 18, B_X_FULL = 19, B_X_EMPTY = 20, B_DRAIN = 21
 };
 
 struct MlaSched {
@@ -127,7 +128,8 @@ __device__ __forceinline__ UCoord ucoord(int64_t u, const SfaParams& p) {
 
 template <class E>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const MlaSched sch) {
+sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mqr,
+               const SfaParams p, const MlaSched sch) {
     using T = typename E::T;
     using L = MlaSmem;
     constexpr bool kBf16 = std::is_same<E, BF16>::value;
@@ -156,12 +158,12 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             mbar_init(bar(B_KV_FULL + s), kProdThreads + kProdThreads / 32);
             mbar_init(bar(B_KV_FREE + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kBufs; ++b) {
             mbar_init(bar(B_S_FULL + b), 1);
-            mbar_init(bar(B_S_FREE + b), kSoftThreads);
+            mbar_init(bar(B_P_FULL + b), kSoftThreads);
+            mbar_init(bar(B_O_DONE + b), 1);
         }
-        mbar_init(bar(B_P_FULL), kSoftThreads);
-        mbar_init(bar(B_O_DONE), 1);
+        mbar_init(bar(B_UNIT_DONE), 1);
         mbar_init(bar(B_X_FULL), 1);      // own arrive.expect_tx + the peer's bulk copy bytes
         mbar_init(bar(B_X_EMPTY), 1);     // the peer has read what this CTA sent it
         fence_barrier_init();
@@ -289,21 +291,27 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         cp_async_wait<0>();
     } else if (warp == kMmaWarp) {
         // ============================ MMA issue ============================
-        // QK runs up to kQkAhead chunks ahead of PV inside a unit: the scores
-        // of a chunk are in tensor memory (two buffers) before the softmax
-        // asks for them, and never queue behind the previous chunk's PV.
+        // QK(j) may be issued once PV(j - 3) is (its S/P buffer j % 3 is then
+        // free in pipe order): QK(i + 1) is required before P(i) can exist,
+        // QK(i + 2) goes in when its rows have landed; PV(i) as soon as P(i)
+        // is there.  An event loop, so that a later chunk's gather never
+        // holds up a ready PV.
         if (lane == 0 && n > 0) {
             tma_prefetch_map(&mq);
+            tma_prefetch_map(&mqr);
             uint32_t qfree_phase = 0, q_phase = 0;
             bool ok = true;
             // the unit's Q rope panel (TMA) and its Q nope half (written to
             // tensor memory by the softmax threads)
             auto unit_q = [&](int u) {
                 const UCoord uc = ucoord(u, p);
-                mbar_arrive_expect_tx(bar(B_QR_FULL), kHeads * 64);
+                mbar_arrive_expect_tx(bar(B_QR_FULL), kHeads * 64 + 2 * kHeads * 128);
                 const int c1 = sch.q_head_inner ? uc.n2 * kHeads : uc.s1;
                 const int c2 = sch.q_head_inner ? uc.s1 : uc.n2 * kHeads;
-                tma_load_4d(sbase + L::qr, &mq, 512 + 32 * (int)rank, c1, c2, uc.b, bar(B_QR_FULL));
+                tma_load_4d(sbase + L::qr, &mqr, 512 + 32 * (int)rank, c1, c2, uc.b, bar(B_QR_FULL));
+                for (int pn = 0; pn < 2; ++pn)
+                    tma_load_4d(sbase + L::qn + pn * (kHeads * 128), &mq, (int)rank * kHalfDv + 128 + 64 * pn,
+                                c1, c2, uc.b, bar(B_QR_FULL));
                 ok = ok && mbar_wait(bar(B_QR_FULL), q_phase, p.err_word, abort_flag);
                 ok = ok && mbar_wait(bar(B_Q_READY), q_phase, p.err_word, abort_flag);
                 q_phase ^= 1;
@@ -312,15 +320,21 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             auto qk = [&](int j) {
                 const int s = j % kStages;
                 ok = ok && mbar_wait(bar(B_KV_FULL + s), (j / kStages) & 1, p.err_word, abort_flag);
-                if (j >= 2) ok = ok && mbar_wait(bar(B_S_FREE + (j & 1)), ((j - 2) / 2) & 1, p.err_word, abort_flag);
                 fence_proxy_async_smem();     // cp.async (generic proxy) data -> tensor core
                 tc_fence_after();
                 const uint32_t kb = sbase + L::kv + s * L::kvStage;
-                const uint32_t d = tmem + kSCol + 64 * (j & 1);
+                const uint32_t d = tmem + kSCol + 64 * (j % kBufs);
+                // nope dims [0, 128): A from tensor memory; [128, 256): A from shared memory
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
+                for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * L::nopePanel + (kk & 3) * 32, 16, 1024);
                     tc_mma_f16_ts(d, tmem + kQnCol + 8 * kk, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 8; kk < 16; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sbase + L::qn + ((kk - 8) >> 2) * (kHeads * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * L::nopePanel + (kk & 3) * 32, 16, 1024);
+                    tc_mma_f16(d, ad, bd, kIdescQK, 1u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
@@ -328,40 +342,69 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
                     const uint64_t bd = sdesc_sw64(kb + 4 * L::nopePanel + kk * 32, 512);
                     tc_mma_f16(d, ad, bd, kIdescQK, 1u);
                 }
-                tc_commit(bar(B_S_FULL + (j & 1)));
+                tc_commit(bar(B_S_FULL + j % kBufs));
             };
             int unit_cur = unit_of(c_begin);
             int unit_end = min(c_end, (unit_cur + 1) * cpu) - c_begin;   // first chunk past this unit
             unit_q(unit_cur);
             int next_qk = 0;
-            for (int i = 0; i < n; ++i) {
-                while (next_qk < unit_end && next_qk <= i + kQkAhead) qk(next_qk++);
+            uint64_t idle_since = 0;
+            for (int i = 0; i < n && ok;) {
+                if (next_qk < unit_end && next_qk <= i + 1) {
+                    qk(next_qk++);
+                    continue;
+                }
+                if (next_qk < unit_end && next_qk == i + 2 &&
+                    mbar_try_wait(bar(B_KV_FULL + next_qk % kStages), (next_qk / kStages) & 1)) {
+                    qk(next_qk++);
+                    continue;
+                }
+                if (!mbar_try_wait(bar(B_P_FULL + i % kBufs), (i / kBufs) & 1)) {
+                    // nothing to issue yet: poll, with the same bound as the waits
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    const uint64_t now = global_timer_ns();
+                    if (idle_since == 0) {
+                        idle_since = now;
+                    } else if (now - idle_since > 2000000000ull) {
+                        atomicOr(p.err_word, kErrWaitTimeout);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    continue;
+                }
+                idle_since = 0;
                 const int s = i % kStages;
-                ok = ok && mbar_wait(bar(B_P_FULL), i & 1, p.err_word, abort_flag);
-                fence_proxy_async_smem();
                 tc_fence_after();
                 const uint32_t kb = sbase + L::kv + s * L::kvStage;
+                const uint32_t pa = tmem + kSCol + 64 * (i % kBufs);
                 const bool first = (i == 0) || (c_begin + i) % cpu == 0;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kChunk / 16; ++kk) {
-                        const uint64_t ad = sdesc_sw128(sbase + L::p + part * (kHeads * 128) + kk * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(kb + kk * 16 * 128, L::nopePanel, 1024);
                         const uint32_t acc = (first && part == 0 && kk == 0) ? 0u : 1u;
-                        tc_mma_f16(tmem + kOCol, ad, bd, kIdescPV, acc);
+                        tc_mma_f16_ts(tmem + kOCol, pa + 32 * part + 8 * kk, bd, kIdescPV, acc);
                     }
-                tc_commit(bar(B_O_DONE));
+                tc_commit(bar(B_O_DONE + i % kBufs));
                 tc_commit(bar(B_KV_FREE + s));
-                if (i + 1 == unit_end && i + 1 < n) {
-                    // the rope panel and Q columns are rewritten once every
-                    // MMA of the unit is done
-                    tc_commit(bar(B_Q_FREE));
-                    ok = ok && mbar_wait(bar(B_Q_FREE), qfree_phase, p.err_word, abort_flag);
-                    qfree_phase ^= 1;
-                    ++unit_cur;
-                    unit_end = min(c_end, (unit_cur + 1) * cpu) - c_begin;
-                    unit_q(unit_cur);
+                ++i;
+                if (i == unit_end) {
+                    tc_commit(bar(B_UNIT_DONE));   // the unit's O is final
+                    if (i < n) {
+                        // the rope panel and Q columns are rewritten once
+                        // every MMA of the unit is done
+                        tc_commit(bar(B_Q_FREE));
+                        ok = ok && mbar_wait(bar(B_Q_FREE), qfree_phase, p.err_word, abort_flag);
+                        qfree_phase ^= 1;
+                        ++unit_cur;
+                        unit_end = min(c_end, (unit_cur + 1) * cpu) - c_begin;
+                        unit_q(unit_cur);
+                    }
                 }
             }
             if (!ok) {
@@ -381,25 +424,22 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         const uint32_t xempty_peer = map_peer(bar(B_X_EMPTY), peer);
         float* red = reinterpret_cast<float*>(smem + L::red);
         float* red2 = reinterpret_cast<float*>(smem + L::red2);
-        unsigned char* p_hi = smem + L::p;
-        unsigned char* p_lo = p_hi + kHeads * 128;
-        // Q nope dims [256 rank + 128 w, +128) of head r into TMEM columns
-        // [64 w, 64 w + 64): two 16-bit dims per column
+        volatile int* early_flag = reinterpret_cast<volatile int*>(smem + L::misc + 8);
+        // Q nope dims [256 rank + 64 w, +64) of head r into TMEM columns
+        // [32 w, 32 w + 32): two 16-bit dims per column (dims [128, 256) of
+        // the CTA's half come by TMA into shared memory)
         auto load_qn = [&](int u) {
             const UCoord uc = ucoord(u, p);
             const uint4* src = reinterpret_cast<const uint4*>(
                 static_cast<const T*>(p.q) + uc.b * p.q_sb + uc.s1 * p.q_ss +
-                (int64_t)(uc.n2 * kHeads + r) * p.q_sh + (int)rank * kHalfDv + 128 * w);
+                (int64_t)(uc.n2 * kHeads + r) * p.q_sh + (int)rank * kHalfDv + 64 * w);
+            uint32_t v[32];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t v[32];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 x = __ldg(src + 8 * half + j);
-                    v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
-                }
-                tmem_st32(lane_base + kQnCol + 64 * w + 32 * half, v);
+            for (int j = 0; j < 8; ++j) {
+                const uint4 x = __ldg(src + j);
+                v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
             }
+            tmem_st32(lane_base + kQnCol + 32 * w, v);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(B_Q_READY));
@@ -409,12 +449,10 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         // keeps them for the sum
         uint32_t sv[32];
         auto send = [&](int j) {
-            mbar_wait(bar(B_S_FULL + (j & 1)), (j / 2) & 1, p.err_word, abort_flag);
+            mbar_wait(bar(B_S_FULL + j % kBufs), (j / kBufs) & 1, p.err_word, abort_flag);
             tc_fence_after();
-            tmem_ld32(lane_base + kSCol + 64 * (j & 1) + 32 * w, sv);
+            tmem_ld32(lane_base + kSCol + 64 * (j % kBufs) + 32 * w, sv);
             tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(B_S_FREE + (j & 1)));
             // the staging buffer is free once the peer has read the last copy
             if (tid == 0 && j > 0)
                 mbar_wait_cluster(bar(B_X_EMPTY), (j - 1) & 1, p.err_word, abort_flag);
@@ -437,6 +475,7 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         }
         float m_used = -INFINITY, l = 0.f;
         bool first_of_unit = true;
+        uint32_t unit_phase = 0;
         for (int i = 0; i < n; ++i) {
             const int c = c_begin + i;
             const int u = unit_of(c);
@@ -464,12 +503,17 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
                 }
             }
             red[w * kHeads + r] = bmax;
+            // send chunk i + 1 before this chunk's softmax when its scores are
+            // already computed (the copy then overlaps the work below), else
+            // after P(i) is out; a new unit's first chunk waits for that unit's
+            // Q, written in the epilogue
+            if (tid == 0)
+                *early_flag = !last_of_unit && mbar_try_wait(bar(B_S_FULL + (i + 1) % kBufs), ((i + 1) / kBufs) & 1);
             named_sync(1, kSoftThreads);      // X read by every thread, row maxima posted
             if (tid == 0) mbar_arrive_remote(xempty_peer);
             bmax = fmaxf(red[r], red[kHeads + r]);
-            // the next chunk's exchange overlaps this chunk's softmax (a new
-            // unit's first chunk waits for that unit's Q, written below)
-            if (!last_of_unit) send(i + 1);
+            const bool early = *early_flag != 0;
+            if (early) send(i + 1);
             // ---- online softmax over the chunk (mask shared by all heads) ----
             const float m_new = fmaxf(m_used, bmax);
             const bool need = m_new > m_used + kRescaleThreshold;
@@ -488,40 +532,41 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
                 lw[e] = E::pack2(p0 - h.x, p1 - h.y);
             }
             l = l * f + lsum;                 // this warpgroup's share of the row sum
-            if (i > 0) {
-                // P.V of the previous chunk is done before O is rescaled and
-                // before the P buffer is rewritten
-                mbar_wait(bar(B_O_DONE), (i - 1) & 1, p.err_word, abort_flag);
+            if (!first_of_unit && __any_sync(0xffffffffu, need)) {
+                // O is rescaled once P.V of the previous chunk is done: its
+                // buffer's barrier, whose previous use (chunk i - 4) is done
+                // and whose next (chunk i + 2) cannot be, so the phase is
+                // unambiguous.
+                const int pb = (i - 1) % kBufs;
+                mbar_wait(bar(B_O_DONE + pb), ((i - 1) / kBufs) & 1, p.err_word, abort_flag);
                 tc_fence_after();
-                if (!first_of_unit && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                    for (int cb = 0; cb < 4; ++cb) {
-                        uint32_t ov[32];
-                        tmem_ld32(lane_base + kOCol + 128 * w + 32 * cb, ov);
-                        tmem_wait_ld();
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t ov[32];
+                    tmem_ld32(lane_base + kOCol + 128 * w + 32 * cb, ov);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
-                        tmem_st32(lane_base + kOCol + 128 * w + 32 * cb, ov);
-                    }
-                    tmem_wait_st();
+                    for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
+                    tmem_st32(lane_base + kOCol + 128 * w + 32 * cb, ov);
                 }
             }
-            // P (K-major, 128-byte swizzle): row r, slots [32 w, 32 w + 32) =
-            // 16-byte chunks 4 w .. 4 w + 3
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int pos = r * 128 + (((4 * w + q) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(p_hi + pos) = make_uint4(hw[4 * q], hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
-                *reinterpret_cast<uint4*>(p_lo + pos) = make_uint4(lw[4 * q], lw[4 * q + 1], lw[4 * q + 2], lw[4 * q + 3]);
-            }
-            fence_proxy_async_smem();
+            // P over the S columns of its chunk: high parts in [sp, sp + 32),
+            // remainders in [sp + 32, sp + 64); slot j -> column j / 2
+            const uint32_t sp = kSCol + 64 * (i % kBufs);
+            tmem_st16(lane_base + sp + 16 * w, hw);
+            tmem_st16(lane_base + sp + 32 + 16 * w, lw);
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(B_P_FULL));
+            mbar_arrive(bar(B_P_FULL + i % kBufs));
             first_of_unit = false;
-            if (!last_of_unit) continue;
+            if (!last_of_unit) {
+                if (!early) send(i + 1);
+                continue;
+            }
 
             // ---- epilogue of unit u: dims [256 rank + 128 w, +128) ----
-            mbar_wait(bar(B_O_DONE), i & 1, p.err_word, abort_flag);
+            mbar_wait(bar(B_UNIT_DONE), unit_phase, p.err_word, abort_flag);
+            unit_phase ^= 1;
             tc_fence_after();
             red2[w * kHeads + r] = l;
             named_sync(1, kSoftThreads);
@@ -671,23 +716,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D map of q ordered by stride: {d, head, s1, b} when heads are adjacent
-// (BSND), else {d, s1, head, b}; box = 32 dims x 128 heads (a CTA's rope
-// dims), 64-byte swizzle.
-bool make_q_map(CUtensorMap* map, const SfaParams& p, bool bf16, bool head_inner) {
+// 4-D maps of q ordered by stride: {d, head, s1, b} when heads are adjacent
+// (BSND), else {d, s1, head, b}.  Box = `box_d` dims x 128 heads: 64 dims with
+// 128-byte swizzle (Q nope panels) or 32 dims with 64-byte swizzle (a CTA's
+// rope dims).
+bool make_q_map(CUtensorMap* map, const SfaParams& p, bool bf16, bool head_inner, int box_d) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t n_a = head_inner ? p.N1 : p.S1, n_b = head_inner ? p.S1 : p.N1;
     const int64_t s_a = head_inner ? p.q_sh : p.q_ss, s_b = head_inner ? p.q_ss : p.q_sh;
     const cuuint64_t gdim[4] = {(cuuint64_t)p.Dk, n_a, n_b, (cuuint64_t)p.B};
     const cuuint64_t gstride[3] = {(cuuint64_t)s_a * 2, (cuuint64_t)s_b * 2, (cuuint64_t)p.q_sb * 2};
-    const cuuint32_t box[4] = {32, head_inner ? (cuuint32_t)kHeads : 1u,
+    const cuuint32_t box[4] = {(cuuint32_t)box_d, head_inner ? (cuuint32_t)kHeads : 1u,
                                head_inner ? 1u : (cuuint32_t)kHeads, 1};
     const cuuint32_t estride[4] = {1, 1, 1, 1};
     return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
               const_cast<void*>(p.q), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              box_d == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Per-device setup of the MLA kernel (cached): the shared-memory opt-in and
@@ -723,8 +769,10 @@ cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaSt
     if (resident < 1) return cudaErrorInvalidConfiguration;
     MlaSched s;
     s.q_head_inner = p.q_sh <= p.q_ss ? 1 : 0;
-    CUtensorMap mq;
-    if (!make_q_map(&mq, p, std::is_same<E, BF16>::value, s.q_head_inner != 0))
+    CUtensorMap mq, mqr;
+    const bool bf16 = std::is_same<E, BF16>::value;
+    if (!make_q_map(&mq, p, bf16, s.q_head_inner != 0, 64) ||
+        !make_q_map(&mqr, p, bf16, s.q_head_inner != 0, 32))
         return cudaErrorInvalidValue;
     s.cpu = (p.topK + kChunk - 1) / kChunk;
     s.units = (int64_t)p.B * p.N2 * p.S1;
@@ -753,7 +801,7 @@ cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaSt
         p.ws_o = static_cast<float*>(ws);
         p.ws_ml = p.ws_o + rows * s.seg_max * kDv;
     }
-    sfa_mla_kernel<E><<<(unsigned)(2 * s.clusters), kThreads, MlaSmem::alloc, stream>>>(mq, p, s);
+    sfa_mla_kernel<E><<<(unsigned)(2 * s.clusters), kThreads, MlaSmem::alloc, stream>>>(mq, mqr, p, s);
     count_launches(1);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || s.seg_max == 1) return err;
