@@ -51,6 +51,9 @@ def parse():
                     choices=sorted(synth.SFA_WORKLOADS) + sorted(synth.BSR_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--replicas", type=int, default=0,
+                    help="input replicas rotated over the steps (0 = enough to exceed L2 4x; "
+                         "1 keeps a profiling capture small)")
     return ap.parse_args()
 
 
@@ -142,27 +145,46 @@ class ClockSampler:
 # traffic figure from a committed ncu summary (only while the kernel source
 # it was taken on is unchanged)
 
-def kernel_source_sha():
+def kernel_source_sha(files):
+    """sha256 over the named kernel sources (file name + bytes, in order)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_serving_sfa_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in files:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()
 
 
 def committed_traffic(workload):
-    path = os.path.join(ROOT, "profiles", f"{workload}_traffic.txt")
+    """DRAM bytes per launch of the workload's main kernel from its committed
+    ncu summary (profiles/<workload>_ncu.md), or None when the summary is
+    missing or its kernel sources have changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{workload}_ncu.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    sha = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
-    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not sha or not val or sha.group(1) != kernel_source_sha():
+    src = re.search(r"^sources:\s*(.+)$", text, re.M)
+    sha = re.search(r"^source_sha256:\s*([0-9a-f]+)", text, re.M)
+    val = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    if not src or not sha or not val:
+        return None
+    try:
+        if sha.group(1) != kernel_source_sha(src.group(1).split()):
+            return None
+    except OSError:
         return None
     return float(val.group(1))
+
+
+# main kernel of each top-K workload (what the roofline object describes)
+MAIN_KERNEL = {
+    "tiny": "generic top-K kernel",
+    "gqa_decode": "sfa_decode_kernel (one launch per sfa_run_ex call; split index lists merged in-kernel)",
+    "sparse_prefill": "sfa_decode_kernel (one launch per sfa_run_ex call; split index lists merged in-kernel)",
+    "mla_decode": "sfa_mla_kernel + sfa_mla_combine (two launches per sfa_run_ex call; time is the call's)",
+    "mla_mtp": "sfa_mla_kernel + sfa_mla_combine (two launches per sfa_run_ex call; time is the call's)",
+}
 
 
 # ---------------------------------------------------------------------------
@@ -223,7 +245,7 @@ def run_bsr(args, rank, world, local):
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
            "roofline": {"bound": "tensor", "achieved": tflops,
                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                        "frac": tflops / peaks["bf16_tflops_sustained"], "traffic": None,
+                        "frac": tflops / peaks["bf16_tflops_sustained"], "traffic": committed_traffic("bsr"),
                         "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 dense rate is the same)",
                         "kernel": "bsr_tc_kernel (one launch per bsr_run)"},
            "gpu_launches": launches, "clocks": clocks,
@@ -250,7 +272,7 @@ def run_ours(args, rank, world, local):
     # copies, and the replicas' gathered bytes together exceed L2 several
     # times, so every step gathers from HBM (no flush needed between steps).
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    reps = max(2, -(-4 * l2 // counts["gathered_bytes"]) + 1)
+    reps = args.replicas if args.replicas > 0 else max(2, -(-4 * l2 // counts["gathered_bytes"]) + 1)
     replicas = []
     for _ in range(reps):
         d = {"q": host["q"].cuda(), "k": host["k"].cuda(), "idx": host["idx"].cuda()}
@@ -347,20 +369,21 @@ def run_ours(args, rank, world, local):
     roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": gbs / peaks["hbm_gbs"], "traffic": committed_traffic(args.workload),
                 "peak_source": f"{peak_src} hbm_gbs (copy, read+write bytes)",
-                "kernel": "one sfa_run_ex call = one launch of the path's kernel "
-                          "(in-kernel merge of split index lists), CUDA events on its stream"}
+                "kernel": MAIN_KERNEL.get(args.workload, "sfa_run_ex call") + "; CUDA events on its stream"}
     t_roof = max(counts["gathered_bytes"] / (peaks["hbm_gbs"] * 1e9),
                  counts["flops"] / (peaks["bf16_tflops"] * 1e12))
     cfg = config_of(case, world)
-    cfg["l2"] = (f"not flushed: {reps} rotating input replicas, "
-                 f"{reps * counts['gathered_bytes'] >> 20} MiB gathered per rotation > L2 "
-                 f"{l2 >> 20} MiB")
+    rot = reps * counts["gathered_bytes"]
+    cfg["l2"] = (f"not flushed: {reps} rotating input replicas, {rot >> 20} MiB gathered per "
+                 f"rotation {'>' if rot > l2 else '<='} L2 {l2 >> 20} MiB"
+                 + ("" if rot > l2 else " (profiling run: not a valid timing)"))
     res = {"metric": METRIC, "value": world * gbs, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": dtype_name(case), "data": "synthetic (seeded generator, shapes of the workload)",
            "config": cfg,
            "tflops": world * tflops, "us_per_call": ms * 1e3,
+           "tensor_frac": tflops / peaks["bf16_tflops"],
            "roofline_time_frac": t_roof / (ms * 1e-3),
            "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
            "clocks": clocks, "wall_s_timed_loop": wall,
