@@ -108,6 +108,25 @@ int bsr_tc_rows_per_item(int Hq, int Hkv);
 cudaError_t launch_bsr_tc(const BsrParams& p, const void* items, int nitems, int* err_word,
                           sfa_dtype dtype, cudaStream_t stream);
 
+// Launches `kern` with programmatic dependent launch allowed: the grid may be
+// scheduled while the previous kernel in the stream finishes; the kernel must
+// call griddepcontrol.wait before its first global-memory access.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Device address of the library's error word on the current device.
 int* device_error_word();
 

@@ -204,6 +204,11 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
         fence_barrier_init();
     }
     fence_proxy_async_smem();    // zero fill above precedes later bulk copies
+    // launched with programmatic dependent launch: nothing above touches
+    // global memory; wait here for the previous grid in the stream (its
+    // writes are then visible), and let the next one start launching
+    grid_dependency_wait();
+    grid_launch_dependents();
     __syncthreads();
 
     if (warp >= kConsWarps) {
@@ -585,9 +590,9 @@ cudaError_t run_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaStrea
         p.ws_o = static_cast<float*>(ws);
         p.ws_ml = p.ws_o + rows * s.seg_max * p.Dv;
     }
-    kern<<<s.ctas, kThreads, L::total, stream>>>(p, s);
+    err = launch_pdl(kern, dim3(s.ctas), dim3(kThreads), L::total, stream, p, s);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 template <class E, int DK, int DV, bool VK>

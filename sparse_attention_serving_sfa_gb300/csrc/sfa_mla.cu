@@ -168,6 +168,11 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         mbar_init(bar(B_X_EMPTY), 1);     // the peer has read what this CTA sent it
         fence_barrier_init();
     }
+    // launched with programmatic dependent launch: nothing above touches
+    // global memory; wait here for the previous grid in the stream, and let
+    // the next one (the merge, or the next call) start launching
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (warp == kMmaWarp) tmem_alloc(sbase + L::misc, kTmemCols);
     tc_fence_before();
     cluster_sync();      // both CTAs' barriers exist before any remote access
@@ -645,6 +650,7 @@ template <class E>
 __global__ void __launch_bounds__(512) sfa_mla_combine(const SfaParams p, const MlaSched sch) {
     using T = typename E::T;
     grid_dependency_wait();
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (row >= sch.units * kHeads) return;
@@ -801,23 +807,14 @@ cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaSt
         p.ws_o = static_cast<float*>(ws);
         p.ws_ml = p.ws_o + rows * s.seg_max * kDv;
     }
-    sfa_mla_kernel<E><<<(unsigned)(2 * s.clusters), kThreads, MlaSmem::alloc, stream>>>(mq, mqr, p, s);
+    cudaError_t err = launch_pdl(sfa_mla_kernel<E>, dim3((unsigned)(2 * s.clusters)), dim3(kThreads),
+                                 (size_t)MlaSmem::alloc, stream, mq, mqr, p, s);
     count_launches(1);
-    cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || s.seg_max == 1) return err;
     // merge of split units; launched early (programmatic dependent launch),
     // it waits for the main kernel's results before reading them
-    cudaLaunchConfig_t cfg = {};
     const int64_t rows = s.units * kHeads;
-    cfg.gridDim = dim3((unsigned)((rows + 15) / 16));
-    cfg.blockDim = dim3(512);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, sfa_mla_combine<E>, p, s);
+    err = launch_pdl(sfa_mla_combine<E>, dim3((unsigned)((rows + 15) / 16)), dim3(512), 0, stream, p, s);
     count_launches(1);
     return err;
 }
