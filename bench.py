@@ -64,6 +64,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, world, device):
+    """The largest of every rank's value (the slowest rank's step time):
+    an all-reduce MAX over the default process group (no-op for one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, ms, world):
+    """Units processed by all ranks together per second, each rank running an
+    independent replica of the workload and the step time being the max over
+    ranks (weak scaling)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -227,14 +245,11 @@ def run_bsr(args, rank, world, local):
     torch.cuda.synchronize()
     launches = sfa.sfa_kernel_launches() - launches0
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, "cuda")
     peaks, peak_src = load_peaks()
     tflops = counts["flops"] / (ms * 1e-3) / 1e12
-    res = {"metric": METRIC, "value": world * tflops, "unit": "TFLOP/s", "n_gpus": world,
+    res = {"metric": METRIC, "value": whole_job_rate(counts["flops"], ms, world) / 1e12,
+           "unit": "TFLOP/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": case.dtype, "data": "synthetic (seeded generator, shapes of the workload)",
@@ -319,11 +334,7 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, "cuda")
 
     # end to end through the same entry point with host buffers: every step
     # copies its q and indices from pinned host memory and reads the output
@@ -353,14 +364,10 @@ def run_ours(args, rank, world, local):
             e2e_step(i)
         ev1.record(stream)
         torch.cuda.synchronize()
-        e_ms = ev0.elapsed_time(ev1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(ev0.elapsed_time(ev1) / n_e2e, world, "cuda")
         h2d = hq.numel() * hq.element_size() + hidx.numel() * 4
         d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
-        e2e = {"value": world * counts["gathered_bytes"] / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+        e2e = {"value": whole_job_rate(counts["gathered_bytes"], e_ms, world) / 1e9, "unit": UNIT,
                "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     peaks, peak_src = load_peaks()
@@ -377,7 +384,8 @@ def run_ours(args, rank, world, local):
     cfg["l2"] = (f"not flushed: {reps} rotating input replicas, {rot >> 20} MiB gathered per "
                  f"rotation {'>' if rot > l2 else '<='} L2 {l2 >> 20} MiB"
                  + ("" if rot > l2 else " (profiling run: not a valid timing)"))
-    res = {"metric": METRIC, "value": world * gbs, "unit": UNIT, "n_gpus": world,
+    res = {"metric": METRIC, "value": whole_job_rate(counts["gathered_bytes"], ms, world) / 1e9,
+           "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": dtype_name(case), "data": "synthetic (seeded generator, shapes of the workload)",
@@ -464,11 +472,17 @@ def run_reference(args, rank, world):
             "gpu_launches": 0}
 
 
+def reference_runs_on(rank):
+    """The reference arm (the CPU oracle) runs on rank 0 only; other ranks
+    exit without work."""
+    return rank == 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
-        if rank != 0:
+        if not reference_runs_on(rank):
             return 0
         print(json.dumps(run_reference(args, rank, world)))
         return 0
