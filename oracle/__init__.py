@@ -55,6 +55,11 @@ def load_library(path: str):
     lib.oracle_bsr.restype = ci
     lib.oracle_bsr_rows.argtypes = bsr_common + [vp, i64, vp, vp]
     lib.oracle_bsr_rows.restype = ci
+    bsr_ex = [vp, vp, vp, vp, vp, vp, ci] + bsr_common[5:]
+    lib.oracle_bsr_ex.argtypes = bsr_ex + [vp, vp]
+    lib.oracle_bsr_ex.restype = ci
+    lib.oracle_bsr_rows_ex.argtypes = bsr_ex + [vp, i64, vp, vp]
+    lib.oracle_bsr_rows_ex.restype = ci
     return lib
 
 
@@ -160,8 +165,27 @@ def sfa_rows(q, k, v, idx, scale, rows, layout="BSND", causal=False):
     return y, lse
 
 
-def bsr(q, k, v, indptr, indices, M, N, R, C, scale):
-    """Block-sparse attention, NHD tensors.  Returns (y (M,Hq,d), lse (M,Hq))."""
+def pack_mask(mask):
+    """plan()'s `mask` (nnz, R, C) bool as the packed bytes the oracle reads:
+    flattened, most significant bit first within each byte."""
+    m = np.ascontiguousarray(np.asarray(mask, dtype=bool).reshape(-1))
+    return np.packbits(m, bitorder="big")
+
+
+def _mask_args(mask, packed_mask):
+    if packed_mask is not None:
+        pm = np.ascontiguousarray(packed_mask, dtype=np.uint8)
+    elif mask is not None:
+        pm = pack_mask(mask)
+    else:
+        return None, 0
+    return pm, pm.ctypes.data
+
+
+def bsr(q, k, v, indptr, indices, M, N, R, C, scale, mask=None, packed_mask=None, causal=False):
+    """Block-sparse attention, NHD tensors.  Returns (y (M,Hq,d), lse (M,Hq)).
+    mask: (nnz, R, C) bool per stored block (or packed_mask bytes); causal
+    applies only without a mask."""
     Hq, d = q.shape[1], q.shape[2]
     Hkv = k.shape[1]
     indptr = indptr.to(torch.int32).contiguous()
@@ -169,13 +193,17 @@ def bsr(q, k, v, indptr, indices, M, N, R, C, scale):
     y = np.empty((M, Hq, d))
     lse = np.empty((M, Hq))
     ind_ptr = _ptr(indices) if indices.numel() else 0
-    rc = _load().oracle_bsr(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, M, N, R, C, Hq,
-                            Hkv, d, float(scale), _dtype_of(q), y.ctypes.data, lse.ctypes.data)
+    keep, pm_ptr = _mask_args(mask, packed_mask)
+    rc = _load().oracle_bsr_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, pm_ptr,
+                               int(bool(causal)), M, N, R, C, Hq, Hkv, d, float(scale),
+                               _dtype_of(q), y.ctypes.data, lse.ctypes.data)
     _check(rc, "oracle_bsr")
+    del keep
     return y, lse
 
 
-def bsr_rows(q, k, v, indptr, indices, M, N, R, C, scale, rows):
+def bsr_rows(q, k, v, indptr, indices, M, N, R, C, scale, rows, mask=None, packed_mask=None,
+             causal=False):
     """Selected rows: rows is (n, 2) of (query row i, qo head h)."""
     Hq, d = q.shape[1], q.shape[2]
     Hkv = k.shape[1]
@@ -186,10 +214,13 @@ def bsr_rows(q, k, v, indptr, indices, M, N, R, C, scale, rows):
     y = np.empty((n, d))
     lse = np.empty(n)
     ind_ptr = _ptr(indices) if indices.numel() else 0
-    rc = _load().oracle_bsr_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, M, N, R, C,
-                                 Hq, Hkv, d, float(scale), _dtype_of(q), rows.ctypes.data, n,
-                                 y.ctypes.data, lse.ctypes.data)
+    keep, pm_ptr = _mask_args(mask, packed_mask)
+    rc = _load().oracle_bsr_rows_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, pm_ptr,
+                                    int(bool(causal)), M, N, R, C, Hq, Hkv, d, float(scale),
+                                    _dtype_of(q), rows.ctypes.data, n, y.ctypes.data,
+                                    lse.ctypes.data)
     _check(rc, "oracle_bsr_rows")
+    del keep
     return y, lse
 
 

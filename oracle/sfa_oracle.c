@@ -33,6 +33,14 @@
  *     block (i / R, j / C) is stored.  num_qo_heads is a multiple of
  *     num_kv_heads (grouped-query attention, qo head h reads kv head
  *     h / (Hq / Hkv)).
+ *     plan() `mask` (nnz, R, C): element (r, c) of the k-th stored block (in
+ *     indices order) says whether query row (i / R) * R + r may attend key
+ *     column indices[k] * C + c; `packed_mask` is that tensor flattened and
+ *     bit-packed.  Bit order within a byte is not given on the page: read as
+ *     most significant bit first (element e is bit 7 - e % 8 of byte e / 8).
+ *     plan() `causal`: applied only when no mask is given; read as the same
+ *     bottom-right rule the prefill page pins with its tril example (key
+ *     column j visible to query row i iff j <= i + (N - M)).
  *   LSE -- run() / run_return_lse(): "log-sum-exp of attention logits".
  *     Read as the natural logarithm of sum_j exp(scaled logit j) over the
  *     unmasked positions; -inf for a fully masked row.
@@ -242,6 +250,8 @@ int oracle_sfa_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, int
 typedef struct {
     int M, N, R, C, Hq, Hkv, d, dtype;
     double scale;
+    const uint8_t* packed_mask;   /* NULL: every stored block is full */
+    int causal;                   /* used only without a mask */
 } oracle_bsr_shape;
 
 static int oracle_bsr_check(const oracle_bsr_shape* s, const int32_t* indptr,
@@ -268,10 +278,21 @@ static void oracle_bsr_row(const oracle_bsr_shape* s, const uint16_t* q, const u
                            double* lse_row) {
     const int kvh = h / (s->Hq / s->Hkv);
     const int br = i / s->R;
-    /* The dense mask row: column j allowed iff its block (br, j / C) is stored. */
+    /* The dense mask row: column j allowed iff its block (br, j / C) is stored
+     * and, with a mask, its element (i % R, j % C) of that block is set. */
     memset(allowed, 0, (size_t)s->N);
     for (int jj = indptr[br]; jj < indptr[br + 1]; ++jj)
-        for (int c = 0; c < s->C; ++c) allowed[(int64_t)indices[jj] * s->C + c] = 1;
+        for (int c = 0; c < s->C; ++c) {
+            unsigned char ok = 1;
+            if (s->packed_mask) {
+                const int64_t e = ((int64_t)jj * s->R + (i - br * s->R)) * s->C + c;
+                ok = (unsigned char)((s->packed_mask[e >> 3] >> (7 - (e & 7))) & 1);
+            }
+            allowed[(int64_t)indices[jj] * s->C + c] = ok;
+        }
+    if (!s->packed_mask && s->causal)
+        for (int j = 0; j < s->N; ++j)
+            if ((int64_t)j > (int64_t)i + (s->N - s->M)) allowed[j] = 0;
 
     const int64_t qo = ((int64_t)i * s->Hq + h) * s->d;
     double mx = -INFINITY;
@@ -304,10 +325,11 @@ static void oracle_bsr_row(const oracle_bsr_shape* s, const uint16_t* q, const u
     if (lse_row) *lse_row = mx + log(sum);
 }
 
-int oracle_bsr(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* indptr,
-               const int32_t* indices, int M, int N, int R, int C, int Hq, int Hkv, int d,
-               double scale, int dtype, double* y, double* lse) {
-    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale};
+int oracle_bsr_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* indptr,
+                  const int32_t* indices, const uint8_t* packed_mask, int causal, int M, int N,
+                  int R, int C, int Hq, int Hkv, int d, double scale, int dtype, double* y,
+                  double* lse) {
+    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale, packed_mask, causal};
     int rc = oracle_bsr_check(&s, indptr, indices);
     if (rc) return rc;
     const int64_t rows = (int64_t)M * Hq;
@@ -333,12 +355,20 @@ int oracle_bsr(const uint16_t* q, const uint16_t* k, const uint16_t* v, const in
     return err;
 }
 
+int oracle_bsr(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* indptr,
+               const int32_t* indices, int M, int N, int R, int C, int Hq, int Hkv, int d,
+               double scale, int dtype, double* y, double* lse) {
+    return oracle_bsr_ex(q, k, v, indptr, indices, NULL, 0, M, N, R, C, Hq, Hkv, d, scale, dtype,
+                         y, lse);
+}
+
 /* Selected rows only: rows[2*r], rows[2*r+1] = (query row i, qo head h). */
-int oracle_bsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                    const int32_t* indptr, const int32_t* indices, int M, int N, int R, int C,
-                    int Hq, int Hkv, int d, double scale, int dtype, const int64_t* rows,
-                    int64_t nrows, double* y_rows, double* lse_rows) {
-    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale};
+int oracle_bsr_rows_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const int32_t* indptr, const int32_t* indices, const uint8_t* packed_mask,
+                       int causal, int M, int N, int R, int C, int Hq, int Hkv, int d, double scale,
+                       int dtype, const int64_t* rows, int64_t nrows, double* y_rows,
+                       double* lse_rows) {
+    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale, packed_mask, causal};
     int rc = oracle_bsr_check(&s, indptr, indices);
     if (rc) return rc;
     int err = ORACLE_OK;
@@ -361,4 +391,12 @@ int oracle_bsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         free(scores);
     }
     return err;
+}
+
+int oracle_bsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    const int32_t* indptr, const int32_t* indices, int M, int N, int R, int C,
+                    int Hq, int Hkv, int d, double scale, int dtype, const int64_t* rows,
+                    int64_t nrows, double* y_rows, double* lse_rows) {
+    return oracle_bsr_rows_ex(q, k, v, indptr, indices, NULL, 0, M, N, R, C, Hq, Hkv, d, scale,
+                              dtype, rows, nrows, y_rows, lse_rows);
 }

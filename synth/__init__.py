@@ -151,6 +151,8 @@ class BsrCase:
     p: float
     sm_scale: float
     seed: int = 1238
+    causal: bool = False            # bottom-right causal (only without a mask)
+    mask_keep: float = 0.0          # > 0: per-element block mask, each element kept with this p
 
     @property
     def MB(self) -> int:
@@ -213,15 +215,26 @@ def make_sfa_inputs(case: SfaCase) -> dict:
     return {"q": q, "k": k, "v": v, "idx": idx}
 
 
+def bsr_mask(seed: int, nnz: int, R: int, C: int, keep: float) -> np.ndarray:
+    """(nnz, R, C) bool per-element block mask, each element set with
+    probability `keep` (numpy PCG64 stream of `seed`)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.random((nnz, R, C)) < keep
+
+
 def make_bsr_inputs(case: BsrCase) -> dict:
-    """CPU tensors q (M,Hq,d), k/v (N,Hkv,d) in NHD order, and int32 indptr/indices."""
+    """CPU tensors q (M,Hq,d), k/v (N,Hkv,d) in NHD order, int32 indptr/indices,
+    and (mask_keep > 0) the (nnz, R, C) bool mask."""
     c = case
     q = normal(c.seed, 0, (c.M, c.Hq, c.d), c.dtype)
     k = normal(c.seed, 1, (c.N, c.Hkv, c.d), c.dtype)
     v = normal(c.seed, 2, (c.N, c.Hkv, c.d), c.dtype)
     indptr, indices = bsr_pattern(c.seed + 1, c.MB, c.NB, c.p)
-    return {"q": q, "k": k, "v": v, "indptr": torch.from_numpy(indptr),
-            "indices": torch.from_numpy(indices.copy())}
+    out = {"q": q, "k": k, "v": v, "indptr": torch.from_numpy(indptr),
+           "indices": torch.from_numpy(indices.copy()), "mask": None}
+    if c.mask_keep > 0:
+        out["mask"] = bsr_mask(c.seed + 2, int(indptr[-1]), c.R, c.C, c.mask_keep)
+    return out
 
 
 def sfa_counts(case: SfaCase, idx: torch.Tensor | None = None) -> dict:

@@ -9,6 +9,7 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_bsr_mask as mpins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "sfa_oracle.c")
@@ -32,8 +33,15 @@ MUTANTS = [
     ("masked_row_not_zero", "for (int e = 0; e < s->Dv; ++e) y_row[e] = 0.0;\n        if (lse_row) *lse_row = -INFINITY;",
      "for (int e = 0; e < s->Dv; ++e) y_row[e] = 1.0;\n        if (lse_row) *lse_row = -INFINITY;"),
     ("bsr_kv_head_map", "const int kvh = h / (s->Hq / s->Hkv);", "const int kvh = h % s->Hkv;"),
-    ("bsr_block_col_unscaled", "allowed[(int64_t)indices[jj] * s->C + c] = 1;",
-     "allowed[(int64_t)indices[jj] + c] = 1;"),
+    ("bsr_block_col_unscaled", "allowed[(int64_t)indices[jj] * s->C + c] = ok;",
+     "allowed[(int64_t)indices[jj] + c] = ok;"),
+    ("bsr_mask_bit_order_lsb", "(s->packed_mask[e >> 3] >> (7 - (e & 7))) & 1",
+     "(s->packed_mask[e >> 3] >> (e & 7)) & 1"),
+    ("bsr_mask_row_in_block", "((int64_t)jj * s->R + (i - br * s->R)) * s->C + c",
+     "((int64_t)jj * s->R) * s->C + c"),
+    ("bsr_causal_top_left", "if ((int64_t)j > (int64_t)i + (s->N - s->M)) allowed[j] = 0;",
+     "if ((int64_t)j > (int64_t)i) allowed[j] = 0;"),
+    ("bsr_causal_with_mask", "if (!s->packed_mask && s->causal)", "if (s->causal)"),
     ("bsr_row_block_reversed", "const int br = i / s->R;", "const int br = (s->M - 1 - i) / s->R;"),
     ("bsr_scale_dropped", "scores[j] = dot * s->scale;", "scores[j] = dot;"),
     ("bf16_as_f16", "return dtype == 1 ? oracle_bf16(p[i]) : oracle_f16(p[i]);",
@@ -55,6 +63,12 @@ def all_pins():
             pins.test_bsr_worked_example, pins.test_bsr_empty_block_row_is_zero]
     for args in ((3, 2, 10, 8), (4, 4, 12, 16), (1, 3, 5, 9)):
         out.append(lambda a=args: pins.test_bsr_equals_block_expanded_mask(*a))
+    # block-sparse mask / causal pins
+    out += [mpins.test_full_mask_equals_no_mask, mpins.test_mask_overrides_causal,
+            mpins.test_packed_bit_order_most_significant_first, mpins.test_fully_masked_rows_zero]
+    for mn in ((128, 128), (96, 128)):
+        out.append(lambda a=mn: mpins.test_causal_matches_dense_bottom_right(*a))
+    out.append(lambda: mpins.test_mask_matches_dense(0.3))
     return out
 
 
