@@ -204,7 +204,11 @@ typedef struct bsr_plan_s* bsr_plan_t;
  *   num_qo_heads, num_kv_heads   num_qo_heads % num_kv_heads == 0; qo head h
  *                 reads kv head h / (num_qo_heads / num_kv_heads).
  *   head_dim      multiple of 64, <= 256 in this build.
- *   causal        must be 0 in this build (SFA_ERR_UNSUPPORTED otherwise).
+ *   causal        nonzero: bottom-right causal mask on top of the block
+ *                 pattern -- key column j is visible to query row i iff
+ *                 j <= i + (N - M) (plan(): "causal", the same rule the
+ *                 prefill page's tril example pins).  Blocks entirely above
+ *                 that diagonal are dropped from the plan.
  *   sm_scale      softmax scale; <= 0 selects 1/sqrt(head_dim).
  *   dtype         element type of q, k, v and out.
  *   int_ws        device buffer the work list is copied into (on `stream`);
@@ -227,13 +231,48 @@ sfa_status bsr_plan_int_workspace_size(const int32_t* indptr_host, int M, int N,
                                        size_t* bytes);
 
 /*
+ * bsr_plan_masked -- bsr_plan with a per-element mask inside the stored
+ * blocks ("flashinfer.sparse", BlockSparseAttentionWrapper.plan(): `mask`
+ * of shape (nnz, R, C) and its bit-packed form `packed_mask`).
+ *
+ *   packed_mask_host  host bytes, ceil(nnz * R * C / 8) of them, or NULL
+ *                 (then this is bsr_plan).  Element (r, c) of the k-th
+ *                 stored block (indices order) says whether query row
+ *                 (i / R) * R + r may attend key column indices[k] * C + c;
+ *                 the (nnz, R, C) tensor is flattened in that order and
+ *                 packed most significant bit first (element e is bit
+ *                 7 - e % 8 of byte e / 8; the page leaves the bit order
+ *                 open).  nnz * R * C must fit in an int32
+ *                 (SFA_ERR_UNSUPPORTED otherwise).
+ *   causal        ignored when a mask is given (plan(): causal applies only
+ *                 without a custom mask).
+ *   int_ws        size from bsr_plan_masked_int_workspace_size(...,
+ *                 with_mask = 1): the work list plus the mask bytes.
+ * Rows whose every element is masked write out = +0 and lse = -inf.  Other
+ * arguments, ownership and errors as bsr_plan.
+ */
+sfa_status bsr_plan_masked(const int32_t* indptr_host, const int32_t* indices_host,
+                           const uint8_t* packed_mask_host, int M, int N, int R, int C,
+                           int num_qo_heads, int num_kv_heads, int head_dim, int causal,
+                           float sm_scale, sfa_dtype dtype, void* int_ws, size_t int_ws_bytes,
+                           void* float_ws, size_t float_ws_bytes, sfa_stream_t stream,
+                           bsr_plan_t* plan_out);
+
+/* Bytes of int workspace bsr_plan_masked needs (with_mask = 0: as
+ * bsr_plan_int_workspace_size).  Host only. */
+sfa_status bsr_plan_masked_int_workspace_size(const int32_t* indptr_host, int M, int N, int R,
+                                              int C, int num_qo_heads, int num_kv_heads,
+                                              int head_dim, int with_mask, size_t* bytes);
+
+/*
  * bsr_run -- block-sparse attention with a plan.
  *   q    device (M, num_qo_heads, head_dim), NHD, dtype.
  *   k, v device (N, num_kv_heads, head_dim), NHD, dtype.
  *   out  device (M, num_qo_heads, head_dim), dtype.
  *   lse  device float32 (M, num_qo_heads) or NULL: natural-log log-sum-exp
  *        of the scaled logits of the row's allowed columns.
- * Rows with no stored block write out = +0 and lse = -inf.
+ * Rows with no visible column (no stored block, or every element masked)
+ * write out = +0 and lse = -inf.
  */
 sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v, void* out,
                    float* lse, sfa_stream_t stream);

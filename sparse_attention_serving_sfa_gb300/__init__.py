@@ -30,7 +30,7 @@ DTYPES = {"f16": 0, "bf16": 1}
 # Every entry point of include/sfa.h.
 EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
            "sfa_status_string", "sfa_kernel_launches", "sfa_run_noalloc", "bsr_plan", "bsr_plan_int_workspace_size", "bsr_run",
-           "bsr_plan_destroy")
+           "bsr_plan_destroy", "bsr_plan_masked", "bsr_plan_masked_int_workspace_size")
 
 
 class SfaError(RuntimeError):
@@ -84,6 +84,11 @@ def load():
             lib.bsr_plan.restype = ci
             lib.bsr_plan_int_workspace_size.argtypes = [vp] + [ci] * 7 + [ctypes.POINTER(sz)]
             lib.bsr_plan_int_workspace_size.restype = ci
+            lib.bsr_plan_masked.argtypes = [vp, vp, vp] + [ci] * 8 + [cf, ci, vp, sz, vp, sz, vp,
+                                                                   ctypes.POINTER(vp)]
+            lib.bsr_plan_masked.restype = ci
+            lib.bsr_plan_masked_int_workspace_size.argtypes = [vp] + [ci] * 8 + [ctypes.POINTER(sz)]
+            lib.bsr_plan_masked_int_workspace_size.restype = ci
             lib.bsr_run.argtypes = [vp, vp, vp, vp, vp, vp, vp]
             lib.bsr_run.restype = ci
             lib.bsr_plan_destroy.argtypes = [vp]
@@ -209,23 +214,51 @@ def bsr_plan_int_workspace_size(indptr_host, M, N, R, C, num_qo_heads, num_kv_he
     return out.value
 
 
+def bsr_plan_masked_int_workspace_size(indptr_host, M, N, R, C, num_qo_heads, num_kv_heads,
+                                       head_dim, with_mask) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().bsr_plan_masked_int_workspace_size(_ptr(indptr_host), M, N, R, C, num_qo_heads,
+                                                     num_kv_heads, head_dim, int(bool(with_mask)),
+                                                     ctypes.byref(out)),
+           "bsr_plan_masked_int_workspace_size")
+    return out.value
+
+
+def pack_block_mask(mask):
+    """plan()'s `mask` (nnz, R, C) bool -> the packed bytes bsr_plan_masked
+    reads: flattened in stored-block order, most significant bit first."""
+    import numpy as np
+    m = mask.detach().cpu().numpy() if hasattr(mask, "detach") else np.asarray(mask)
+    return np.packbits(np.ascontiguousarray(m.astype(bool).reshape(-1)), bitorder="big")
+
+
 def bsr_plan(indptr_host, indices_host, M, N, R, C, num_qo_heads, num_kv_heads, head_dim,
              causal=False, sm_scale=0.0, dtype="f16", int_ws=None, float_ws=None,
-             stream=None) -> BsrPlan:
-    """Forwards to bsr_plan().  indptr/indices are host int32 tensors; int_ws a
-    device uint8 tensor (allocated here with torch if None)."""
+             stream=None, mask=None, packed_mask=None) -> BsrPlan:
+    """Forwards to bsr_plan(), or to bsr_plan_masked() when a per-element
+    mask ((nnz, R, C) bool) or its packed bytes are given.  indptr/indices are
+    host int32 tensors; int_ws a device uint8 tensor (allocated here with
+    torch if None)."""
+    import numpy as np
     import torch
+    if mask is not None and packed_mask is None:
+        packed_mask = pack_block_mask(mask)
+    if packed_mask is not None:
+        packed_mask = np.ascontiguousarray(packed_mask, dtype=np.uint8)
     if int_ws is None:
-        need = bsr_plan_int_workspace_size(indptr_host, M, N, R, C, num_qo_heads, num_kv_heads,
-                                           head_dim)
+        need = bsr_plan_masked_int_workspace_size(indptr_host, M, N, R, C, num_qo_heads,
+                                                  num_kv_heads, head_dim, packed_mask is not None)
         int_ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
     fws_bytes = 0 if float_ws is None else float_ws.numel() * float_ws.element_size()
     handle = ctypes.c_void_p(0)
-    st = load().bsr_plan(_ptr(indptr_host), _ptr(indices_host) if indices_host.numel() else None,
-                         M, N, R, C, num_qo_heads, num_kv_heads, head_dim, int(bool(causal)),
-                         float(sm_scale), _enum(dtype, DTYPES), _ptr(int_ws),
-                         int_ws.numel() * int_ws.element_size(), _ptr(float_ws), fws_bytes,
-                         _stream(stream), ctypes.byref(handle))
+    args = (M, N, R, C, num_qo_heads, num_kv_heads, head_dim, int(bool(causal)), float(sm_scale),
+            _enum(dtype, DTYPES), _ptr(int_ws), int_ws.numel() * int_ws.element_size(),
+            _ptr(float_ws), fws_bytes, _stream(stream), ctypes.byref(handle))
+    ind = _ptr(indices_host) if indices_host.numel() else None
+    if packed_mask is None:
+        st = load().bsr_plan(_ptr(indptr_host), ind, *args)
+    else:
+        st = load().bsr_plan_masked(_ptr(indptr_host), ind, packed_mask.ctypes.data, *args)
     _check(st, "bsr_plan")
     return BsrPlan(handle.value, int_ws, M, N, num_qo_heads, head_dim)
 

@@ -4,7 +4,11 @@
 // run() launches the kernels with that plan.
 #include <math.h>
 
+#include <stdint.h>
+#include <string.h>
+
 #include <algorithm>
+#include <cstring>
 #include <new>
 #include <vector>
 
@@ -17,9 +21,11 @@ struct bsr_plan_s {
     float scale;
     int MB, NB, nnz, ntiles;
     bool tc;                        // tensor-core path (work items) vs generic (row tiles)
+    int mask_mode;                  // 0 none, 1 causal, 2 per-element bits
     const int32_t* d_indptr;
     const int32_t* d_indices;
     const void* d_work;             // BsrTile list (generic) or 4-int items (tensor cores)
+    const uint8_t* d_mask;          // packed element mask (mode 2)
     std::vector<int32_t> staging;   // host copy kept alive for the async upload
 };
 
@@ -60,6 +66,12 @@ size_t int_ws_bytes(int MB, int nnz, int ntiles) {
     return 4 * (round4((size_t)MB + 1) + round4((size_t)nnz) + 4 * (size_t)ntiles);
 }
 
+// Bytes of the packed element mask: nnz * R * C bits, rounded up to 16.
+size_t mask_bytes(int nnz, int R, int C) {
+    const size_t bits = (size_t)nnz * (size_t)R * (size_t)C;
+    return (((bits + 7) / 8) + 15) & ~size_t(15);
+}
+
 }  // namespace
 
 extern "C" {
@@ -77,11 +89,33 @@ sfa_status bsr_plan_int_workspace_size(const int32_t* indptr_host, int M, int N,
     return SFA_OK;
 }
 
+sfa_status bsr_plan_masked_int_workspace_size(const int32_t* indptr_host, int M, int N, int R,
+                                              int C, int num_qo_heads, int num_kv_heads,
+                                              int head_dim, int with_mask, size_t* bytes) {
+    sfa_status st = bsr_plan_int_workspace_size(indptr_host, M, N, R, C, num_qo_heads,
+                                                num_kv_heads, head_dim, bytes);
+    if (st != SFA_OK || !with_mask) return st;
+    const int MB = (M + R - 1) / R;
+    *bytes += mask_bytes(indptr_host[MB], R, C);
+    return SFA_OK;
+}
+
 sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int M, int N,
                     int R, int C, int num_qo_heads, int num_kv_heads, int head_dim, int causal,
                     float sm_scale, sfa_dtype dtype, void* int_ws, size_t int_ws_bytes_given,
                     void* float_ws, size_t float_ws_bytes, sfa_stream_t stream,
                     bsr_plan_t* plan_out) {
+    return bsr_plan_masked(indptr_host, indices_host, nullptr, M, N, R, C, num_qo_heads,
+                           num_kv_heads, head_dim, causal, sm_scale, dtype, int_ws,
+                           int_ws_bytes_given, float_ws, float_ws_bytes, stream, plan_out);
+}
+
+sfa_status bsr_plan_masked(const int32_t* indptr_host, const int32_t* indices_host,
+                           const uint8_t* packed_mask_host, int M, int N, int R, int C,
+                           int num_qo_heads, int num_kv_heads, int head_dim, int causal,
+                           float sm_scale, sfa_dtype dtype, void* int_ws,
+                           size_t int_ws_bytes_given, void* float_ws, size_t float_ws_bytes,
+                           sfa_stream_t stream, bsr_plan_t* plan_out) {
     (void)float_ws;
     (void)float_ws_bytes;
     if (!plan_out || !indptr_host) return SFA_ERR_INVALID_ARG;
@@ -90,7 +124,6 @@ sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int
     if (st != SFA_OK) return st;
     if (dtype != SFA_DTYPE_F16 && dtype != SFA_DTYPE_BF16) return SFA_ERR_INVALID_ARG;
     if (!isfinite(sm_scale)) return SFA_ERR_INVALID_ARG;
-    if (causal) return SFA_ERR_UNSUPPORTED;
     const int MB = (M + R - 1) / R, NB = N / C;
     // indptr: starts at 0, non-decreasing
     if (indptr_host[0] != 0) return SFA_ERR_INVALID_ARG;
@@ -110,9 +143,30 @@ sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int
             for (int j = indptr_host[i]; j < indptr_host[i + 1]; ++j) seen[(size_t)indices_host[j]] = 0;
         }
     }
+    // masked elements: the per-element mask wins over causal (plan() applies
+    // causal only without a mask); its bit index must fit an int
+    const int mask_mode = packed_mask_host ? 2 : (causal ? 1 : 0);
+    if (mask_mode == 2 && (int64_t)nnz * R * C > (int64_t)INT32_MAX) return SFA_ERR_UNSUPPORTED;
+    // causal: blocks entirely above the bottom-right diagonal drop out (no
+    // element of them is visible); the kernels test the others per element
+    std::vector<int32_t> f_indptr(indptr_host, indptr_host + MB + 1);
+    std::vector<int32_t> f_indices(indices_host ? indices_host : indptr_host,
+                                   indices_host ? indices_host + nnz : indptr_host);
+    if (mask_mode == 1) {
+        f_indptr[0] = 0;
+        f_indices.clear();
+        for (int i = 0; i < MB; ++i) {
+            const int64_t last_row = std::min((int64_t)(i + 1) * R, (int64_t)M) - 1;
+            for (int j = indptr_host[i]; j < indptr_host[i + 1]; ++j)
+                if ((int64_t)indices_host[j] * C <= last_row + (N - M)) f_indices.push_back(indices_host[j]);
+            f_indptr[i + 1] = (int32_t)f_indices.size();
+        }
+    }
+    const int f_nnz = f_indptr[MB];
     const bool tc = sfa::bsr_tc_supported(head_dim, C, num_qo_heads, num_kv_heads);
     const int ntiles = count_work(M, R, C, num_qo_heads, num_kv_heads, head_dim);
-    const size_t need = int_ws_bytes(MB, nnz, ntiles);
+    const size_t base_bytes = int_ws_bytes(MB, f_nnz, ntiles);
+    const size_t need = base_bytes + (mask_mode == 2 ? mask_bytes(nnz, R, C) : 0);
     if (!int_ws || int_ws_bytes_given < need) return SFA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(int_ws) & 15u) return SFA_ERR_INVALID_ARG;
 
@@ -122,8 +176,9 @@ sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int
     plan->Hq = num_qo_heads; plan->Hkv = num_kv_heads; plan->d = head_dim;
     plan->dtype = dtype;
     plan->scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)head_dim);
-    plan->MB = MB; plan->NB = NB; plan->nnz = nnz; plan->ntiles = ntiles;
+    plan->MB = MB; plan->NB = NB; plan->nnz = f_nnz; plan->ntiles = ntiles;
     plan->tc = tc;
+    plan->mask_mode = mask_mode;
 
     // Work list, heaviest block rows first: generic row tiles of <= 64 rows
     // (the kernel's grid.y spans the qo heads), or tensor-core items of
@@ -142,20 +197,28 @@ sfa_status bsr_plan(const int32_t* indptr_host, const int32_t* indices_host, int
         }
     }
     std::stable_sort(tiles.begin(), tiles.end(), [&](const sfa::BsrTile& a, const sfa::BsrTile& b) {
-        return (indptr_host[a.rb + 1] - indptr_host[a.rb]) > (indptr_host[b.rb + 1] - indptr_host[b.rb]);
+        return (f_indptr[a.rb + 1] - f_indptr[a.rb]) > (f_indptr[b.rb + 1] - f_indptr[b.rb]);
     });
 
-    const size_t n_indptr = round4((size_t)MB + 1), n_indices = round4((size_t)nnz);
+    const size_t n_indptr = round4((size_t)MB + 1), n_indices = round4((size_t)f_nnz);
     plan->staging.assign(need / 4, 0);
-    std::copy(indptr_host, indptr_host + MB + 1, plan->staging.begin());
-    if (nnz) std::copy(indices_host, indices_host + nnz, plan->staging.begin() + n_indptr);
+    std::copy(f_indptr.begin(), f_indptr.end(), plan->staging.begin());
+    if (f_nnz) std::copy(f_indices.begin(), f_indices.end(), plan->staging.begin() + n_indptr);
     std::copy(reinterpret_cast<const int32_t*>(tiles.data()),
               reinterpret_cast<const int32_t*>(tiles.data()) + 4 * tiles.size(),
               plan->staging.begin() + n_indptr + n_indices);
+    if (mask_mode == 2) {
+        const size_t mbits = (size_t)nnz * R * C;
+        std::memcpy(reinterpret_cast<unsigned char*>(plan->staging.data()) + base_bytes,
+                    packed_mask_host, (mbits + 7) / 8);
+    }
     int32_t* base = static_cast<int32_t*>(int_ws);
     plan->d_indptr = base;
     plan->d_indices = base + n_indptr;
     plan->d_work = base + n_indptr + n_indices;
+    plan->d_mask = mask_mode == 2 ? reinterpret_cast<const uint8_t*>(
+                                        static_cast<unsigned char*>(int_ws) + base_bytes)
+                                  : nullptr;
     cudaError_t err = cudaMemcpyAsync(int_ws, plan->staging.data(), need, cudaMemcpyHostToDevice,
                                       reinterpret_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) {
@@ -181,6 +244,8 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
     p.M = plan->M; p.N = plan->N; p.R = plan->R; p.C = plan->C;
     p.Hq = plan->Hq; p.Hkv = plan->Hkv; p.d = plan->d;
     p.scale_log2 = plan->scale * sfa::kLog2e;
+    p.mask_mode = plan->mask_mode;
+    p.mask = plan->d_mask;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
     if (plan->tc) {

@@ -10,7 +10,8 @@
 // keys (any C: a chunk may span several blocks).  Per chunk: S = Q K^T as a
 // 64 x 64 register-tiled product (each thread 4 x 4), online softmax per row
 // (row max / sum across the 16 threads of a row), O += P V (each thread 4
-// rows x d/16 columns).
+// rows x d/16 columns).  plan()'s causal (bottom-right) and per-element mask
+// set the masked scores to -inf before the softmax.
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,7 +24,7 @@ constexpr int kThreads = 256;
 constexpr int kSPad = 4;       // float padding of transposed tiles
 
 struct BsrSmem {
-    int q, k, v, p, cols, total;
+    int q, k, v, p, cols, ecols, total;
 };
 
 __host__ __device__ inline BsrSmem bsr_smem(int d) {
@@ -34,6 +35,7 @@ __host__ __device__ inline BsrSmem bsr_smem(int d) {
     s.v = off;    off += kKeys * d * 4;             // v    [64 keys][d]
     s.p = off;    off += kKeys * (kRows + kSPad) * 4;  // p^T [64 keys][64 rows]
     s.cols = off; off += kKeys * 4;
+    s.ecols = off; off += kKeys * 4;   // mask bit of (row 0 of the block, key)
     s.total = off;
     return s;
 }
@@ -49,6 +51,7 @@ __global__ void __launch_bounds__(kThreads) bsr_generic_kernel(const BsrParams p
     float* vs = reinterpret_cast<float*>(smem + L.v);
     float* pT = reinterpret_cast<float*>(smem + L.p);
     int* cols = reinterpret_cast<int*>(smem + L.cols);
+    int* ecols = reinterpret_cast<int*>(smem + L.ecols);
     constexpr int QLD = kRows + kSPad, KLD = kKeys + kSPad, PLD = kRows + kSPad;
 
     const BsrTile tile = p.tiles[blockIdx.x];
@@ -84,12 +87,15 @@ __global__ void __launch_bounds__(kThreads) bsr_generic_kernel(const BsrParams p
         const int nk = min(kKeys, nkeys - k0);
         __syncthreads();   // previous chunk fully consumed
         if (tid < kKeys) {
-            int col = -1;
+            int col = -1, ecol = 0;
             if (tid < nk) {
-                int pos = k0 + tid;
-                col = p.indices[blk0 + pos / p.C] * p.C + pos % p.C;
+                const int pos = k0 + tid;
+                const int kb = blk0 + pos / p.C, cc = pos % p.C;
+                col = p.indices[kb] * p.C + cc;
+                ecol = kb * p.R * p.C + cc;
             }
             cols[tid] = col;
+            ecols[tid] = ecol;
         }
         __syncthreads();
         // K (transposed) and V chunk as fp32; missing keys are zero.
@@ -138,9 +144,23 @@ __global__ void __launch_bounds__(kThreads) bsr_generic_kernel(const BsrParams p
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float cm = -INFINITY;
+            const int rl = ty * 4 + i;                    // row of the tile
+            const int rin = tile.row0 + rl - tile.rb * p.R;    // row inside its block
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (tx * 4 + j >= nk) s[i][j] = -INFINITY;
+                const int kj = tx * 4 + j;
+                if (kj >= nk) {
+                    s[i][j] = -INFINITY;
+                } else if (p.mask_mode != 0 && rl < tile.nrows) {
+                    bool ok;
+                    if (p.mask_mode == 1) {
+                        ok = (int64_t)cols[kj] <= (int64_t)(tile.row0 + rl) + (p.N - p.M);
+                    } else {
+                        const int e = ecols[kj] + rin * p.C;
+                        ok = ((p.mask[e >> 3] >> (7 - (e & 7))) & 1) != 0;
+                    }
+                    if (!ok) s[i][j] = -INFINITY;
+                }
                 cm = fmaxf(cm, s[i][j]);
             }
 #pragma unroll

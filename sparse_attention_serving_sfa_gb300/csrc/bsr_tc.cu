@@ -19,7 +19,10 @@
 //     max is kept: same softmax, exponentials bounded by 256), and writes
 //     P = exp2(s - m) as a 16-bit high part plus a 16-bit remainder, so that
 //     P.V carries P to ~fp32 accuracy.
-// One CTA per SM (all 512 TMEM columns: S and O of both tiles).
+// One CTA per SM (all 512 TMEM columns: S and O of both tiles).  plan()'s
+// causal (bottom-right) and per-element block mask become a 64-bit allowed
+// mask per thread and 64-key block (a compile-time mode, so the plain path
+// carries no test); masked scores are -inf before the softmax.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -74,11 +77,21 @@ struct BsrTcParams {
     const int32_t* indices;
     const BsrTcItem* items;
     int* err_word;
-    int M, R, C, Hq, G, TR;
+    int M, N, R, C, Hq, G, TR;
     float scale_log2;
+    const uint8_t* mask;    // per-element bits (MODE 2)
 };
 
-template <class E, int D>
+// The 64-bit word whose bit j is element j of 64 mask elements stored most
+// significant bit first from `p` (8-byte aligned).
+__device__ __forceinline__ uint64_t mask_bits64(const uint8_t* p) {
+    const uint64_t raw = *reinterpret_cast<const uint64_t*>(p);
+    const uint64_t rev = __brevll(raw);     // bit j of byte t now at bit 8 (7 - t) + j
+    const uint32_t lo = (uint32_t)rev, hi = (uint32_t)(rev >> 32);
+    return ((uint64_t)__byte_perm(lo, 0, 0x0123) << 32) | __byte_perm(hi, 0, 0x0123);
+}
+
+template <class E, int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const BsrTcParams p) {
@@ -221,6 +234,25 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
             tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
             tmem_wait_ld();
+            // allowed keys of this 64-key block for this row (bit j = key j)
+            uint64_t am = ~0ull;
+            if constexpr (MODE != 0) {
+                const int i = item.row0 + t * p.TR + r / p.G;     // query row of this thread
+                if (i < row_end && r / p.G < p.TR) {
+                    const int kb = blk0 + b / sub, sb = b % sub;
+                    if constexpr (MODE == 1) {
+                        const int64_t lim = (int64_t)i + (p.N - p.M) -
+                                            ((int64_t)p.indices[kb] * p.C + sb * kKeys);
+                        am = lim < 0 ? 0ull : (lim >= 63 ? ~0ull : ((2ull << lim) - 1ull));
+                    } else {
+                        const int64_t e0 = ((int64_t)kb * p.R + (i - item.rb * p.R)) * p.C + sb * kKeys;
+                        am = mask_bits64(p.mask + (e0 >> 3));
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
+            }
             float bmax = -INFINITY;
 #pragma unroll
             for (int j = 0; j < 64; ++j) bmax = fmaxf(bmax, __uint_as_float(sv[j]) * p.scale_log2);
@@ -252,8 +284,13 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(__uint_as_float(sv[8 * c + 2 * e]) * p.scale_log2 - m_used);
-                    const float p1 = fast_exp2(__uint_as_float(sv[8 * c + 2 * e + 1]) * p.scale_log2 - m_used);
+                    float p0 = fast_exp2(__uint_as_float(sv[8 * c + 2 * e]) * p.scale_log2 - m_used);
+                    float p1 = fast_exp2(__uint_as_float(sv[8 * c + 2 * e + 1]) * p.scale_log2 - m_used);
+                    if constexpr (MODE != 0) {
+                        // masked keys give 0, also while the row has seen none (m = -inf)
+                        if (!((am >> (8 * c + 2 * e)) & 1ull)) p0 = 0.f;
+                        if (!((am >> (8 * c + 2 * e + 1)) & 1ull)) p1 = 0.f;
+                    }
                     l += p0 + p1;
                     hw[e] = E::pack2(p0, p1);
                     const float2 h = E::unpack2(hw[e]);
@@ -341,7 +378,7 @@ bool make_map(CUtensorMap* map, const void* base, bool bf16, int dim, int heads,
     return r == CUDA_SUCCESS;
 }
 
-template <class E, int D>
+template <class E, int D, int MODE>
 cudaError_t launch_tc_t(const BsrParams& bp, const BsrTcParams& tp, int nitems, cudaStream_t stream) {
     using L = TcSmem<D>;
     const bool bf16 = std::is_same<E, BF16>::value;
@@ -350,7 +387,7 @@ cudaError_t launch_tc_t(const BsrParams& bp, const BsrTcParams& tp, int nitems, 
         !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kKeys) ||
         !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kKeys))
         return cudaErrorInvalidValue;
-    auto kern = bsr_tc_kernel<E, D>;
+    auto kern = bsr_tc_kernel<E, D, MODE>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
     if (err != cudaSuccess) return err;
     kern<<<nitems, kThreads, L::alloc, stream>>>(mq, mk, mv, tp);
@@ -379,6 +416,8 @@ cudaError_t launch_bsr_tc(const BsrParams& bp, const void* items, int nitems, in
     tp.items = static_cast<const BsrTcItem*>(items);
     tp.err_word = err_word;
     tp.M = bp.M;
+    tp.N = bp.N;
+    tp.mask = bp.mask;
     tp.R = bp.R;
     tp.C = bp.C;
     tp.Hq = bp.Hq;
@@ -386,10 +425,19 @@ cudaError_t launch_bsr_tc(const BsrParams& bp, const void* items, int nitems, in
     tp.TR = kTileM / tp.G;
     tp.scale_log2 = bp.scale_log2;
     const bool bf16 = dtype == SFA_DTYPE_BF16;
-    if (bp.d == 128)
-        return bf16 ? launch_tc_t<BF16, 128>(bp, tp, nitems, stream) : launch_tc_t<F16, 128>(bp, tp, nitems, stream);
-    if (bp.d == 64)
-        return bf16 ? launch_tc_t<BF16, 64>(bp, tp, nitems, stream) : launch_tc_t<F16, 64>(bp, tp, nitems, stream);
+#define SFA_BSR_TC_MODE(MODE_)                                                                   \
+    if (bp.mask_mode == MODE_) {                                                                 \
+        if (bp.d == 128)                                                                         \
+            return bf16 ? launch_tc_t<BF16, 128, MODE_>(bp, tp, nitems, stream)                  \
+                        : launch_tc_t<F16, 128, MODE_>(bp, tp, nitems, stream);                  \
+        if (bp.d == 64)                                                                          \
+            return bf16 ? launch_tc_t<BF16, 64, MODE_>(bp, tp, nitems, stream)                   \
+                        : launch_tc_t<F16, 64, MODE_>(bp, tp, nitems, stream);                   \
+    }
+    SFA_BSR_TC_MODE(0)
+    SFA_BSR_TC_MODE(1)
+    SFA_BSR_TC_MODE(2)
+#undef SFA_BSR_TC_MODE
     return cudaErrorInvalidValue;
 }
 

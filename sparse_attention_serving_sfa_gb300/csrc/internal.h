@@ -96,6 +96,12 @@ struct BsrParams {
     int ntiles;
     int M, N, R, C, Hq, Hkv, d;
     float scale_log2;
+    // element masking inside stored blocks: 0 none, 1 causal (bottom-right,
+    // key column j visible to row i iff j <= i + N - M), 2 per-element bits
+    // (`mask`: element (r, c) of the k-th stored block is bit
+    // (k * R + r) * C + c, most significant bit first within each byte)
+    int mask_mode;
+    const uint8_t* mask;
 };
 
 cudaError_t launch_bsr_generic(const BsrParams& p, sfa_dtype dtype, cudaStream_t stream);

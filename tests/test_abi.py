@@ -115,7 +115,6 @@ def bsr_call(indptr, indices, M, N, R, C, Hq=4, Hkv=2, d=64, causal=0, ws_bytes=
     (([0, 1, 2], [0, 1], 4, 4, 2, 2, 3, 2), sfa.SFA_ERR_INVALID_ARG),  # Hq % Hkv != 0
     (([0, 1, 2], [0, 1], 4, 4, 2, 2, 4, 2, 96), sfa.SFA_ERR_INVALID_ARG),   # head_dim % 64
     (([0, 1, 2], [0, 1], 4, 4, 2, 2, 4, 2, 320), sfa.SFA_ERR_UNSUPPORTED),  # head_dim > 256
-    (([0, 1, 2], [0, 1], 4, 4, 2, 2, 4, 2, 64, 1), sfa.SFA_ERR_UNSUPPORTED),  # causal
 ])
 def test_bsr_plan_rejects(lib, args, status):
     assert bsr_call(*args) == status
@@ -130,6 +129,42 @@ def test_bsr_int_workspace_size(lib):
     n = sfa.bsr_plan_int_workspace_size(ip, 3, 3, 1, 1, 32, 8, 128)
     # indptr (4) + indices (5 -> 8) + 3 tiles x 4 ints
     assert n == 4 * (4 + 8 + 12)
+
+
+def test_bsr_causal_plan_passes_validation(lib):
+    # causal is supported: validation passes and only the workspace is checked
+    assert bsr_call([0, 1, 2], [0, 1], 4, 4, 2, 2, causal=1, ws_bytes=8) == sfa.SFA_ERR_WORKSPACE
+
+
+def test_bsr_masked_int_workspace_size(lib):
+    ip = torch.tensor([0, 1, 3, 5], dtype=torch.int32)
+    base = sfa.bsr_plan_int_workspace_size(ip, 48, 48, 16, 16, 32, 8, 128)
+    assert sfa.bsr_plan_masked_int_workspace_size(ip, 48, 48, 16, 16, 32, 8, 128, False) == base
+    # 5 blocks x 16 x 16 bits = 160 bytes (a multiple of 16)
+    assert sfa.bsr_plan_masked_int_workspace_size(ip, 48, 48, 16, 16, 32, 8, 128, True) == base + 160
+    ip1 = torch.tensor([0, 1], dtype=torch.int32)
+    base1 = sfa.bsr_plan_int_workspace_size(ip1, 3, 3, 3, 3, 4, 2, 64)
+    # 9 bits -> 2 bytes -> rounded up to 16
+    assert sfa.bsr_plan_masked_int_workspace_size(ip1, 3, 3, 3, 3, 4, 2, 64, True) == base1 + 16
+
+
+def test_bsr_masked_plan_needs_room_for_the_mask(lib):
+    handle = ctypes.c_void_p(0)
+    ip = torch.tensor([0, 1, 2], dtype=torch.int32)
+    ix = torch.tensor([0, 1], dtype=torch.int32)
+    mask = sfa.pack_block_mask(torch.ones(2, 2, 2, dtype=torch.bool))
+    base = sfa.bsr_plan_int_workspace_size(ip, 4, 4, 2, 2, 4, 2, 64)
+    st = sfa.load().bsr_plan_masked(ip.data_ptr(), ix.data_ptr(), mask.ctypes.data, 4, 4, 2, 2, 4,
+                                    2, 64, 0, 0.0, 0, FAKE, base, None, 0, None,
+                                    ctypes.byref(handle))
+    assert st == sfa.SFA_ERR_WORKSPACE and not handle.value
+
+
+def test_pack_block_mask_bit_order():
+    m = torch.zeros(1, 2, 8, dtype=torch.bool)
+    m[0, 0, 1] = True
+    m[0, 1, 7] = True
+    assert list(sfa.pack_block_mask(m)) == [0x40, 0x01]
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

@@ -153,3 +153,88 @@ def test_tensor_core_large_scores_rescale():
     out, lse = run_bsr(q, k, v, indptr, indices, M, N, R, C, 0.0884, "f16")
     y, l = oracle.bsr(q, k, v, indptr, indices, M, N, R, C, 0.0884)
     compare(out, lse, y, l, "f16")
+
+
+# ---------------------------------------------------------------------------
+# plan()'s per-element mask and causal, on both kernels (tensor cores: head_dim
+# 64/128 with C % 64 == 0; register-tiled kernel otherwise)
+
+def run_bsr_masked(q, k, v, indptr, indices, M, N, R, C, scale, dtype, mask=None, causal=False):
+    Hq, d, Hkv = q.shape[1], q.shape[2], k.shape[1]
+    plan = sfa.bsr_plan(indptr, indices, M, N, R, C, Hq, Hkv, d, sm_scale=scale, dtype=dtype,
+                        mask=mask, causal=causal)
+    out = torch.empty_like(q.cuda())
+    lse = torch.empty((M, Hq), dtype=torch.float32, device="cuda")
+    sfa.bsr_run(plan, q.cuda(), k.cuda(), v.cuda(), out, lse)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+MASK_SHAPES = [
+    # M, N, R, C, Hq, Hkv, d, dtype
+    (256, 256, 64, 64, 8, 2, 128, "f16"),     # tensor cores, G = 4
+    (200, 256, 64, 128, 4, 4, 64, "bf16"),    # tensor cores, C = 2 x 64, ragged last row block
+    (130, 192, 32, 64, 16, 1, 128, "bf16"),   # tensor cores, G = 16
+    (97, 120, 16, 24, 6, 3, 192, "f16"),      # register-tiled kernel
+    (64, 96, 8, 32, 2, 1, 64, "f16"),         # register-tiled kernel (C % 64 != 0)
+]
+
+
+@pytest.mark.parametrize("M,N,R,C,Hq,Hkv,d,dtype", MASK_SHAPES)
+@pytest.mark.parametrize("keep", [0.5, 0.05])
+def test_element_mask(M, N, R, C, Hq, Hkv, d, dtype, keep):
+    case = synth.BsrCase("m", M=M, N=N, R=R, C=C, Hq=Hq, Hkv=Hkv, d=d, dtype=dtype, p=0.4,
+                         sm_scale=1 / math.sqrt(d), seed=81, mask_keep=keep)
+    x = synth.make_bsr_inputs(case)
+    out, lse = run_bsr_masked(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                              case.sm_scale, dtype, mask=x["mask"])
+    y, l = oracle.bsr(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                      case.sm_scale, mask=x["mask"])
+    compare(out, lse, y, l, dtype)
+
+
+@pytest.mark.parametrize("M,N,R,C,Hq,Hkv,d,dtype", MASK_SHAPES)
+def test_causal(M, N, R, C, Hq, Hkv, d, dtype):
+    case = synth.BsrCase("c", M=M, N=N, R=R, C=C, Hq=Hq, Hkv=Hkv, d=d, dtype=dtype, p=0.5,
+                         sm_scale=1 / math.sqrt(d), seed=82)
+    x = synth.make_bsr_inputs(case)
+    out, lse = run_bsr_masked(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                              case.sm_scale, dtype, causal=True)
+    y, l = oracle.bsr(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                      case.sm_scale, causal=True)
+    compare(out, lse, y, l, dtype)
+
+
+def test_mask_wins_over_causal_and_masked_rows_are_zero():
+    M, N, R, C, Hq, Hkv, d = 256, 256, 64, 64, 8, 2, 128
+    case = synth.BsrCase("z", M=M, N=N, R=R, C=C, Hq=Hq, Hkv=Hkv, d=d, dtype="f16", p=0.5,
+                         sm_scale=1 / math.sqrt(d), seed=83, mask_keep=0.5)
+    x = synth.make_bsr_inputs(case)
+    mask = x["mask"].copy()
+    mask[:, 5, :] = False          # row 5 of every block row: nothing visible
+    out, lse = run_bsr_masked(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                              case.sm_scale, "f16", mask=mask, causal=True)
+    y, l = oracle.bsr(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                      case.sm_scale, mask=mask)
+    compare(out, lse, y, l, "f16")
+    rows = np.arange(5, M, R)
+    assert torch.all(out[rows] == 0) and torch.all(torch.isneginf(lse[rows]))
+
+
+def test_masked_plan_reuse():
+    """A masked plan stays valid for several runs on different inputs."""
+    M, N, R, C, Hq, Hkv, d = 128, 192, 64, 64, 4, 1, 64
+    case = synth.BsrCase("r", M=M, N=N, R=R, C=C, Hq=Hq, Hkv=Hkv, d=d, dtype="bf16", p=0.6,
+                         sm_scale=0.125, seed=84, mask_keep=0.7)
+    x = synth.make_bsr_inputs(case)
+    plan = sfa.bsr_plan(x["indptr"], x["indices"], M, N, R, C, Hq, Hkv, d, sm_scale=0.125,
+                        dtype="bf16", mask=x["mask"])
+    for seed in (1, 2):
+        q = synth.normal(seed, 0, (M, Hq, d), "bf16")
+        out = torch.empty_like(q.cuda())
+        lse = torch.empty((M, Hq), dtype=torch.float32, device="cuda")
+        sfa.bsr_run(plan, q.cuda(), x["k"].cuda(), x["v"].cuda(), out, lse)
+        torch.cuda.synchronize()
+        y, l = oracle.bsr(q, x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C, 0.125,
+                          mask=x["mask"])
+        compare(out.cpu(), lse.cpu(), y, l, "bf16")
