@@ -220,10 +220,11 @@ def run_bsr(args, rank, world, local):
     sfa.load()
     case = synth.BSR_WORKLOADS[args.workload]
     x = synth.make_bsr_inputs(case)
-    counts = synth.bsr_counts(case, x["indptr"])
+    counts = synth.bsr_counts(case, x["indptr"], x["indices"], x["mask"])
     q, k, v = x["q"].cuda(), x["k"].cuda(), x["v"].cuda()
     plan = sfa.bsr_plan(x["indptr"], x["indices"], case.M, case.N, case.R, case.C, case.Hq,
-                        case.Hkv, case.d, sm_scale=case.sm_scale, dtype=case.dtype)
+                        case.Hkv, case.d, sm_scale=case.sm_scale, dtype=case.dtype,
+                        causal=case.causal, mask=x["mask"])
     out = torch.empty_like(q)
     lse = torch.empty((case.M, case.Hq), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -255,7 +256,8 @@ def run_bsr(args, rank, world, local):
            "dtype": case.dtype, "data": "synthetic (seeded generator, shapes of the workload)",
            "config": {"workload": case.name, "M": case.M, "N": case.N, "R": case.R, "C": case.C,
                       "Hq": case.Hq, "Hkv": case.Hkv, "d": case.d, "p": case.p,
-                      "nnz_blocks": counts["nnz"],
+                      "nnz_blocks": counts["nnz"], "causal": case.causal,
+                      "element_mask_keep": case.mask_keep or None,
                       "l2": "q, out (268 MiB) stream through; K/V (67 MiB) L2-resident by design",
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
            "roofline": {"bound": "tensor", "achieved": tflops,

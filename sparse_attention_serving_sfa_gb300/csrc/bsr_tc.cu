@@ -82,10 +82,9 @@ struct BsrTcParams {
     const uint8_t* mask;    // per-element bits (MODE 2)
 };
 
-// The 64-bit word whose bit j is element j of 64 mask elements stored most
-// significant bit first from `p` (8-byte aligned).
-__device__ __forceinline__ uint64_t mask_bits64(const uint8_t* p) {
-    const uint64_t raw = *reinterpret_cast<const uint64_t*>(p);
+// The 64-bit word whose bit j is element j of the 64 mask elements held,
+// most significant bit first, by the 8 bytes `raw` was loaded from.
+__device__ __forceinline__ uint64_t mask_bits64(uint64_t raw) {
     const uint64_t rev = __brevll(raw);     // bit j of byte t now at bit 8 (7 - t) + j
     const uint32_t lo = (uint32_t)rev, hi = (uint32_t)(rev >> 32);
     return ((uint64_t)__byte_perm(lo, 0, 0x0123) << 32) | __byte_perm(hi, 0, 0x0123);
@@ -227,6 +226,19 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         unsigned char* p_hi = smem + L::p + (2 * t) * L::pTile;
         unsigned char* p_lo = p_hi + L::pTile;
         float m_used = -INFINITY, l = 0.f;
+        // per-element mask: this row's 64 bits of block b + 1 are loaded while
+        // block b is processed (8 bytes per row and 64-key block)
+        uint64_t mask_next = 0;
+        auto mask_word = [&](int bb) -> uint64_t {
+            const int i = item.row0 + t * p.TR + r / p.G;
+            if (!(i < row_end && r / p.G < p.TR)) return 0;
+            const int64_t e0 = ((int64_t)(blk0 + bb / sub) * p.R + (i - item.rb * p.R)) * p.C +
+                               (bb % sub) * kKeys;
+            return __ldg(reinterpret_cast<const unsigned long long*>(p.mask + (e0 >> 3)));
+        };
+        if constexpr (MODE == 2) {
+            if (nb > 0) mask_next = mask_word(0);
+        }
         for (int b = 0; b < nb; ++b) {
             mbar_wait(bar(B_S_FULL + t), b & 1, p.err_word, abort_flag);
             tc_fence_after();
@@ -245,13 +257,17 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                                             ((int64_t)p.indices[kb] * p.C + sb * kKeys);
                         am = lim < 0 ? 0ull : (lim >= 63 ? ~0ull : ((2ull << lim) - 1ull));
                     } else {
-                        const int64_t e0 = ((int64_t)kb * p.R + (i - item.rb * p.R)) * p.C + sb * kKeys;
-                        am = mask_bits64(p.mask + (e0 >> 3));
+                        (void)kb;
+                        (void)sb;
+                        am = mask_bits64(mask_next);
                     }
                 }
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
                     if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
+                if constexpr (MODE == 2) {
+                    if (b + 1 < nb) mask_next = mask_word(b + 1);
+                }
             }
             float bmax = -INFINITY;
 #pragma unroll

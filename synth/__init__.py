@@ -183,7 +183,9 @@ BSR = BsrCase("bsr", M=16384, N=16384, R=64, C=64, Hq=32, Hkv=8, d=128, dtype="f
               sm_scale=1.0 / math.sqrt(128), seed=1238)
 
 SFA_WORKLOADS = {c.name: c for c in (TINY, GQA_DECODE, MLA_DECODE, MLA_MTP, PREFILL)}
-BSR_WORKLOADS = {BSR.name: BSR}
+BSR_CAUSAL = BSR.replace(name="bsr_causal", causal=True)
+BSR_MASK = BSR.replace(name="bsr_mask", mask_keep=0.5)
+BSR_WORKLOADS = {c.name: c for c in (BSR, BSR_CAUSAL, BSR_MASK)}
 
 
 def _to_layout(t: torch.Tensor, layout: str) -> torch.Tensor:
@@ -259,16 +261,41 @@ def sfa_counts(case: SfaCase, idx: torch.Tensor | None = None) -> dict:
             "slots": slots, "unmasked_slots": unmasked}
 
 
-def bsr_counts(case: BsrCase, indptr: torch.Tensor) -> dict:
+def bsr_counts(case: BsrCase, indptr: torch.Tensor, indices: torch.Tensor | None = None,
+               mask: np.ndarray | None = None) -> dict:
     """Useful FLOPs (2*2*d per allowed (row, column, qo head)) and the K/V bytes
-    each (row block, kv head) work item reads (64x64 blocks of K and V)."""
+    each (row block, kv head) work item reads (64x64 blocks of K and V).  With
+    a mask the allowed elements are its set bits; with causal (and no mask)
+    those on or below the bottom-right diagonal, and blocks wholly above it
+    are not read."""
     c = case
     ip = indptr.to(torch.int64)
     rows_in_block = torch.full((c.MB,), c.R, dtype=torch.int64)
     rows_in_block[-1] = c.M - (c.MB - 1) * c.R
     blocks_per_row = ip[1:] - ip[:-1]
-    allowed = int((blocks_per_row * rows_in_block).sum()) * c.C
     nnz = int(ip[-1])
+    read_blocks = nnz
+    if mask is not None:
+        # rows past M in the last block row are not query rows
+        valid = np.ones((nnz, c.R, 1), dtype=bool)
+        last0 = int(ip[c.MB - 1])
+        valid[last0:, int(rows_in_block[-1]):, :] = False
+        allowed = int((mask & valid).sum())
+    elif c.causal and indices is not None:
+        ix = indices.to(torch.int64).numpy()
+        allowed, read_blocks = 0, 0
+        off = c.N - c.M
+        for br in range(c.MB):
+            r0, r1 = br * c.R, br * c.R + int(rows_in_block[br])
+            for k in range(int(ip[br]), int(ip[br + 1])):
+                c0 = int(ix[k]) * c.C
+                if c0 > r1 - 1 + off:
+                    continue
+                read_blocks += 1
+                rows = np.arange(r0, r1)
+                allowed += int(np.clip(rows + off - c0 + 1, 0, c.C).sum())
+    else:
+        allowed = int((blocks_per_row * rows_in_block).sum()) * c.C
     flops = 4 * c.d * allowed * c.Hq
-    gathered = nnz * c.C * c.Hkv * c.d * 2 * 2
+    gathered = read_blocks * c.C * c.Hkv * c.d * 2 * 2
     return {"flops": flops, "gathered_bytes": gathered, "nnz": nnz, "allowed": allowed}

@@ -146,3 +146,16 @@ def test_rows_entry_agrees_with_full():
     for n, (i, h) in enumerate(rows):
         np.testing.assert_array_equal(yr[n], y[i, h])
         assert lr[n] == lse[i, h]
+
+
+@pytest.mark.parametrize("kind", ["plain", "causal", "mask"])
+def test_work_counts_match_dense_allowed(kind):
+    """The benchmark's useful-FLOP count is the number of allowed (row, key)
+    pairs of the same dense mask the pins above use."""
+    case = _case(M=100, N=160, causal=(kind == "causal"), mask_keep=(0.4 if kind == "mask" else 0))
+    x = _inputs(case)
+    counts = synth.bsr_counts(case, x["indptr"], x["indices"], x["mask"])
+    allowed = _dense_allowed(x["indptr"], x["indices"], case.M, case.N, case.R, case.C,
+                             mask=x["mask"], causal=case.causal)
+    assert counts["allowed"] == int(allowed.sum())
+    assert counts["flops"] == 4 * case.d * int(allowed.sum()) * case.Hq
