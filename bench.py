@@ -202,6 +202,7 @@ MAIN_KERNEL = {
     "sparse_prefill": "sfa_decode_kernel (one launch per sfa_run_ex call; split index lists merged in-kernel)",
     "mla_decode": "sfa_mla_kernel + sfa_mla_combine (two launches per sfa_run_ex call; time is the call's)",
     "mla_mtp": "sfa_mla_kernel + sfa_mla_combine (two launches per sfa_run_ex call; time is the call's)",
+    "call_example": "sfa_decode_kernel (one launch per sfa_run_ex call; whole index lists per CTA)",
 }
 
 

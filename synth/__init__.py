@@ -182,7 +182,12 @@ PREFILL = SfaCase("sparse_prefill", B=2, S1=2048, S2=16384, N1=64, N2=8, Dk=192,
 BSR = BsrCase("bsr", M=16384, N=16384, R=64, C=64, Hq=32, Hkv=8, d=128, dtype="f16", p=0.10,
               sm_scale=1.0 / math.sqrt(128), seed=1238)
 
-SFA_WORKLOADS = {c.name: c for c in (TINY, GQA_DECODE, MLA_DECODE, MLA_MTP, PREFILL)}
+# The operator page's call example (§6 额外信息): B=2, S1=1024, S2=8192, 32/8 heads,
+# Dk=Dv=128, topK=512, fp16, BSND, non-causal, indices a random permutation prefix per row.
+CALL_EXAMPLE = SfaCase("call_example", B=2, S1=1024, S2=8192, N1=32, N2=8, Dk=128, Dv=128,
+                       topK=512, dtype="f16", layout="BSND", causal=False,
+                       scale=1.0 / math.sqrt(128), seed=1239)
+SFA_WORKLOADS = {c.name: c for c in (TINY, GQA_DECODE, MLA_DECODE, MLA_MTP, PREFILL, CALL_EXAMPLE)}
 BSR_CAUSAL = BSR.replace(name="bsr_causal", causal=True)
 BSR_MASK = BSR.replace(name="bsr_mask", mask_keep=0.5)
 BSR_WORKLOADS = {c.name: c for c in (BSR, BSR_CAUSAL, BSR_MASK)}

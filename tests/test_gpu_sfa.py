@@ -181,7 +181,8 @@ def test_stream_argument():
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled rows
 
-@pytest.mark.parametrize("name", ["gqa_decode", "mla_decode", "mla_mtp", "sparse_prefill"])
+@pytest.mark.parametrize("name", ["gqa_decode", "mla_decode", "mla_mtp", "sparse_prefill",
+                                  "call_example"])
 def test_full_workload_sampled(name):
     case = synth.SFA_WORKLOADS[name]
     d = synth.make_sfa_inputs(case)
