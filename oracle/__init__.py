@@ -60,6 +60,8 @@ def load_library(path: str):
     lib.oracle_bsr_ex.restype = ci
     lib.oracle_bsr_rows_ex.argtypes = bsr_ex + [vp, i64, vp, vp]
     lib.oracle_bsr_rows_ex.restype = ci
+    lib.oracle_varbsr.argtypes = [vp] * 6 + [ci] * 8 + [cd, ci, vp, vp]
+    lib.oracle_varbsr.restype = ci
     return lib
 
 
@@ -221,6 +223,26 @@ def bsr_rows(q, k, v, indptr, indices, M, N, R, C, scale, rows, mask=None, packe
                                     lse.ctypes.data)
     _check(rc, "oracle_bsr_rows")
     del keep
+    return y, lse
+
+
+def varbsr(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, causal=False):
+    """Variable block-sparse attention, HND tensors: q (Hq, M, d), k/v (Hkv, N, d),
+    block_mask_map (Hkv, MB, NB) bool, block_row_sz (Hkv, MB), block_col_sz
+    (Hkv, NB).  Returns (y (Hq, M, d), lse (Hq, M))."""
+    Hq, M, d = q.shape
+    Hkv, N = k.shape[0], k.shape[1]
+    mm = np.ascontiguousarray(np.asarray(block_mask_map, dtype=bool).astype(np.uint8))
+    rs = np.ascontiguousarray(np.asarray(block_row_sz, dtype=np.int32))
+    cs = np.ascontiguousarray(np.asarray(block_col_sz, dtype=np.int32))
+    MB, NB = mm.shape[1], mm.shape[2]
+    y = np.empty((Hq, M, d))
+    lse = np.empty((Hq, M))
+    rc = _load().oracle_varbsr(_ptr(q.contiguous()), _ptr(k.contiguous()), _ptr(v.contiguous()),
+                               mm.ctypes.data, rs.ctypes.data, cs.ctypes.data, MB, NB, M, N, Hq,
+                               Hkv, d, int(bool(causal)), float(scale), _dtype_of(q),
+                               y.ctypes.data, lse.ctypes.data)
+    _check(rc, "oracle_varbsr")
     return y, lse
 
 

@@ -400,3 +400,93 @@ int oracle_bsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     return oracle_bsr_rows_ex(q, k, v, indptr, indices, NULL, 0, M, N, R, C, Hq, Hkv, d, scale,
                               dtype, rows, nrows, y_rows, lse_rows);
 }
+
+/* ---------------------------------------------------------------------- */
+/* Variable block-sparse form -- "flashinfer.sparse",
+ * VariableBlockSparseAttentionWrapper: per kv head g, the query rows are cut
+ * into MB blocks of sizes row_sz[g][0..MB) and the key columns into NB blocks
+ * of sizes col_sz[g][0..NB); query row i of qo head h (kv head
+ * g = h / (Hq / Hkv)) may attend key column j iff
+ * mask_map[g][row block of i][column block of j].  plan() `causal`: read as
+ * the bottom-right rule (j visible to i iff j <= i + (N - M)), applied on top
+ * of the block mask.  Layouts as run(): q (Hq, M, d), k / v (Hkv, N, d)
+ * (HND); y (Hq, M, d) and lse (Hq, M) follow q's layout (the page's return
+ * description prints [M, num_qo_heads, head_dim]; read as q's own layout).
+ * mask_map bytes are 0 / nonzero.  Every g's row sizes sum to M and column
+ * sizes to N (else -1). */
+int oracle_varbsr(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                  const uint8_t* mask_map, const int32_t* row_sz, const int32_t* col_sz, int MB,
+                  int NB, int M, int N, int Hq, int Hkv, int d, int causal, double scale,
+                  int dtype, double* y, double* lse) {
+    if (MB < 1 || NB < 1 || M < 1 || N < 1 || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0)
+        return ORACLE_BAD_ARG;
+    if (dtype != 0 && dtype != 1) return ORACLE_BAD_ARG;
+    for (int g = 0; g < Hkv; ++g) {
+        int64_t sr = 0, sc = 0;
+        for (int b = 0; b < MB; ++b) {
+            if (row_sz[(int64_t)g * MB + b] < 0) return ORACLE_BAD_ARG;
+            sr += row_sz[(int64_t)g * MB + b];
+        }
+        for (int b = 0; b < NB; ++b) {
+            if (col_sz[(int64_t)g * NB + b] < 0) return ORACLE_BAD_ARG;
+            sc += col_sz[(int64_t)g * NB + b];
+        }
+        if (sr != M || sc != N) return ORACLE_BAD_ARG;
+    }
+    const int G = Hq / Hkv;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        int* colblk = (int*)malloc(sizeof(int) * (size_t)N);
+        double* scores = (double*)malloc(sizeof(double) * (size_t)N);
+        unsigned char* allowed = (unsigned char*)malloc((size_t)N);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < (int64_t)Hq * M; ++r) {
+            if (!colblk || !scores || !allowed) {
+#pragma omp atomic write
+                err = ORACLE_BAD_ARG;
+                continue;
+            }
+            const int h = (int)(r / M), i = (int)(r % M), g = h / G;
+            /* row block of i, column block of every j, for kv head g */
+            int rb = 0, acc = 0;
+            while (acc + row_sz[(int64_t)g * MB + rb] <= i) acc += row_sz[(int64_t)g * MB + rb++];
+            for (int cb = 0, j = 0; cb < NB; ++cb)
+                for (int c = 0; c < col_sz[(int64_t)g * NB + cb]; ++c) colblk[j++] = cb;
+            double mx = -INFINITY;
+            for (int j = 0; j < N; ++j) {
+                allowed[j] = mask_map[((int64_t)g * MB + rb) * NB + colblk[j]] != 0;
+                if (causal && (int64_t)j > (int64_t)i + (N - M)) allowed[j] = 0;
+                if (!allowed[j]) continue;
+                double dot = 0.0;
+                for (int e = 0; e < d; ++e)
+                    dot += oracle_load(q, ((int64_t)h * M + i) * d + e, dtype) *
+                           oracle_load(k, ((int64_t)g * N + j) * d + e, dtype);
+                scores[j] = dot * scale;
+                if (scores[j] > mx) mx = scores[j];
+            }
+            double* yr = y + r * d;
+            for (int e = 0; e < d; ++e) yr[e] = 0.0;
+            if (mx == -INFINITY) {
+                if (lse) lse[r] = -INFINITY;
+                continue;
+            }
+            double sum = 0.0;
+            for (int j = 0; j < N; ++j)
+                if (allowed[j]) {
+                    scores[j] = exp(scores[j] - mx);
+                    sum += scores[j];
+                }
+            for (int j = 0; j < N; ++j) {
+                if (!allowed[j]) continue;
+                const double w = scores[j] / sum;
+                for (int e = 0; e < d; ++e) yr[e] += w * oracle_load(v, ((int64_t)g * N + j) * d + e, dtype);
+            }
+            if (lse) lse[r] = mx + log(sum);
+        }
+        free(colblk);
+        free(scores);
+        free(allowed);
+    }
+    return err;
+}

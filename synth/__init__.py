@@ -193,6 +193,35 @@ BSR_MASK = BSR.replace(name="bsr_mask", mask_keep=0.5)
 BSR_WORKLOADS = {c.name: c for c in (BSR, BSR_CAUSAL, BSR_MASK)}
 
 
+@dataclasses.dataclass(frozen=True)
+class VarBsrCase:
+    """One variable block-sparse problem (per-kv-head block masks and block
+    sizes, HND tensors) and its input recipe."""
+
+    name: str
+    M: int              # qo_len
+    N: int              # kv_len
+    MB: int             # row blocks per kv head
+    NB: int             # column blocks per kv head
+    Hq: int
+    Hkv: int
+    d: int
+    dtype: str
+    p: float            # each (kv head, row block, column block) set with this probability
+    sm_scale: float
+    seed: int = 1240
+    causal: bool = False
+
+    def replace(self, **kw) -> "VarBsrCase":
+        return dataclasses.replace(self, **kw)
+
+
+# 16384 x 16384 per head, 256 x 256 blocks of random sizes (mean 64), 10% set
+VARBSR = VarBsrCase("varbsr", M=16384, N=16384, MB=256, NB=256, Hq=32, Hkv=8, d=128,
+                    dtype="f16", p=0.10, sm_scale=1.0 / math.sqrt(128))
+VARBSR_WORKLOADS = {VARBSR.name: VARBSR}
+
+
 def _to_layout(t: torch.Tensor, layout: str) -> torch.Tensor:
     """Canonical [B, S, N, D] -> the requested layout (contiguous)."""
     return t if layout == "BSND" else t.permute(0, 2, 1, 3).contiguous()
@@ -242,6 +271,56 @@ def make_bsr_inputs(case: BsrCase) -> dict:
     if c.mask_keep > 0:
         out["mask"] = bsr_mask(c.seed + 2, int(indptr[-1]), c.R, c.C, c.mask_keep)
     return out
+
+
+def block_sizes(rng, heads: int, nblocks: int, total: int) -> np.ndarray:
+    """(heads, nblocks) int32 sizes summing to `total` per head: nblocks - 1
+    cut points drawn uniformly from [0, total] (so a block may be empty)."""
+    cuts = np.sort(rng.integers(0, total + 1, size=(heads, nblocks - 1)), axis=1)
+    edges = np.concatenate([np.zeros((heads, 1), np.int64), cuts,
+                            np.full((heads, 1), total, np.int64)], axis=1)
+    return np.diff(edges, axis=1).astype(np.int32)
+
+
+def make_varbsr_inputs(case: VarBsrCase) -> dict:
+    """CPU tensors q (Hq,M,d), k/v (Hkv,N,d) in HND order, and (numpy PCG64
+    streams of seed + 1) the (Hkv,MB,NB) bool block mask map and int32 row
+    (Hkv,MB) and column (Hkv,NB) block sizes."""
+    c = case
+    q = normal(c.seed, 0, (c.Hq, c.M, c.d), c.dtype)
+    k = normal(c.seed, 1, (c.Hkv, c.N, c.d), c.dtype)
+    v = normal(c.seed, 2, (c.Hkv, c.N, c.d), c.dtype)
+    rng = np.random.Generator(np.random.PCG64(c.seed + 1))
+    row_sz = block_sizes(rng, c.Hkv, c.MB, c.M)
+    col_sz = block_sizes(rng, c.Hkv, c.NB, c.N)
+    mask_map = rng.random((c.Hkv, c.MB, c.NB)) < c.p
+    return {"q": q, "k": k, "v": v, "block_mask_map": mask_map, "block_row_sz": row_sz,
+            "block_col_sz": col_sz}
+
+
+def varbsr_counts(case: VarBsrCase, mask_map, row_sz, col_sz) -> dict:
+    """Useful FLOPs (2*2*d per allowed (row, column, qo head)).  Without causal
+    the allowed elements of kv head g are the sum over set blocks of
+    row size x column size; with causal, those on or below the bottom-right
+    diagonal."""
+    c = case
+    G = c.Hq // c.Hkv
+    allowed = 0
+    for g in range(c.Hkv):
+        rs = np.asarray(row_sz[g], np.int64)
+        cs = np.asarray(col_sz[g], np.int64)
+        mm = np.asarray(mask_map[g], bool)
+        if not c.causal:
+            allowed += int((rs[:, None] * cs[None, :] * mm).sum())
+            continue
+        r0 = np.concatenate([[0], np.cumsum(rs)[:-1]])
+        c0 = np.concatenate([[0], np.cumsum(cs)[:-1]])
+        off = c.N - c.M
+        for rb in range(c.MB):
+            rows = np.arange(r0[rb], r0[rb] + rs[rb])
+            for cb in np.nonzero(mm[rb])[0]:
+                allowed += int(np.clip(rows + off - c0[cb] + 1, 0, cs[cb]).sum())
+    return {"flops": 4 * c.d * allowed * G, "allowed": allowed * G}   # (row, column, qo head)
 
 
 def sfa_counts(case: SfaCase, idx: torch.Tensor | None = None) -> dict:

@@ -16,6 +16,8 @@ def _read(name):
             key, *vals = line.split()
             if key in ("row", "mask_row"):
                 out["rows"].append([int(x) for x in vals])
+            elif key == "block_mask_row":
+                out.setdefault("block_rows", []).append([int(x) for x in vals])
             elif len(vals) == 1:
                 out[key] = int(vals[0])
             else:
@@ -32,4 +34,13 @@ def bsr_3x3_example():
 def causal_bottom_right():
     d = _read("causal_bottom_right.txt")
     d["mask"] = np.array(d.pop("rows"), dtype=bool)
+    return d
+
+
+def varbsr_example():
+    d = _read("varbsr_example.txt")
+    d["mask"] = np.array(d.pop("rows"), dtype=bool)
+    d["block_mask_map"] = np.array(d.pop("block_rows"), dtype=bool)[None]
+    d["block_row_sz"] = np.array(d["block_row_sz"], dtype=np.int32)[None]
+    d["block_col_sz"] = np.array(d["block_col_sz"], dtype=np.int32)[None]
     return d

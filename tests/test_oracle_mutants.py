@@ -11,6 +11,7 @@ import pytest
 import oracle
 from tests import test_oracle_bsr_mask as mpins
 from tests import test_oracle_pins as pins
+from tests import test_oracle_varbsr as vpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "sfa_oracle.c")
 
@@ -44,6 +45,15 @@ MUTANTS = [
     ("bsr_causal_with_mask", "if (!s->packed_mask && s->causal)", "if (s->causal)"),
     ("bsr_row_block_reversed", "const int br = i / s->R;", "const int br = (s->M - 1 - i) / s->R;"),
     ("bsr_scale_dropped", "scores[j] = dot * s->scale;", "scores[j] = dot;"),
+    ("varbsr_kv_head_map", "i = (int)(r % M), g = h / G;", "i = (int)(r % M), g = h % Hkv;"),
+    ("varbsr_row_block_off_by_one", "while (acc + row_sz[(int64_t)g * MB + rb] <= i)",
+     "while (acc + row_sz[(int64_t)g * MB + rb] < i)"),
+    ("varbsr_col_sizes_of_head0", "for (int c = 0; c < col_sz[(int64_t)g * NB + cb]; ++c)",
+     "for (int c = 0; c < col_sz[cb]; ++c)"),
+    ("varbsr_mask_map_transposed", "mask_map[((int64_t)g * MB + rb) * NB + colblk[j]]",
+     "mask_map[((int64_t)g * NB + colblk[j]) * MB + rb]"),
+    ("varbsr_causal_top_left", "if (causal && (int64_t)j > (int64_t)i + (N - M)) allowed[j] = 0;",
+     "if (causal && (int64_t)j > (int64_t)i) allowed[j] = 0;"),
     ("bf16_as_f16", "return dtype == 1 ? oracle_bf16(p[i]) : oracle_f16(p[i]);",
      "return oracle_f16(p[i]);"),
 ]
@@ -69,6 +79,12 @@ def all_pins():
     for mn in ((128, 128), (96, 128)):
         out.append(lambda a=mn: mpins.test_causal_matches_dense_bottom_right(*a))
     out.append(lambda: mpins.test_mask_matches_dense(0.3))
+    # variable block-sparse pins
+    out += [vpins.test_worked_example_expands_as_printed, vpins.test_kv_heads_keep_their_own_masks,
+            vpins.test_single_block_equals_dense_sdpa, vpins.test_empty_blocks_and_fully_masked_rows,
+            vpins.test_uniform_keys_give_mean_of_allowed_values]
+    for causal in (False, True):
+        out.append(lambda c=causal: vpins.test_matches_dense_brute_force(c, "f16"))
     return out
 
 
