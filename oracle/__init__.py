@@ -62,6 +62,8 @@ def load_library(path: str):
     lib.oracle_bsr_rows_ex.restype = ci
     lib.oracle_varbsr.argtypes = [vp] * 6 + [ci] * 8 + [cd, ci, vp, vp]
     lib.oracle_varbsr.restype = ci
+    lib.oracle_varbsr_rows.argtypes = [vp] * 6 + [ci] * 8 + [cd, ci, vp, ctypes.c_int64, vp, vp]
+    lib.oracle_varbsr_rows.restype = ci
     return lib
 
 
@@ -243,6 +245,26 @@ def varbsr(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, causal=Fa
                                Hkv, d, int(bool(causal)), float(scale), _dtype_of(q),
                                y.ctypes.data, lse.ctypes.data)
     _check(rc, "oracle_varbsr")
+    return y, lse
+
+
+def varbsr_rows(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, rows, causal=False):
+    """Rows `rows` (flat h * M + i) of varbsr(): (y (n, d), lse (n))."""
+    Hq, M, d = q.shape
+    Hkv, N = k.shape[0], k.shape[1]
+    mm = np.ascontiguousarray(np.asarray(block_mask_map, dtype=bool).astype(np.uint8))
+    rs = np.ascontiguousarray(np.asarray(block_row_sz, dtype=np.int32))
+    cs = np.ascontiguousarray(np.asarray(block_col_sz, dtype=np.int32))
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows.shape[0]
+    y = np.empty((n, d))
+    lse = np.empty(n)
+    rc = _load().oracle_varbsr_rows(_ptr(q.contiguous()), _ptr(k.contiguous()),
+                                    _ptr(v.contiguous()), mm.ctypes.data, rs.ctypes.data,
+                                    cs.ctypes.data, mm.shape[1], mm.shape[2], M, N, Hq, Hkv, d,
+                                    int(bool(causal)), float(scale), _dtype_of(q),
+                                    rows.ctypes.data, n, y.ctypes.data, lse.ctypes.data)
+    _check(rc, "oracle_varbsr_rows")
     return y, lse
 
 

@@ -414,27 +414,121 @@ int oracle_bsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * description prints [M, num_qo_heads, head_dim]; read as q's own layout).
  * mask_map bytes are 0 / nonzero.  Every g's row sizes sum to M and column
  * sizes to N (else -1). */
+typedef struct {
+    const uint16_t *q, *k, *v;
+    const uint8_t* mask_map;
+    const int32_t *row_sz, *col_sz;
+    int MB, NB, M, N, Hq, Hkv, d, causal, dtype;
+    double scale;
+} varbsr_problem;
+
+/* Row r = h * M + i of the variable block-sparse output (y_row: d values).
+ * colblk, scores, allowed: N-element scratch. */
+static void varbsr_row(const varbsr_problem* s, int64_t r, int* colblk, double* scores,
+                       unsigned char* allowed, double* y_row, double* lse_row) {
+    const int G = s->Hq / s->Hkv;
+    const int h = (int)(r / s->M), i = (int)(r % s->M), g = h / G;
+    const int MB = s->MB, NB = s->NB, N = s->N, M = s->M, d = s->d;
+    const int32_t *row_sz = s->row_sz, *col_sz = s->col_sz;
+    /* row block of i, column block of every j, for kv head g */
+    int rb = 0, acc = 0;
+    while (acc + row_sz[(int64_t)g * MB + rb] <= i) acc += row_sz[(int64_t)g * MB + rb++];
+    for (int cb = 0, j = 0; cb < NB; ++cb)
+        for (int c = 0; c < col_sz[(int64_t)g * NB + cb]; ++c) colblk[j++] = cb;
+    double mx = -INFINITY;
+    for (int j = 0; j < N; ++j) {
+        allowed[j] = s->mask_map[((int64_t)g * MB + rb) * NB + colblk[j]] != 0;
+        if (s->causal && (int64_t)j > (int64_t)i + (N - M)) allowed[j] = 0;
+        if (!allowed[j]) continue;
+        double dot = 0.0;
+        for (int e = 0; e < d; ++e)
+            dot += oracle_load(s->q, ((int64_t)h * M + i) * d + e, s->dtype) *
+                   oracle_load(s->k, ((int64_t)g * N + j) * d + e, s->dtype);
+        scores[j] = dot * s->scale;
+        if (scores[j] > mx) mx = scores[j];
+    }
+    for (int e = 0; e < d; ++e) y_row[e] = 0.0;
+    if (mx == -INFINITY) {
+        if (lse_row) *lse_row = -INFINITY;
+        return;
+    }
+    double sum = 0.0;
+    for (int j = 0; j < N; ++j)
+        if (allowed[j]) {
+            scores[j] = exp(scores[j] - mx);
+            sum += scores[j];
+        }
+    for (int j = 0; j < N; ++j) {
+        if (!allowed[j]) continue;
+        const double w = scores[j] / sum;
+        for (int e = 0; e < d; ++e) y_row[e] += w * oracle_load(s->v, ((int64_t)g * N + j) * d + e, s->dtype);
+    }
+    if (lse_row) *lse_row = mx + log(sum);
+}
+
+static int varbsr_setup(varbsr_problem* s) {
+    const int MB = s->MB, NB = s->NB;
+    if (MB < 1 || NB < 1 || s->M < 1 || s->N < 1 || s->Hq < 1 || s->Hkv < 1 || s->d < 1 ||
+        s->Hq % s->Hkv != 0)
+        return ORACLE_BAD_ARG;
+    if (s->dtype != 0 && s->dtype != 1) return ORACLE_BAD_ARG;
+    for (int g = 0; g < s->Hkv; ++g) {
+        int64_t sr = 0, sc = 0;
+        for (int b = 0; b < MB; ++b) {
+            if (s->row_sz[(int64_t)g * MB + b] < 0) return ORACLE_BAD_ARG;
+            sr += s->row_sz[(int64_t)g * MB + b];
+        }
+        for (int b = 0; b < NB; ++b) {
+            if (s->col_sz[(int64_t)g * NB + b] < 0) return ORACLE_BAD_ARG;
+            sc += s->col_sz[(int64_t)g * NB + b];
+        }
+        if (sr != s->M || sc != s->N) return ORACLE_BAD_ARG;
+    }
+    return ORACLE_OK;
+}
+
+/* Rows rows[0..n) (each h * M + i) of the output: y (n, d), lse (n). */
+int oracle_varbsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const uint8_t* mask_map, const int32_t* row_sz, const int32_t* col_sz,
+                       int MB, int NB, int M, int N, int Hq, int Hkv, int d, int causal,
+                       double scale, int dtype, const int64_t* rows, int64_t n, double* y,
+                       double* lse) {
+    varbsr_problem s = {q, k, v, mask_map, row_sz, col_sz, MB, NB, M, N, Hq, Hkv, d, causal, dtype,
+                        scale};
+    int err = varbsr_setup(&s);
+    if (err != ORACLE_OK) return err;
+    for (int64_t t = 0; t < n; ++t)
+        if (rows[t] < 0 || rows[t] >= (int64_t)Hq * M) return ORACLE_BAD_ARG;
+#pragma omp parallel
+    {
+        int* colblk = (int*)malloc(sizeof(int) * (size_t)N);
+        double* scores = (double*)malloc(sizeof(double) * (size_t)N);
+        unsigned char* allowed = (unsigned char*)malloc((size_t)N);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < n; ++t) {
+            if (!colblk || !scores || !allowed) {
+#pragma omp atomic write
+                err = ORACLE_BAD_ARG;
+                continue;
+            }
+            varbsr_row(&s, rows[t], colblk, scores, allowed, y + t * d, lse ? lse + t : NULL);
+        }
+        free(colblk);
+        free(scores);
+        free(allowed);
+    }
+    return err;
+}
+
+/* The whole output: y (Hq, M, d), lse (Hq, M). */
 int oracle_varbsr(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                   const uint8_t* mask_map, const int32_t* row_sz, const int32_t* col_sz, int MB,
                   int NB, int M, int N, int Hq, int Hkv, int d, int causal, double scale,
                   int dtype, double* y, double* lse) {
-    if (MB < 1 || NB < 1 || M < 1 || N < 1 || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv != 0)
-        return ORACLE_BAD_ARG;
-    if (dtype != 0 && dtype != 1) return ORACLE_BAD_ARG;
-    for (int g = 0; g < Hkv; ++g) {
-        int64_t sr = 0, sc = 0;
-        for (int b = 0; b < MB; ++b) {
-            if (row_sz[(int64_t)g * MB + b] < 0) return ORACLE_BAD_ARG;
-            sr += row_sz[(int64_t)g * MB + b];
-        }
-        for (int b = 0; b < NB; ++b) {
-            if (col_sz[(int64_t)g * NB + b] < 0) return ORACLE_BAD_ARG;
-            sc += col_sz[(int64_t)g * NB + b];
-        }
-        if (sr != M || sc != N) return ORACLE_BAD_ARG;
-    }
-    const int G = Hq / Hkv;
-    int err = ORACLE_OK;
+    varbsr_problem s = {q, k, v, mask_map, row_sz, col_sz, MB, NB, M, N, Hq, Hkv, d, causal, dtype,
+                        scale};
+    int err = varbsr_setup(&s);
+    if (err != ORACLE_OK) return err;
 #pragma omp parallel
     {
         int* colblk = (int*)malloc(sizeof(int) * (size_t)N);
@@ -447,42 +541,7 @@ int oracle_varbsr(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                 err = ORACLE_BAD_ARG;
                 continue;
             }
-            const int h = (int)(r / M), i = (int)(r % M), g = h / G;
-            /* row block of i, column block of every j, for kv head g */
-            int rb = 0, acc = 0;
-            while (acc + row_sz[(int64_t)g * MB + rb] <= i) acc += row_sz[(int64_t)g * MB + rb++];
-            for (int cb = 0, j = 0; cb < NB; ++cb)
-                for (int c = 0; c < col_sz[(int64_t)g * NB + cb]; ++c) colblk[j++] = cb;
-            double mx = -INFINITY;
-            for (int j = 0; j < N; ++j) {
-                allowed[j] = mask_map[((int64_t)g * MB + rb) * NB + colblk[j]] != 0;
-                if (causal && (int64_t)j > (int64_t)i + (N - M)) allowed[j] = 0;
-                if (!allowed[j]) continue;
-                double dot = 0.0;
-                for (int e = 0; e < d; ++e)
-                    dot += oracle_load(q, ((int64_t)h * M + i) * d + e, dtype) *
-                           oracle_load(k, ((int64_t)g * N + j) * d + e, dtype);
-                scores[j] = dot * scale;
-                if (scores[j] > mx) mx = scores[j];
-            }
-            double* yr = y + r * d;
-            for (int e = 0; e < d; ++e) yr[e] = 0.0;
-            if (mx == -INFINITY) {
-                if (lse) lse[r] = -INFINITY;
-                continue;
-            }
-            double sum = 0.0;
-            for (int j = 0; j < N; ++j)
-                if (allowed[j]) {
-                    scores[j] = exp(scores[j] - mx);
-                    sum += scores[j];
-                }
-            for (int j = 0; j < N; ++j) {
-                if (!allowed[j]) continue;
-                const double w = scores[j] / sum;
-                for (int e = 0; e < d; ++e) yr[e] += w * oracle_load(v, ((int64_t)g * N + j) * d + e, dtype);
-            }
-            if (lse) lse[r] = mx + log(sum);
+            varbsr_row(&s, r, colblk, scores, allowed, y + r * d, lse ? lse + r : NULL);
         }
         free(colblk);
         free(scores);

@@ -24,7 +24,10 @@ MUTANTS = [
     ("softmax_unnormalised", "weights[i] /= sum;", "weights[i] /= 1.0;"),
     ("lse_base2", "weights[i] /= sum;\n    if (lse_row) *lse_row = mx + log(sum);",
      "weights[i] /= sum;\n    if (lse_row) *lse_row = mx + log2(sum);"),
-    ("bsr_lse_base2", "if (lse_row) *lse_row = mx + log(sum);\n}", "if (lse_row) *lse_row = mx + log2(sum);\n}"),
+    ("bsr_lse_base2", "y_row[e] += w * oracle_load(v, vo + e, s->dtype);\n    }\n    if (lse_row) *lse_row = mx + log(sum);",
+     "y_row[e] += w * oracle_load(v, vo + e, s->dtype);\n    }\n    if (lse_row) *lse_row = mx + log2(sum);"),
+    ("varbsr_lse_base2", "* d + e, s->dtype);\n    }\n    if (lse_row) *lse_row = mx + log(sum);",
+     "* d + e, s->dtype);\n    }\n    if (lse_row) *lse_row = mx + log2(sum);"),
     ("bnsd_index_as_bsnd", ": (((int64_t)b * s->N2 + n2) * s->S1 + s1) * s->topK;",
      ": (((int64_t)b * s->S1 + s1) * s->N2 + n2) * s->topK;"),
     ("value_stride_dv", "const int64_t vo = row_kv(s, b, n2, si[i]) * s->ldv;",
@@ -44,16 +47,19 @@ MUTANTS = [
      "if ((int64_t)j > (int64_t)i) allowed[j] = 0;"),
     ("bsr_causal_with_mask", "if (!s->packed_mask && s->causal)", "if (s->causal)"),
     ("bsr_row_block_reversed", "const int br = i / s->R;", "const int br = (s->M - 1 - i) / s->R;"),
-    ("bsr_scale_dropped", "scores[j] = dot * s->scale;", "scores[j] = dot;"),
-    ("varbsr_kv_head_map", "i = (int)(r % M), g = h / G;", "i = (int)(r % M), g = h % Hkv;"),
+    ("bsr_scale_dropped", "oracle_load(k, ko + e, s->dtype);\n        scores[j] = dot * s->scale;",
+     "oracle_load(k, ko + e, s->dtype);\n        scores[j] = dot;"),
+    ("varbsr_scale_dropped", "* d + e, s->dtype);\n        scores[j] = dot * s->scale;",
+     "* d + e, s->dtype);\n        scores[j] = dot;"),
+    ("varbsr_kv_head_map", "i = (int)(r % s->M), g = h / G;", "i = (int)(r % s->M), g = h % s->Hkv;"),
     ("varbsr_row_block_off_by_one", "while (acc + row_sz[(int64_t)g * MB + rb] <= i)",
      "while (acc + row_sz[(int64_t)g * MB + rb] < i)"),
     ("varbsr_col_sizes_of_head0", "for (int c = 0; c < col_sz[(int64_t)g * NB + cb]; ++c)",
      "for (int c = 0; c < col_sz[cb]; ++c)"),
     ("varbsr_mask_map_transposed", "mask_map[((int64_t)g * MB + rb) * NB + colblk[j]]",
      "mask_map[((int64_t)g * NB + colblk[j]) * MB + rb]"),
-    ("varbsr_causal_top_left", "if (causal && (int64_t)j > (int64_t)i + (N - M)) allowed[j] = 0;",
-     "if (causal && (int64_t)j > (int64_t)i) allowed[j] = 0;"),
+    ("varbsr_causal_top_left", "if (s->causal && (int64_t)j > (int64_t)i + (N - M)) allowed[j] = 0;",
+     "if (s->causal && (int64_t)j > (int64_t)i) allowed[j] = 0;"),
     ("bf16_as_f16", "return dtype == 1 ? oracle_bf16(p[i]) : oracle_f16(p[i]);",
      "return oracle_f16(p[i]);"),
 ]

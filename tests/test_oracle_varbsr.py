@@ -160,6 +160,18 @@ def test_rejects_sizes_that_do_not_sum():
                       np.array([[7, -1]], np.int32), 0.5)
 
 
+def test_rows_entry_equals_full_output():
+    c = _case(causal=True, Hq=8, Hkv=2)
+    x = synth.make_varbsr_inputs(c)
+    args = (x["q"], x["k"], x["v"], x["block_mask_map"], x["block_row_sz"], x["block_col_sz"],
+            c.sm_scale)
+    y, lse = oracle.varbsr(*args, causal=True)
+    rows = np.array([0, 5, c.M - 1, c.M, 3 * c.M + 17, c.Hq * c.M - 1])
+    yr, lr = oracle.varbsr_rows(*args, rows=rows, causal=True)
+    np.testing.assert_array_equal(yr, y.reshape(-1, c.d)[rows])
+    np.testing.assert_array_equal(lr, lse.reshape(-1)[rows])
+
+
 def test_counts_match_dense_mask():
     for causal in (False, True):
         c = _case(causal=causal)
