@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_decode",
-                    choices=sorted(synth.SFA_WORKLOADS) + sorted(synth.BSR_WORKLOADS))
+                    choices=sorted(synth.SFA_WORKLOADS) + sorted(synth.BSR_WORKLOADS)
+                    + sorted(synth.VARBSR_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--replicas", type=int, default=0,
@@ -209,8 +210,9 @@ MAIN_KERNEL = {
 # ---------------------------------------------------------------------------
 
 def run_bsr(args, rank, world, local):
-    """Block-sparse workload (tensor-bound): one step = one bsr_run over the
-    whole 16384 x 16384 pattern (plan built once, outside the timed region)."""
+    """Block-sparse workloads (tensor-bound): one step = one bsr_run (or
+    varbsr_run) over the whole 16384 x 16384 pattern (plan built once, outside
+    the timed region)."""
     import sparse_attention_serving_sfa_gb300 as sfa
 
     torch.cuda.set_device(local)
@@ -219,18 +221,40 @@ def run_bsr(args, rank, world, local):
         dist.init_process_group("nccl")
     sfa.build()
     sfa.load()
-    case = synth.BSR_WORKLOADS[args.workload]
-    x = synth.make_bsr_inputs(case)
-    counts = synth.bsr_counts(case, x["indptr"], x["indices"], x["mask"])
+    variable = args.workload in synth.VARBSR_WORKLOADS
+    if variable:
+        case = synth.VARBSR_WORKLOADS[args.workload]
+        x = synth.make_varbsr_inputs(case)
+        counts = synth.varbsr_counts(case, x["block_mask_map"], x["block_row_sz"],
+                                     x["block_col_sz"])
+        plan = sfa.varbsr_plan(x["block_mask_map"], x["block_row_sz"], x["block_col_sz"],
+                               case.Hq, case.Hkv, case.d, causal=case.causal,
+                               sm_scale=case.sm_scale, dtype=case.dtype)
+        run = sfa.varbsr_run
+        lse_shape = (case.Hq, case.M)
+        shape_cfg = {"layout": "HND", "MB": case.MB, "NB": case.NB,
+                     "block_sizes": "per kv head, uniform random cut points (mean "
+                                    f"{case.M // case.MB} x {case.N // case.NB})",
+                     "key_tiles": int(plan.int_ws.cpu().view(torch.int32)[case.Hkv * case.MB])}
+        kernel = "bsr_tc_kernel, variable mode (one launch per varbsr_run)"
+    else:
+        case = synth.BSR_WORKLOADS[args.workload]
+        x = synth.make_bsr_inputs(case)
+        counts = synth.bsr_counts(case, x["indptr"], x["indices"], x["mask"])
+        plan = sfa.bsr_plan(x["indptr"], x["indices"], case.M, case.N, case.R, case.C, case.Hq,
+                            case.Hkv, case.d, sm_scale=case.sm_scale, dtype=case.dtype,
+                            causal=case.causal, mask=x["mask"])
+        run = sfa.bsr_run
+        lse_shape = (case.M, case.Hq)
+        shape_cfg = {"layout": "NHD", "R": case.R, "C": case.C, "nnz_blocks": counts["nnz"],
+                     "element_mask_keep": case.mask_keep or None}
+        kernel = "bsr_tc_kernel (one launch per bsr_run)"
     q, k, v = x["q"].cuda(), x["k"].cuda(), x["v"].cuda()
-    plan = sfa.bsr_plan(x["indptr"], x["indices"], case.M, case.N, case.R, case.C, case.Hq,
-                        case.Hkv, case.d, sm_scale=case.sm_scale, dtype=case.dtype,
-                        causal=case.causal, mask=x["mask"])
     out = torch.empty_like(q)
-    lse = torch.empty((case.M, case.Hq), dtype=torch.float32, device="cuda")
+    lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     for _ in range(max(args.warmup, 3)):
-        sfa.bsr_run(plan, q, k, v, out, lse, stream)
+        run(plan, q, k, v, out, lse, stream)
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
@@ -242,7 +266,7 @@ def run_bsr(args, rank, world, local):
     launches0 = sfa.sfa_kernel_launches()
     ev0.record(stream)
     for _ in range(args.steps):
-        sfa.bsr_run(plan, q, k, v, out, lse, stream)
+        run(plan, q, k, v, out, lse, stream)
     ev1.record(stream)
     torch.cuda.synchronize()
     launches = sfa.sfa_kernel_launches() - launches0
@@ -255,19 +279,19 @@ def run_bsr(args, rank, world, local):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": case.dtype, "data": "synthetic (seeded generator, shapes of the workload)",
-           "config": {"workload": case.name, "M": case.M, "N": case.N, "R": case.R, "C": case.C,
+           "config": {"workload": case.name, "M": case.M, "N": case.N, **shape_cfg,
                       "Hq": case.Hq, "Hkv": case.Hkv, "d": case.d, "p": case.p,
-                      "nnz_blocks": counts["nnz"], "causal": case.causal,
-                      "element_mask_keep": case.mask_keep or None,
+                      "causal": case.causal,
                       "l2": "q, out (268 MiB) stream through; K/V (67 MiB) L2-resident by design",
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
            "roofline": {"bound": "tensor", "achieved": tflops,
                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                        "frac": tflops / peaks["bf16_tflops_sustained"], "traffic": committed_traffic("bsr"),
+                        "frac": tflops / peaks["bf16_tflops_sustained"],
+                        "traffic": committed_traffic("varbsr" if variable else "bsr"),
                         "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 dense rate is the same)",
-                        "kernel": "bsr_tc_kernel (one launch per bsr_run)"},
+                        "kernel": kernel},
            "gpu_launches": launches, "clocks": clocks,
-           "work": {"flops": counts["flops"], "gathered_bytes": counts["gathered_bytes"]}}
+           "work": {"flops": counts["flops"], "allowed_elements": counts["allowed"]}}
     if world > 1:
         torch.distributed.destroy_process_group()
     return res
@@ -489,7 +513,7 @@ def main():
             return 0
         print(json.dumps(run_reference(args, rank, world)))
         return 0
-    if args.workload in synth.BSR_WORKLOADS:
+    if args.workload in synth.BSR_WORKLOADS or args.workload in synth.VARBSR_WORKLOADS:
         res = run_bsr(args, rank, world, local)
     else:
         res = run_ours(args, rank, world, local)

@@ -281,6 +281,81 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
  * caller's workspaces. */
 void bsr_plan_destroy(bsr_plan_t plan);
 
+/* ------------------------------------------------------------------------ */
+/* Variable block-sparse attention ("flashinfer.sparse",
+ * VariableBlockSparseAttentionWrapper: blocks of any size given per kv head
+ * by block_row_sz / block_col_sz, and each kv head its own block mask). */
+
+typedef struct varbsr_plan_s* varbsr_plan_t;
+
+/*
+ * varbsr_plan -- validate the block mask map and sizes and build the device
+ * work list (plan()).
+ *
+ *   block_mask_map_host  host bytes (num_kv_heads, MB, NB), row-major; a
+ *                 nonzero byte marks block (row block, column block) of that
+ *                 kv head as attended.
+ *   block_row_sz_host    host int32 (num_kv_heads, MB), each >= 0; every kv
+ *                 head's row sizes sum to the same qo_len >= 1.
+ *   block_col_sz_host    host int32 (num_kv_heads, NB), each >= 0; every kv
+ *                 head's column sizes sum to the same kv_len >= 1.
+ *                 Query row i of qo head h attends key column j iff the
+ *                 block of kv head g = h / (num_qo_heads / num_kv_heads)
+ *                 holding (i, j) is set: row block b spans the rows after
+ *                 the first b row sizes of g, column blocks likewise.
+ *   MB, NB        number of row / column blocks (>= 1).
+ *   num_qo_heads, num_kv_heads   num_qo_heads % num_kv_heads == 0; this
+ *                 build needs 128 % (num_qo_heads / num_kv_heads) == 0
+ *                 (SFA_ERR_UNSUPPORTED otherwise).
+ *   head_dim      64 or 128 in this build (SFA_ERR_UNSUPPORTED otherwise).
+ *   causal        nonzero: also key j <= i + (kv_len - qo_len) (the
+ *                 bottom-right rule bsr_plan uses; the page does not state
+ *                 the alignment for qo_len != kv_len).
+ *   sm_scale      softmax scale; <= 0 selects 1/sqrt(head_dim).
+ *   dtype         element type of q, k, v and out.
+ *   int_ws        device buffer, 16-byte aligned, that the key tile lists
+ *                 and work list are copied into (on `stream`); size from
+ *                 varbsr_plan_int_workspace_size() with the same arguments.
+ *   plan_out      receives a handle, valid until varbsr_plan_destroy(); the
+ *                 workspace must stay allocated as long as it is used.
+ * No float workspace: each work item keeps all of its keys in one CTA.
+ * Errors: SFA_ERR_INVALID_ARG (NULL pointer, negative size, sizes that do not
+ * sum alike, unaligned workspace), SFA_ERR_WORKSPACE (int_ws too small),
+ * SFA_ERR_UNSUPPORTED, SFA_ERR_CUDA (the upload failed).
+ */
+sfa_status varbsr_plan(const uint8_t* block_mask_map_host, const int32_t* block_row_sz_host,
+                       const int32_t* block_col_sz_host, int MB, int NB, int num_qo_heads,
+                       int num_kv_heads, int head_dim, int causal, float sm_scale,
+                       sfa_dtype dtype, void* int_ws, size_t int_ws_bytes, sfa_stream_t stream,
+                       varbsr_plan_t* plan_out);
+
+/* Bytes of int workspace varbsr_plan needs for these arguments.  Host only. */
+sfa_status varbsr_plan_int_workspace_size(const uint8_t* block_mask_map_host,
+                                          const int32_t* block_row_sz_host,
+                                          const int32_t* block_col_sz_host, int MB, int NB,
+                                          int num_qo_heads, int num_kv_heads, int head_dim,
+                                          int causal, size_t* bytes);
+
+/* qo_len and kv_len (the sums of the block sizes) of a plan.  Host only. */
+sfa_status varbsr_plan_dims(varbsr_plan_t plan, int* qo_len, int* kv_len);
+
+/*
+ * varbsr_run -- variable block-sparse attention with a plan (run()).
+ *   q    device (num_qo_heads, qo_len, head_dim), HND, dtype, 16-byte aligned.
+ *   k, v device (num_kv_heads, kv_len, head_dim), HND, dtype.
+ *   out  device (num_qo_heads, qo_len, head_dim), dtype: q's own layout (the
+ *        page prints the return shape as [M, num_qo_heads, head_dim] but
+ *        takes q as (num_qo_heads, qo_len, head_dim); read as q's layout).
+ *   lse  device float32 (num_qo_heads, qo_len) or NULL: natural-log
+ *        log-sum-exp of the scaled logits of the row's allowed columns.
+ * Rows with no allowed column write out = +0 and lse = -inf.
+ */
+sfa_status varbsr_run(varbsr_plan_t plan, const void* q, const void* k, const void* v,
+                      void* out, float* lse, sfa_stream_t stream);
+
+/* Frees the plan's host state.  Safe on NULL. */
+void varbsr_plan_destroy(varbsr_plan_t plan);
+
 #ifdef __cplusplus
 }
 #endif

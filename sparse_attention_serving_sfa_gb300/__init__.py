@@ -30,7 +30,9 @@ DTYPES = {"f16": 0, "bf16": 1}
 # Every entry point of include/sfa.h.
 EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
            "sfa_status_string", "sfa_kernel_launches", "sfa_run_noalloc", "bsr_plan", "bsr_plan_int_workspace_size", "bsr_run",
-           "bsr_plan_destroy", "bsr_plan_masked", "bsr_plan_masked_int_workspace_size")
+           "bsr_plan_destroy", "bsr_plan_masked", "bsr_plan_masked_int_workspace_size",
+           "varbsr_plan", "varbsr_plan_int_workspace_size", "varbsr_plan_dims", "varbsr_run",
+           "varbsr_plan_destroy")
 
 
 class SfaError(RuntimeError):
@@ -93,6 +95,17 @@ def load():
             lib.bsr_run.restype = ci
             lib.bsr_plan_destroy.argtypes = [vp]
             lib.bsr_plan_destroy.restype = None
+            lib.varbsr_plan.argtypes = [vp, vp, vp] + [ci] * 6 + [cf, ci, vp, sz, vp,
+                                                               ctypes.POINTER(vp)]
+            lib.varbsr_plan.restype = ci
+            lib.varbsr_plan_int_workspace_size.argtypes = [vp, vp, vp] + [ci] * 6 + [ctypes.POINTER(sz)]
+            lib.varbsr_plan_int_workspace_size.restype = ci
+            lib.varbsr_plan_dims.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci)]
+            lib.varbsr_plan_dims.restype = ci
+            lib.varbsr_run.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+            lib.varbsr_run.restype = ci
+            lib.varbsr_plan_destroy.argtypes = [vp]
+            lib.varbsr_plan_destroy.restype = None
             _lib = lib
     return _lib
 
@@ -271,6 +284,83 @@ def bsr_run(plan: BsrPlan, q, k, v, out, lse=None, stream=None):
 def bsr_plan_destroy(plan: BsrPlan):
     if plan.handle:
         load().bsr_plan_destroy(plan.handle)
+        plan.handle = None
+
+
+class VarBsrPlan:
+    """Owner of a varbsr_plan_t handle (destroyed with the object)."""
+
+    def __init__(self, handle: int, int_ws, Hq, d):
+        self.handle = handle
+        self.int_ws = int_ws          # keeps the device tile and work lists alive
+        self.Hq, self.d = Hq, d
+        qo, kv = ctypes.c_int(0), ctypes.c_int(0)
+        _check(load().varbsr_plan_dims(handle, ctypes.byref(qo), ctypes.byref(kv)),
+               "varbsr_plan_dims")
+        self.qo_len, self.kv_len = qo.value, kv.value
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.varbsr_plan_destroy(self.handle)
+            self.handle = None
+
+
+def _varbsr_host_args(block_mask_map, block_row_sz, block_col_sz):
+    import numpy as np
+
+    def host(x, dt):
+        x = x.detach().cpu().numpy() if hasattr(x, "detach") else np.asarray(x)
+        return np.ascontiguousarray(x.astype(dt))
+    mm = host(block_mask_map, bool).view(np.uint8)
+    rs = host(block_row_sz, np.int32)
+    cs = host(block_col_sz, np.int32)
+    if mm.ndim != 3 or rs.shape != mm.shape[:2] or cs.shape != (mm.shape[0], mm.shape[2]):
+        raise ValueError("block_mask_map (Hkv, MB, NB), block_row_sz (Hkv, MB), "
+                         "block_col_sz (Hkv, NB) expected")
+    return mm, rs, cs
+
+
+def varbsr_plan_int_workspace_size(block_mask_map, block_row_sz, block_col_sz, num_qo_heads,
+                                   num_kv_heads, head_dim, causal=False) -> int:
+    mm, rs, cs = _varbsr_host_args(block_mask_map, block_row_sz, block_col_sz)
+    out = ctypes.c_size_t(0)
+    _check(load().varbsr_plan_int_workspace_size(mm.ctypes.data, rs.ctypes.data, cs.ctypes.data,
+                                                 mm.shape[1], mm.shape[2], num_qo_heads,
+                                                 num_kv_heads, head_dim, int(bool(causal)),
+                                                 ctypes.byref(out)),
+           "varbsr_plan_int_workspace_size")
+    return out.value
+
+
+def varbsr_plan(block_mask_map, block_row_sz, block_col_sz, num_qo_heads, num_kv_heads,
+                head_dim, causal=False, sm_scale=0.0, dtype="f16", int_ws=None,
+                stream=None) -> VarBsrPlan:
+    """Forwards to varbsr_plan().  The block mask map and sizes may be numpy
+    arrays or tensors on any device (they are read on the host); int_ws is a
+    device uint8 tensor (allocated here with torch if None)."""
+    import torch
+    mm, rs, cs = _varbsr_host_args(block_mask_map, block_row_sz, block_col_sz)
+    if int_ws is None:
+        need = varbsr_plan_int_workspace_size(mm, rs, cs, num_qo_heads, num_kv_heads, head_dim,
+                                              causal)
+        int_ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    handle = ctypes.c_void_p(0)
+    _check(load().varbsr_plan(mm.ctypes.data, rs.ctypes.data, cs.ctypes.data, mm.shape[1],
+                              mm.shape[2], num_qo_heads, num_kv_heads, head_dim,
+                              int(bool(causal)), float(sm_scale), _enum(dtype, DTYPES),
+                              _ptr(int_ws), int_ws.numel() * int_ws.element_size(),
+                              _stream(stream), ctypes.byref(handle)), "varbsr_plan")
+    return VarBsrPlan(handle.value, int_ws, num_qo_heads, head_dim)
+
+
+def varbsr_run(plan: VarBsrPlan, q, k, v, out, lse=None, stream=None):
+    _check(load().varbsr_run(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                             _stream(stream)), "varbsr_run")
+
+
+def varbsr_plan_destroy(plan: VarBsrPlan):
+    if plan.handle:
+        load().varbsr_plan_destroy(plan.handle)
         plan.handle = None
 
 

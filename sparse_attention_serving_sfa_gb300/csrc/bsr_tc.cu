@@ -23,6 +23,13 @@
 // causal (bottom-right) and per-element block mask become a 64-bit allowed
 // mask per thread and 64-key block (a compile-time mode, so the plain path
 // carries no test); masked scores are -inf before the softmax.
+//
+// Mode 3 is VariableBlockSparseAttentionWrapper (same page): HND tensors
+// (q (Hq, M, d), k / v (Hkv, N, d), out (Hq, M, d)), and per (kv head, row
+// block) a list of key tiles, each a start key plus a 64-bit mask of the
+// allowed keys among the 64 that follow, so blocks of any size and position
+// are read as whole 64-key tiles.  The Q tile then holds the G heads one
+// after the other (row r = head r / TR, query row r % TR).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -70,6 +77,13 @@ struct BsrTcItem {
     int rb, row0, kvh, pad;
 };
 
+// Mode 3 key tile: keys [key0, key0 + 64), bit j of (hi:lo) = key0 + j allowed.
+struct VarTile {
+    int key0;
+    unsigned lo, hi;
+    int pad;
+};
+
 struct BsrTcParams {
     void* out;
     float* lse;
@@ -80,6 +94,7 @@ struct BsrTcParams {
     int M, N, R, C, Hq, G, TR;
     float scale_log2;
     const uint8_t* mask;    // per-element bits (MODE 2)
+    int causal;             // MODE 3: bottom-right causal on top of the tiles
 };
 
 // The 64-bit word whose bit j is element j of the 64 mask elements held,
@@ -111,7 +126,9 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const int blk0 = p.indptr[item.rb];
     const int sub = p.C / kKeys;
     const int nb = (p.indptr[item.rb + 1] - blk0) * sub;
-    const int row_end = min((item.rb + 1) * p.R, p.M);
+    // mode 3: rb = key tile list, pad = end of the row block
+    const int row_end = MODE == 3 ? item.pad : min((item.rb + 1) * p.R, p.M);
+    const VarTile* vtiles = reinterpret_cast<const VarTile*>(p.indices);
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::abort);
     if (tid == 0) {
@@ -143,18 +160,30 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             tma_prefetch_map(&mv);
             mbar_arrive_expect_tx(bar(B_Q), 2 * L::qTile);
             for (int t = 0; t < 2; ++t)
-                for (int pn = 0; pn < L::panels; ++pn)
-                    tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
-                                item.kvh * p.G, item.row0 + t * p.TR, bar(B_Q));
+                for (int pn = 0; pn < L::panels; ++pn) {
+                    if constexpr (MODE == 3)
+                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
+                                    item.row0 + t * p.TR, item.kvh * p.G, bar(B_Q));
+                    else
+                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
+                                    item.kvh * p.G, item.row0 + t * p.TR, bar(B_Q));
+                }
             auto load_kv = [&](int b) {
                 const int s = b % kStages;
-                const int col = p.indices[blk0 + b / sub] * p.C + (b % sub) * kKeys;
+                const int col = MODE == 3 ? vtiles[blk0 + b].key0
+                                          : p.indices[blk0 + b / sub] * p.C + (b % sub) * kKeys;
                 const uint32_t dst = sbase + L::kv + s * 2 * L::kvTile;
                 mbar_arrive_expect_tx(bar(B_KV_FULL + s), 2 * L::kvTile);
                 for (int pn = 0; pn < L::panels; ++pn) {
-                    tma_load_3d(dst + pn * (kKeys * 128), &mk, pn * 64, item.kvh, col, bar(B_KV_FULL + s));
-                    tma_load_3d(dst + L::kvTile + pn * (kKeys * 128), &mv, pn * 64, item.kvh, col,
-                                bar(B_KV_FULL + s));
+                    if constexpr (MODE == 3) {
+                        tma_load_3d(dst + pn * (kKeys * 128), &mk, pn * 64, col, item.kvh, bar(B_KV_FULL + s));
+                        tma_load_3d(dst + L::kvTile + pn * (kKeys * 128), &mv, pn * 64, col, item.kvh,
+                                    bar(B_KV_FULL + s));
+                    } else {
+                        tma_load_3d(dst + pn * (kKeys * 128), &mk, pn * 64, item.kvh, col, bar(B_KV_FULL + s));
+                        tma_load_3d(dst + L::kvTile + pn * (kKeys * 128), &mv, pn * 64, item.kvh, col,
+                                    bar(B_KV_FULL + s));
+                    }
                 }
             };
             for (int b = 0; b < min(kStages, nb); ++b) load_kv(b);
@@ -226,6 +255,9 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         unsigned char* p_hi = smem + L::p + (2 * t) * L::pTile;
         unsigned char* p_lo = p_hi + L::pTile;
         float m_used = -INFINITY, l = 0.f;
+        // query row / qo head of this thread's tile row
+        const int my_i = MODE == 3 ? item.row0 + t * p.TR + r % p.TR : item.row0 + t * p.TR + r / p.G;
+        const int my_h = MODE == 3 ? item.kvh * p.G + r / p.TR : item.kvh * p.G + r % p.G;
         // per-element mask: this row's 64 bits of block b + 1 are loaded while
         // block b is processed (8 bytes per row and 64-key block)
         uint64_t mask_next = 0;
@@ -239,6 +271,11 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if constexpr (MODE == 2) {
             if (nb > 0) mask_next = mask_word(0);
         }
+        // mode 3: the key tile of block b + 1 is loaded while block b is processed
+        VarTile vt_next{};
+        if constexpr (MODE == 3) {
+            if (nb > 0) vt_next = vtiles[blk0];
+        }
         for (int b = 0; b < nb; ++b) {
             mbar_wait(bar(B_S_FULL + t), b & 1, p.err_word, abort_flag);
             tc_fence_after();
@@ -248,7 +285,17 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             tmem_wait_ld();
             // allowed keys of this 64-key block for this row (bit j = key j)
             uint64_t am = ~0ull;
-            if constexpr (MODE != 0) {
+            if constexpr (MODE == 3) {
+                am = ((uint64_t)vt_next.hi << 32) | vt_next.lo;
+                if (p.causal) {
+                    const int64_t lim = (int64_t)my_i + (p.N - p.M) - vt_next.key0;
+                    am &= lim < 0 ? 0ull : (lim >= 63 ? ~0ull : ((2ull << lim) - 1ull));
+                }
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
+                if (b + 1 < nb) vt_next = vtiles[blk0 + b + 1];
+            } else if constexpr (MODE != 0) {
                 const int i = item.row0 + t * p.TR + r / p.G;     // query row of this thread
                 if (i < row_end && r / p.G < p.TR) {
                     const int kb = blk0 + b / sub, sb = b % sub;
@@ -321,8 +368,7 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             mbar_arrive(bar(B_P_FULL + t));
         }
         // ---- epilogue: O / l for the rows of this tile ----
-        const int i = item.row0 + t * p.TR + r / p.G;
-        const int h = item.kvh * p.G + r % p.G;
+        const int i = my_i, h = my_h;
         const bool valid_row = i < row_end && r / p.G < p.TR;
         if (nb > 0) {
             mbar_wait(bar(B_O_DONE + t), (nb - 1) & 1, p.err_word, abort_flag);
@@ -330,7 +376,8 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
         const bool empty = !(l > 0.f);
         const float inv = empty ? 0.f : 1.f / l;
-        T* orow = static_cast<T*>(p.out) + ((int64_t)i * p.Hq + h) * D;
+        const int64_t orow_idx = MODE == 3 ? (int64_t)h * p.M + i : (int64_t)i * p.Hq + h;
+        T* orow = static_cast<T*>(p.out) + orow_idx * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
@@ -351,7 +398,7 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             }
         }
         if (valid_row && p.lse)
-            p.lse[(int64_t)i * p.Hq + h] = empty ? -INFINITY : (m_used + __log2f(l)) * kLn2;
+            p.lse[orow_idx] = empty ? -INFINITY : (m_used + __log2f(l)) * kLn2;
     }
     tc_fence_before();
     __syncthreads();
@@ -394,14 +441,36 @@ bool make_map(CUtensorMap* map, const void* base, bool bf16, int dim, int heads,
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a [heads][rows][dim] (HND) tensor: box = 64 dims x rb rows x
+// hb heads, 128-byte swizzle.
+bool make_map_hnd(CUtensorMap* map, const void* base, bool bf16, int dim, int rows, int heads,
+                  int rb, int hb) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)rows, (cuuint64_t)heads};
+    const cuuint64_t gstride[2] = {(cuuint64_t)dim * 2, (cuuint64_t)dim * rows * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)rb, (cuuint32_t)hb};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                    const_cast<void*>(base), gdim, gstride, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <class E, int D, int MODE>
 cudaError_t launch_tc_t(const BsrParams& bp, const BsrTcParams& tp, int nitems, cudaStream_t stream) {
     using L = TcSmem<D>;
     const bool bf16 = std::is_same<E, BF16>::value;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, tp.G, tp.TR) ||
-        !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kKeys) ||
-        !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kKeys))
+    if (MODE == 3) {
+        if (!make_map_hnd(&mq, bp.q, bf16, D, bp.M, bp.Hq, tp.TR, tp.G) ||
+            !make_map_hnd(&mk, bp.k, bf16, D, bp.N, bp.Hkv, kKeys, 1) ||
+            !make_map_hnd(&mv, bp.v, bf16, D, bp.N, bp.Hkv, kKeys, 1))
+            return cudaErrorInvalidValue;
+    } else if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, tp.G, tp.TR) ||
+               !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kKeys) ||
+               !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kKeys))
         return cudaErrorInvalidValue;
     auto kern = bsr_tc_kernel<E, D, MODE>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
@@ -434,8 +503,9 @@ cudaError_t launch_bsr_tc(const BsrParams& bp, const void* items, int nitems, in
     tp.M = bp.M;
     tp.N = bp.N;
     tp.mask = bp.mask;
+    tp.causal = bp.causal;
     tp.R = bp.R;
-    tp.C = bp.C;
+    tp.C = bp.mask_mode == 3 ? kKeys : bp.C;
     tp.Hq = bp.Hq;
     tp.G = bp.Hq / bp.Hkv;
     tp.TR = kTileM / tp.G;
@@ -453,6 +523,7 @@ cudaError_t launch_bsr_tc(const BsrParams& bp, const void* items, int nitems, in
     SFA_BSR_TC_MODE(0)
     SFA_BSR_TC_MODE(1)
     SFA_BSR_TC_MODE(2)
+    SFA_BSR_TC_MODE(3)
 #undef SFA_BSR_TC_MODE
     return cudaErrorInvalidValue;
 }

@@ -99,16 +99,21 @@ struct BsrParams {
     // element masking inside stored blocks: 0 none, 1 causal (bottom-right,
     // key column j visible to row i iff j <= i + N - M), 2 per-element bits
     // (`mask`: element (r, c) of the k-th stored block is bit
-    // (k * R + r) * C + c, most significant bit first within each byte)
+    // (k * R + r) * C + c, most significant bit first within each byte),
+    // 3 variable blocks (HND tensors; `indptr` = key tile list offsets,
+    // `indices` = the key tiles, 4 ints each: start key, allowed-key mask
+    // low / high word, -; `causal` adds the bottom-right rule)
     int mask_mode;
     const uint8_t* mask;
+    int causal;
 };
 
 cudaError_t launch_bsr_generic(const BsrParams& p, sfa_dtype dtype, cudaStream_t stream);
 
 // Tensor-core BSR path (head_dim 64 or 128, C % 64 == 0, G | 128).  A work
 // item (4 ints: block row, first row, kv head, -) covers
-// bsr_tc_rows_per_item() rows of one block row.
+// bsr_tc_rows_per_item() rows of one block row; in mode 3 the 4 ints are
+// (key tile list, first row, kv head, end of the row block).
 bool bsr_tc_supported(int head_dim, int C, int Hq, int Hkv);
 int bsr_tc_rows_per_item(int Hq, int Hkv);
 cudaError_t launch_bsr_tc(const BsrParams& p, const void* items, int nitems, int* err_word,

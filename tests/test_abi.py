@@ -6,6 +6,7 @@ import glob
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
 
@@ -165,6 +166,56 @@ def test_pack_block_mask_bit_order():
     m[0, 0, 1] = True
     m[0, 1, 7] = True
     assert list(sfa.pack_block_mask(m)) == [0x40, 0x01]
+
+
+# ---- variable block-sparse plan (host logic only) ----
+
+def _varbsr_example():
+    mm = np.array([[[0, 0, 1], [1, 0, 1], [0, 1, 1]]], dtype=np.uint8)
+    rs = np.array([[1, 2, 3]], dtype=np.int32)
+    cs = np.array([[3, 1, 2]], dtype=np.int32)
+    return mm, rs, cs
+
+
+def test_varbsr_int_workspace_size(lib):
+    mm, rs, cs = _varbsr_example()
+    # 3 lists (offsets 4 ints) + 3 key tiles x 4 ints + 3 items x 4 ints
+    assert sfa.varbsr_plan_int_workspace_size(mm, rs, cs, 1, 1, 128) == 4 * (4 + 12 + 12)
+    # causal (qo_len == kv_len == 6): row block 0 (row 0) sees no allowed key
+    # (its set block holds keys 4, 5), so one tile fewer
+    assert sfa.varbsr_plan_int_workspace_size(mm, rs, cs, 1, 1, 128, causal=True) == 4 * (4 + 8 + 12)
+    # a 64-key window per tile: one set block of 130 keys needs 3 tiles
+    n = sfa.varbsr_plan_int_workspace_size(np.ones((1, 1, 1), np.uint8), [[10]], [[130]], 4, 1, 64)
+    assert n == 4 * (4 + 12 + 4)
+
+
+@pytest.mark.parametrize("rs,cs,Hq,Hkv,d,status", [
+    ([[1, 2, 3]], [[3, 1, 2]], 3, 2, 128, sfa.SFA_ERR_INVALID_ARG),     # Hq % Hkv != 0
+    ([[1, 2, 3]], [[3, 1, 2]], 3, 1, 128, sfa.SFA_ERR_UNSUPPORTED),     # 128 % G != 0
+    ([[1, 2, 3]], [[3, 1, 2]], 1, 1, 96, sfa.SFA_ERR_UNSUPPORTED),      # head_dim not 64 / 128
+    ([[1, -2, 3]], [[3, 1, 2]], 1, 1, 128, sfa.SFA_ERR_INVALID_ARG),    # negative size
+    ([[0, 0, 0]], [[3, 1, 2]], 1, 1, 128, sfa.SFA_ERR_INVALID_ARG),     # qo_len 0
+])
+def test_varbsr_plan_rejects(lib, rs, cs, Hq, Hkv, d, status):
+    mm = np.ones((1, 3, 3), np.uint8)
+    with pytest.raises(sfa.SfaError) as e:
+        sfa.varbsr_plan_int_workspace_size(mm, rs, cs, Hq, Hkv, d)
+    assert e.value.status == status
+
+
+def test_varbsr_heads_must_agree_on_lengths(lib):
+    mm = np.ones((2, 2, 2), np.uint8)
+    with pytest.raises(sfa.SfaError) as e:
+        sfa.varbsr_plan_int_workspace_size(mm, [[2, 2], [1, 2]], [[3, 3], [3, 3]], 2, 2, 64)
+    assert e.value.status == sfa.SFA_ERR_INVALID_ARG
+
+
+def test_varbsr_plan_workspace_too_small(lib):
+    mm, rs, cs = _varbsr_example()
+    handle = ctypes.c_void_p(0)
+    st = sfa.load().varbsr_plan(mm.ctypes.data, rs.ctypes.data, cs.ctypes.data, 3, 3, 1, 1, 128, 0,
+                                0.0, 0, FAKE, 8, None, ctypes.byref(handle))
+    assert st == sfa.SFA_ERR_WORKSPACE and not handle.value
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
