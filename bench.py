@@ -287,7 +287,7 @@ def run_bsr(args, rank, world, local):
            "roofline": {"bound": "tensor", "achieved": tflops,
                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                         "frac": tflops / peaks["bf16_tflops_sustained"],
-                        "traffic": committed_traffic("varbsr" if variable else "bsr"),
+                        "traffic": committed_traffic(case.name),
                         "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 dense rate is the same)",
                         "kernel": kernel},
            "gpu_launches": launches, "clocks": clocks,
