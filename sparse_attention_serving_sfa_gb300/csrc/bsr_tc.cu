@@ -491,8 +491,11 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
 }
 
-// ---- host: tensor maps -------------------------------------------------
+}  // namespace
 
+// ---- host: tensor maps (shared with the 128-key kernel) ------------------
+
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -506,6 +509,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     });
     return fn;
 }
+
+}  // namespace
 
 // 3-D map over a [rows][heads][dim] tensor: box = 64 dims x hb heads x rb rows,
 // 128-byte swizzle.
@@ -540,6 +545,8 @@ bool make_map_hnd(CUtensorMap* map, const void* base, bool bf16, int dim, int ro
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <class E, int D, int MODE>
 cudaError_t launch_tc_t(const BsrParams& bp, const BsrTcParams& tp, int nitems, cudaStream_t stream) {

@@ -1,0 +1,401 @@
+// Block-sparse (BSR) attention, plain blocks, on the tensor cores in steps of
+// 128 keys.
+//
+// "flashinfer.sparse", BlockSparseAttentionWrapper: query row i attends to
+// key column j iff block (i / R, j / C) is stored; qo head h reads kv head
+// h / (Hq / Hkv).  Same work items, support (head_dim 64 or 128, C % 64 == 0,
+// Hq / Hkv dividing 128) and warp roles as the 64-key kernel, but each step
+// takes two 64-key blocks, so the per-step round trip (Q.K^T -> softmax ->
+// P.V and the barriers between them) is paid once per 128 keys:
+//   - control warp (one thread): TMA loads of the two Q tiles and of two
+//     64-key K / V blocks per step into a two-stage ring (a step with one
+//     block left loads rows past the end, which TMA fills with zeros), and
+//     the tcgen05.mma issue: S_t = Q_t K^T (N = 128) into tensor memory, then
+//     O_t += P_t V with P read from tensor memory (written over S) and V an
+//     MN-major shared-memory operand;
+//   - two softmax warpgroups, thread r = row r of its tile (TMEM lane r):
+//     the step's max over 128 scores, the conditional O rescale (only when the
+//     running max grows by more than 2^8), and P = exp2(s - m) as a 16-bit
+//     high part plus the 16-bit rounding of the remainder, stored over S.
+// TMEM per tile: S / P in columns [0, 128), O in [128, 128 + D).
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace sfa {
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kBlk = 64;            // keys per K/V block
+constexpr int kStep = 2 * kBlk;     // keys per step
+constexpr int kStages = 2;
+constexpr int kSoftWarps = 8;
+constexpr int kThreads = kSoftWarps * 32 + 32;
+constexpr int kTmemCols = 512;
+constexpr int kTileCols = 256;      // TMEM columns per M-tile
+constexpr int kOCol = 128;          // O after the 128 S / P columns
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int D>
+struct WideSmem {
+    static constexpr int panels = D / 64;
+    static constexpr int qTile = kTileM * D * 2;          // panels x 128 rows x 128 B
+    static constexpr int kPanel = kStep * 128;            // 128 keys x 128 B
+    static constexpr int kvHalf = kBlk * 128;             // one block's rows of a panel
+    static constexpr int kvTile = panels * kPanel;        // K (or V) of one step
+    static constexpr int q = 0;
+    static constexpr int kv = q + 2 * qTile;              // [stage][K, V]
+    static constexpr int bars = kv + kStages * 2 * kvTile;
+    static constexpr int tmem_slot = bars + 16 * 8;
+    static constexpr int abort = tmem_slot + 4;
+    static constexpr int total = tmem_slot + 16;
+    static constexpr int alloc = total + 1024;            // room to align the base to 1024
+    static_assert(alloc <= 232448, "dynamic shared memory per block");
+};
+
+enum { B_Q = 0, B_KV_FULL = 1, B_KV_FREE = 3, B_S_FULL = 5, B_P_FULL = 7, B_O_DONE = 9, B_DRAIN = 11 };
+
+struct WideItem {
+    int rb, row0, kvh, pad;
+};
+
+struct WideParams {
+    void* out;
+    float* lse;
+    const int32_t* indptr;
+    const int32_t* indices;
+    const WideItem* items;
+    int* err_word;
+    int M, N, R, C, Hq, G, TR;
+    float scale_log2;
+};
+
+// 32 columns from the even (ODD = 0) or odd (ODD = 1) entries of r[64].
+template <int ODD>
+__device__ __forceinline__ void tmem_st32_strided(uint32_t taddr, const uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0 + ODD]), "r"(r[2 + ODD]), "r"(r[4 + ODD]), "r"(r[6 + ODD]), "r"(r[8 + ODD]),
+        "r"(r[10 + ODD]), "r"(r[12 + ODD]), "r"(r[14 + ODD]), "r"(r[16 + ODD]), "r"(r[18 + ODD]),
+        "r"(r[20 + ODD]), "r"(r[22 + ODD]), "r"(r[24 + ODD]), "r"(r[26 + ODD]), "r"(r[28 + ODD]),
+        "r"(r[30 + ODD]), "r"(r[32 + ODD]), "r"(r[34 + ODD]), "r"(r[36 + ODD]), "r"(r[38 + ODD]),
+        "r"(r[40 + ODD]), "r"(r[42 + ODD]), "r"(r[44 + ODD]), "r"(r[46 + ODD]), "r"(r[48 + ODD]),
+        "r"(r[50 + ODD]), "r"(r[52 + ODD]), "r"(r[54 + ODD]), "r"(r[56 + ODD]), "r"(r[58 + ODD]),
+        "r"(r[60 + ODD]), "r"(r[62 + ODD])
+        : "memory");
+}
+
+template <class E, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, const WideParams p) {
+    using L = WideSmem<D>;
+    constexpr bool kBf16 = std::is_same<E, BF16>::value;
+    constexpr uint32_t kIdescQK = idesc_f16(kTileM, kStep, kBf16, false, false);
+    constexpr uint32_t kIdescPV = idesc_f16(kTileM, D, kBf16, false, true);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    auto bar = [&](int i) { return sbase + L::bars + 8 * i; };
+
+    const WideItem item = p.items[blockIdx.x];
+    const int blk0 = p.indptr[item.rb];
+    const int sub = p.C / kBlk;
+    const int nb = (p.indptr[item.rb + 1] - blk0) * sub;     // 64-key blocks
+    const int ns = (nb + 1) / 2;                              // steps
+    const int row_end = min((item.rb + 1) * p.R, p.M);
+
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::abort);
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bar(B_Q), 1);
+        mbar_init(bar(B_DRAIN), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(B_KV_FULL + s), 1);
+            mbar_init(bar(B_KV_FREE + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(B_S_FULL + t), 1);
+            mbar_init(bar(B_P_FULL + t), 128);
+            mbar_init(bar(B_O_DONE + t), 1);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(sbase + L::tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::tmem_slot);
+
+    if (warp == kSoftWarps) {
+        // ============================ control ============================
+        if (lane == 0 && ns > 0) {
+            tma_prefetch_map(&mq);
+            tma_prefetch_map(&mk);
+            tma_prefetch_map(&mv);
+            mbar_arrive_expect_tx(bar(B_Q), 2 * L::qTile);
+            for (int t = 0; t < 2; ++t)
+                for (int pn = 0; pn < L::panels; ++pn)
+                    tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
+                                item.kvh * p.G, item.row0 + t * p.TR, bar(B_Q));
+            // step st: blocks 2 st and 2 st + 1; a missing second block reads
+            // rows N.. (all outside the tensor: zeros, full byte count)
+            auto load_step = [&](int st) {
+                const int s = st % kStages;
+                const uint32_t dst = sbase + L::kv + s * 2 * L::kvTile;
+                mbar_arrive_expect_tx(bar(B_KV_FULL + s), 2 * L::kvTile);
+                for (int h = 0; h < 2; ++h) {
+                    const int b = 2 * st + h;
+                    const int col = b < nb ? p.indices[blk0 + b / sub] * p.C + (b % sub) * kBlk : p.N;
+                    for (int pn = 0; pn < L::panels; ++pn) {
+                        tma_load_3d(dst + pn * L::kPanel + h * L::kvHalf, &mk, pn * 64, item.kvh, col,
+                                    bar(B_KV_FULL + s));
+                        tma_load_3d(dst + L::kvTile + pn * L::kPanel + h * L::kvHalf, &mv, pn * 64,
+                                    item.kvh, col, bar(B_KV_FULL + s));
+                    }
+                }
+            };
+            for (int st = 0; st < min(kStages, ns); ++st) load_step(st);
+            int loaded = min(kStages, ns) - 1, waited = -1;     // steps issued / landed
+            bool ok = mbar_wait(bar(B_Q), 0, p.err_word, abort_flag);
+            for (int st = 0; st < ns && ok; ++st) {
+                const int s = st % kStages;
+                ok = mbar_wait(bar(B_KV_FULL + s), (st / kStages) & 1, p.err_word, abort_flag);
+                if (!ok) break;
+                waited = st;
+                tc_fence_after();
+                const uint32_t kbase = sbase + L::kv + s * 2 * L::kvTile;
+                // S_t = Q_t K^T, 128 keys
+                for (int t = 0; t < 2; ++t) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;
+                        const uint64_t ad = sdesc_sw128(
+                            sbase + L::q + t * L::qTile + (kk >> 2) * (kTileM * 128) + off, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * L::kPanel + off, 16, 1024);
+                        tc_mma_f16(tmem + t * kTileCols, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(B_S_FULL + t));
+                }
+                // refill the stage that step st - 1 used with step st + 1
+                if (st >= 1 && st + 1 < ns) {
+                    ok = mbar_wait(bar(B_KV_FREE + (st - 1) % kStages), ((st - 1) / kStages) & 1,
+                                   p.err_word, abort_flag);
+                    if (!ok) break;
+                    load_step(st + 1);
+                    loaded = st + 1;
+                }
+                // O_t += P_t V: P from TMEM (16 keys = 8 columns per MMA; high
+                // parts of keys 64 h .. 64 h + 63 at 64 h, remainders at 64 h + 32)
+                for (int t = 0; t < 2 && ok; ++t) {
+                    ok = mbar_wait(bar(B_P_FULL + t), st & 1, p.err_word, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < kStep / 16; ++kk) {
+                            const uint32_t a = tmem + t * kTileCols + 64 * (kk >> 2) + 32 * part +
+                                               8 * (kk & 3);
+                            const uint64_t bd =
+                                sdesc_sw128(kbase + L::kvTile + kk * 16 * 128, L::kPanel, 1024);
+                            const uint32_t acc = (st > 0 || part > 0 || kk > 0) ? 1u : 0u;
+                            tc_mma_f16_ts(tmem + t * kTileCols + kOCol, a, bd, kIdescPV, acc);
+                        }
+                    if (st == ns - 1) tc_commit(bar(B_O_DONE + t));
+                }
+                if (!ok) break;
+                tc_commit(bar(B_KV_FREE + s));
+            }
+            if (!ok) {
+                // a wait gave up (the abort flag is set): let every MMA and
+                // copy this thread issued finish (bounded) before leaving
+                tc_commit(bar(B_DRAIN));
+                mbar_wait(bar(B_DRAIN), 0, nullptr, nullptr, 100000000ull);
+                mbar_wait(bar(B_Q), 0, nullptr, nullptr, 100000000ull);
+                for (int x = waited + 1; x <= loaded; ++x)
+                    mbar_wait(bar(B_KV_FULL + x % kStages), (x / kStages) & 1, nullptr, nullptr,
+                              100000000ull);
+            }
+        }
+    } else {
+        // ============================ softmax ============================
+        const int t = warp >> 2, wq = warp & 3;
+        const int r = wq * 32 + lane;                       // row of the tile = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16) + t * kTileCols;
+        float m_used = -INFINITY, l = 0.f;
+        uint32_t sv[64];
+        // P of one 64-key half from the scores in sv, written over that
+        // half's S columns; returns the half's sum of P
+        auto make_p = [&](int h) -> float {
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float p0 = fast_exp2(__uint_as_float(sv[2 * k]) * p.scale_log2 - m_used);
+                const float p1 = fast_exp2(__uint_as_float(sv[2 * k + 1]) * p.scale_log2 - m_used);
+                ls[k & 3] += p0 + p1;
+                const uint32_t hw = E::pack2(p0, p1);
+                const float2 hf = E::unpack2(hw);
+                sv[2 * k] = hw;
+                sv[2 * k + 1] = E::pack2(p0 - hf.x, p1 - hf.y);
+            }
+            tmem_st32_strided<0>(lane_base + 64 * h, sv);
+            tmem_st32_strided<1>(lane_base + 64 * h + 32, sv);
+            return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        };
+        for (int st = 0; st < ns; ++st) {
+            mbar_wait(bar(B_S_FULL + t), st & 1, p.err_word, abort_flag);
+            tc_fence_after();
+            const bool two = 2 * st + 1 < nb;
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
+            if (two) {
+                tmem_ld32(lane_base + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tmem_ld32(lane_base + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
+            }
+            // the scale is positive and rounding monotonic: max of scaled = scaled max
+            const float bmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            const float m_new = fmaxf(m_used, bmax);
+            const bool need = m_new > m_used + kRescaleThreshold;
+            // P.V of step st - 1 ran on the tensor core before this step's
+            // Q.K^T, whose completion this thread waited for: O is settled
+            if (st > 0 && __any_sync(0xffffffffu, need)) {
+                const float f = need ? fast_exp2(m_used - m_new) : 1.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(lane_base + kOCol + 32 * c, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
+                    tmem_st32(lane_base + kOCol + 32 * c, ov);
+                }
+                l *= f;
+            }
+            if (need) m_used = m_new;
+            if (two) {
+                l += make_p(1);                    // keys 64..127 are in sv
+                tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                tmem_wait_ld();
+                l += make_p(0);
+            } else {
+                l += make_p(0);                    // keys 0..63 are in sv
+                // the second block is zeros (V rows of zeros): P = 0 there
+                uint32_t z[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) z[j] = 0u;
+                tmem_st32(lane_base + 64, z);
+                tmem_st32(lane_base + 96, z);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(B_P_FULL + t));
+        }
+        // ---- epilogue: O / l for the rows of this tile ----
+        const int i = item.row0 + t * p.TR + r / p.G;
+        const int h = item.kvh * p.G + r % p.G;
+        const bool valid_row = i < row_end && r / p.G < p.TR;
+        if (ns > 0) {
+            mbar_wait(bar(B_O_DONE + t), 0, p.err_word, abort_flag);
+            tc_fence_after();
+        }
+        const bool empty = !(l > 0.f);
+        const float inv = empty ? 0.f : 1.f / l;
+        using T = typename E::T;
+        T* orow = static_cast<T*>(p.out) + ((int64_t)i * p.Hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            if (ns > 0) {
+                tmem_ld32(lane_base + kOCol + 32 * c, ov);
+                tmem_wait_ld();
+            }
+            if (valid_row) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    uint4 w;
+                    w.x = empty ? 0u : E::pack2(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+                    w.y = empty ? 0u : E::pack2(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+                    w.z = empty ? 0u : E::pack2(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
+                    w.w = empty ? 0u : E::pack2(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
+                    *reinterpret_cast<uint4*>(orow + 32 * c + j) = w;
+                }
+            }
+        }
+        if (valid_row && p.lse)
+            p.lse[(int64_t)i * p.Hq + h] = empty ? -INFINITY : (m_used + __log2f(l)) * kLn2;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <class E, int D>
+cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems, cudaStream_t stream) {
+    using L = WideSmem<D>;
+    const bool bf16 = std::is_same<E, BF16>::value;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, wp.G, wp.TR) ||
+        !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kBlk) ||
+        !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kBlk))
+        return cudaErrorInvalidValue;
+    auto kern = bsr_tc_wide_kernel<E, D>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
+    if (err != cudaSuccess) return err;
+    kern<<<nitems, kThreads, L::alloc, stream>>>(mq, mk, mv, wp);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bsr_tc_wide(const BsrParams& bp, const void* items, int nitems, int* err_word,
+                               sfa_dtype dtype, cudaStream_t stream) {
+    if (nitems == 0) return cudaSuccess;
+    if (bp.mask_mode != 0) return cudaErrorInvalidValue;
+    WideParams wp{};
+    wp.out = bp.out;
+    wp.lse = bp.lse;
+    wp.indptr = bp.indptr;
+    wp.indices = bp.indices;
+    wp.items = static_cast<const WideItem*>(items);
+    wp.err_word = err_word;
+    wp.M = bp.M;
+    wp.N = bp.N;
+    wp.R = bp.R;
+    wp.C = bp.C;
+    wp.Hq = bp.Hq;
+    wp.G = bp.Hq / bp.Hkv;
+    wp.TR = kTileM / wp.G;
+    wp.scale_log2 = bp.scale_log2;
+    const bool bf16 = dtype == SFA_DTYPE_BF16;
+    if (bp.d == 128)
+        return bf16 ? launch_wide_t<BF16, 128>(bp, wp, nitems, stream)
+                    : launch_wide_t<F16, 128>(bp, wp, nitems, stream);
+    if (bp.d == 64)
+        return bf16 ? launch_wide_t<BF16, 64>(bp, wp, nitems, stream)
+                    : launch_wide_t<F16, 64>(bp, wp, nitems, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sfa

@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI layer and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -118,6 +119,19 @@ bool bsr_tc_supported(int head_dim, int C, int Hq, int Hkv);
 int bsr_tc_rows_per_item(int Hq, int Hkv);
 cudaError_t launch_bsr_tc(const BsrParams& p, const void* items, int nitems, int* err_word,
                           sfa_dtype dtype, cudaStream_t stream);
+
+// Plain blocks (mask mode 0) on the tensor cores in 128-key steps: same
+// support and work items as launch_bsr_tc.
+cudaError_t launch_bsr_tc_wide(const BsrParams& p, const void* items, int nitems, int* err_word,
+                               sfa_dtype dtype, cudaStream_t stream);
+
+// TMA tiled 3-D maps, 128-byte swizzle, box 64 dims wide: over a
+// [rows][heads][dim] tensor (box hb heads x rb rows) and over a
+// [heads][rows][dim] tensor (box rb rows x hb heads).
+bool make_map(CUtensorMap* map, const void* base, bool bf16, int dim, int heads, int rows, int hb,
+              int rb);
+bool make_map_hnd(CUtensorMap* map, const void* base, bool bf16, int dim, int rows, int heads,
+                  int rb, int hb);
 
 // Launches `kern` with programmatic dependent launch allowed: the grid may be
 // scheduled while the previous kernel in the stream finishes; the kernel must
