@@ -1,38 +1,31 @@
-// Block-sparse (BSR) attention on the 5th-generation tensor cores (tcgen05).
+// Block-sparse (BSR) attention with plan()'s per-element block mask, on the
+// 5th-generation tensor cores (tcgen05), in 64-key blocks.
 //
 // "flashinfer.sparse", BlockSparseAttentionWrapper: query row i attends to
-// key column j iff block (i / R, j / C) is stored; qo head h reads kv head
-// h / (Hq / Hkv).  This path takes C a multiple of 64 and head_dim 64 or 128:
-// every stored block is a run of dense 64-key blocks of K and V, so after the
-// block list is resolved the work is dense flash attention.
+// key column j iff block (i / R, j / C) is stored and the mask element of
+// (i, j) inside that block is set; qo head h reads kv head h / (Hq / Hkv).
+// This path takes C a multiple of 64 and head_dim 64 or 128: every stored
+// block is a run of dense 64-key blocks of K and V.  (Plain, causal and
+// variable blocks run in the 128-key kernel, bsr_tc_wide.cu; with the
+// per-element mask this 64-key kernel measured faster.)
 //
 // CTA = one kv head x 2 M-tiles of 128 query vectors (TR = 128 / G rows of
 // one block row x the G qo heads that share the kv head), 9 warps:
 //   - control warp (one thread): TMA tiled loads of the two Q tiles and of
-//     each 64-key K and V block (128-byte swizzle, two- or three-stage ring),
-//     and the tcgen05.mma issue: S_t = Q_t K^T into tensor memory, then
-//     O_t += P_t V (P in shared memory, V as an MN-major operand); in the
-//     masked and variable modes the two tiles run half a block apart
-//     (PV(b,0) QK(b+1,0) PV(b,1) QK(b+1,1)) so the tensor core works on one
-//     tile while the other tile's softmax runs;
-//   - two softmax warpgroups, one per M-tile, ping-ponging with the tensor
-//     core: thread r owns row r of its tile (TMEM lane r): it loads S, keeps
-//     the online-softmax max / sum in registers, rescales O in tensor memory
-//     only when the running max grows by more than 2^8 (otherwise the stale
-//     max is kept: same softmax, exponentials bounded by 256), and writes
-//     P = exp2(s - m) as a 16-bit high part plus a 16-bit remainder, so that
-//     P.V carries P to ~fp32 accuracy.
-// One CTA per SM (all 512 TMEM columns: S and O of both tiles).  plan()'s
-// causal (bottom-right) and per-element block mask become a 64-bit allowed
-// mask per thread and 64-key block (a compile-time mode, so the plain path
-// carries no test); masked scores are -inf before the softmax.
-//
-// Mode 3 is VariableBlockSparseAttentionWrapper (same page): HND tensors
-// (q (Hq, M, d), k / v (Hkv, N, d), out (Hq, M, d)), and per (kv head, row
-// block) a list of key tiles, each a start key plus a 64-bit mask of the
-// allowed keys among the 64 that follow, so blocks of any size and position
-// are read as whole 64-key tiles.  The Q tile then holds the G heads one
-// after the other (row r = head r / TR, query row r % TR).
+//     each 64-key K and V block (128-byte swizzle, three-stage ring), and the
+//     tcgen05.mma issue: S_t = Q_t K^T into tensor memory, then O_t += P_t V
+//     (P in shared memory, V as an MN-major operand), the two tiles half a
+//     block apart (PV(b,0) QK(b+1,0) PV(b,1) QK(b+1,1)) so the tensor core
+//     works on one tile while the other tile's softmax runs;
+//   - two softmax warpgroups, one per M-tile: thread r owns row r of its tile
+//     (TMEM lane r): it loads S, masks the scores whose element bit is clear
+//     (-inf; the row's 64 bits of the next block are loaded one block ahead),
+//     keeps the online-softmax max / sum in registers, rescales O in tensor
+//     memory only when the running max grows by more than 2^8 (otherwise the
+//     stale max is kept: same softmax, exponentials bounded by 256), and
+//     writes P = exp2(s - m) as a 16-bit high part plus a 16-bit remainder,
+//     so that P.V carries P to ~fp32 accuracy.
+// One CTA per SM (all 512 TMEM columns: S and O of both tiles).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -49,7 +42,7 @@ namespace {
 
 constexpr int kTileM = 128;
 constexpr int kKeys = 64;           // keys per K/V block (N of Q.K^T, K of P.V)
-constexpr int kMaxStages = 3;
+constexpr int kStages = 3;
 constexpr int kSoftWarps = 8;
 constexpr int kThreads = kSoftWarps * 32 + 32;
 constexpr int kTmemCols = 512;
@@ -57,17 +50,7 @@ constexpr int kTileCols = 256;      // TMEM columns per M-tile: S [0, 64), O [64
 constexpr int kOCol = 64;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
-// K/V ring depth and issue order per mode.  Plain blocks (mode 0): QK of both
-// tiles, then PV of both, two stages.  Masked and variable modes: the tiles
-// half a block apart and three stages (measured: 8-14% faster there, 4%
-// slower for plain blocks, whose shorter softmax leaves less to overlap).
-template <int MODE>
-struct TcSchedule {
-    static constexpr bool stagger = MODE != 0;
-    static constexpr int stages = stagger ? 3 : 2;
-};
-
-template <int D, int kStages>
+template <int D>
 struct TcSmem {
     static constexpr int panels = D / 64;
     static constexpr int qTile = kTileM * D * 2;          // panels x 128 rows x 128 B
@@ -88,8 +71,8 @@ struct TcSmem {
 enum {
     B_Q = 0,
     B_KV_FULL = 1,
-    B_KV_FREE = B_KV_FULL + kMaxStages,
-    B_S_FULL = B_KV_FREE + kMaxStages,
+    B_KV_FREE = B_KV_FULL + kStages,
+    B_S_FULL = B_KV_FREE + kStages,
     B_P_FULL = B_S_FULL + 2,
     B_O_DONE = B_P_FULL + 2,
     B_DRAIN = B_O_DONE + 2,
@@ -101,13 +84,6 @@ struct BsrTcItem {
     int rb, row0, kvh, pad;
 };
 
-// Mode 3 key tile: keys [key0, key0 + 64), bit j of (hi:lo) = key0 + j allowed.
-struct VarTile {
-    int key0;
-    unsigned lo, hi;
-    int pad;
-};
-
 struct BsrTcParams {
     void* out;
     float* lse;
@@ -117,8 +93,7 @@ struct BsrTcParams {
     int* err_word;
     int M, N, R, C, Hq, G, TR;
     float scale_log2;
-    const uint8_t* mask;    // per-element bits (MODE 2)
-    int causal;             // MODE 3: bottom-right causal on top of the tiles
+    const uint8_t* mask;    // per-element bits, most significant first
 };
 
 // The 64-bit word whose bit j is element j of the 64 mask elements held,
@@ -129,13 +104,12 @@ __device__ __forceinline__ uint64_t mask_bits64(uint64_t raw) {
     return ((uint64_t)__byte_perm(lo, 0, 0x0123) << 32) | __byte_perm(hi, 0, 0x0123);
 }
 
-template <class E, int D, int MODE>
+template <class E, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const BsrTcParams p) {
     using T = typename E::T;
-    constexpr int kStages = TcSchedule<MODE>::stages;
-    using L = TcSmem<D, kStages>;
+    using L = TcSmem<D>;
     constexpr bool kBf16 = std::is_same<E, BF16>::value;
     constexpr uint32_t kIdescQK = idesc_f16(kTileM, kKeys, kBf16, false, false);
     constexpr uint32_t kIdescPV = idesc_f16(kTileM, D, kBf16, false, true);
@@ -151,9 +125,7 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const int blk0 = p.indptr[item.rb];
     const int sub = p.C / kKeys;
     const int nb = (p.indptr[item.rb + 1] - blk0) * sub;
-    // mode 3: rb = key tile list, pad = end of the row block
-    const int row_end = MODE == 3 ? item.pad : min((item.rb + 1) * p.R, p.M);
-    const VarTile* vtiles = reinterpret_cast<const VarTile*>(p.indices);
+    const int row_end = min((item.rb + 1) * p.R, p.M);
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::abort);
     if (tid == 0) {
@@ -185,30 +157,18 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             tma_prefetch_map(&mv);
             mbar_arrive_expect_tx(bar(B_Q), 2 * L::qTile);
             for (int t = 0; t < 2; ++t)
-                for (int pn = 0; pn < L::panels; ++pn) {
-                    if constexpr (MODE == 3)
-                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
-                                    item.row0 + t * p.TR, item.kvh * p.G, bar(B_Q));
-                    else
-                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
-                                    item.kvh * p.G, item.row0 + t * p.TR, bar(B_Q));
-                }
+                for (int pn = 0; pn < L::panels; ++pn)
+                    tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
+                                item.kvh * p.G, item.row0 + t * p.TR, bar(B_Q));
             auto load_kv = [&](int b) {
                 const int s = b % kStages;
-                const int col = MODE == 3 ? vtiles[blk0 + b].key0
-                                          : p.indices[blk0 + b / sub] * p.C + (b % sub) * kKeys;
+                const int col = p.indices[blk0 + b / sub] * p.C + (b % sub) * kKeys;
                 const uint32_t dst = sbase + L::kv + s * 2 * L::kvTile;
                 mbar_arrive_expect_tx(bar(B_KV_FULL + s), 2 * L::kvTile);
                 for (int pn = 0; pn < L::panels; ++pn) {
-                    if constexpr (MODE == 3) {
-                        tma_load_3d(dst + pn * (kKeys * 128), &mk, pn * 64, col, item.kvh, bar(B_KV_FULL + s));
-                        tma_load_3d(dst + L::kvTile + pn * (kKeys * 128), &mv, pn * 64, col, item.kvh,
-                                    bar(B_KV_FULL + s));
-                    } else {
-                        tma_load_3d(dst + pn * (kKeys * 128), &mk, pn * 64, item.kvh, col, bar(B_KV_FULL + s));
-                        tma_load_3d(dst + L::kvTile + pn * (kKeys * 128), &mv, pn * 64, item.kvh, col,
-                                    bar(B_KV_FULL + s));
-                    }
+                    tma_load_3d(dst + pn * (kKeys * 128), &mk, pn * 64, item.kvh, col, bar(B_KV_FULL + s));
+                    tma_load_3d(dst + L::kvTile + pn * (kKeys * 128), &mv, pn * 64, item.kvh, col,
+                                bar(B_KV_FULL + s));
                 }
             };
             for (int b = 0; b < min(kStages, nb); ++b) load_kv(b);
@@ -241,77 +201,48 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 tc_commit(bar(B_O_DONE + t));
             };
             bool ok = mbar_wait(bar(B_Q), 0, p.err_word, abort_flag);
-            if constexpr (!TcSchedule<MODE>::stagger) {
-                for (int b = 0; b < nb && ok; ++b) {
-                    ok = mbar_wait(bar(B_KV_FULL + b % kStages), (b / kStages) & 1, p.err_word,
-                                   abort_flag);
-                    if (!ok) break;
-                    waited = b;
+            // The two M-tiles run half a block apart: while the softmax of
+            // one tile runs, the tensor core does the other tile's P.V and
+            // its next Q.K^T.  Order: PV(b,0) QK(b+1,0) PV(b,1) QK(b+1,1).
+            if (ok && nb > 0) {
+                ok = mbar_wait(bar(B_KV_FULL), 0, p.err_word, abort_flag);
+                if (ok) {
+                    waited = 0;
                     tc_fence_after();
-                    qk(b, 0);
-                    qk(b, 1);
-                    // refill the stage that block b - 1 used
-                    const int nxt = b - 1 + kStages;
-                    if (b >= 1 && nxt < nb) {
-                        ok = mbar_wait(bar(B_KV_FREE + (b - 1) % kStages), ((b - 1) / kStages) & 1,
-                                       p.err_word, abort_flag);
-                        if (!ok) break;
-                        load_kv(nxt);
-                        loaded = nxt;
-                    }
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        ok = mbar_wait(bar(B_P_FULL + t), b & 1, p.err_word, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                        pv(b, t);
-                    }
-                    if (!ok) break;
-                    tc_commit(bar(B_KV_FREE + b % kStages));
+                    qk(0, 0);
+                    qk(0, 1);
                 }
-            } else {
-                // The two M-tiles run half a block apart: while the softmax of
-                // one tile runs, the tensor core does the other tile's P.V and
-                // its next Q.K^T.  Order: PV(b,0) QK(b+1,0) PV(b,1) QK(b+1,1).
-                if (ok && nb > 0) {
-                    ok = mbar_wait(bar(B_KV_FULL), 0, p.err_word, abort_flag);
-                    if (ok) {
-                        waited = 0;
-                        tc_fence_after();
-                        qk(0, 0);
-                        qk(0, 1);
-                    }
-                }
-                for (int b = 0; b < nb && ok; ++b) {
-                    ok = mbar_wait(bar(B_P_FULL + 0), b & 1, p.err_word, abort_flag);
+            }
+            for (int b = 0; b < nb && ok; ++b) {
+                ok = mbar_wait(bar(B_P_FULL + 0), b & 1, p.err_word, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                pv(b, 0);
+                // refill the stage that block b - 1 used (its last P.V ran on
+                // the tensor core before Q.K^T of block b, which the softmax
+                // of P(b,0) waited for, so this wait is short)
+                const int nxt = b - 1 + kStages;
+                if (b >= 1 && nxt < nb) {
+                    ok = mbar_wait(bar(B_KV_FREE + (b - 1) % kStages), ((b - 1) / kStages) & 1,
+                                   p.err_word, abort_flag);
                     if (!ok) break;
+                    load_kv(nxt);
+                    loaded = nxt;
+                }
+                if (b + 1 < nb) {
+                    ok = mbar_wait(bar(B_KV_FULL + (b + 1) % kStages), ((b + 1) / kStages) & 1,
+                                   p.err_word, abort_flag);
+                    if (!ok) break;
+                    waited = b + 1;
                     tc_fence_after();
-                    pv(b, 0);
-                    // refill the stage that block b - 1 used (its last P.V ran on
-                    // the tensor core before Q.K^T of block b, which the softmax
-                    // of P(b,0) waited for, so this wait is short)
-                    const int nxt = b - 1 + kStages;
-                    if (b >= 1 && nxt < nb) {
-                        ok = mbar_wait(bar(B_KV_FREE + (b - 1) % kStages), ((b - 1) / kStages) & 1,
-                                       p.err_word, abort_flag);
-                        if (!ok) break;
-                        load_kv(nxt);
-                        loaded = nxt;
-                    }
-                    if (b + 1 < nb) {
-                        ok = mbar_wait(bar(B_KV_FULL + (b + 1) % kStages), ((b + 1) / kStages) & 1,
-                                       p.err_word, abort_flag);
-                        if (!ok) break;
-                        waited = b + 1;
-                        tc_fence_after();
-                        qk(b + 1, 0);
-                    }
-                    ok = mbar_wait(bar(B_P_FULL + 1), b & 1, p.err_word, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    pv(b, 1);
-                    tc_commit(bar(B_KV_FREE + b % kStages));
-                    if (b + 1 < nb) qk(b + 1, 1);
+                    qk(b + 1, 0);
                 }
+                ok = mbar_wait(bar(B_P_FULL + 1), b & 1, p.err_word, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                pv(b, 1);
+                tc_commit(bar(B_KV_FREE + b % kStages));
+                if (b + 1 < nb) qk(b + 1, 1);
             }
             if (!ok) {
                 // a wait gave up (the abort flag is set): let every MMA and
@@ -332,9 +263,6 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         unsigned char* p_hi = smem + L::p + (2 * t) * L::pTile;
         unsigned char* p_lo = p_hi + L::pTile;
         float m_used = -INFINITY, l = 0.f;
-        // query row / qo head of this thread's tile row
-        const int my_i = MODE == 3 ? item.row0 + t * p.TR + r % p.TR : item.row0 + t * p.TR + r / p.G;
-        const int my_h = MODE == 3 ? item.kvh * p.G + r / p.TR : item.kvh * p.G + r % p.G;
         // per-element mask: this row's 64 bits of block b + 1 are loaded while
         // block b is processed (8 bytes per row and 64-key block)
         uint64_t mask_next = 0;
@@ -345,14 +273,7 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                                (bb % sub) * kKeys;
             return __ldg(reinterpret_cast<const unsigned long long*>(p.mask + (e0 >> 3)));
         };
-        if constexpr (MODE == 2) {
-            if (nb > 0) mask_next = mask_word(0);
-        }
-        // mode 3: the key tile of block b + 1 is loaded while block b is processed
-        VarTile vt_next{};
-        if constexpr (MODE == 3) {
-            if (nb > 0) vt_next = vtiles[blk0];
-        }
+        if (nb > 0) mask_next = mask_word(0);
         for (int b = 0; b < nb; ++b) {
             mbar_wait(bar(B_S_FULL + t), b & 1, p.err_word, abort_flag);
             tc_fence_after();
@@ -362,37 +283,14 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             tmem_wait_ld();
             // allowed keys of this 64-key block for this row (bit j = key j)
             uint64_t am = ~0ull;
-            if constexpr (MODE == 3) {
-                am = ((uint64_t)vt_next.hi << 32) | vt_next.lo;
-                if (p.causal) {
-                    const int64_t lim = (int64_t)my_i + (p.N - p.M) - vt_next.key0;
-                    am &= lim < 0 ? 0ull : (lim >= 63 ? ~0ull : ((2ull << lim) - 1ull));
-                }
-#pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
-                if (b + 1 < nb) vt_next = vtiles[blk0 + b + 1];
-            } else if constexpr (MODE != 0) {
+            {
                 const int i = item.row0 + t * p.TR + r / p.G;     // query row of this thread
-                if (i < row_end && r / p.G < p.TR) {
-                    const int kb = blk0 + b / sub, sb = b % sub;
-                    if constexpr (MODE == 1) {
-                        const int64_t lim = (int64_t)i + (p.N - p.M) -
-                                            ((int64_t)p.indices[kb] * p.C + sb * kKeys);
-                        am = lim < 0 ? 0ull : (lim >= 63 ? ~0ull : ((2ull << lim) - 1ull));
-                    } else {
-                        (void)kb;
-                        (void)sb;
-                        am = mask_bits64(mask_next);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
-                if constexpr (MODE == 2) {
-                    if (b + 1 < nb) mask_next = mask_word(b + 1);
-                }
+                if (i < row_end && r / p.G < p.TR) am = mask_bits64(mask_next);
             }
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+                if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
+            if (b + 1 < nb) mask_next = mask_word(b + 1);
             // block max in four independent chains, scaled once (the scale is
             // positive and rounding monotonic, so this equals the max of the
             // scaled scores)
@@ -431,11 +329,9 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 for (int e = 0; e < 4; ++e) {
                     float p0 = fast_exp2(__uint_as_float(sv[8 * c + 2 * e]) * p.scale_log2 - m_used);
                     float p1 = fast_exp2(__uint_as_float(sv[8 * c + 2 * e + 1]) * p.scale_log2 - m_used);
-                    if constexpr (MODE != 0) {
-                        // masked keys give 0, also while the row has seen none (m = -inf)
-                        if (!((am >> (8 * c + 2 * e)) & 1ull)) p0 = 0.f;
-                        if (!((am >> (8 * c + 2 * e + 1)) & 1ull)) p1 = 0.f;
-                    }
+                    // masked keys give 0, also while the row has seen none (m = -inf)
+                    if (!((am >> (8 * c + 2 * e)) & 1ull)) p0 = 0.f;
+                    if (!((am >> (8 * c + 2 * e + 1)) & 1ull)) p1 = 0.f;
                     ls[e] += p0 + p1;
                     hw[e] = E::pack2(p0, p1);
                     const float2 h = E::unpack2(hw[e]);
@@ -451,7 +347,8 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             mbar_arrive(bar(B_P_FULL + t));
         }
         // ---- epilogue: O / l for the rows of this tile ----
-        const int i = my_i, h = my_h;
+        const int i = item.row0 + t * p.TR + r / p.G;
+        const int h = item.kvh * p.G + r % p.G;
         const bool valid_row = i < row_end && r / p.G < p.TR;
         if (nb > 0) {
             mbar_wait(bar(B_O_DONE + t), (nb - 1) & 1, p.err_word, abort_flag);
@@ -459,7 +356,7 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
         const bool empty = !(l > 0.f);
         const float inv = empty ? 0.f : 1.f / l;
-        const int64_t orow_idx = MODE == 3 ? (int64_t)h * p.M + i : (int64_t)i * p.Hq + h;
+        const int64_t orow_idx = (int64_t)i * p.Hq + h;
         T* orow = static_cast<T*>(p.out) + orow_idx * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -548,21 +445,16 @@ bool make_map_hnd(CUtensorMap* map, const void* base, bool bf16, int dim, int ro
 
 namespace {
 
-template <class E, int D, int MODE>
+template <class E, int D>
 cudaError_t launch_tc_t(const BsrParams& bp, const BsrTcParams& tp, int nitems, cudaStream_t stream) {
-    using L = TcSmem<D, TcSchedule<MODE>::stages>;
+    using L = TcSmem<D>;
     const bool bf16 = std::is_same<E, BF16>::value;
     CUtensorMap mq, mk, mv;
-    if (MODE == 3) {
-        if (!make_map_hnd(&mq, bp.q, bf16, D, bp.M, bp.Hq, tp.TR, tp.G) ||
-            !make_map_hnd(&mk, bp.k, bf16, D, bp.N, bp.Hkv, kKeys, 1) ||
-            !make_map_hnd(&mv, bp.v, bf16, D, bp.N, bp.Hkv, kKeys, 1))
-            return cudaErrorInvalidValue;
-    } else if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, tp.G, tp.TR) ||
-               !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kKeys) ||
-               !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kKeys))
+    if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, tp.G, tp.TR) ||
+        !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kKeys) ||
+        !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kKeys))
         return cudaErrorInvalidValue;
-    auto kern = bsr_tc_kernel<E, D, MODE>;
+    auto kern = bsr_tc_kernel<E, D>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
     if (err != cudaSuccess) return err;
     kern<<<nitems, kThreads, L::alloc, stream>>>(mq, mk, mv, tp);
@@ -583,6 +475,7 @@ int bsr_tc_rows_per_item(int Hq, int Hkv) { return 2 * (kTileM / (Hq / Hkv)); }
 cudaError_t launch_bsr_tc(const BsrParams& bp, const void* items, int nitems, int* err_word,
                           sfa_dtype dtype, cudaStream_t stream) {
     if (nitems == 0) return cudaSuccess;
+    if (bp.mask_mode != 2) return cudaErrorInvalidValue;   // the per-element mask mode only
     BsrTcParams tp{};
     tp.out = bp.out;
     tp.lse = bp.lse;
@@ -593,28 +486,19 @@ cudaError_t launch_bsr_tc(const BsrParams& bp, const void* items, int nitems, in
     tp.M = bp.M;
     tp.N = bp.N;
     tp.mask = bp.mask;
-    tp.causal = bp.causal;
     tp.R = bp.R;
-    tp.C = bp.mask_mode == 3 ? kKeys : bp.C;
+    tp.C = bp.C;
     tp.Hq = bp.Hq;
     tp.G = bp.Hq / bp.Hkv;
     tp.TR = kTileM / tp.G;
     tp.scale_log2 = bp.scale_log2;
     const bool bf16 = dtype == SFA_DTYPE_BF16;
-#define SFA_BSR_TC_MODE(MODE_)                                                                   \
-    if (bp.mask_mode == MODE_) {                                                                 \
-        if (bp.d == 128)                                                                         \
-            return bf16 ? launch_tc_t<BF16, 128, MODE_>(bp, tp, nitems, stream)                  \
-                        : launch_tc_t<F16, 128, MODE_>(bp, tp, nitems, stream);                  \
-        if (bp.d == 64)                                                                          \
-            return bf16 ? launch_tc_t<BF16, 64, MODE_>(bp, tp, nitems, stream)                   \
-                        : launch_tc_t<F16, 64, MODE_>(bp, tp, nitems, stream);                   \
-    }
-    SFA_BSR_TC_MODE(0)
-    SFA_BSR_TC_MODE(1)
-    SFA_BSR_TC_MODE(2)
-    SFA_BSR_TC_MODE(3)
-#undef SFA_BSR_TC_MODE
+    if (bp.d == 128)
+        return bf16 ? launch_tc_t<BF16, 128>(bp, tp, nitems, stream)
+                    : launch_tc_t<F16, 128>(bp, tp, nitems, stream);
+    if (bp.d == 64)
+        return bf16 ? launch_tc_t<BF16, 64>(bp, tp, nitems, stream)
+                    : launch_tc_t<F16, 64>(bp, tp, nitems, stream);
     return cudaErrorInvalidValue;
 }
 

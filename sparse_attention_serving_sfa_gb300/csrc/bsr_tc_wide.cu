@@ -1,12 +1,16 @@
-// Block-sparse (BSR) attention, plain blocks, on the tensor cores in steps of
-// 128 keys.
+// Block-sparse (BSR) attention on the tensor cores in steps of 128 keys.
 //
 // "flashinfer.sparse", BlockSparseAttentionWrapper: query row i attends to
 // key column j iff block (i / R, j / C) is stored; qo head h reads kv head
 // h / (Hq / Hkv).  Same work items, support (head_dim 64 or 128, C % 64 == 0,
-// Hq / Hkv dividing 128) and warp roles as the 64-key kernel, but each step
-// takes two 64-key blocks, so the per-step round trip (Q.K^T -> softmax ->
-// P.V and the barriers between them) is paid once per 128 keys:
+// Hq / Hkv dividing 128) and warp roles as the 64-key kernel (bsr_tc.cu,
+// which serves plan()'s per-element block mask), for plain blocks (mode 0),
+// bottom-right causal (mode 1) and VariableBlockSparseAttentionWrapper's
+// variable blocks over HND tensors (mode 3: per (kv head, row block) a list
+// of 64-key windows, each a start key and a 64-bit mask of its allowed
+// keys).  Each step takes two 64-key blocks (or windows), so the per-step
+// round trip (Q.K^T -> softmax -> P.V and the barriers between them) is paid
+// once per 128 keys:
 //   - control warp (one thread): TMA loads of the two Q tiles and of two
 //     64-key K / V blocks per step into a two-stage ring (a step with one
 //     block left loads rows past the end, which TMA fills with zeros), and
@@ -64,6 +68,13 @@ struct WideItem {
     int rb, row0, kvh, pad;
 };
 
+// Mode 3 key window: keys [key0, key0 + 64), bit j of (hi:lo) = key0 + j allowed.
+struct WideWindow {
+    int key0;
+    unsigned lo, hi;
+    int pad;
+};
+
 struct WideParams {
     void* out;
     float* lse;
@@ -73,7 +84,13 @@ struct WideParams {
     int* err_word;
     int M, N, R, C, Hq, G, TR;
     float scale_log2;
+    int causal;             // mode 3: bottom-right causal on top of the windows
 };
+
+// Keys j <= lim allowed among the 64 of a block (lim relative to its first key).
+__device__ __forceinline__ uint64_t causal_bits64(int64_t lim) {
+    return lim < 0 ? 0ull : (lim >= 63 ? ~0ull : ((2ull << lim) - 1ull));
+}
 
 // 32 columns from the even (ODD = 0) or odd (ODD = 1) entries of r[64].
 template <int ODD>
@@ -92,7 +109,7 @@ __device__ __forceinline__ void tmem_st32_strided(uint32_t taddr, const uint32_t
         : "memory");
 }
 
-template <class E, int D>
+template <class E, int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const WideParams p) {
@@ -113,7 +130,14 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     const int sub = p.C / kBlk;
     const int nb = (p.indptr[item.rb + 1] - blk0) * sub;     // 64-key blocks
     const int ns = (nb + 1) / 2;                              // steps
-    const int row_end = min((item.rb + 1) * p.R, p.M);
+    // mode 3: rb = key window list, pad = end of the row block
+    const int row_end = MODE == 3 ? item.pad : min((item.rb + 1) * p.R, p.M);
+    const WideWindow* wins = reinterpret_cast<const WideWindow*>(p.indices);
+    // first key of 64-key block b
+    auto block_key0 = [&](int b) -> int {
+        if constexpr (MODE == 3) return wins[blk0 + b].key0;
+        return p.indices[blk0 + b / sub] * p.C + (b % sub) * kBlk;
+    };
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::abort);
     if (tid == 0) {
@@ -145,9 +169,14 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tma_prefetch_map(&mv);
             mbar_arrive_expect_tx(bar(B_Q), 2 * L::qTile);
             for (int t = 0; t < 2; ++t)
-                for (int pn = 0; pn < L::panels; ++pn)
-                    tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
-                                item.kvh * p.G, item.row0 + t * p.TR, bar(B_Q));
+                for (int pn = 0; pn < L::panels; ++pn) {
+                    if constexpr (MODE == 3)
+                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
+                                    item.row0 + t * p.TR, item.kvh * p.G, bar(B_Q));
+                    else
+                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
+                                    item.kvh * p.G, item.row0 + t * p.TR, bar(B_Q));
+                }
             // step st: blocks 2 st and 2 st + 1; a missing second block reads
             // rows N.. (all outside the tensor: zeros, full byte count)
             auto load_step = [&](int st) {
@@ -156,12 +185,17 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 mbar_arrive_expect_tx(bar(B_KV_FULL + s), 2 * L::kvTile);
                 for (int h = 0; h < 2; ++h) {
                     const int b = 2 * st + h;
-                    const int col = b < nb ? p.indices[blk0 + b / sub] * p.C + (b % sub) * kBlk : p.N;
+                    const int col = b < nb ? block_key0(b) : p.N;
                     for (int pn = 0; pn < L::panels; ++pn) {
-                        tma_load_3d(dst + pn * L::kPanel + h * L::kvHalf, &mk, pn * 64, item.kvh, col,
-                                    bar(B_KV_FULL + s));
-                        tma_load_3d(dst + L::kvTile + pn * L::kPanel + h * L::kvHalf, &mv, pn * 64,
-                                    item.kvh, col, bar(B_KV_FULL + s));
+                        const uint32_t kd = dst + pn * L::kPanel + h * L::kvHalf;
+                        const uint32_t vd = kd + L::kvTile;
+                        if constexpr (MODE == 3) {
+                            tma_load_3d(kd, &mk, pn * 64, col, item.kvh, bar(B_KV_FULL + s));
+                            tma_load_3d(vd, &mv, pn * 64, col, item.kvh, bar(B_KV_FULL + s));
+                        } else {
+                            tma_load_3d(kd, &mk, pn * 64, item.kvh, col, bar(B_KV_FULL + s));
+                            tma_load_3d(vd, &mv, pn * 64, item.kvh, col, bar(B_KV_FULL + s));
+                        }
                     }
                 }
             };
@@ -234,14 +268,49 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16) + t * kTileCols;
         float m_used = -INFINITY, l = 0.f;
         uint32_t sv[64];
+        // query row / qo head of this thread's tile row
+        // (recomputed where used, so the plain mode keeps no registers for them)
+        auto my_i = [&]() {
+            return MODE == 3 ? item.row0 + t * p.TR + r % p.TR : item.row0 + t * p.TR + r / p.G;
+        };
+        auto my_h = [&]() { return MODE == 3 ? item.kvh * p.G + r / p.TR : item.kvh * p.G + r % p.G; };
+        auto my_valid = [&]() { return my_i() < row_end && r / p.G < p.TR; };
+        // allowed keys of block b for this row (bit j = key j of the block)
+        auto allowed = [&](int b) -> uint64_t {
+            if constexpr (MODE == 1) {
+                return causal_bits64((int64_t)my_i() + (p.N - p.M) - block_key0(b));
+            } else if constexpr (MODE == 3) {
+                const WideWindow w = wins[blk0 + b];
+                uint64_t am = ((uint64_t)w.hi << 32) | w.lo;
+                if (p.causal) am &= causal_bits64((int64_t)my_i() + (p.N - p.M) - w.key0);
+                return am;
+            }
+            return ~0ull;
+        };
+        // the two halves' masks of the next step are loaded during this one
+        uint64_t am_next[2] = {~0ull, ~0ull};
+        if constexpr (MODE != 0) {
+            if (nb > 0) am_next[0] = allowed(0);
+            if (nb > 1) am_next[1] = allowed(1);
+        }
+        auto apply_mask = [&](uint64_t am) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+                if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
+        };
         // P of one 64-key half from the scores in sv, written over that
         // half's S columns; returns the half's sum of P
-        auto make_p = [&](int h) -> float {
+        auto make_p = [&](int h, uint64_t am) -> float {
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                const float p0 = fast_exp2(__uint_as_float(sv[2 * k]) * p.scale_log2 - m_used);
-                const float p1 = fast_exp2(__uint_as_float(sv[2 * k + 1]) * p.scale_log2 - m_used);
+                float p0 = fast_exp2(__uint_as_float(sv[2 * k]) * p.scale_log2 - m_used);
+                float p1 = fast_exp2(__uint_as_float(sv[2 * k + 1]) * p.scale_log2 - m_used);
+                if constexpr (MODE != 0) {
+                    // masked keys give 0, also while the row has seen none (m = -inf)
+                    if (!((am >> (2 * k)) & 1ull)) p0 = 0.f;
+                    if (!((am >> (2 * k + 1)) & 1ull)) p1 = 0.f;
+                }
                 ls[k & 3] += p0 + p1;
                 const uint32_t hw = E::pack2(p0, p1);
                 const float2 hf = E::unpack2(hw);
@@ -256,16 +325,23 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             mbar_wait(bar(B_S_FULL + t), st & 1, p.err_word, abort_flag);
             tc_fence_after();
             const bool two = 2 * st + 1 < nb;
+            const uint64_t am0 = am_next[0], am1 = am_next[1];
+            if constexpr (MODE != 0) {
+                if (2 * st + 2 < nb) am_next[0] = allowed(2 * st + 2);
+                if (2 * st + 3 < nb) am_next[1] = allowed(2 * st + 3);
+            }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
             tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
             tmem_wait_ld();
+            if constexpr (MODE != 0) apply_mask(am0);
 #pragma unroll
             for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
             if (two) {
                 tmem_ld32(lane_base + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                 tmem_ld32(lane_base + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tmem_wait_ld();
+                if constexpr (MODE != 0) apply_mask(am1);
 #pragma unroll
                 for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
             }
@@ -290,13 +366,13 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             if (need) m_used = m_new;
             if (two) {
-                l += make_p(1);                    // keys 64..127 are in sv
+                l += make_p(1, am1);               // keys 64..127 are in sv
                 tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                 tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tmem_wait_ld();
-                l += make_p(0);
+                l += make_p(0, am0);
             } else {
-                l += make_p(0);                    // keys 0..63 are in sv
+                l += make_p(0, am0);               // keys 0..63 are in sv
                 // the second block is zeros (V rows of zeros): P = 0 there
                 uint32_t z[32];
 #pragma unroll
@@ -309,9 +385,8 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             mbar_arrive(bar(B_P_FULL + t));
         }
         // ---- epilogue: O / l for the rows of this tile ----
-        const int i = item.row0 + t * p.TR + r / p.G;
-        const int h = item.kvh * p.G + r % p.G;
-        const bool valid_row = i < row_end && r / p.G < p.TR;
+        const int i = my_i(), h = my_h();
+        const bool valid_row = my_valid();
         if (ns > 0) {
             mbar_wait(bar(B_O_DONE + t), 0, p.err_word, abort_flag);
             tc_fence_after();
@@ -319,7 +394,8 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         const bool empty = !(l > 0.f);
         const float inv = empty ? 0.f : 1.f / l;
         using T = typename E::T;
-        T* orow = static_cast<T*>(p.out) + ((int64_t)i * p.Hq + h) * D;
+        const int64_t orow_idx = MODE == 3 ? (int64_t)h * p.M + i : (int64_t)i * p.Hq + h;
+        T* orow = static_cast<T*>(p.out) + orow_idx * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
@@ -340,7 +416,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
         }
         if (valid_row && p.lse)
-            p.lse[(int64_t)i * p.Hq + h] = empty ? -INFINITY : (m_used + __log2f(l)) * kLn2;
+            p.lse[orow_idx] = empty ? -INFINITY : (m_used + __log2f(l)) * kLn2;
     }
     tc_fence_before();
     __syncthreads();
@@ -350,16 +426,21 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     }
 }
 
-template <class E, int D>
+template <class E, int D, int MODE>
 cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems, cudaStream_t stream) {
     using L = WideSmem<D>;
     const bool bf16 = std::is_same<E, BF16>::value;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, wp.G, wp.TR) ||
-        !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kBlk) ||
-        !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kBlk))
+    if (MODE == 3) {
+        if (!make_map_hnd(&mq, bp.q, bf16, D, bp.M, bp.Hq, wp.TR, wp.G) ||
+            !make_map_hnd(&mk, bp.k, bf16, D, bp.N, bp.Hkv, kBlk, 1) ||
+            !make_map_hnd(&mv, bp.v, bf16, D, bp.N, bp.Hkv, kBlk, 1))
+            return cudaErrorInvalidValue;
+    } else if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, wp.G, wp.TR) ||
+               !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kBlk) ||
+               !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kBlk))
         return cudaErrorInvalidValue;
-    auto kern = bsr_tc_wide_kernel<E, D>;
+    auto kern = bsr_tc_wide_kernel<E, D, MODE>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
     if (err != cudaSuccess) return err;
     kern<<<nitems, kThreads, L::alloc, stream>>>(mq, mk, mv, wp);
@@ -372,7 +453,6 @@ cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems,
 cudaError_t launch_bsr_tc_wide(const BsrParams& bp, const void* items, int nitems, int* err_word,
                                sfa_dtype dtype, cudaStream_t stream) {
     if (nitems == 0) return cudaSuccess;
-    if (bp.mask_mode != 0) return cudaErrorInvalidValue;
     WideParams wp{};
     wp.out = bp.out;
     wp.lse = bp.lse;
@@ -383,18 +463,26 @@ cudaError_t launch_bsr_tc_wide(const BsrParams& bp, const void* items, int nitem
     wp.M = bp.M;
     wp.N = bp.N;
     wp.R = bp.R;
-    wp.C = bp.C;
+    wp.C = bp.mask_mode == 3 ? kBlk : bp.C;
+    wp.causal = bp.causal;
     wp.Hq = bp.Hq;
     wp.G = bp.Hq / bp.Hkv;
     wp.TR = kTileM / wp.G;
     wp.scale_log2 = bp.scale_log2;
     const bool bf16 = dtype == SFA_DTYPE_BF16;
-    if (bp.d == 128)
-        return bf16 ? launch_wide_t<BF16, 128>(bp, wp, nitems, stream)
-                    : launch_wide_t<F16, 128>(bp, wp, nitems, stream);
-    if (bp.d == 64)
-        return bf16 ? launch_wide_t<BF16, 64>(bp, wp, nitems, stream)
-                    : launch_wide_t<F16, 64>(bp, wp, nitems, stream);
+#define SFA_BSR_WIDE_MODE(MODE_)                                                                 \
+    if (bp.mask_mode == MODE_) {                                                                 \
+        if (bp.d == 128)                                                                         \
+            return bf16 ? launch_wide_t<BF16, 128, MODE_>(bp, wp, nitems, stream)                \
+                        : launch_wide_t<F16, 128, MODE_>(bp, wp, nitems, stream);                \
+        if (bp.d == 64)                                                                          \
+            return bf16 ? launch_wide_t<BF16, 64, MODE_>(bp, wp, nitems, stream)                 \
+                        : launch_wide_t<F16, 64, MODE_>(bp, wp, nitems, stream);                 \
+    }
+    SFA_BSR_WIDE_MODE(0)
+    SFA_BSR_WIDE_MODE(1)
+    SFA_BSR_WIDE_MODE(3)
+#undef SFA_BSR_WIDE_MODE
     return cudaErrorInvalidValue;
 }
 

@@ -114,14 +114,15 @@ cudaError_t launch_bsr_generic(const BsrParams& p, sfa_dtype dtype, cudaStream_t
 // Tensor-core BSR path (head_dim 64 or 128, C % 64 == 0, G | 128).  A work
 // item (4 ints: block row, first row, kv head, -) covers
 // bsr_tc_rows_per_item() rows of one block row; in mode 3 the 4 ints are
-// (key tile list, first row, kv head, end of the row block).
+// (key window list, first row, kv head, end of the row block).
+// launch_bsr_tc runs the per-element mask mode (2) only, in 64-key blocks.
 bool bsr_tc_supported(int head_dim, int C, int Hq, int Hkv);
 int bsr_tc_rows_per_item(int Hq, int Hkv);
 cudaError_t launch_bsr_tc(const BsrParams& p, const void* items, int nitems, int* err_word,
                           sfa_dtype dtype, cudaStream_t stream);
 
-// Plain blocks (mask mode 0) on the tensor cores in 128-key steps: same
-// support and work items as launch_bsr_tc.
+// Modes 0 (plain), 1 (causal) and 3 (variable blocks) on the tensor cores in
+// 128-key steps; same support and work items as launch_bsr_tc.
 cudaError_t launch_bsr_tc_wide(const BsrParams& p, const void* items, int nitems, int* err_word,
                                sfa_dtype dtype, cudaStream_t stream);
 

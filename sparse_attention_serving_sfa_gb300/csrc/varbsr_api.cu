@@ -262,8 +262,8 @@ sfa_status varbsr_run(varbsr_plan_t plan, const void* q, const void* k, const vo
     p.causal = plan->causal;
     int* ew = sfa::device_error_word();
     if (!ew) return SFA_ERR_CUDA;
-    cudaError_t err = sfa::launch_bsr_tc(p, plan->d_items, plan->nitems, ew, plan->dtype,
-                                         reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t err = sfa::launch_bsr_tc_wide(p, plan->d_items, plan->nitems, ew, plan->dtype,
+                                              reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }
 
