@@ -14,13 +14,16 @@
 //   - control warp (one thread): TMA loads of the two Q tiles and of two
 //     64-key K / V blocks per step into a two-stage ring (a step with one
 //     block left loads rows past the end, which TMA fills with zeros), and
-//     the tcgen05.mma issue: S_t = Q_t K^T (N = 128) into tensor memory, then
-//     O_t += P_t V with P read from tensor memory (written over S) and V an
-//     MN-major shared-memory operand;
+//     the tcgen05.mma issue: S_t = Q_t K^T
+//     (N = 128) into tensor memory, then O_t += P_t V with P read from tensor
+//     memory (written over S) and V an MN-major shared-memory operand (in the
+//     causal and variable modes in two halves: keys 64..127 of both tiles as
+//     soon as the softmax has written them, then keys 0..63);
 //   - two softmax warpgroups, thread r = row r of its tile (TMEM lane r):
 //     the step's max over 128 scores, the conditional O rescale (only when the
 //     running max grows by more than 2^8), and P = exp2(s - m) as a 16-bit
-//     high part plus the 16-bit rounding of the remainder, stored over S.
+//     high part plus the 16-bit rounding of the remainder, stored over S,
+//     keys 64..127 first (still in registers from the max pass).
 // TMEM per tile: S / P in columns [0, 128), O in [128, 128 + D).
 #include <cudaTypedefs.h>
 
@@ -62,7 +65,17 @@ struct WideSmem {
     static_assert(alloc <= 232448, "dynamic shared memory per block");
 };
 
-enum { B_Q = 0, B_KV_FULL = 1, B_KV_FREE = 3, B_S_FULL = 5, B_P_FULL = 7, B_O_DONE = 9, B_DRAIN = 11 };
+// P_HALF(t): P of keys 64..127 of tile t written; P_FULL(t): all of P written
+enum {
+    B_Q = 0,
+    B_KV_FULL = 1,
+    B_KV_FREE = 3,
+    B_S_FULL = 5,
+    B_P_FULL = 7,
+    B_O_DONE = 9,
+    B_P_HALF = 11,
+    B_DRAIN = 13
+};
 
 struct WideItem {
     int rb, row0, kvh, pad;
@@ -109,6 +122,16 @@ __device__ __forceinline__ void tmem_st32_strided(uint32_t taddr, const uint32_t
         : "memory");
 }
 
+// Per mode (measured): the causal and variable modes hand P to the tensor
+// core in two halves and skip a second M-tile that has no rows of the item
+// (row blocks of any size); plain blocks do neither (both measured slower
+// there: 647 -> 666 / 702 us).
+template <int MODE>
+struct WideSchedule {
+    static constexpr bool split_p = MODE != 0;
+    static constexpr bool tile_skip = MODE != 0;
+};
+
 template <class E, int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -132,6 +155,9 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     const int ns = (nb + 1) / 2;                              // steps
     // mode 3: rb = key window list, pad = end of the row block
     const int row_end = MODE == 3 ? item.pad : min((item.rb + 1) * p.R, p.M);
+    // M-tiles with rows of this item: the second only when the row block
+    // extends past the first tile's TR rows
+    const int ntl = (WideSchedule<MODE>::tile_skip && item.row0 + p.TR >= row_end) ? 1 : 2;
     const WideWindow* wins = reinterpret_cast<const WideWindow*>(p.indices);
     // first key of 64-key block b
     auto block_key0 = [&](int b) -> int {
@@ -151,6 +177,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(B_S_FULL + t), 1);
             mbar_init(bar(B_P_FULL + t), 128);
+            mbar_init(bar(B_P_HALF + t), 128);
             mbar_init(bar(B_O_DONE + t), 1);
         }
         fence_barrier_init();
@@ -167,8 +194,8 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tma_prefetch_map(&mq);
             tma_prefetch_map(&mk);
             tma_prefetch_map(&mv);
-            mbar_arrive_expect_tx(bar(B_Q), 2 * L::qTile);
-            for (int t = 0; t < 2; ++t)
+            mbar_arrive_expect_tx(bar(B_Q), ntl * L::qTile);
+            for (int t = 0; t < ntl; ++t)
                 for (int pn = 0; pn < L::panels; ++pn) {
                     if constexpr (MODE == 3)
                         tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
@@ -210,7 +237,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 tc_fence_after();
                 const uint32_t kbase = sbase + L::kv + s * 2 * L::kvTile;
                 // S_t = Q_t K^T, 128 keys
-                for (int t = 0; t < 2; ++t) {
+                for (int t = 0; t < ntl; ++t) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk & 3) * 32;
@@ -229,23 +256,59 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     load_step(st + 1);
                     loaded = st + 1;
                 }
-                // O_t += P_t V: P from TMEM (16 keys = 8 columns per MMA; high
-                // parts of keys 64 h .. 64 h + 63 at 64 h, remainders at 64 h + 32)
-                for (int t = 0; t < 2 && ok; ++t) {
-                    ok = mbar_wait(bar(B_P_FULL + t), st & 1, p.err_word, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
+                // O_t += P_t V over keys 64 h .. 64 h + 63: P from TMEM (16 keys
+                // = 8 columns per MMA; high parts at 64 h, remainders at 64 h + 32).
+                // The softmax writes keys 64..127 first, so their P.V runs while
+                // it works on keys 0..63; a step with one block has no P.V for
+                // the second half.
+                const bool two = 2 * st + 1 < nb;
+                auto pv_half = [&](int t, int h, bool first) {
                     for (int part = 0; part < 2; ++part)
 #pragma unroll
-                        for (int kk = 0; kk < kStep / 16; ++kk) {
-                            const uint32_t a = tmem + t * kTileCols + 64 * (kk >> 2) + 32 * part +
-                                               8 * (kk & 3);
+                        for (int kq = 0; kq < 4; ++kq) {
+                            const int kk = 4 * h + kq;
+                            const uint32_t a = tmem + t * kTileCols + 64 * h + 32 * part + 8 * kq;
                             const uint64_t bd =
                                 sdesc_sw128(kbase + L::kvTile + kk * 16 * 128, L::kPanel, 1024);
-                            const uint32_t acc = (st > 0 || part > 0 || kk > 0) ? 1u : 0u;
+                            const uint32_t acc = (first && part == 0 && kq == 0) ? 0u : 1u;
                             tc_mma_f16_ts(tmem + t * kTileCols + kOCol, a, bd, kIdescPV, acc);
                         }
-                    if (st == ns - 1) tc_commit(bar(B_O_DONE + t));
+                };
+                if constexpr (WideSchedule<MODE>::split_p) {
+                    for (int t = 0; t < ntl && ok; ++t) {
+                        ok = mbar_wait(bar(B_P_HALF + t), st & 1, p.err_word, abort_flag);
+                        if (!ok) break;
+                        if (two) {
+                            tc_fence_after();
+                            pv_half(t, 1, st == 0);
+                        }
+                    }
+                    for (int t = 0; t < ntl && ok; ++t) {
+                        ok = mbar_wait(bar(B_P_FULL + t), st & 1, p.err_word, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        pv_half(t, 0, st == 0 && !two);
+                        if (st == ns - 1) tc_commit(bar(B_O_DONE + t));
+                    }
+                } else {
+                    // whole P at once; a one-block step's second half is
+                    // P = 0 against V rows of zeros
+                    for (int t = 0; t < ntl && ok; ++t) {
+                        ok = mbar_wait(bar(B_P_FULL + t), st & 1, p.err_word, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        for (int part = 0; part < 2; ++part)
+#pragma unroll
+                            for (int kk = 0; kk < kStep / 16; ++kk) {
+                                const uint32_t a = tmem + t * kTileCols + 64 * (kk >> 2) + 32 * part +
+                                                   8 * (kk & 3);
+                                const uint64_t bd =
+                                    sdesc_sw128(kbase + L::kvTile + kk * 16 * 128, L::kPanel, 1024);
+                                const uint32_t acc = (st > 0 || part > 0 || kk > 0) ? 1u : 0u;
+                                tc_mma_f16_ts(tmem + t * kTileCols + kOCol, a, bd, kIdescPV, acc);
+                            }
+                        if (st == ns - 1) tc_commit(bar(B_O_DONE + t));
+                    }
                 }
                 if (!ok) break;
                 tc_commit(bar(B_KV_FREE + s));
@@ -321,7 +384,9 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tmem_st32_strided<1>(lane_base + 64 * h + 32, sv);
             return (ls[0] + ls[1]) + (ls[2] + ls[3]);
         };
-        for (int st = 0; st < ns; ++st) {
+        // a second tile without rows of this item has no work
+        const int ns_t = t < ntl ? ns : 0;
+        for (int st = 0; st < ns_t; ++st) {
             mbar_wait(bar(B_S_FULL + t), st & 1, p.err_word, abort_flag);
             tc_fence_after();
             const bool two = 2 * st + 1 < nb;
@@ -367,10 +432,20 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             if (need) m_used = m_new;
             if (two) {
                 l += make_p(1, am1);               // keys 64..127 are in sv
+                if constexpr (WideSchedule<MODE>::split_p) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(B_P_HALF + t));
+                }
                 tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                 tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tmem_wait_ld();
                 l += make_p(0, am0);
+            } else if constexpr (WideSchedule<MODE>::split_p) {
+                // one block: no P.V for the second half (its barrier still
+                // completes once per step)
+                mbar_arrive(bar(B_P_HALF + t));
+                l += make_p(0, am0);               // keys 0..63 are in sv
             } else {
                 l += make_p(0, am0);               // keys 0..63 are in sv
                 // the second block is zeros (V rows of zeros): P = 0 there
@@ -387,7 +462,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         // ---- epilogue: O / l for the rows of this tile ----
         const int i = my_i(), h = my_h();
         const bool valid_row = my_valid();
-        if (ns > 0) {
+        if (ns_t > 0) {
             mbar_wait(bar(B_O_DONE + t), 0, p.err_word, abort_flag);
             tc_fence_after();
         }
@@ -399,7 +474,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
-            if (ns > 0) {
+            if (ns_t > 0) {
                 tmem_ld32(lane_base + kOCol + 32 * c, ov);
                 tmem_wait_ld();
             }
