@@ -58,6 +58,15 @@ def load_library(path: str):
     bsr_ex = [vp, vp, vp, vp, vp, vp, ci] + bsr_common[5:]
     lib.oracle_bsr_ex.argtypes = bsr_ex + [vp, vp]
     lib.oracle_bsr_ex.restype = ci
+    bsr_cap = bsr_ex[:-1] + [cd] + bsr_ex[-1:]          # ..., scale, softcap, dtype
+    lib.oracle_bsr_cap.argtypes = bsr_cap + [vp, vp]
+    lib.oracle_bsr_cap.restype = ci
+    lib.oracle_bsr_rows_cap.argtypes = bsr_cap + [vp, i64, vp, vp]
+    lib.oracle_bsr_rows_cap.restype = ci
+    lib.oracle_varbsr_cap.argtypes = [vp] * 6 + [ci] * 8 + [cd, cd, ci, vp, vp]
+    lib.oracle_varbsr_cap.restype = ci
+    lib.oracle_varbsr_rows_cap.argtypes = [vp] * 6 + [ci] * 8 + [cd, cd, ci, vp, i64, vp, vp]
+    lib.oracle_varbsr_rows_cap.restype = ci
     lib.oracle_bsr_rows_ex.argtypes = bsr_ex + [vp, i64, vp, vp]
     lib.oracle_bsr_rows_ex.restype = ci
     lib.oracle_varbsr.argtypes = [vp] * 6 + [ci] * 8 + [cd, ci, vp, vp]
@@ -186,10 +195,11 @@ def _mask_args(mask, packed_mask):
     return pm, pm.ctypes.data
 
 
-def bsr(q, k, v, indptr, indices, M, N, R, C, scale, mask=None, packed_mask=None, causal=False):
+def bsr(q, k, v, indptr, indices, M, N, R, C, scale, mask=None, packed_mask=None, causal=False,
+        softcap=0.0):
     """Block-sparse attention, NHD tensors.  Returns (y (M,Hq,d), lse (M,Hq)).
     mask: (nnz, R, C) bool per stored block (or packed_mask bytes); causal
-    applies only without a mask."""
+    applies only without a mask; softcap > 0 soft-caps the scaled logits."""
     Hq, d = q.shape[1], q.shape[2]
     Hkv = k.shape[1]
     indptr = indptr.to(torch.int32).contiguous()
@@ -198,16 +208,16 @@ def bsr(q, k, v, indptr, indices, M, N, R, C, scale, mask=None, packed_mask=None
     lse = np.empty((M, Hq))
     ind_ptr = _ptr(indices) if indices.numel() else 0
     keep, pm_ptr = _mask_args(mask, packed_mask)
-    rc = _load().oracle_bsr_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, pm_ptr,
-                               int(bool(causal)), M, N, R, C, Hq, Hkv, d, float(scale),
-                               _dtype_of(q), y.ctypes.data, lse.ctypes.data)
+    rc = _load().oracle_bsr_cap(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, pm_ptr,
+                                int(bool(causal)), M, N, R, C, Hq, Hkv, d, float(scale),
+                                float(softcap), _dtype_of(q), y.ctypes.data, lse.ctypes.data)
     _check(rc, "oracle_bsr")
     del keep
     return y, lse
 
 
 def bsr_rows(q, k, v, indptr, indices, M, N, R, C, scale, rows, mask=None, packed_mask=None,
-             causal=False):
+             causal=False, softcap=0.0):
     """Selected rows: rows is (n, 2) of (query row i, qo head h)."""
     Hq, d = q.shape[1], q.shape[2]
     Hkv = k.shape[1]
@@ -219,16 +229,16 @@ def bsr_rows(q, k, v, indptr, indices, M, N, R, C, scale, rows, mask=None, packe
     lse = np.empty(n)
     ind_ptr = _ptr(indices) if indices.numel() else 0
     keep, pm_ptr = _mask_args(mask, packed_mask)
-    rc = _load().oracle_bsr_rows_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, pm_ptr,
-                                    int(bool(causal)), M, N, R, C, Hq, Hkv, d, float(scale),
-                                    _dtype_of(q), rows.ctypes.data, n, y.ctypes.data,
-                                    lse.ctypes.data)
+    rc = _load().oracle_bsr_rows_cap(_ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, pm_ptr,
+                                     int(bool(causal)), M, N, R, C, Hq, Hkv, d, float(scale),
+                                     float(softcap), _dtype_of(q), rows.ctypes.data, n,
+                                     y.ctypes.data, lse.ctypes.data)
     _check(rc, "oracle_bsr_rows")
     del keep
     return y, lse
 
 
-def varbsr(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, causal=False):
+def varbsr(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, causal=False, softcap=0.0):
     """Variable block-sparse attention, HND tensors: q (Hq, M, d), k/v (Hkv, N, d),
     block_mask_map (Hkv, MB, NB) bool, block_row_sz (Hkv, MB), block_col_sz
     (Hkv, NB).  Returns (y (Hq, M, d), lse (Hq, M))."""
@@ -240,15 +250,17 @@ def varbsr(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, causal=Fa
     MB, NB = mm.shape[1], mm.shape[2]
     y = np.empty((Hq, M, d))
     lse = np.empty((Hq, M))
-    rc = _load().oracle_varbsr(_ptr(q.contiguous()), _ptr(k.contiguous()), _ptr(v.contiguous()),
-                               mm.ctypes.data, rs.ctypes.data, cs.ctypes.data, MB, NB, M, N, Hq,
-                               Hkv, d, int(bool(causal)), float(scale), _dtype_of(q),
-                               y.ctypes.data, lse.ctypes.data)
+    rc = _load().oracle_varbsr_cap(_ptr(q.contiguous()), _ptr(k.contiguous()),
+                                   _ptr(v.contiguous()), mm.ctypes.data, rs.ctypes.data,
+                                   cs.ctypes.data, MB, NB, M, N, Hq, Hkv, d, int(bool(causal)),
+                                   float(scale), float(softcap), _dtype_of(q), y.ctypes.data,
+                                   lse.ctypes.data)
     _check(rc, "oracle_varbsr")
     return y, lse
 
 
-def varbsr_rows(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, rows, causal=False):
+def varbsr_rows(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, rows, causal=False,
+                softcap=0.0):
     """Rows `rows` (flat h * M + i) of varbsr(): (y (n, d), lse (n))."""
     Hq, M, d = q.shape
     Hkv, N = k.shape[0], k.shape[1]
@@ -259,11 +271,12 @@ def varbsr_rows(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, rows
     n = rows.shape[0]
     y = np.empty((n, d))
     lse = np.empty(n)
-    rc = _load().oracle_varbsr_rows(_ptr(q.contiguous()), _ptr(k.contiguous()),
-                                    _ptr(v.contiguous()), mm.ctypes.data, rs.ctypes.data,
-                                    cs.ctypes.data, mm.shape[1], mm.shape[2], M, N, Hq, Hkv, d,
-                                    int(bool(causal)), float(scale), _dtype_of(q),
-                                    rows.ctypes.data, n, y.ctypes.data, lse.ctypes.data)
+    rc = _load().oracle_varbsr_rows_cap(_ptr(q.contiguous()), _ptr(k.contiguous()),
+                                        _ptr(v.contiguous()), mm.ctypes.data, rs.ctypes.data,
+                                        cs.ctypes.data, mm.shape[1], mm.shape[2], M, N, Hq, Hkv,
+                                        d, int(bool(causal)), float(scale), float(softcap),
+                                        _dtype_of(q), rows.ctypes.data, n, y.ctypes.data,
+                                        lse.ctypes.data)
     _check(rc, "oracle_varbsr_rows")
     return y, lse
 

@@ -44,6 +44,10 @@
  *   LSE -- run() / run_return_lse(): "log-sum-exp of attention logits".
  *     Read as the natural logarithm of sum_j exp(scaled logit j) over the
  *     unmasked positions; -inf for a fully masked row.
+ *   Soft cap -- plan() `logits_soft_cap` of both block-sparse wrappers: when
+ *     cap > 0 a logit x becomes cap * tanh(x / cap).  The page does not say
+ *     whether x includes sm_scale; read as the scaled logit sm_scale * q.k
+ *     (the softmax input), so the LSE is over the capped logits.
  *
  * Return codes: 0 ok, -1 bad argument, -2 an index outside [0, S2) (the
  * operator spec makes in-range indices a precondition).
@@ -252,7 +256,12 @@ typedef struct {
     double scale;
     const uint8_t* packed_mask;   /* NULL: every stored block is full */
     int causal;                   /* used only without a mask */
+    double softcap;               /* > 0: logits become softcap * tanh(logit / softcap) */
 } oracle_bsr_shape;
+
+/* plan()'s logits_soft_cap ("flashinfer.sparse", both wrappers): a logit x
+ * (the scaled score sm_scale * q.k) becomes cap * tanh(x / cap) when cap > 0. */
+static double oracle_soft_cap(double x, double cap) { return cap > 0.0 ? cap * tanh(x / cap) : x; }
 
 static int oracle_bsr_check(const oracle_bsr_shape* s, const int32_t* indptr,
                             const int32_t* indices) {
@@ -302,7 +311,7 @@ static void oracle_bsr_row(const oracle_bsr_shape* s, const uint16_t* q, const u
         double dot = 0.0;
         for (int e = 0; e < s->d; ++e)
             dot += oracle_load(q, qo + e, s->dtype) * oracle_load(k, ko + e, s->dtype);
-        scores[j] = dot * s->scale;
+        scores[j] = oracle_soft_cap(dot * s->scale, s->softcap);
         if (scores[j] > mx) mx = scores[j];
     }
     for (int e = 0; e < s->d; ++e) y_row[e] = 0.0;
@@ -325,11 +334,11 @@ static void oracle_bsr_row(const oracle_bsr_shape* s, const uint16_t* q, const u
     if (lse_row) *lse_row = mx + log(sum);
 }
 
-int oracle_bsr_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* indptr,
-                  const int32_t* indices, const uint8_t* packed_mask, int causal, int M, int N,
-                  int R, int C, int Hq, int Hkv, int d, double scale, int dtype, double* y,
-                  double* lse) {
-    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale, packed_mask, causal};
+int oracle_bsr_cap(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* indptr,
+                   const int32_t* indices, const uint8_t* packed_mask, int causal, int M, int N,
+                   int R, int C, int Hq, int Hkv, int d, double scale, double softcap, int dtype,
+                   double* y, double* lse) {
+    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale, packed_mask, causal, softcap};
     int rc = oracle_bsr_check(&s, indptr, indices);
     if (rc) return rc;
     const int64_t rows = (int64_t)M * Hq;
@@ -355,6 +364,14 @@ int oracle_bsr_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
     return err;
 }
 
+int oracle_bsr_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* indptr,
+                  const int32_t* indices, const uint8_t* packed_mask, int causal, int M, int N,
+                  int R, int C, int Hq, int Hkv, int d, double scale, int dtype, double* y,
+                  double* lse) {
+    return oracle_bsr_cap(q, k, v, indptr, indices, packed_mask, causal, M, N, R, C, Hq, Hkv, d,
+                          scale, 0.0, dtype, y, lse);
+}
+
 int oracle_bsr(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* indptr,
                const int32_t* indices, int M, int N, int R, int C, int Hq, int Hkv, int d,
                double scale, int dtype, double* y, double* lse) {
@@ -363,12 +380,12 @@ int oracle_bsr(const uint16_t* q, const uint16_t* k, const uint16_t* v, const in
 }
 
 /* Selected rows only: rows[2*r], rows[2*r+1] = (query row i, qo head h). */
-int oracle_bsr_rows_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                       const int32_t* indptr, const int32_t* indices, const uint8_t* packed_mask,
-                       int causal, int M, int N, int R, int C, int Hq, int Hkv, int d, double scale,
-                       int dtype, const int64_t* rows, int64_t nrows, double* y_rows,
-                       double* lse_rows) {
-    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale, packed_mask, causal};
+int oracle_bsr_rows_cap(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const int32_t* indptr, const int32_t* indices, const uint8_t* packed_mask,
+                        int causal, int M, int N, int R, int C, int Hq, int Hkv, int d,
+                        double scale, double softcap, int dtype, const int64_t* rows,
+                        int64_t nrows, double* y_rows, double* lse_rows) {
+    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale, packed_mask, causal, softcap};
     int rc = oracle_bsr_check(&s, indptr, indices);
     if (rc) return rc;
     int err = ORACLE_OK;
@@ -391,6 +408,15 @@ int oracle_bsr_rows_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         free(scores);
     }
     return err;
+}
+
+int oracle_bsr_rows_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const int32_t* indptr, const int32_t* indices, const uint8_t* packed_mask,
+                       int causal, int M, int N, int R, int C, int Hq, int Hkv, int d, double scale,
+                       int dtype, const int64_t* rows, int64_t nrows, double* y_rows,
+                       double* lse_rows) {
+    return oracle_bsr_rows_cap(q, k, v, indptr, indices, packed_mask, causal, M, N, R, C, Hq, Hkv,
+                               d, scale, 0.0, dtype, rows, nrows, y_rows, lse_rows);
 }
 
 int oracle_bsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -420,6 +446,7 @@ typedef struct {
     const int32_t *row_sz, *col_sz;
     int MB, NB, M, N, Hq, Hkv, d, causal, dtype;
     double scale;
+    double softcap;               /* > 0: soft-capped logits, as oracle_soft_cap */
 } varbsr_problem;
 
 /* Row r = h * M + i of the variable block-sparse output (y_row: d values).
@@ -444,7 +471,7 @@ static void varbsr_row(const varbsr_problem* s, int64_t r, int* colblk, double* 
         for (int e = 0; e < d; ++e)
             dot += oracle_load(s->q, ((int64_t)h * M + i) * d + e, s->dtype) *
                    oracle_load(s->k, ((int64_t)g * N + j) * d + e, s->dtype);
-        scores[j] = dot * s->scale;
+        scores[j] = oracle_soft_cap(dot * s->scale, s->softcap);
         if (scores[j] > mx) mx = scores[j];
     }
     for (int e = 0; e < d; ++e) y_row[e] = 0.0;
@@ -487,14 +514,15 @@ static int varbsr_setup(varbsr_problem* s) {
     return ORACLE_OK;
 }
 
-/* Rows rows[0..n) (each h * M + i) of the output: y (n, d), lse (n). */
-int oracle_varbsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                       const uint8_t* mask_map, const int32_t* row_sz, const int32_t* col_sz,
-                       int MB, int NB, int M, int N, int Hq, int Hkv, int d, int causal,
-                       double scale, int dtype, const int64_t* rows, int64_t n, double* y,
-                       double* lse) {
+/* Rows rows[0..n) (each h * M + i) of the output: y (n, d), lse (n);
+ * softcap > 0 soft-caps the logits. */
+int oracle_varbsr_rows_cap(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const uint8_t* mask_map, const int32_t* row_sz, const int32_t* col_sz,
+                           int MB, int NB, int M, int N, int Hq, int Hkv, int d, int causal,
+                           double scale, double softcap, int dtype, const int64_t* rows, int64_t n,
+                           double* y, double* lse) {
     varbsr_problem s = {q, k, v, mask_map, row_sz, col_sz, MB, NB, M, N, Hq, Hkv, d, causal, dtype,
-                        scale};
+                        scale, softcap};
     int err = varbsr_setup(&s);
     if (err != ORACLE_OK) return err;
     for (int64_t t = 0; t < n; ++t)
@@ -520,13 +548,13 @@ int oracle_varbsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     return err;
 }
 
-/* The whole output: y (Hq, M, d), lse (Hq, M). */
-int oracle_varbsr(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                  const uint8_t* mask_map, const int32_t* row_sz, const int32_t* col_sz, int MB,
-                  int NB, int M, int N, int Hq, int Hkv, int d, int causal, double scale,
-                  int dtype, double* y, double* lse) {
+/* The whole output: y (Hq, M, d), lse (Hq, M); softcap > 0 soft-caps the logits. */
+int oracle_varbsr_cap(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      const uint8_t* mask_map, const int32_t* row_sz, const int32_t* col_sz, int MB,
+                      int NB, int M, int N, int Hq, int Hkv, int d, int causal, double scale,
+                      double softcap, int dtype, double* y, double* lse) {
     varbsr_problem s = {q, k, v, mask_map, row_sz, col_sz, MB, NB, M, N, Hq, Hkv, d, causal, dtype,
-                        scale};
+                        scale, softcap};
     int err = varbsr_setup(&s);
     if (err != ORACLE_OK) return err;
 #pragma omp parallel
@@ -548,4 +576,21 @@ int oracle_varbsr(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         free(allowed);
     }
     return err;
+}
+
+int oracle_varbsr(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                  const uint8_t* mask_map, const int32_t* row_sz, const int32_t* col_sz, int MB,
+                  int NB, int M, int N, int Hq, int Hkv, int d, int causal, double scale,
+                  int dtype, double* y, double* lse) {
+    return oracle_varbsr_cap(q, k, v, mask_map, row_sz, col_sz, MB, NB, M, N, Hq, Hkv, d, causal,
+                             scale, 0.0, dtype, y, lse);
+}
+
+int oracle_varbsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const uint8_t* mask_map, const int32_t* row_sz, const int32_t* col_sz,
+                       int MB, int NB, int M, int N, int Hq, int Hkv, int d, int causal,
+                       double scale, int dtype, const int64_t* rows, int64_t n, double* y,
+                       double* lse) {
+    return oracle_varbsr_rows_cap(q, k, v, mask_map, row_sz, col_sz, MB, NB, M, N, Hq, Hkv, d,
+                                  causal, scale, 0.0, dtype, rows, n, y, lse);
 }

@@ -11,6 +11,7 @@ import pytest
 import oracle
 from tests import test_oracle_bsr_mask as mpins
 from tests import test_oracle_pins as pins
+from tests import test_oracle_softcap as cpins
 from tests import test_oracle_varbsr as vpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "sfa_oracle.c")
@@ -47,10 +48,10 @@ MUTANTS = [
      "if ((int64_t)j > (int64_t)i) allowed[j] = 0;"),
     ("bsr_causal_with_mask", "if (!s->packed_mask && s->causal)", "if (s->causal)"),
     ("bsr_row_block_reversed", "const int br = i / s->R;", "const int br = (s->M - 1 - i) / s->R;"),
-    ("bsr_scale_dropped", "oracle_load(k, ko + e, s->dtype);\n        scores[j] = dot * s->scale;",
-     "oracle_load(k, ko + e, s->dtype);\n        scores[j] = dot;"),
-    ("varbsr_scale_dropped", "* d + e, s->dtype);\n        scores[j] = dot * s->scale;",
-     "* d + e, s->dtype);\n        scores[j] = dot;"),
+    ("bsr_scale_dropped", "oracle_load(k, ko + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot * s->scale,",
+     "oracle_load(k, ko + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot,"),
+    ("varbsr_scale_dropped", "* d + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot * s->scale,",
+     "* d + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot,"),
     ("varbsr_kv_head_map", "i = (int)(r % s->M), g = h / G;", "i = (int)(r % s->M), g = h % s->Hkv;"),
     ("varbsr_row_block_off_by_one", "while (acc + row_sz[(int64_t)g * MB + rb] <= i)",
      "while (acc + row_sz[(int64_t)g * MB + rb] < i)"),
@@ -60,6 +61,12 @@ MUTANTS = [
      "mask_map[((int64_t)g * NB + colblk[j]) * MB + rb]"),
     ("varbsr_causal_top_left", "if (s->causal && (int64_t)j > (int64_t)i + (N - M)) allowed[j] = 0;",
      "if (s->causal && (int64_t)j > (int64_t)i) allowed[j] = 0;"),
+    ("softcap_before_scale", "* d + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot * s->scale, s->softcap);",
+     "* d + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot, s->softcap) * s->scale;"),
+    ("softcap_no_multiplier", "return cap > 0.0 ? cap * tanh(x / cap) : x;",
+     "return cap > 0.0 ? tanh(x / cap) : x;"),
+    ("softcap_ignored_in_bsr", "oracle_load(k, ko + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot * s->scale, s->softcap);",
+     "oracle_load(k, ko + e, s->dtype);\n        scores[j] = dot * s->scale;"),
     ("bf16_as_f16", "return dtype == 1 ? oracle_bf16(p[i]) : oracle_f16(p[i]);",
      "return oracle_f16(p[i]);"),
 ]
@@ -91,6 +98,10 @@ def all_pins():
             vpins.test_uniform_keys_give_mean_of_allowed_values]
     for causal in (False, True):
         out.append(lambda c=causal: vpins.test_matches_dense_brute_force(c, "f16"))
+    # soft-cap pins
+    out += [cpins.test_large_cap_is_no_cap, cpins.test_tiny_cap_gives_mean_of_allowed_values,
+            lambda: cpins.test_bsr_matches_dense_brute_force("plain", 0.7),
+            lambda: cpins.test_varbsr_matches_dense_brute_force(False)]
     return out
 
 
