@@ -277,6 +277,17 @@ sfa_status bsr_plan_masked_int_workspace_size(const int32_t* indptr_host, int M,
 sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v, void* out,
                    float* lse, sfa_stream_t stream);
 
+/*
+ * bsr_plan_set_logits_soft_cap -- plan()'s logits_soft_cap ("flashinfer.sparse",
+ * BlockSparseAttentionWrapper.plan()): with cap > 0 every logit x (the scaled
+ * score sm_scale * q.k; the page does not say whether x includes sm_scale)
+ * becomes cap * tanh(x / cap) before the softmax, and lse is over the capped
+ * logits.  cap <= 0 turns it off (the page's default 0).  Applies to every
+ * later bsr_run with this plan.  Host only.
+ * Errors: SFA_ERR_INVALID_ARG (NULL plan, non-finite cap).
+ */
+sfa_status bsr_plan_set_logits_soft_cap(bsr_plan_t plan, float logits_soft_cap);
+
 /* Frees the plan's host state.  Safe on NULL.  Does not touch the
  * caller's workspaces. */
 void bsr_plan_destroy(bsr_plan_t plan);
@@ -352,6 +363,11 @@ sfa_status varbsr_plan_dims(varbsr_plan_t plan, int* qo_len, int* kv_len);
  */
 sfa_status varbsr_run(varbsr_plan_t plan, const void* q, const void* k, const void* v,
                       void* out, float* lse, sfa_stream_t stream);
+
+/* varbsr_plan_set_logits_soft_cap -- plan()'s logits_soft_cap
+ * (VariableBlockSparseAttentionWrapper.plan()), as
+ * bsr_plan_set_logits_soft_cap.  Host only. */
+sfa_status varbsr_plan_set_logits_soft_cap(varbsr_plan_t plan, float logits_soft_cap);
 
 /* Frees the plan's host state.  Safe on NULL. */
 void varbsr_plan_destroy(varbsr_plan_t plan);

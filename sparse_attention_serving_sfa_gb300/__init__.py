@@ -32,7 +32,8 @@ EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
            "sfa_status_string", "sfa_kernel_launches", "sfa_run_noalloc", "bsr_plan", "bsr_plan_int_workspace_size", "bsr_run",
            "bsr_plan_destroy", "bsr_plan_masked", "bsr_plan_masked_int_workspace_size",
            "varbsr_plan", "varbsr_plan_int_workspace_size", "varbsr_plan_dims", "varbsr_run",
-           "varbsr_plan_destroy")
+           "varbsr_plan_destroy", "bsr_plan_set_logits_soft_cap",
+           "varbsr_plan_set_logits_soft_cap")
 
 
 class SfaError(RuntimeError):
@@ -106,6 +107,10 @@ def load():
             lib.varbsr_run.restype = ci
             lib.varbsr_plan_destroy.argtypes = [vp]
             lib.varbsr_plan_destroy.restype = None
+            lib.bsr_plan_set_logits_soft_cap.argtypes = [vp, cf]
+            lib.bsr_plan_set_logits_soft_cap.restype = ci
+            lib.varbsr_plan_set_logits_soft_cap.argtypes = [vp, cf]
+            lib.varbsr_plan_set_logits_soft_cap.restype = ci
             _lib = lib
     return _lib
 
@@ -247,10 +252,11 @@ def pack_block_mask(mask):
 
 def bsr_plan(indptr_host, indices_host, M, N, R, C, num_qo_heads, num_kv_heads, head_dim,
              causal=False, sm_scale=0.0, dtype="f16", int_ws=None, float_ws=None,
-             stream=None, mask=None, packed_mask=None) -> BsrPlan:
+             stream=None, mask=None, packed_mask=None, logits_soft_cap=0.0) -> BsrPlan:
     """Forwards to bsr_plan(), or to bsr_plan_masked() when a per-element
-    mask ((nnz, R, C) bool) or its packed bytes are given.  indptr/indices are
-    host int32 tensors; int_ws a device uint8 tensor (allocated here with
+    mask ((nnz, R, C) bool) or its packed bytes are given, then to
+    bsr_plan_set_logits_soft_cap() when logits_soft_cap > 0.  indptr/indices
+    are host int32 tensors; int_ws a device uint8 tensor (allocated here with
     torch if None)."""
     import numpy as np
     import torch
@@ -273,7 +279,15 @@ def bsr_plan(indptr_host, indices_host, M, N, R, C, num_qo_heads, num_kv_heads, 
     else:
         st = load().bsr_plan_masked(_ptr(indptr_host), ind, packed_mask.ctypes.data, *args)
     _check(st, "bsr_plan")
-    return BsrPlan(handle.value, int_ws, M, N, num_qo_heads, head_dim)
+    plan = BsrPlan(handle.value, int_ws, M, N, num_qo_heads, head_dim)
+    if logits_soft_cap > 0:
+        bsr_plan_set_logits_soft_cap(plan, logits_soft_cap)
+    return plan
+
+
+def bsr_plan_set_logits_soft_cap(plan: BsrPlan, logits_soft_cap: float):
+    _check(load().bsr_plan_set_logits_soft_cap(plan.handle, float(logits_soft_cap)),
+           "bsr_plan_set_logits_soft_cap")
 
 
 def bsr_run(plan: BsrPlan, q, k, v, out, lse=None, stream=None):
@@ -334,7 +348,7 @@ def varbsr_plan_int_workspace_size(block_mask_map, block_row_sz, block_col_sz, n
 
 def varbsr_plan(block_mask_map, block_row_sz, block_col_sz, num_qo_heads, num_kv_heads,
                 head_dim, causal=False, sm_scale=0.0, dtype="f16", int_ws=None,
-                stream=None) -> VarBsrPlan:
+                stream=None, logits_soft_cap=0.0) -> VarBsrPlan:
     """Forwards to varbsr_plan().  The block mask map and sizes may be numpy
     arrays or tensors on any device (they are read on the host); int_ws is a
     device uint8 tensor (allocated here with torch if None)."""
@@ -350,7 +364,15 @@ def varbsr_plan(block_mask_map, block_row_sz, block_col_sz, num_qo_heads, num_kv
                               int(bool(causal)), float(sm_scale), _enum(dtype, DTYPES),
                               _ptr(int_ws), int_ws.numel() * int_ws.element_size(),
                               _stream(stream), ctypes.byref(handle)), "varbsr_plan")
-    return VarBsrPlan(handle.value, int_ws, num_qo_heads, head_dim)
+    plan = VarBsrPlan(handle.value, int_ws, num_qo_heads, head_dim)
+    if logits_soft_cap > 0:
+        varbsr_plan_set_logits_soft_cap(plan, logits_soft_cap)
+    return plan
+
+
+def varbsr_plan_set_logits_soft_cap(plan: VarBsrPlan, logits_soft_cap: float):
+    _check(load().varbsr_plan_set_logits_soft_cap(plan.handle, float(logits_soft_cap)),
+           "varbsr_plan_set_logits_soft_cap")
 
 
 def varbsr_run(plan: VarBsrPlan, q, k, v, out, lse=None, stream=None):

@@ -22,6 +22,7 @@ struct bsr_plan_s {
     int MB, NB, nnz, ntiles;
     bool tc;                        // tensor-core path (work items) vs generic (row tiles)
     int mask_mode;                  // 0 none, 1 causal, 2 per-element bits
+    float softcap_log2 = 0.f;       // logits_soft_cap * log2(e); 0 = none
     const int32_t* d_indptr;
     const int32_t* d_indices;
     const void* d_work;             // BsrTile list (generic) or 4-int items (tensor cores)
@@ -246,6 +247,7 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
     p.scale_log2 = plan->scale * sfa::kLog2e;
     p.mask_mode = plan->mask_mode;
     p.mask = plan->d_mask;
+    p.softcap_log2 = plan->softcap_log2;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
     if (plan->tc) {
@@ -259,6 +261,12 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
         err = sfa::launch_bsr_generic(p, plan->dtype, s);
     }
     return err == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+sfa_status bsr_plan_set_logits_soft_cap(bsr_plan_t plan, float logits_soft_cap) {
+    if (!plan || !isfinite(logits_soft_cap)) return SFA_ERR_INVALID_ARG;
+    plan->softcap_log2 = logits_soft_cap > 0.f ? logits_soft_cap * sfa::kLog2e : 0.f;
+    return SFA_OK;
 }
 
 void bsr_plan_destroy(bsr_plan_t plan) { delete plan; }

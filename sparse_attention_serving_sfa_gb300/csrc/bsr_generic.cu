@@ -149,6 +149,9 @@ __global__ void __launch_bounds__(kThreads) bsr_generic_kernel(const BsrParams p
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int kj = tx * 4 + j;
+                // logits soft cap (scores are already in log2 units)
+                if (p.softcap_log2 > 0.f)
+                    s[i][j] = soft_cap_log2(s[i][j], p.softcap_log2, 1.f / p.softcap_log2);
                 if (kj >= nk) {
                     s[i][j] = -INFINITY;
                 } else if (p.mask_mode != 0 && rl < tile.nrows) {

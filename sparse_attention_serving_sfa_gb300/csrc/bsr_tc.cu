@@ -94,6 +94,7 @@ struct BsrTcParams {
     int M, N, R, C, Hq, G, TR;
     float scale_log2;
     const uint8_t* mask;    // per-element bits, most significant first
+    float capl2, inv_capl2; // logits soft cap in log2 units (CAP instantiations)
 };
 
 // The 64-bit word whose bit j is element j of the 64 mask elements held,
@@ -104,7 +105,7 @@ __device__ __forceinline__ uint64_t mask_bits64(uint64_t raw) {
     return ((uint64_t)__byte_perm(lo, 0, 0x0123) << 32) | __byte_perm(hi, 0, 0x0123);
 }
 
-template <class E, int D>
+template <class E, int D, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
 bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const BsrTcParams p) {
@@ -297,7 +298,10 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
-            const float bmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            float bmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            // the soft cap is increasing too: capped max = max of capped
+            if constexpr (CAP)
+                if (bmax != -INFINITY) bmax = soft_cap_log2(bmax, p.capl2, p.inv_capl2);
             const float m_new = fmaxf(m_used, bmax);
             const bool need = m_new > m_used + kRescaleThreshold;
             if (b > 0) {
@@ -327,8 +331,14 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    float p0 = fast_exp2(__uint_as_float(sv[8 * c + 2 * e]) * p.scale_log2 - m_used);
-                    float p1 = fast_exp2(__uint_as_float(sv[8 * c + 2 * e + 1]) * p.scale_log2 - m_used);
+                    float u0 = __uint_as_float(sv[8 * c + 2 * e]) * p.scale_log2;
+                    float u1 = __uint_as_float(sv[8 * c + 2 * e + 1]) * p.scale_log2;
+                    if constexpr (CAP) {
+                        u0 = soft_cap_log2(u0, p.capl2, p.inv_capl2);
+                        u1 = soft_cap_log2(u1, p.capl2, p.inv_capl2);
+                    }
+                    float p0 = fast_exp2(u0 - m_used);
+                    float p1 = fast_exp2(u1 - m_used);
                     // masked keys give 0, also while the row has seen none (m = -inf)
                     if (!((am >> (8 * c + 2 * e)) & 1ull)) p0 = 0.f;
                     if (!((am >> (8 * c + 2 * e + 1)) & 1ull)) p1 = 0.f;
@@ -445,7 +455,7 @@ bool make_map_hnd(CUtensorMap* map, const void* base, bool bf16, int dim, int ro
 
 namespace {
 
-template <class E, int D>
+template <class E, int D, bool CAP>
 cudaError_t launch_tc_t(const BsrParams& bp, const BsrTcParams& tp, int nitems, cudaStream_t stream) {
     using L = TcSmem<D>;
     const bool bf16 = std::is_same<E, BF16>::value;
@@ -454,7 +464,7 @@ cudaError_t launch_tc_t(const BsrParams& bp, const BsrTcParams& tp, int nitems, 
         !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kKeys) ||
         !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kKeys))
         return cudaErrorInvalidValue;
-    auto kern = bsr_tc_kernel<E, D>;
+    auto kern = bsr_tc_kernel<E, D, CAP>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
     if (err != cudaSuccess) return err;
     kern<<<nitems, kThreads, L::alloc, stream>>>(mq, mk, mv, tp);
@@ -492,13 +502,22 @@ cudaError_t launch_bsr_tc(const BsrParams& bp, const void* items, int nitems, in
     tp.G = bp.Hq / bp.Hkv;
     tp.TR = kTileM / tp.G;
     tp.scale_log2 = bp.scale_log2;
+    const bool cap = bp.softcap_log2 > 0.f;
+    tp.capl2 = cap ? bp.softcap_log2 : 0.f;
+    tp.inv_capl2 = cap ? 1.f / bp.softcap_log2 : 0.f;
     const bool bf16 = dtype == SFA_DTYPE_BF16;
-    if (bp.d == 128)
-        return bf16 ? launch_tc_t<BF16, 128>(bp, tp, nitems, stream)
-                    : launch_tc_t<F16, 128>(bp, tp, nitems, stream);
-    if (bp.d == 64)
-        return bf16 ? launch_tc_t<BF16, 64>(bp, tp, nitems, stream)
-                    : launch_tc_t<F16, 64>(bp, tp, nitems, stream);
+#define SFA_BSR_TC_CAP(CAP_)                                                                     \
+    if (cap == CAP_) {                                                                           \
+        if (bp.d == 128)                                                                         \
+            return bf16 ? launch_tc_t<BF16, 128, CAP_>(bp, tp, nitems, stream)                   \
+                        : launch_tc_t<F16, 128, CAP_>(bp, tp, nitems, stream);                   \
+        if (bp.d == 64)                                                                          \
+            return bf16 ? launch_tc_t<BF16, 64, CAP_>(bp, tp, nitems, stream)                    \
+                        : launch_tc_t<F16, 64, CAP_>(bp, tp, nitems, stream);                    \
+    }
+    SFA_BSR_TC_CAP(false)
+    SFA_BSR_TC_CAP(true)
+#undef SFA_BSR_TC_CAP
     return cudaErrorInvalidValue;
 }
 

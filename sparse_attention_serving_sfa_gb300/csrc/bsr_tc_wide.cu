@@ -98,6 +98,7 @@ struct WideParams {
     int M, N, R, C, Hq, G, TR;
     float scale_log2;
     int causal;             // mode 3: bottom-right causal on top of the windows
+    float capl2, inv_capl2; // logits soft cap in log2 units (CAP instantiations)
 };
 
 // Keys j <= lim allowed among the 64 of a block (lim relative to its first key).
@@ -132,7 +133,7 @@ struct WideSchedule {
     static constexpr bool tile_skip = MODE != 0;
 };
 
-template <class E, int D, int MODE>
+template <class E, int D, int MODE, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
 bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const WideParams p) {
@@ -367,8 +368,14 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                float p0 = fast_exp2(__uint_as_float(sv[2 * k]) * p.scale_log2 - m_used);
-                float p1 = fast_exp2(__uint_as_float(sv[2 * k + 1]) * p.scale_log2 - m_used);
+                float u0 = __uint_as_float(sv[2 * k]) * p.scale_log2;
+                float u1 = __uint_as_float(sv[2 * k + 1]) * p.scale_log2;
+                if constexpr (CAP) {
+                    u0 = soft_cap_log2(u0, p.capl2, p.inv_capl2);
+                    u1 = soft_cap_log2(u1, p.capl2, p.inv_capl2);
+                }
+                float p0 = fast_exp2(u0 - m_used);
+                float p1 = fast_exp2(u1 - m_used);
                 if constexpr (MODE != 0) {
                     // masked keys give 0, also while the row has seen none (m = -inf)
                     if (!((am >> (2 * k)) & 1ull)) p0 = 0.f;
@@ -411,7 +418,10 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
             }
             // the scale is positive and rounding monotonic: max of scaled = scaled max
-            const float bmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            float bmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            // the soft cap is increasing too: capped max = max of capped
+            if constexpr (CAP)
+                if (bmax != -INFINITY) bmax = soft_cap_log2(bmax, p.capl2, p.inv_capl2);
             const float m_new = fmaxf(m_used, bmax);
             const bool need = m_new > m_used + kRescaleThreshold;
             // P.V of step st - 1 ran on the tensor core before this step's
@@ -501,7 +511,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     }
 }
 
-template <class E, int D, int MODE>
+template <class E, int D, int MODE, bool CAP>
 cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems, cudaStream_t stream) {
     using L = WideSmem<D>;
     const bool bf16 = std::is_same<E, BF16>::value;
@@ -515,7 +525,7 @@ cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems,
                !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kBlk) ||
                !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kBlk))
         return cudaErrorInvalidValue;
-    auto kern = bsr_tc_wide_kernel<E, D, MODE>;
+    auto kern = bsr_tc_wide_kernel<E, D, MODE, CAP>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
     if (err != cudaSuccess) return err;
     kern<<<nitems, kThreads, L::alloc, stream>>>(mq, mk, mv, wp);
@@ -544,20 +554,25 @@ cudaError_t launch_bsr_tc_wide(const BsrParams& bp, const void* items, int nitem
     wp.G = bp.Hq / bp.Hkv;
     wp.TR = kTileM / wp.G;
     wp.scale_log2 = bp.scale_log2;
+    const bool cap = bp.softcap_log2 > 0.f;
+    wp.capl2 = cap ? bp.softcap_log2 : 0.f;
+    wp.inv_capl2 = cap ? 1.f / bp.softcap_log2 : 0.f;
     const bool bf16 = dtype == SFA_DTYPE_BF16;
-#define SFA_BSR_WIDE_MODE(MODE_)                                                                 \
-    if (bp.mask_mode == MODE_) {                                                                 \
+#define SFA_BSR_WIDE_MODE_CAP(MODE_, CAP_)                                                       \
+    if (bp.mask_mode == MODE_ && cap == CAP_) {                                                  \
         if (bp.d == 128)                                                                         \
-            return bf16 ? launch_wide_t<BF16, 128, MODE_>(bp, wp, nitems, stream)                \
-                        : launch_wide_t<F16, 128, MODE_>(bp, wp, nitems, stream);                \
+            return bf16 ? launch_wide_t<BF16, 128, MODE_, CAP_>(bp, wp, nitems, stream)          \
+                        : launch_wide_t<F16, 128, MODE_, CAP_>(bp, wp, nitems, stream);          \
         if (bp.d == 64)                                                                          \
-            return bf16 ? launch_wide_t<BF16, 64, MODE_>(bp, wp, nitems, stream)                 \
-                        : launch_wide_t<F16, 64, MODE_>(bp, wp, nitems, stream);                 \
+            return bf16 ? launch_wide_t<BF16, 64, MODE_, CAP_>(bp, wp, nitems, stream)           \
+                        : launch_wide_t<F16, 64, MODE_, CAP_>(bp, wp, nitems, stream);           \
     }
+#define SFA_BSR_WIDE_MODE(MODE_) SFA_BSR_WIDE_MODE_CAP(MODE_, false) SFA_BSR_WIDE_MODE_CAP(MODE_, true)
     SFA_BSR_WIDE_MODE(0)
     SFA_BSR_WIDE_MODE(1)
     SFA_BSR_WIDE_MODE(3)
 #undef SFA_BSR_WIDE_MODE
+#undef SFA_BSR_WIDE_MODE_CAP
     return cudaErrorInvalidValue;
 }
 

@@ -96,6 +96,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// plan()'s logits_soft_cap in log2 units: a logit u = x * log2(e) becomes
+// capl2 * tanh(u / capl2) with capl2 = cap * log2(e), i.e. cap * tanh(x / cap)
+// scaled to log2 units (tanhf: the accurate library function).
+__device__ __forceinline__ float soft_cap_log2(float u, float capl2, float inv_capl2) {
+    return capl2 * tanhf(u * inv_capl2);
+}
+
 // Rescale factor exp2(m_old - m_new) of an online softmax, defined as 1 when
 // both maxima are still -inf (no visible slot yet).
 __device__ __forceinline__ float rescale_factor(float m_old, float m_new) {

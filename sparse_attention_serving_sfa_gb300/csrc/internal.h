@@ -107,6 +107,8 @@ struct BsrParams {
     int mask_mode;
     const uint8_t* mask;
     int causal;
+    // plan()'s logits_soft_cap times log2(e); 0 = no cap
+    float softcap_log2;
 };
 
 cudaError_t launch_bsr_generic(const BsrParams& p, sfa_dtype dtype, cudaStream_t stream);

@@ -18,6 +18,7 @@ struct varbsr_plan_s {
     sfa_dtype dtype;
     float scale;
     int causal;
+    float softcap_log2 = 0.f;       // logits_soft_cap * log2(e); 0 = none
     int nlists, ntiles, nitems;
     const int32_t* d_lists;
     const int32_t* d_tiles;
@@ -260,11 +261,18 @@ sfa_status varbsr_run(varbsr_plan_t plan, const void* q, const void* k, const vo
     p.scale_log2 = plan->scale * sfa::kLog2e;
     p.mask_mode = 3;
     p.causal = plan->causal;
+    p.softcap_log2 = plan->softcap_log2;
     int* ew = sfa::device_error_word();
     if (!ew) return SFA_ERR_CUDA;
     cudaError_t err = sfa::launch_bsr_tc_wide(p, plan->d_items, plan->nitems, ew, plan->dtype,
                                               reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+sfa_status varbsr_plan_set_logits_soft_cap(varbsr_plan_t plan, float logits_soft_cap) {
+    if (!plan || !isfinite(logits_soft_cap)) return SFA_ERR_INVALID_ARG;
+    plan->softcap_log2 = logits_soft_cap > 0.f ? logits_soft_cap * sfa::kLog2e : 0.f;
+    return SFA_OK;
 }
 
 void varbsr_plan_destroy(varbsr_plan_t plan) { delete plan; }

@@ -218,6 +218,12 @@ def test_varbsr_plan_workspace_too_small(lib):
     assert st == sfa.SFA_ERR_WORKSPACE and not handle.value
 
 
+def test_soft_cap_setters_reject_bad_arguments(lib):
+    assert lib.bsr_plan_set_logits_soft_cap(None, 1.0) == sfa.SFA_ERR_INVALID_ARG
+    assert lib.varbsr_plan_set_logits_soft_cap(None, 1.0) == sfa.SFA_ERR_INVALID_ARG
+    # (making a plan needs a device; the NaN / inf checks run in test_gpu_softcap.py)
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(sfa, "LIB_PATH", str(tmp_path / "absent.so"))
     monkeypatch.setattr(sfa, "_lib", None)
