@@ -229,3 +229,50 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(sfa, "_lib", None)
     with pytest.raises(RuntimeError):
         sfa.load()
+
+
+def _varbsr_expected_bytes(mm, rs, cs, Hq, Hkv, causal):
+    """Workspace bytes from an independent count: per (kv head, row block) the
+    fewest 64-key windows covering the allowed keys (greedy from the first
+    uncovered key), and ceil(rows / (2 * 128 / G)) work items per non-empty
+    row block."""
+    Hkv_, MB, NB = mm.shape
+    M, N = int(rs[0].sum()), int(cs[0].sum())
+    rows_per = 2 * (128 // (Hq // Hkv))
+    ntiles = nitems = 0
+    for g in range(Hkv_):
+        cstart = np.concatenate([[0], np.cumsum(cs[g])])
+        r0 = 0
+        for rb in range(MB):
+            s = int(rs[g][rb])
+            if s > 0:
+                keys = np.zeros(N, bool)
+                for cb in np.nonzero(mm[g][rb])[0]:
+                    keys[cstart[cb]:cstart[cb + 1]] = True
+                if causal:
+                    keys[max(0, r0 + s - 1 + N - M + 1):] = False
+                j = 0
+                while j < N:
+                    if keys[j]:
+                        ntiles += 1
+                        j += 64
+                    else:
+                        j += 1
+                nitems += -(-s // rows_per)
+            r0 += s
+    nlists = Hkv_ * MB
+    return 4 * (((nlists + 1 + 3) // 4) * 4 + 4 * ntiles + 4 * nitems)
+
+
+@pytest.mark.parametrize("seed,causal,Hq,Hkv", [(1, False, 8, 2), (2, True, 8, 2),
+                                               (3, False, 16, 1), (4, True, 4, 4)])
+def test_varbsr_workspace_matches_independent_tiling(lib, seed, causal, Hq, Hkv):
+    import synth
+    c = synth.VarBsrCase("w", M=900, N=1300, MB=13, NB=17, Hq=Hq, Hkv=Hkv, d=128, dtype="f16",
+                         p=0.4, sm_scale=0.1, seed=seed, causal=causal)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rs = synth.block_sizes(rng, Hkv, c.MB, c.M)
+    cs = synth.block_sizes(rng, Hkv, c.NB, c.N)
+    mm = rng.random((Hkv, c.MB, c.NB)) < c.p
+    got = sfa.varbsr_plan_int_workspace_size(mm, rs, cs, Hq, Hkv, 128, causal=causal)
+    assert got == _varbsr_expected_bytes(mm.astype(np.uint8), rs, cs, Hq, Hkv, causal)
