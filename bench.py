@@ -236,7 +236,7 @@ def run_bsr(args, rank, world, local):
                      "block_sizes": "per kv head, uniform random cut points (mean "
                                     f"{case.M // case.MB} x {case.N // case.NB})",
                      "key_tiles": int(plan.int_ws.cpu().view(torch.int32)[case.Hkv * case.MB])}
-        kernel = "bsr_tc_kernel, variable mode (one launch per varbsr_run)"
+        kernel = "bsr_tc_wide_kernel, variable mode (one launch per varbsr_run)"
     else:
         case = synth.BSR_WORKLOADS[args.workload]
         x = synth.make_bsr_inputs(case)
@@ -248,7 +248,8 @@ def run_bsr(args, rank, world, local):
         lse_shape = (case.M, case.Hq)
         shape_cfg = {"layout": "NHD", "R": case.R, "C": case.C, "nnz_blocks": counts["nnz"],
                      "element_mask_keep": case.mask_keep or None}
-        kernel = "bsr_tc_kernel (one launch per bsr_run)"
+        kernel = ("bsr_tc_kernel, per-element mask (one launch per bsr_run)" if case.mask_keep > 0
+                  else "bsr_tc_wide_kernel (one launch per bsr_run)")
     q, k, v = x["q"].cuda(), x["k"].cuda(), x["v"].cuda()
     out = torch.empty_like(q)
     lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
