@@ -1,18 +1,28 @@
 """Benchmark of the sparse-attention hot path on GB300.
 
-One step = one call of the top-K sparse flash attention entry point over the
-GQA-decode workload (B=16, S1=1, S2=8192, N1=32, N2=8, Dk=Dv=128, topK=1024,
-bf16, BNSD, causal), inputs resident in HBM.  Steps run back to back over
-rotating replicas of the inputs whose gathered bytes exceed L2 several times,
-so every step gathers from HBM.  Prints one JSON line (rank 0).
+Headline: the sparse-prefill workload (B=2, S1=2048, S2=16384, N1=64, N2=8,
+Dk=192, Dv=128 with value = key prefix, topK=2048, fp16, BSND, causal), the
+largest top-K configuration.  One step = one call of the top-K entry point
+over the whole workload, inputs resident in HBM.  The same JSON line carries a
+`workloads` object with one record per other workload (GQA decode, MLA decode
+and MTP, the operator page's call example, block-sparse plain / causal /
+per-element mask, variable block-sparse), each with its own step time,
+roofline, end-to-end figure and CPU-oracle baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--sub all|none|a,b,...]
+
+The K timed steps of a workload are captured once into a CUDA graph (the
+public entry point called K times on one stream) and replayed, timed with
+CUDA events on that stream: the device time of K back-to-back calls, without
+the Python-side cost of each call.  `e2e` times the same entry point called
+eagerly from Python with the step's inputs copied in from pinned host memory
+and its outputs read back every step.
 
 --impl reference times the CPU oracle (test infrastructure) on the host cores
-on a bounded sample of the same workload.  Under torchrun every rank runs an
-independent replica of the workload (weak scaling, no collective on the data
-path); timing is the max over ranks.
+on a bounded sample of the headline workload.  Under torchrun every rank runs
+an independent replica of the workload (weak scaling, no collective on the
+data path); timing is the max over ranks.
 """
 from __future__ import annotations
 
@@ -37,25 +47,46 @@ import torch  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "sparse-attn effective TFLOP/s & gathered-KV GB/s, fraction of GB300 roofline"
-UNIT = "GB/s"   # gathered-KV bytes per second (the decode workload is HBM-bound)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HEADLINE = "sparse_prefill"
+SUB_WORKLOADS = ("gqa_decode", "mla_decode", "mla_mtp", "call_example", "bsr", "bsr_causal",
+                 "bsr_mask", "varbsr")
+ALL_WORKLOADS = sorted(synth.SFA_WORKLOADS) + sorted(synth.BSR_WORKLOADS) + \
+    sorted(synth.VARBSR_WORKLOADS)
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa_decode",
-                    choices=sorted(synth.SFA_WORKLOADS) + sorted(synth.BSR_WORKLOADS)
-                    + sorted(synth.VARBSR_WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=ALL_WORKLOADS)
+    ap.add_argument("--sub", default="auto",
+                    help="other workloads recorded under `workloads`: all, none or a comma "
+                         "list (auto = all with the default headline, none otherwise)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager calls instead of a captured CUDA graph")
     ap.add_argument("--replicas", type=int, default=0,
                     help="input replicas rotated over the steps (0 = enough to exceed L2 4x; "
                          "1 keeps a profiling capture small)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def sub_workloads(args):
+    if args.sub == "auto":
+        return list(SUB_WORKLOADS) if args.workload == HEADLINE else []
+    if args.sub == "none":
+        return []
+    if args.sub == "all":
+        return [w for w in SUB_WORKLOADS if w != args.workload]
+    names = [w for w in args.sub.split(",") if w]
+    bad = [w for w in names if w not in ALL_WORKLOADS]
+    if bad:
+        raise SystemExit(f"unknown workloads: {bad}")
+    return [w for w in names if w != args.workload]
 
 
 def dist_env():
@@ -92,16 +123,9 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def dtype_name(case):
-    return {"f16": "f16", "bf16": "bf16"}[case.dtype]
-
-
-def config_of(case, world):
-    return {"workload": case.name, "B": case.B, "S1": case.S1, "S2": case.S2, "N1": case.N1,
-            "N2": case.N2, "Dk": case.Dk, "Dv": case.Dv, "topK": case.topK,
-            "layout": case.layout, "causal": case.causal,
-            "value_is_key_prefix": case.value_is_key_prefix, "index": case.index_kind,
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
 
 
 # ---------------------------------------------------------------------------
@@ -160,9 +184,21 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def merge_clocks(parts):
+    parts = [c for c in parts if c]
+    if not parts:
+        return None
+    sm = [c["sm_mhz"] for c in parts if c.get("sm_mhz") is not None]
+    smax = [c["sm_max_mhz"] for c in parts if c.get("sm_max_mhz") is not None]
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted({r for c in parts for r in c["reasons"]}),
+            "samples": sum(c["samples"] for c in parts)}
+
+
 # ---------------------------------------------------------------------------
-# traffic figure from a committed ncu summary (only while the kernel source
-# it was taken on is unchanged)
+# figures from a committed ncu summary (only while the kernel sources it was
+# taken on are unchanged)
 
 def kernel_source_sha(files):
     """sha256 over the named kernel sources (file name + bytes, in order)."""
@@ -175,10 +211,11 @@ def kernel_source_sha(files):
     return h.hexdigest()
 
 
-def committed_traffic(workload):
-    """DRAM bytes per launch of the workload's main kernel from its committed
-    ncu summary (profiles/<workload>_ncu.md), or None when the summary is
-    missing or its kernel sources have changed since it was taken."""
+def committed_profile(workload):
+    """Per-launch figures of the workload's main kernel from its committed ncu
+    summary (profiles/<workload>_ncu.md): {"dram": bytes, "lts": bytes or
+    None}, or None when the summary is missing or its kernel sources have
+    changed since it was taken."""
     path = os.path.join(ROOT, "profiles", f"{workload}_ncu.md")
     if not os.path.exists(path):
         return None
@@ -193,129 +230,128 @@ def committed_traffic(workload):
             return None
     except OSError:
         return None
-    return float(val.group(1))
+    lts = re.search(r"^lts_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    return {"dram": float(val.group(1)), "lts": float(lts.group(1)) if lts else None}
 
 
-# main kernel of each top-K workload (what the roofline object describes)
+def committed_traffic(workload):
+    prof = committed_profile(workload)
+    return None if prof is None else prof["dram"]
+
+
+# main kernel of each workload (what the roofline object describes)
 MAIN_KERNEL = {
     "tiny": "generic top-K kernel",
-    "gqa_decode": "sfa_decode_kernel (one launch per sfa_run_ex call; split index lists merged in-kernel)",
-    "sparse_prefill": "sfa_decode_kernel (one launch per sfa_run_ex call; split index lists merged in-kernel)",
-    "mla_decode": "sfa_mla_kernel + sfa_mla_combine (two launches per sfa_run_ex call; time is the call's)",
-    "mla_mtp": "sfa_mla_kernel + sfa_mla_combine (two launches per sfa_run_ex call; time is the call's)",
-    "call_example": "sfa_decode_kernel (one launch per sfa_run_ex call; whole index lists per CTA)",
+    "gqa_decode": "sfa_decode_kernel (one launch per call; split index lists merged in-kernel)",
+    "sparse_prefill": "sfa_decode_kernel (one launch per call; whole index lists per CTA)",
+    "mla_decode": "sfa_mla_kernel + sfa_mla_combine (two launches per call; time is the call's)",
+    "mla_mtp": "sfa_mla_kernel + sfa_mla_combine (two launches per call; time is the call's)",
+    "call_example": "sfa_decode_kernel (one launch per call; whole index lists per CTA)",
+    "bsr": "bsr_tc_wide_kernel (one launch per bsr_run)",
+    "bsr_causal": "bsr_tc_wide_kernel, causal mode (one launch per bsr_run)",
+    "bsr_mask": "bsr_tc_kernel, per-element mask (one launch per bsr_run)",
+    "varbsr": "bsr_tc_wide_kernel, variable mode (one launch per varbsr_run)",
 }
 
 
 # ---------------------------------------------------------------------------
+# timing
 
-def run_bsr(args, rank, world, local):
-    """Block-sparse workloads (tensor-bound): one step = one bsr_run (or
-    varbsr_run) over the whole 16384 x 16384 pattern (plan built once, outside
-    the timed region)."""
+def device_time(step, steps, eager, world):
+    """Device time of `steps` back-to-back calls of step(i) on the current
+    stream: captured once into a CUDA graph and replayed (or, with `eager` or
+    when capture fails, called from Python), CUDA events on that stream,
+    barrier + synchronize on both sides.  Returns (ms per step, kernels
+    launched in the timed region, how the steps were launched)."""
     import sparse_attention_serving_sfa_gb300 as sfa
-
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    sfa.build()
-    sfa.load()
-    variable = args.workload in synth.VARBSR_WORKLOADS
-    if variable:
-        case = synth.VARBSR_WORKLOADS[args.workload]
-        x = synth.make_varbsr_inputs(case)
-        counts = synth.varbsr_counts(case, x["block_mask_map"], x["block_row_sz"],
-                                     x["block_col_sz"])
-        plan = sfa.varbsr_plan(x["block_mask_map"], x["block_row_sz"], x["block_col_sz"],
-                               case.Hq, case.Hkv, case.d, causal=case.causal,
-                               sm_scale=case.sm_scale, dtype=case.dtype)
-        run = sfa.varbsr_run
-        lse_shape = (case.Hq, case.M)
-        shape_cfg = {"layout": "HND", "MB": case.MB, "NB": case.NB,
-                     "block_sizes": "per kv head, uniform random cut points (mean "
-                                    f"{case.M // case.MB} x {case.N // case.NB})",
-                     "key_tiles": int(plan.int_ws.cpu().view(torch.int32)[case.Hkv * case.MB])}
-        kernel = "bsr_tc_wide_kernel, variable mode (one launch per varbsr_run)"
-    else:
-        case = synth.BSR_WORKLOADS[args.workload]
-        x = synth.make_bsr_inputs(case)
-        counts = synth.bsr_counts(case, x["indptr"], x["indices"], x["mask"])
-        plan = sfa.bsr_plan(x["indptr"], x["indices"], case.M, case.N, case.R, case.C, case.Hq,
-                            case.Hkv, case.d, sm_scale=case.sm_scale, dtype=case.dtype,
-                            causal=case.causal, mask=x["mask"])
-        run = sfa.bsr_run
-        lse_shape = (case.M, case.Hq)
-        shape_cfg = {"layout": "NHD", "R": case.R, "C": case.C, "nnz_blocks": counts["nnz"],
-                     "element_mask_keep": case.mask_keep or None}
-        kernel = ("bsr_tc_kernel, per-element mask (one launch per bsr_run)" if case.mask_keep > 0
-                  else "bsr_tc_wide_kernel (one launch per bsr_run)")
-    q, k, v = x["q"].cuda(), x["k"].cuda(), x["v"].cuda()
-    out = torch.empty_like(q)
-    lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
-    for _ in range(max(args.warmup, 3)):
-        run(plan, q, k, v, out, lse, stream)
-    torch.cuda.synchronize()
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.2)
+    graph, mode, per_graph = None, "eager", 0
+    if not eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            l0 = sfa.sfa_kernel_launches()
+            with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+                for i in range(steps):
+                    step(i)
+            per_graph = sfa.sfa_kernel_launches() - l0
+            graph.replay()           # one untimed replay
+            torch.cuda.synchronize()
+            mode = f"CUDA graph of the {steps} calls, replayed once"
+        except Exception as e:  # noqa: BLE001 - fall back to eager calls
+            graph = None
+            mode = f"eager (graph capture failed: {type(e).__name__})"
+            torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     torch.cuda.synchronize()
-    launches0 = sfa.sfa_kernel_launches()
+    l0 = sfa.sfa_kernel_launches()
     ev0.record(stream)
-    for _ in range(args.steps):
-        run(plan, q, k, v, out, lse, stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(steps):
+            step(i)
     ev1.record(stream)
     torch.cuda.synchronize()
-    launches = sfa.sfa_kernel_launches() - launches0
-    clocks = sampler.stop()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, "cuda")
-    peaks, peak_src = load_peaks()
-    tflops = counts["flops"] / (ms * 1e-3) / 1e12
-    res = {"metric": METRIC, "value": whole_job_rate(counts["flops"], ms, world) / 1e12,
-           "unit": "TFLOP/s", "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": case.dtype, "data": "synthetic (seeded generator, shapes of the workload)",
-           "config": {"workload": case.name, "M": case.M, "N": case.N, **shape_cfg,
-                      "Hq": case.Hq, "Hkv": case.Hkv, "d": case.d, "p": case.p,
-                      "causal": case.causal,
-                      "l2": "q, out (268 MiB) stream through; K/V (67 MiB) L2-resident by design",
-                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-           "roofline": {"bound": "tensor", "achieved": tflops,
-                        "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                        "frac": tflops / peaks["bf16_tflops_sustained"],
-                        "traffic": committed_traffic(case.name),
-                        "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 dense rate is the same)",
-                        "kernel": kernel},
-           "gpu_launches": launches, "clocks": clocks,
-           "work": {"flops": counts["flops"], "allowed_elements": counts["allowed"]}}
-    if world > 1:
-        torch.distributed.destroy_process_group()
-    return res
+    barrier(world)
+    launches = per_graph if graph is not None else sfa.sfa_kernel_launches() - l0
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / steps, world, "cuda")
+    return ms, int(launches), mode
 
 
-def run_ours(args, rank, world, local):
+def e2e_time(step_host, n, warm, world):
+    """Event-timed eager calls of step_host(i), each copying its inputs in from
+    pinned host memory and its outputs back."""
+    stream = torch.cuda.current_stream()
+    for i in range(warm):
+        step_host(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(n):
+        step_host(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return max_over_ranks(ev0.elapsed_time(ev1) / n, world, "cuda")
+
+
+def nbytes(t):
+    return t.numel() * t.element_size()
+
+
+# ---------------------------------------------------------------------------
+# top-K workloads
+
+def sfa_config(case, world):
+    return {"workload": case.name, "B": case.B, "S1": case.S1, "S2": case.S2, "N1": case.N1,
+            "N2": case.N2, "Dk": case.Dk, "Dv": case.Dv, "topK": case.topK,
+            "layout": case.layout, "causal": case.causal,
+            "value_is_key_prefix": case.value_is_key_prefix, "index": case.index_kind,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def roofline_terms(work, peaks):
+    """Time bounds of the survey's roofline: gathered bytes at the measured
+    HBM copy peak and useful FLOPs at the measured bf16 burst tensor peak."""
+    t_hbm = work["gathered_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = work["flops"] / (peaks["bf16_tflops"] * 1e12)
+    return t_hbm, t_tc
+
+
+def run_sfa(name, args, world, rank, cpu_target_s):
     import sparse_attention_serving_sfa_gb300 as sfa
-
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    sfa.build()
-    sfa.load()
-    case = synth.SFA_WORKLOADS[args.workload]
+    case = synth.SFA_WORKLOADS[name]
     host = synth.make_sfa_inputs(case)
     counts = synth.sfa_counts(case, host["idx"])
     prefix = case.value_is_key_prefix
-    # Rotating replicas of the inputs: consecutive steps read different
-    # copies, and the replicas' gathered bytes together exceed L2 several
-    # times, so every step gathers from HBM (no flush needed between steps).
-    l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    reps = args.replicas if args.replicas > 0 else max(2, -(-4 * l2 // counts["gathered_bytes"]) + 1)
+    # Rotating replicas: consecutive steps read different copies whose
+    # gathered bytes together exceed L2 several times, so every step gathers
+    # from HBM (no flush needed between steps).
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    reps = args.replicas if args.replicas > 0 else max(1, -(-4 * l2 // counts["gathered_bytes"]) + 1)
+    reps = min(reps, 12)
     replicas = []
     for _ in range(reps):
         d = {"q": host["q"].cuda(), "k": host["k"].cuda(), "idx": host["idx"].cuda()}
@@ -328,111 +364,84 @@ def run_ours(args, rank, world, local):
     tdt = replicas[0]["q"].dtype
     out = torch.empty(out_shape, dtype=tdt, device="cuda")
     lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
     ws_bytes = sfa.sfa_workspace_size(case.B, case.S1, case.N1, case.N2, case.Dk, case.Dv,
                                       case.topK)
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
 
-    def step(d, q=None, idx=None):
+    def call(d, q=None, idx=None):
         sfa.sfa_run_ex(d["q"] if q is None else q, d["k"], d["v"], d["idx"] if idx is None else idx,
                        case.B, case.S1, case.S2, case.N1, case.N2, case.Dk, case.Dv, case.topK,
-                       case.scale, case.layout, case.causal, case.dtype, out, lse, stream,
-                       workspace=ws, value_is_key_prefix=prefix)
+                       case.scale, case.layout, case.causal, case.dtype, out, lse,
+                       torch.cuda.current_stream(), workspace=ws, value_is_key_prefix=prefix)
 
     for i in range(max(args.warmup, 3) + reps):
-        step(replicas[i % reps])
+        call(replicas[i % reps])
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     time.sleep(0.2)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    launches0 = sfa.sfa_kernel_launches()
-    wall0 = time.perf_counter()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(replicas[i % reps])
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    launches = sfa.sfa_kernel_launches() - launches0
-    if world > 1:
-        torch.distributed.barrier()
+    ms, launches, mode = device_time(lambda i: call(replicas[i % reps]), args.steps, args.eager,
+                                     world)
     clocks = sampler.stop()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, "cuda")
 
-    # end to end through the same entry point with host buffers: every step
-    # copies its q and indices from pinned host memory and reads the output
-    # and lse back (the KV cache stays resident, as it does in serving)
     e2e = None
     if not args.no_e2e:
-        hq = host["q"].pin_memory()
-        hidx = host["idx"].pin_memory()
+        # the KV cache stays resident (as in serving); q and the indices come
+        # in from pinned host memory, out and lse go back, every step
+        hq, hidx = host["q"].pin_memory(), host["idx"].pin_memory()
         hout = torch.empty(out_shape, dtype=tdt).pin_memory()
         hlse = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
-        dq = torch.empty_like(replicas[0]["q"])
-        didx = torch.empty_like(replicas[0]["idx"])
-        n_e2e = max(args.steps // 4, 20)
+        dq, didx = torch.empty_like(replicas[0]["q"]), torch.empty_like(replicas[0]["idx"])
 
-        def e2e_step(i):
+        def step_host(i):
             dq.copy_(hq, non_blocking=True)
             didx.copy_(hidx, non_blocking=True)
-            step(replicas[i % reps], q=dq, idx=didx)
+            call(replicas[i % reps], q=dq, idx=didx)
             hout.copy_(out, non_blocking=True)
             hlse.copy_(lse, non_blocking=True)
 
-        for i in range(reps):
-            e2e_step(i)
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for i in range(n_e2e):
-            e2e_step(i)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        e_ms = max_over_ranks(ev0.elapsed_time(ev1) / n_e2e, world, "cuda")
-        h2d = hq.numel() * hq.element_size() + hidx.numel() * 4
-        d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
-        e2e = {"value": whole_job_rate(counts["gathered_bytes"], e_ms, world) / 1e9, "unit": UNIT,
-               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        n_e2e = max(min(args.steps, 50), 5)
+        e_ms = e2e_time(step_host, n_e2e, min(reps, 3), world)
+        e2e = {"value": whole_job_rate(counts["gathered_bytes"], e_ms, world) / 1e9,
+               "unit": "GB/s", "ms_per_step": e_ms, "steps": n_e2e,
+               "h2d_bytes_per_step": nbytes(hq) + nbytes(hidx),
+               "d2h_bytes_per_step": nbytes(hout) + nbytes(hlse)}
 
     peaks, peak_src = load_peaks()
     gbs = counts["gathered_bytes"] / (ms * 1e-3) / 1e9
     tflops = counts["flops"] / (ms * 1e-3) / 1e12
+    t_hbm, t_tc = roofline_terms(counts, peaks)
+    prof = committed_profile(name)
     roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"], "traffic": committed_traffic(args.workload),
+                "frac": gbs / peaks["hbm_gbs"], "traffic": None if prof is None else prof["dram"],
                 "peak_source": f"{peak_src} hbm_gbs (copy, read+write bytes)",
-                "kernel": MAIN_KERNEL.get(args.workload, "sfa_run_ex call") + "; CUDA events on its stream"}
-    t_roof = max(counts["gathered_bytes"] / (peaks["hbm_gbs"] * 1e9),
-                 counts["flops"] / (peaks["bf16_tflops"] * 1e12))
-    cfg = config_of(case, world)
+                "algorithmic": "gathered K/V bytes of the selected slots per launch",
+                "kernel": MAIN_KERNEL.get(name, "sfa_run_ex call") + "; CUDA events on its stream"}
+    if prof is not None and prof.get("lts") is not None:
+        roofline["l2_traffic"] = prof["lts"]
+    cfg = sfa_config(case, world)
     rot = reps * counts["gathered_bytes"]
-    cfg["l2"] = (f"not flushed: {reps} rotating input replicas, {rot >> 20} MiB gathered per "
+    cfg["l2"] = (f"not flushed: {reps} rotating input replica(s), {rot >> 20} MiB gathered per "
                  f"rotation {'>' if rot > l2 else '<='} L2 {l2 >> 20} MiB"
                  + ("" if rot > l2 else " (profiling run: not a valid timing)"))
-    res = {"metric": METRIC, "value": whole_job_rate(counts["gathered_bytes"], ms, world) / 1e9,
-           "unit": UNIT, "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": dtype_name(case), "data": "synthetic (seeded generator, shapes of the workload)",
-           "config": cfg,
-           "tflops": world * tflops, "us_per_call": ms * 1e3,
+    cfg["launch"] = mode
+    rec = {"workload": name, "value": whole_job_rate(counts["gathered_bytes"], ms, world) / 1e9,
+           "unit": "GB/s", "ms_per_step": ms, "us_per_call": ms * 1e3, "dtype": case.dtype,
+           "config": cfg, "gathered_gbs": world * gbs, "tflops": world * tflops,
            "tensor_frac": tflops / peaks["bf16_tflops"],
-           "roofline_time_frac": t_roof / (ms * 1e-3),
-           "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-           "clocks": clocks, "wall_s_timed_loop": wall,
+           "roofline_time_frac": max(t_hbm, t_tc) / (ms * 1e-3),
+           "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
            "work": {"flops": counts["flops"], "gathered_bytes": counts["gathered_bytes"],
                     "unmasked_slots": counts["unmasked_slots"]}}
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(case, host, counts)
-    if world > 1:
-        torch.distributed.destroy_process_group()
-    return res
+        rec["cpu_baseline"] = sfa_cpu_baseline(case, host, counts, cpu_target_s)
+    del replicas, out, lse, ws
+    torch.cuda.empty_cache()
+    return rec
 
 
-def cpu_baseline(case, host, counts, target_s=10.0):
+def sfa_cpu_baseline(case, host, counts, target_s=10.0):
     """The oracle as it stands on the host cores, on a bounded sample of the
     workload (whole calls while they fit in ~target_s, else sampled rows
     scaled to a whole call)."""
@@ -467,35 +476,223 @@ def cpu_baseline(case, host, counts, target_s=10.0):
                         case.layout, case.causal)
         sec = (time.perf_counter() - t0) * rows_total / n
         sample = f"{n} of {rows_total} output rows, time scaled to a whole call"
-    return {"value": counts["gathered_bytes"] / sec / 1e9, "unit": UNIT,
+    return {"value": counts["gathered_bytes"] / sec / 1e9, "unit": "GB/s",
             "cores": oracle.threads(), "kind": "oracle", "sample": sample,
             "seconds_per_call": sec}
 
 
-def run_reference(args, rank, world):
+# ---------------------------------------------------------------------------
+# block-sparse workloads
+
+def run_bsr(name, args, world, rank, cpu_target_s):
+    """Block-sparse workloads (tensor-bound): one step = one bsr_run (or
+    varbsr_run) over the whole 16384 x 16384 pattern (plan built once,
+    outside the timed region)."""
+    import sparse_attention_serving_sfa_gb300 as sfa
+    variable = name in synth.VARBSR_WORKLOADS
+    if variable:
+        case = synth.VARBSR_WORKLOADS[name]
+        x = synth.make_varbsr_inputs(case)
+        counts = synth.varbsr_counts(case, x["block_mask_map"], x["block_row_sz"],
+                                     x["block_col_sz"])
+        plan = sfa.varbsr_plan(x["block_mask_map"], x["block_row_sz"], x["block_col_sz"],
+                               case.Hq, case.Hkv, case.d, causal=case.causal,
+                               sm_scale=case.sm_scale, dtype=case.dtype)
+        run = sfa.varbsr_run
+        lse_shape = (case.Hq, case.M)
+        shape_cfg = {"layout": "HND", "MB": case.MB, "NB": case.NB,
+                     "block_sizes": "per kv head, uniform random cut points (mean "
+                                    f"{case.M // case.MB} x {case.N // case.NB})",
+                     "key_tiles": int(plan.int_ws.cpu().view(torch.int32)[case.Hkv * case.MB])}
+    else:
+        case = synth.BSR_WORKLOADS[name]
+        x = synth.make_bsr_inputs(case)
+        counts = synth.bsr_counts(case, x["indptr"], x["indices"], x["mask"])
+        plan = sfa.bsr_plan(x["indptr"], x["indices"], case.M, case.N, case.R, case.C, case.Hq,
+                            case.Hkv, case.d, sm_scale=case.sm_scale, dtype=case.dtype,
+                            causal=case.causal, mask=x["mask"])
+        run = sfa.bsr_run
+        lse_shape = (case.M, case.Hq)
+        shape_cfg = {"layout": "NHD", "R": case.R, "C": case.C, "nnz_blocks": counts["nnz"],
+                     "element_mask_keep": case.mask_keep or None}
+    q, k, v = x["q"].cuda(), x["k"].cuda(), x["v"].cuda()
+    out = torch.empty_like(q)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
+
+    def call(qq):
+        run(plan, qq, k, v, out, lse, torch.cuda.current_stream())
+
+    for _ in range(max(args.warmup, 3)):
+        call(q)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.2)
+    ms, launches, mode = device_time(lambda i: call(q), args.steps, args.eager, world)
+    clocks = sampler.stop()
+
+    e2e = None
+    if not args.no_e2e:
+        # K/V resident (the KV cache); q in from pinned host memory, out and
+        # lse back, every step
+        hq = x["q"].pin_memory()
+        hout = torch.empty_like(hq).pin_memory()
+        hlse = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
+        dq = torch.empty_like(q)
+
+        def step_host(i):
+            dq.copy_(hq, non_blocking=True)
+            call(dq)
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        n_e2e = max(min(args.steps, 20), 5)
+        e_ms = e2e_time(step_host, n_e2e, 2, world)
+        e2e = {"value": whole_job_rate(counts["flops"], e_ms, world) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms, "steps": n_e2e, "h2d_bytes_per_step": nbytes(hq),
+               "d2h_bytes_per_step": nbytes(hout) + nbytes(hlse)}
+
+    peaks, peak_src = load_peaks()
+    tflops = counts["flops"] / (ms * 1e-3) / 1e12
+    prof = committed_profile(name)
+    cfg = {"workload": case.name, "M": case.M, "N": case.N, **shape_cfg, "Hq": case.Hq,
+           "Hkv": case.Hkv, "d": case.d, "p": case.p, "causal": case.causal,
+           "l2": "q, out (268 MiB) stream through; K/V (67 MiB) L2-resident by design",
+           "launch": mode,
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    rec = {"workload": name, "value": whole_job_rate(counts["flops"], ms, world) / 1e12,
+           "unit": "TFLOP/s", "ms_per_step": ms, "us_per_call": ms * 1e3, "dtype": case.dtype,
+           "config": cfg, "tflops": world * tflops,
+           "tensor_frac": tflops / peaks["bf16_tflops"],
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                        "traffic": None if prof is None else prof["dram"],
+                        "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed "
+                                       "alone; the fp16 dense rate is the bf16 rate)",
+                        "algorithmic": "useful FLOPs (4 * d per allowed row, column, qo head)",
+                        "kernel": MAIN_KERNEL[name] + "; CUDA events on its stream"},
+           "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+           "work": {"flops": counts["flops"], "allowed_elements": counts["allowed"]}}
+    if rank == 0 and not args.no_cpu_baseline:
+        rec["cpu_baseline"] = bsr_cpu_baseline(case, x, counts, variable, cpu_target_s)
+    del q, k, v, out, lse, plan
+    torch.cuda.empty_cache()
+    return rec
+
+
+def bsr_cpu_baseline(case, x, counts, variable, target_s):
+    """The oracle on sampled query rows (all heads of each row), time scaled
+    to the whole pattern."""
     import oracle
-    case = synth.SFA_WORKLOADS[args.workload]
-    host = synth.make_sfa_inputs(case)
-    counts = synth.sfa_counts(case, host["idx"])
+    rng = np.random.default_rng(0)
+
+    def run_rows(qrows):
+        # every qo head of each query row
+        heads = np.arange(case.Hq, dtype=np.int64)
+        if variable:
+            flat = (heads[None, :] * case.M + qrows[:, None]).reshape(-1)
+            oracle.varbsr_rows(x["q"], x["k"], x["v"], x["block_mask_map"], x["block_row_sz"],
+                               x["block_col_sz"], case.sm_scale, flat, causal=case.causal)
+        else:
+            pairs = np.stack([np.repeat(qrows, case.Hq), np.tile(heads, len(qrows))], axis=1)
+            oracle.bsr_rows(x["q"], x["k"], x["v"], x["indptr"], x["indices"], case.M, case.N,
+                            case.R, case.C, case.sm_scale, pairs, mask=x["mask"],
+                            causal=case.causal)
+
+    t0 = time.perf_counter()
+    run_rows(np.array([case.M // 2], dtype=np.int64))
+    per_row = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(max(target_s / per_row * max(oracle.threads(), 1) / 2, 16), case.M))
+    rows = np.sort(rng.choice(case.M, size=n, replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    run_rows(rows)
+    sec = (time.perf_counter() - t0) * case.M / n
+    return {"value": counts["flops"] / sec / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle", "sample": f"{n} of {case.M} query rows (all heads), time scaled "
+                                        "to the whole pattern", "seconds_per_call": sec}
+
+
+def run_workload(name, args, world, rank, cpu_target_s):
+    if name in synth.SFA_WORKLOADS:
+        return run_sfa(name, args, world, rank, cpu_target_s)
+    return run_bsr(name, args, world, rank, cpu_target_s)
+
+
+def run_ours(args, rank, world, local):
+    import sparse_attention_serving_sfa_gb300 as sfa
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    sfa.build()
+    sfa.load()
+    # one non-default stream for every call, copy and event (a CUDA graph
+    # cannot be captured on the legacy default stream)
+    torch.cuda.set_stream(torch.cuda.Stream())
+    head = run_workload(args.workload, args, world, rank, cpu_target_s=12.0)
+    subs = {}
+    for name in sub_workloads(args):
+        subs[name] = run_workload(name, args, world, rank, cpu_target_s=4.0)
+    res = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": head["dtype"], "data": "synthetic (seeded generator, shapes of the workload)",
+           "config": head["config"]}
+    for key in ("us_per_call", "gathered_gbs", "tflops", "tensor_frac", "roofline_time_frac",
+                "roofline", "e2e", "gpu_launches", "cpu_baseline", "work"):
+        if key in head:
+            res[key] = head[key]
+    res["gpu_launches"] = head["gpu_launches"]
+    res["clocks"] = merge_clocks([head.get("clocks")] + [r.get("clocks") for r in subs.values()])
+    if subs:
+        for r in subs.values():
+            r.pop("clocks", None)
+        res["workloads"] = subs
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return res
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as it stands on the headline workload's config: each
+    step is one bounded sample of the workload."""
+    import oracle
     oracle.build()
-    cb = cpu_baseline(case, host, counts, target_s=4.0)
-    # steps: each step is one bounded sample of the workload
-    secs = []
+    name = args.workload
+    if name in synth.SFA_WORKLOADS:
+        case = synth.SFA_WORKLOADS[name]
+        host = synth.make_sfa_inputs(case)
+        counts = synth.sfa_counts(case, host["idx"])
+
+        def sample(t):
+            return sfa_cpu_baseline(case, host, counts, target_s=t)
+        unit, units, cfg = "GB/s", counts["gathered_bytes"] / 1e9, sfa_config(case, world)
+    else:
+        variable = name in synth.VARBSR_WORKLOADS
+        case = (synth.VARBSR_WORKLOADS if variable else synth.BSR_WORKLOADS)[name]
+        x = synth.make_varbsr_inputs(case) if variable else synth.make_bsr_inputs(case)
+        counts = (synth.varbsr_counts(case, x["block_mask_map"], x["block_row_sz"],
+                                      x["block_col_sz"]) if variable
+                  else synth.bsr_counts(case, x["indptr"], x["indices"], x["mask"]))
+
+        def sample(t):
+            return bsr_cpu_baseline(case, x, counts, variable, t)
+        unit, units, cfg = "TFLOP/s", counts["flops"] / 1e12, {"workload": name}
+    cb = sample(4.0)
     for _ in range(max(args.warmup, 0)):
-        cpu_baseline(case, host, counts, target_s=1.0)
-    n_steps = min(args.steps, 5)
-    for _ in range(n_steps):
-        secs.append(cpu_baseline(case, host, counts, target_s=2.0)["seconds_per_call"])
+        sample(1.0)
+    n_steps = max(min(args.steps, 5), 1)
+    secs = [sample(3.0)["seconds_per_call"] for _ in range(n_steps)]
     sec = float(np.mean(secs))
-    val = counts["gathered_bytes"] / sec / 1e9
-    return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+    val = units / sec
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": unit, "n_gpus": world,
             "steps": n_steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded generator, shapes of the workload)",
-            "config": config_of(case, world),
-            "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.threads(),
+            "config": cfg,
+            "cpu_baseline": {"value": val, "unit": unit, "cores": oracle.threads(),
                              "kind": "oracle", "sample": cb["sample"]},
-            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
@@ -514,10 +711,7 @@ def main():
             return 0
         print(json.dumps(run_reference(args, rank, world)))
         return 0
-    if args.workload in synth.BSR_WORKLOADS or args.workload in synth.VARBSR_WORKLOADS:
-        res = run_bsr(args, rank, world, local)
-    else:
-        res = run_ours(args, rank, world, local)
+    res = run_ours(args, rank, world, local)
     if rank == 0:
         print(json.dumps(res))
     return 0
