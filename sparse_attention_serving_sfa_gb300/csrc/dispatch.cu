@@ -50,6 +50,11 @@ Plan choose_plan(const SfaParams& p, sfa_dtype, int num_sms, int forced_splits) 
         pl.extra_ws_bytes = decode_ws_bytes(p);
         return pl;
     }
+    return generic_split_plan(p, num_sms, forced_splits);
+}
+
+Plan generic_split_plan(const SfaParams& p, int num_sms, int forced_splits) {
+    Plan pl;
     pl.kind = PATH_GENERIC;
     const int hb = p.G > 4 ? 8 : 4;
     const int64_t ctas = (int64_t)p.B * p.N2 * p.S1 * ceil_div(p.G, hb);

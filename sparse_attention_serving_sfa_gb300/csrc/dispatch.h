@@ -32,4 +32,9 @@ size_t plan_extra_ws_bytes(int B, int S1, int N1, int N2, int Dk, int Dv, int to
 // Largest split count any plan uses for this topK.
 int max_splits_for(int topK);
 
+// Split plan of the generic warp-FMA kernel for `p` (sizes filled): about two
+// CTAs per SM, at most max_splits_for(topK) splits of whole 32-slot chunks,
+// unless `forced_splits` > 0.  kind = PATH_GENERIC.
+Plan generic_split_plan(const SfaParams& p, int num_sms, int forced_splits);
+
 }  // namespace sfa

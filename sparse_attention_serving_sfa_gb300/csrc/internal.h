@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "sfa.h"
 
 namespace sfa {
@@ -109,6 +111,9 @@ struct BsrParams {
     int causal;
     // plan()'s logits_soft_cap times log2(e); 0 = no cap
     float softcap_log2;
+    // 1: k and v are (Hkv, N, d) (HND) instead of (N, Hkv, d) (NHD); modes
+    // 0-2 only (mode 3 is HND throughout)
+    int kv_hnd;
 };
 
 cudaError_t launch_bsr_generic(const BsrParams& p, sfa_dtype dtype, cudaStream_t stream);
@@ -157,5 +162,20 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // Device address of the library's error word on the current device.
 int* device_error_word();
+
+// Id of the calling thread's current CUDA context (0 if none).
+unsigned long long current_context_id();
+
+// Device addresses of one __device__ symbol, looked up once per device and
+// again whenever that device's current context differs from the one of the
+// lookup (after a device reset the module is loaded anew).  address() takes
+// the symbol's host-side stand-in (&symbol) and returns nullptr on failure.
+constexpr int kMaxDevices = 64;
+struct SymbolCache {
+    std::mutex mu;
+    void* ptr[kMaxDevices] = {};
+    unsigned long long ctx[kMaxDevices] = {};
+    void* address(const void* symbol);
+};
 
 }  // namespace sfa

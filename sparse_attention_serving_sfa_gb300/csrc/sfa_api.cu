@@ -3,7 +3,10 @@
 #include <math.h>
 
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <thread>
+#include <tuple>
 
 #include "common.cuh"
 #include "dispatch.h"
@@ -19,65 +22,90 @@ __device__ int g_error_word = 0;
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+unsigned long long current_context_id() {
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (cuCtxGetCurrent(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (cuCtxGetId(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+void* SymbolCache::address(const void* symbol) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    const unsigned long long id = current_context_id();
+    if (!ptr[dev] || id == 0 || ctx[dev] != id) {
+        // first use on this device, or a context made after a device reset:
+        // the lookup also creates the device's primary context if needed
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) return nullptr;
+        ptr[dev] = p;
+        ctx[dev] = current_context_id();
+    }
+    return ptr[dev];
+}
+
 namespace {
 
-// Device address of g_error_word on the current device (looked up once).
-int* error_word_ptr() {
-    static std::mutex mu;
-    static void* cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cached[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
-        cached[dev] = ptr;
-    }
-    return static_cast<int*>(cached[dev]);
-}
+SymbolCache g_error_word_cache;
 
 }  // namespace
 
-int* device_error_word() { return error_word_ptr(); }
+int* device_error_word() {
+    return static_cast<int*>(g_error_word_cache.address(reinterpret_cast<const void*>(&g_error_word)));
+}
 
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Library-owned split workspace, one per device, grown on demand.
-struct OwnedWorkspace {
-    std::mutex mu;
-    void* ptr[64] = {};
-    size_t bytes[64] = {};
+// Library-owned workspaces, one per (device, stream): calls on one stream run
+// in stream order, calls on different streams never share one.  The
+// per-thread default stream handle names a different stream in each host
+// thread, so it is also keyed by the calling thread.
+struct OwnedBuffer {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+    unsigned long long ctx = 0;   // context the buffer was allocated in
 };
-OwnedWorkspace g_ws;
+std::mutex g_ws_mu;
+std::map<std::tuple<int, cudaStream_t, std::thread::id>, OwnedBuffer> g_ws;
 
-cudaError_t owned_workspace(size_t need, void** out) {
+cudaError_t owned_workspace(size_t need, cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_ws.mu);
-    if (g_ws.bytes[dev] < need) {
-        if (g_ws.ptr[dev]) {
-            err = cudaDeviceSynchronize();   // the old buffer may still be in use
+    const std::thread::id who =
+        stream == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id();
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    OwnedBuffer& b = g_ws[std::make_tuple(dev, stream, who)];
+    const unsigned long long id = current_context_id();
+    if (b.ptr && id != 0 && b.ctx != id) {
+        // allocated in a context that no longer exists (device reset): the
+        // memory went with it
+        b = OwnedBuffer{};
+    }
+    if (b.bytes < need) {
+        if (b.ptr) {
+            err = cudaStreamSynchronize(stream);   // the old buffer may still be in use
             if (err != cudaSuccess) return err;
-            cudaFree(g_ws.ptr[dev]);
-            g_ws.ptr[dev] = nullptr;
-            g_ws.bytes[dev] = 0;
+            cudaFree(b.ptr);
+            b = OwnedBuffer{};
         }
         size_t sz = need < (size_t(1) << 20) ? (size_t(1) << 20) : need;
-        err = cudaMalloc(&g_ws.ptr[dev], sz);
+        err = cudaMalloc(&b.ptr, sz);
         if (err != cudaSuccess) {
-            g_ws.ptr[dev] = nullptr;
+            b = OwnedBuffer{};
             return err;
         }
         // the counter region must start at zero (kernels leave it zero)
-        err = cudaMemset(g_ws.ptr[dev], 0, sz);
+        err = cudaMemset(b.ptr, 0, sz);
         if (err != cudaSuccess) return err;
-        g_ws.bytes[dev] = sz;
+        b.bytes = sz;
+        b.ctx = current_context_id();
     }
-    *out = g_ws.ptr[dev];
+    *out = b.ptr;
     return cudaSuccess;
 }
 
@@ -197,7 +225,7 @@ sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t
     p.validate = (opt && opt->validate_indices) ? 1 : 0;
     p.ctas_per_sm = opt ? opt->ctas_per_sm : 0;
     p.num_ctas = opt ? opt->num_ctas : 0;
-    p.err_word = error_word_ptr();     // index checks (if validating) and wait timeouts
+    p.err_word = device_error_word();  // index checks (if validating) and wait timeouts
     if (!p.err_word) return SFA_ERR_CUDA;
     p.scale_log2 = scale * kLog2e;
     resolve_strides(p, (int)layout, prefix);
@@ -218,7 +246,7 @@ sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t
             if (opt->workspace_bytes < need) return SFA_ERR_WORKSPACE;
             ws = opt->workspace;
         } else {
-            if (owned_workspace(need, &ws) != cudaSuccess) return SFA_ERR_CUDA;
+            if (owned_workspace(need, s, &ws) != cudaSuccess) return SFA_ERR_CUDA;
         }
         p.counters = static_cast<unsigned*>(ws);
     }

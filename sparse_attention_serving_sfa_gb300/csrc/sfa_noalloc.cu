@@ -3,8 +3,6 @@
 // cannot allocate device memory (see include/sfa.h).
 #include <math.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "dispatch.h"
 #include "internal.h"
@@ -13,28 +11,11 @@ namespace sfa {
 namespace {
 
 // The scratch array.  In host code this name is only a host-side stand-in;
-// its device address comes from cudaGetSymbolAddress, once per device.
+// its device address comes from cudaGetSymbolAddress (SymbolCache), with the
+// device current, once per device and context.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SFA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-constexpr int kChunk = 32;      // slot granule of the generic kernel's splits
-
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the array on the current device (looked up on first use,
-// with that device current).  nullptr on failure.
-void* scratch_for_current_device() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
-        g_scratch_ptr[dev] = ptr;
-    }
-    return g_scratch_ptr[dev];
-}
+SymbolCache g_scratch_cache;
 
 }  // namespace
 }  // namespace sfa
@@ -49,11 +30,12 @@ extern "C" sfa_status sfa_run_noalloc(const void* q, const void* k, const void* 
     sfa_status st = check_args(q, k, v, sparse_idx, B, S1, S2, N1, N2, Dk, Dv, topK, scale,
                                (int)layout, causal, (int)dtype, out, lse, nullptr);
     if (st != SFA_OK) return st;
-    size_t bound = 0;
-    st = sfa_workspace_size(B, S1, N1, N2, Dk, Dv, topK, 0, &bound);
-    if (st != SFA_OK) return st;
-    if (bound > SFA_NOALLOC_SCRATCH_BYTES) return SFA_ERR_WORKSPACE;
-    void* scratch = scratch_for_current_device();
+    // the largest split count this entry point can choose must fit the array
+    // (the same bound on every device, whatever its SM count)
+    if (sfa_split_ws_bytes((int64_t)B * S1 * N1, max_splits_for(topK), Dv) >
+        SFA_NOALLOC_SCRATCH_BYTES)
+        return SFA_ERR_WORKSPACE;
+    void* scratch = g_scratch_cache.address(reinterpret_cast<const void*>(&g_noalloc_scratch));
     if (!scratch) return SFA_ERR_CUDA;
 
     SfaParams p{};
@@ -64,20 +46,11 @@ extern "C" sfa_status sfa_run_noalloc(const void* q, const void* k, const void* 
     p.scale_log2 = scale * kLog2e;
     resolve_strides(p, (int)layout, v == k);
 
-    // Split count of the generic kernel: about two CTAs per SM, at most
-    // max_splits_for(topK) (the count sfa_workspace_size bounds).
-    const int hb = p.G > 4 ? 8 : 4;
-    const int64_t ctas = (int64_t)B * N2 * S1 * ((p.G + hb - 1) / hb);
-    int want = (int)((2LL * num_sms() + ctas - 1) / ctas);
-    if (want > max_splits_for(topK)) want = max_splits_for(topK);
-    if (want < 1) want = 1;
-    int per = (topK + want - 1) / want;
-    per = ((per + kChunk - 1) / kChunk) * kChunk;
-    p.slots_per_split = per;
-    p.splits = (topK + per - 1) / per;
+    // the generic kernel's own split plan (the one sfa_run_ex uses for it)
+    const Plan plan = generic_split_plan(p, num_sms(), 0);
+    p.splits = plan.splits;
+    p.slots_per_split = plan.slots_per_split;
     if (p.splits > 1) {
-        if (sfa_split_ws_bytes((int64_t)B * S1 * N1, p.splits, Dv) > SFA_NOALLOC_SCRATCH_BYTES)
-            return SFA_ERR_WORKSPACE;
         p.ws_o = static_cast<float*>(scratch);
         p.ws_ml = p.ws_o + (int64_t)B * S1 * N1 * p.splits * Dv;
     }

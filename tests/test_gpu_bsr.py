@@ -98,7 +98,15 @@ def test_full_workload_sampled():
                        case.C, case.sm_scale, case.dtype)
     rng = np.random.default_rng(1)
     rows = np.stack([rng.integers(0, case.M, 48), rng.integers(0, case.Hq, 48)], axis=1)
-    rows = np.concatenate([rows, [[0, 0], [case.M - 1, case.Hq - 1]]])
+    # the edges of every work item (one row block x one kv head, two M-tiles
+    # of 128 / G rows): rows 0, TR - 1, TR and R - 1 of each row block, the
+    # qo head rotating over the heads from block to block
+    tr = 128 // (case.Hq // case.Hkv)
+    edge = [[rb * case.R + off, (7 * rb + j) % case.Hq]
+            for rb in range(case.MB) for j, off in enumerate((0, tr - 1, tr, case.R - 1))
+            if rb * case.R + off < case.M]
+    rows = np.concatenate([rows, edge, [[0, 0], [case.M - 1, case.Hq - 1]]])
+    assert len(rows) > 1000
     y, l = oracle.bsr_rows(x["q"], x["k"], x["v"], x["indptr"], x["indices"], case.M, case.N,
                            case.R, case.C, case.sm_scale, rows)
     got = torch.stack([out[i, h] for i, h in rows])

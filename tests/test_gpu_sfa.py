@@ -181,23 +181,56 @@ def test_stream_argument():
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled rows
 
-@pytest.mark.parametrize("name", ["gqa_decode", "mla_decode", "mla_mtp", "sparse_prefill",
-                                  "call_example"])
-def test_full_workload_sampled(name):
+@pytest.mark.parametrize("name", ["gqa_decode", "mla_decode", "mla_mtp", "call_example"])
+def test_full_workload_every_row(name):
+    """The full-size workloads whose oracle finishes in seconds: every output
+    row compared element by element (so every stream-K range boundary, split
+    index list and cluster of the launch bench.py times is covered)."""
     case = synth.SFA_WORKLOADS[name]
     d = synth.make_sfa_inputs(case)
     dev = T.to_dev(d)
     out, lse = T.run_gpu(case, dev)
-    rows = T.sample_rows(case, 96 if name != "sparse_prefill" else 64)
-    if name == "sparse_prefill":
-        # include fully masked rows (b = 0, s1 < 8) and the last rows
-        extra = np.array([[0, n1, s1] for n1 in (0, 63) for s1 in (0, 7, 8)] +
-                         [[1, 5, 2047], [1, 63, 2046]])
-        rows = np.unique(np.concatenate([rows, extra]), axis=0)
+    T.check_full(case, d, out, lse)
+    assert torch.isfinite(out.float()).all()
+
+
+def aligned_range_boundary_rows(case, ctas_options):
+    """(b, n1, s1) rows of the first and last index list of every CTA's range
+    when whole index lists are dealt out in equal contiguous ranges to `ctas`
+    CTAs (list u = (b * N2 + n2) * S1 + s1), for each grid size given; the
+    first and last query head of each such list."""
+    units = case.B * case.N2 * case.S1
+    lists = set()
+    for ctas in ctas_options:
+        for c in range(ctas):
+            lo, hi = c * units // ctas, (c + 1) * units // ctas - 1
+            if hi >= lo:
+                lists.update((lo, hi))
+    rows = []
+    for u in sorted(lists):
+        s1, n2, b = u % case.S1, (u // case.S1) % case.N2, u // (case.S1 * case.N2)
+        rows += [[b, n2 * case.G, s1], [b, n2 * case.G + case.G - 1, s1]]
+    return np.array(rows, dtype=np.int64)
+
+
+def test_full_workload_sampled_prefill():
+    """Sparse prefill (the oracle needs ~1.7 ms per row): random rows, the
+    fully masked rows (b = 0, s1 < 8), the last rows, and the first and last
+    index list of every persistent CTA's range for one and two CTAs per SM."""
+    case = synth.PREFILL
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    out, lse = T.run_gpu(case, dev)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = T.sample_rows(case, 64)
+    extra = np.array([[0, n1, s1] for n1 in (0, 63) for s1 in (0, 7, 8)] +
+                     [[1, 5, 2047], [1, 63, 2046]])
+    rows = np.unique(np.concatenate([rows, extra,
+                                     aligned_range_boundary_rows(case, (sms, 2 * sms))]), axis=0)
+    assert len(rows) > 500
     T.check_rows(case, d, out, lse, rows)
     assert torch.isfinite(out.float()).all()
-    if name == "sparse_prefill":
-        assert torch.all(out[0, :8] == 0)
+    assert torch.all(out[0, :8] == 0)
 
 
 # ---------------------------------------------------------------------------

@@ -177,7 +177,24 @@ def test_full_workload_sampled():
     x = synth.make_varbsr_inputs(c)
     out, lse = run_varbsr(x, c.Hq, c.Hkv, c.d, c.sm_scale, c.dtype, c.causal)
     rng = np.random.default_rng(3)
-    rows = np.concatenate([rng.integers(0, c.Hq * c.M, 64), [0, c.Hq * c.M - 1]])
+    # the edges of the work items: items take 2 * 128 / G rows of one
+    # (kv head, row block) in two M-tiles; rows at offsets 0, 31, 32, 63, 64
+    # and the last row of every row block of kv heads 0 and Hkv - 1, and the
+    # first and last row of every row block of the others (one qo head each)
+    G = c.Hq // c.Hkv
+    tr = 128 // G
+    edge = []
+    for g in range(c.Hkv):
+        starts = np.concatenate([[0], np.cumsum(x["block_row_sz"][g])[:-1]])
+        for rb, (r0, sz) in enumerate(zip(starts, x["block_row_sz"][g])):
+            if sz == 0:
+                continue
+            offs = ((0, tr - 1, tr, 2 * tr - 1, 2 * tr, sz - 1) if g in (0, c.Hkv - 1)
+                    else (0, sz - 1))
+            h = g * G + rb % G
+            edge += [h * c.M + r0 + o for o in set(offs) if o < sz]
+    rows = np.concatenate([rng.integers(0, c.Hq * c.M, 64), edge, [0, c.Hq * c.M - 1]])
+    assert len(rows) > 2000
     y, l = oracle.varbsr_rows(x["q"], x["k"], x["v"], x["block_mask_map"], x["block_row_sz"],
                               x["block_col_sz"], c.sm_scale, rows, causal=c.causal)
     got = out.reshape(-1, c.d)[rows]

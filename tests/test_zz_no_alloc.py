@@ -3,9 +3,10 @@ memory (for example a serving engine that reserved nearly all HBM for its KV
 cache up front, or a plugin host that forbids libraries from allocating).  It
 keeps its split partials in a fixed device array inside the library instead
 of an allocated workspace.  These tests call it through the C ABI and check
-its output against sfa_run's on the same inputs, on consecutive calls (the
-array keeps the previous call's contents), and that a shape needing more
-scratch than the array holds is rejected.
+its output against sfa_run's and against the CPU oracle on the same inputs,
+on consecutive calls of shapes whose partials differ (the array keeps the
+previous call's contents), and that a shape needing more scratch than the
+array holds is rejected.
 
 This file is named so that pytest collects it last."""
 import numpy as np
@@ -50,38 +51,65 @@ def same_within_tolerance(case, out_a, lse_a, out_b, lse_b):
     np.testing.assert_allclose(la[fin], lb[fin], atol=T.LSE_ATOL, rtol=T.LSE_RTOL)
 
 
+def generic_splits(case, num_sms):
+    """Split count of the generic kernel's plan as the header documents it:
+    about two CTAs per SM (one CTA per 4 query heads, or per 8 when the group
+    is larger than 4), at most min(ceil(topK / 64), 32) splits of whole
+    32-slot chunks."""
+    hb = 8 if case.G > 4 else 4
+    ctas = case.B * case.N2 * case.S1 * (-(-case.G // hb))
+    want = min(-(-2 * num_sms // ctas), min(-(-case.topK // 64), 32))
+    per = -(-case.topK // max(want, 1))
+    per = -(-per // 32) * 32
+    return -(-case.topK // per)
+
+
+# Three shapes, each with splits > 1, called in turn: every call finds the
+# previous shape's partials (other rows, Dv or values) in the array, so a
+# partial the kernel failed to write would show up as a mismatch.
 CASES = [
-    synth.GQA_DECODE,       # splits > 1: partials go through the scratch array
-    synth.SfaCase("noalloc_causal", B=2, S1=16, S2=64, N1=8, N2=2, Dk=192, Dv=128, topK=40,
-                  dtype="f16", layout="BSND", causal=True, scale=0.07,
-                  value_is_key_prefix=True, index_kind="causal_mix", masked_frac=0.1,
-                  full_masked_rows=4, seed=99),
+    synth.GQA_DECODE,
+    synth.SfaCase("noalloc_small_dv", B=1, S1=2, S2=900, N1=4, N2=2, Dk=128, Dv=64, topK=512,
+                  dtype="f16", layout="BSND", causal=True, scale=0.09,
+                  index_kind="causal_mix", masked_frac=0.1, full_masked_rows=1, seed=99),
+    synth.GQA_DECODE.replace(name="gqa_decode_other_values", seed=777),
 ]
 
 
-def test_noalloc_matches_sfa_run_on_consecutive_calls():
+def test_cases_use_the_scratch_array():
+    num_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for case in CASES:
+        assert generic_splits(case, num_sms) > 1, case.name
+    rows = {(c.B * c.S1 * c.N1, c.Dv) for c in CASES[:2]}
+    assert len(rows) == 2
+
+
+def test_noalloc_matches_sfa_run_and_the_oracle_on_consecutive_calls():
     prepared = []
     for case in CASES:
-        dev = T.to_dev(synth.make_sfa_inputs(case))
+        host = synth.make_sfa_inputs(case)
+        dev = T.to_dev(host)
         ref_out, ref_lse = outputs(case, dev)
         assert call(sfa.sfa_run, case, dev, ref_out, ref_lse) == sfa.SFA_OK
-        prepared.append((case, dev, ref_out, ref_lse))
+        prepared.append((case, host, dev, ref_out, ref_lse))
     torch.cuda.synchronize()
-    # two calls in a row per case, alternating cases so the array always holds
-    # the other shape's partials when a call starts
-    for _ in range(2):
-        for case, dev, ref_out, ref_lse in prepared:
+    # two rounds over the three shapes: two calls in a row of each entry
+    for rnd in range(2):
+        for case, host, dev, ref_out, ref_lse in prepared:
             out, lse = outputs(case, dev)
             out.fill_(7.0)
             lse.fill_(7.0)
             assert call(sfa.sfa_run_noalloc, case, dev, out, lse) == sfa.SFA_OK
             torch.cuda.synchronize()
             same_within_tolerance(case, out, lse, ref_out, ref_lse)
+            if rnd == 0:
+                T.check_full(case, host, out, lse)
 
 
 def test_noalloc_rejects_shapes_beyond_the_array():
     case = synth.MLA_DECODE.replace(B=4)
-    need = sfa.sfa_workspace_size(case.B, case.S1, case.N1, case.N2, case.Dk, case.Dv, case.topK)
+    rows = case.B * case.S1 * case.N1
+    need = rows * min(-(-case.topK // 64), 32) * (case.Dv + 2) * 4
     assert need > sfa.SFA_NOALLOC_SCRATCH_BYTES
     dev = T.to_dev(synth.make_sfa_inputs(case))
     out, lse = outputs(case, dev)
