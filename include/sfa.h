@@ -77,15 +77,19 @@ typedef enum { SFA_DTYPE_F16 = 0, SFA_DTYPE_BF16 = 1 } sfa_dtype;
  *   sparse_idx    device int32 in [0, S2).  Out-of-range positions are never
  *                 dereferenced: their slot is treated as masked.
  *   B,S1,S2,N1,N2 sizes; N1 % N2 == 0; causal requires S1 <= S2.
- *   Dk, Dv        multiples of 64, Dv <= Dk; this build: Dk <= 1024, Dv <= 512.
+ *   Dk, Dv        multiples of 64, Dv <= Dk; this build: Dk <= 576, Dv <= 512.
  *   topK          1 <= topK <= S2.
  *   scale         softmax scale (usually 1/sqrt(Dk)); any finite value.
  *   out           device, dtype, layout above.
  *   lse           device float32 or NULL.
  *   stream        CUDA stream for every launch of the call.
- * Workspace: a library-owned device workspace is allocated (and grown) on
- * first use per device; the growing call synchronises the device once.  Use
- * sfa_run_ex to pass your own.
+ * Workspace: a library-owned device workspace is allocated on first use for
+ * each (device, stream) pair and grown when a larger shape needs it (the
+ * growing call synchronises that stream once).  Calls on different streams
+ * therefore never share a workspace and may overlap on the GPU; calls on one
+ * stream share it and run in stream order.  The per-thread default stream
+ * (cudaStreamPerThread) gets one workspace per host thread.  Each workspace
+ * is held until the process exits.  Use sfa_run_ex to pass your own.
  * Errors: SFA_ERR_INVALID_ARG / SFA_ERR_UNSUPPORTED before any launch;
  * SFA_ERR_CUDA if a launch fails.
  */
@@ -168,12 +172,16 @@ uint64_t sfa_kernel_launches(void);
  *
  * Arguments, layouts and results are those of sfa_run (value-prefix mode is
  * inferred from v == k; no index validation).
- * Limits: a shape whose sfa_workspace_size(..., num_splits = 0) exceeds
- * SFA_NOALLOC_SCRATCH_BYTES is rejected with SFA_ERR_WORKSPACE before
- * anything is launched; other argument errors as in sfa_run.
+ * Limits: the split partials of the largest split count the generic kernel
+ * can choose for topK -- rows = B * S1 * N1 rows of (Dv + 2) floats times
+ * min(ceil(topK / 64), 32) splits -- must fit SFA_NOALLOC_SCRATCH_BYTES;
+ * larger shapes are rejected with SFA_ERR_WORKSPACE before anything is
+ * launched (the same rule on every GPU, whatever its SM count).  Other
+ * argument errors as in sfa_run.
  * Set-up: the first call on each device looks up the device address of the
- * array (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.
+ * array (cudaGetSymbolAddress) with that device current, and looks it up
+ * again after the device's context has been re-created (cudaDeviceReset);
+ * make the first call on a device before any stream capture.
  * Sharing: all calls on a device share the one array and it keeps the last
  * call's contents.  Nothing in it needs clearing (every split partial is
  * written before it is read), but calls whose kernels overlap on the GPU --
@@ -264,10 +272,25 @@ sfa_status bsr_plan_masked_int_workspace_size(const int32_t* indptr_host, int M,
                                               int C, int num_qo_heads, int num_kv_heads,
                                               int head_dim, int with_mask, size_t* bytes);
 
+/* Layout of the k / v tensors of bsr_run ("flashinfer.prefill.
+ * single_prefill_with_kv_cache", parameter kv_layout: NHD or HND). */
+typedef enum { SFA_KV_LAYOUT_NHD = 0, SFA_KV_LAYOUT_HND = 1 } sfa_kv_layout;
+
+/*
+ * bsr_plan_set_kv_layout -- the layout of the k and v tensors of every later
+ * bsr_run with this plan: SFA_KV_LAYOUT_NHD (N, num_kv_heads, head_dim), the
+ * default, or SFA_KV_LAYOUT_HND (num_kv_heads, N, head_dim), as the
+ * single-request prefill page's kv_layout defines them.  q and out stay
+ * (M, num_qo_heads, head_dim).  Host only.
+ * Errors: SFA_ERR_INVALID_ARG (NULL plan, another value).
+ */
+sfa_status bsr_plan_set_kv_layout(bsr_plan_t plan, sfa_kv_layout kv_layout);
+
 /*
  * bsr_run -- block-sparse attention with a plan.
  *   q    device (M, num_qo_heads, head_dim), NHD, dtype.
- *   k, v device (N, num_kv_heads, head_dim), NHD, dtype.
+ *   k, v device (N, num_kv_heads, head_dim), NHD, dtype, or
+ *        (num_kv_heads, N, head_dim) after bsr_plan_set_kv_layout(HND).
  *   out  device (M, num_qo_heads, head_dim), dtype.
  *   lse  device float32 (M, num_qo_heads) or NULL: natural-log log-sum-exp
  *        of the scaled logits of the row's allowed columns.

@@ -25,6 +25,7 @@ SFA_ERR_CUDA = 5
 SFA_ERR_DEVICE_TIMEOUT = 6
 
 LAYOUTS = {"BSND": 0, "BNSD": 1}
+KV_LAYOUTS = {"NHD": 0, "HND": 1}
 DTYPES = {"f16": 0, "bf16": 1}
 
 # Every entry point of include/sfa.h.
@@ -33,7 +34,7 @@ EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
            "bsr_plan_destroy", "bsr_plan_masked", "bsr_plan_masked_int_workspace_size",
            "varbsr_plan", "varbsr_plan_int_workspace_size", "varbsr_plan_dims", "varbsr_run",
            "varbsr_plan_destroy", "bsr_plan_set_logits_soft_cap",
-           "varbsr_plan_set_logits_soft_cap")
+           "varbsr_plan_set_logits_soft_cap", "bsr_plan_set_kv_layout")
 
 
 class SfaError(RuntimeError):
@@ -111,6 +112,8 @@ def load():
             lib.bsr_plan_set_logits_soft_cap.restype = ci
             lib.varbsr_plan_set_logits_soft_cap.argtypes = [vp, cf]
             lib.varbsr_plan_set_logits_soft_cap.restype = ci
+            lib.bsr_plan_set_kv_layout.argtypes = [vp, ci]
+            lib.bsr_plan_set_kv_layout.restype = ci
             _lib = lib
     return _lib
 
@@ -252,11 +255,13 @@ def pack_block_mask(mask):
 
 def bsr_plan(indptr_host, indices_host, M, N, R, C, num_qo_heads, num_kv_heads, head_dim,
              causal=False, sm_scale=0.0, dtype="f16", int_ws=None, float_ws=None,
-             stream=None, mask=None, packed_mask=None, logits_soft_cap=0.0) -> BsrPlan:
+             stream=None, mask=None, packed_mask=None, logits_soft_cap=0.0,
+             kv_layout="NHD") -> BsrPlan:
     """Forwards to bsr_plan(), or to bsr_plan_masked() when a per-element
     mask ((nnz, R, C) bool) or its packed bytes are given, then to
-    bsr_plan_set_logits_soft_cap() when logits_soft_cap > 0.  indptr/indices
-    are host int32 tensors; int_ws a device uint8 tensor (allocated here with
+    bsr_plan_set_logits_soft_cap() when logits_soft_cap > 0 and to
+    bsr_plan_set_kv_layout() when kv_layout is not NHD.  indptr/indices are
+    host int32 tensors; int_ws a device uint8 tensor (allocated here with
     torch if None)."""
     import numpy as np
     import torch
@@ -282,7 +287,15 @@ def bsr_plan(indptr_host, indices_host, M, N, R, C, num_qo_heads, num_kv_heads, 
     plan = BsrPlan(handle.value, int_ws, M, N, num_qo_heads, head_dim)
     if logits_soft_cap > 0:
         bsr_plan_set_logits_soft_cap(plan, logits_soft_cap)
+    if _enum(kv_layout, KV_LAYOUTS) != 0:
+        bsr_plan_set_kv_layout(plan, kv_layout)
     return plan
+
+
+def bsr_plan_set_kv_layout(plan: BsrPlan, kv_layout):
+    """k / v layout of later bsr_run calls: "NHD" (N, Hkv, d) or "HND" (Hkv, N, d)."""
+    _check(load().bsr_plan_set_kv_layout(plan.handle, _enum(kv_layout, KV_LAYOUTS)),
+           "bsr_plan_set_kv_layout")
 
 
 def bsr_plan_set_logits_soft_cap(plan: BsrPlan, logits_soft_cap: float):

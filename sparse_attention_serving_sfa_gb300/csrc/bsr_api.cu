@@ -23,6 +23,7 @@ struct bsr_plan_s {
     bool tc;                        // tensor-core path (work items) vs generic (row tiles)
     int mask_mode;                  // 0 none, 1 causal, 2 per-element bits
     float softcap_log2 = 0.f;       // logits_soft_cap * log2(e); 0 = none
+    int kv_layout = SFA_KV_LAYOUT_NHD;
     const int32_t* d_indptr;
     const int32_t* d_indices;
     const void* d_work;             // BsrTile list (generic) or 4-int items (tensor cores)
@@ -248,6 +249,7 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
     p.mask_mode = plan->mask_mode;
     p.mask = plan->d_mask;
     p.softcap_log2 = plan->softcap_log2;
+    p.kv_hnd = plan->kv_layout == SFA_KV_LAYOUT_HND ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
     if (plan->tc) {
@@ -266,6 +268,13 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
 sfa_status bsr_plan_set_logits_soft_cap(bsr_plan_t plan, float logits_soft_cap) {
     if (!plan || !isfinite(logits_soft_cap)) return SFA_ERR_INVALID_ARG;
     plan->softcap_log2 = logits_soft_cap > 0.f ? logits_soft_cap * sfa::kLog2e : 0.f;
+    return SFA_OK;
+}
+
+sfa_status bsr_plan_set_kv_layout(bsr_plan_t plan, sfa_kv_layout kv_layout) {
+    if (!plan || (kv_layout != SFA_KV_LAYOUT_NHD && kv_layout != SFA_KV_LAYOUT_HND))
+        return SFA_ERR_INVALID_ARG;
+    plan->kv_layout = kv_layout;
     return SFA_OK;
 }
 

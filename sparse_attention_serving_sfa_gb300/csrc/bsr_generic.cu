@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(kThreads) bsr_generic_kernel(const BsrParams p
             int col = cols[j];
             uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
             if (col >= 0) {
-                const int64_t off = ((int64_t)col * p.Hkv + kvh) * D + piece * 8;
+                const int64_t off = (p.kv_hnd ? (int64_t)kvh * p.N + col
+                                              : (int64_t)col * p.Hkv + kvh) * D + piece * 8;
                 kv = *reinterpret_cast<const uint4*>(kg + off);
                 vv = *reinterpret_cast<const uint4*>(vg + off);
             }

@@ -95,6 +95,7 @@ struct BsrTcParams {
     float scale_log2;
     const uint8_t* mask;    // per-element bits, most significant first
     float capl2, inv_capl2; // logits soft cap in log2 units (CAP instantiations)
+    int kv_hnd;             // K / V maps over (Hkv, N, d)
 };
 
 // The 64-bit word whose bit j is element j of the 64 mask elements held,
@@ -166,9 +167,11 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 const int col = p.indices[blk0 + b / sub] * p.C + (b % sub) * kKeys;
                 const uint32_t dst = sbase + L::kv + s * 2 * L::kvTile;
                 mbar_arrive_expect_tx(bar(B_KV_FULL + s), 2 * L::kvTile);
+                // NHD maps take (dim, kv head, key), HND maps (dim, key, kv head)
+                const int y = p.kv_hnd ? col : item.kvh, z = p.kv_hnd ? item.kvh : col;
                 for (int pn = 0; pn < L::panels; ++pn) {
-                    tma_load_3d(dst + pn * (kKeys * 128), &mk, pn * 64, item.kvh, col, bar(B_KV_FULL + s));
-                    tma_load_3d(dst + L::kvTile + pn * (kKeys * 128), &mv, pn * 64, item.kvh, col,
+                    tma_load_3d(dst + pn * (kKeys * 128), &mk, pn * 64, y, z, bar(B_KV_FULL + s));
+                    tma_load_3d(dst + L::kvTile + pn * (kKeys * 128), &mv, pn * 64, y, z,
                                 bar(B_KV_FULL + s));
                 }
             };
@@ -460,9 +463,12 @@ cudaError_t launch_tc_t(const BsrParams& bp, const BsrTcParams& tp, int nitems, 
     using L = TcSmem<D>;
     const bool bf16 = std::is_same<E, BF16>::value;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, tp.G, tp.TR) ||
-        !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kKeys) ||
-        !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kKeys))
+    if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, tp.G, tp.TR))
+        return cudaErrorInvalidValue;
+    if (bp.kv_hnd ? (!make_map_hnd(&mk, bp.k, bf16, D, bp.N, bp.Hkv, kKeys, 1) ||
+                     !make_map_hnd(&mv, bp.v, bf16, D, bp.N, bp.Hkv, kKeys, 1))
+                  : (!make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kKeys) ||
+                     !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kKeys)))
         return cudaErrorInvalidValue;
     auto kern = bsr_tc_kernel<E, D, CAP>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
@@ -500,6 +506,7 @@ cudaError_t launch_bsr_tc(const BsrParams& bp, const void* items, int nitems, in
     tp.C = bp.C;
     tp.Hq = bp.Hq;
     tp.G = bp.Hq / bp.Hkv;
+    tp.kv_hnd = bp.kv_hnd;
     tp.TR = kTileM / tp.G;
     tp.scale_log2 = bp.scale_log2;
     const bool cap = bp.softcap_log2 > 0.f;

@@ -99,6 +99,7 @@ struct WideParams {
     float scale_log2;
     int causal;             // mode 3: bottom-right causal on top of the windows
     float capl2, inv_capl2; // logits soft cap in log2 units (CAP instantiations)
+    int kv_hnd;             // modes 0 / 1: K / V maps over (Hkv, N, d)
 };
 
 // Keys j <= lim allowed among the 64 of a block (lim relative to its first key).
@@ -217,7 +218,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     for (int pn = 0; pn < L::panels; ++pn) {
                         const uint32_t kd = dst + pn * L::kPanel + h * L::kvHalf;
                         const uint32_t vd = kd + L::kvTile;
-                        if constexpr (MODE == 3) {
+                        if (MODE == 3 || p.kv_hnd) {
                             tma_load_3d(kd, &mk, pn * 64, col, item.kvh, bar(B_KV_FULL + s));
                             tma_load_3d(vd, &mv, pn * 64, col, item.kvh, bar(B_KV_FULL + s));
                         } else {
@@ -521,10 +522,14 @@ cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems,
             !make_map_hnd(&mk, bp.k, bf16, D, bp.N, bp.Hkv, kBlk, 1) ||
             !make_map_hnd(&mv, bp.v, bf16, D, bp.N, bp.Hkv, kBlk, 1))
             return cudaErrorInvalidValue;
-    } else if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, wp.G, wp.TR) ||
-               !make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kBlk) ||
-               !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kBlk))
+    } else if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, wp.G, wp.TR)) {
         return cudaErrorInvalidValue;
+    } else if (bp.kv_hnd ? (!make_map_hnd(&mk, bp.k, bf16, D, bp.N, bp.Hkv, kBlk, 1) ||
+                            !make_map_hnd(&mv, bp.v, bf16, D, bp.N, bp.Hkv, kBlk, 1))
+                         : (!make_map(&mk, bp.k, bf16, D, bp.Hkv, bp.N, 1, kBlk) ||
+                            !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kBlk))) {
+        return cudaErrorInvalidValue;
+    }
     auto kern = bsr_tc_wide_kernel<E, D, MODE, CAP>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
     if (err != cudaSuccess) return err;
@@ -550,6 +555,7 @@ cudaError_t launch_bsr_tc_wide(const BsrParams& bp, const void* items, int nitem
     wp.R = bp.R;
     wp.C = bp.mask_mode == 3 ? kBlk : bp.C;
     wp.causal = bp.causal;
+    wp.kv_hnd = bp.mask_mode == 3 ? 1 : bp.kv_hnd;
     wp.Hq = bp.Hq;
     wp.G = bp.Hq / bp.Hkv;
     wp.TR = kTileM / wp.G;

@@ -22,11 +22,37 @@ __device__ int g_error_word = 0;
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+namespace {
+
+// Driver entry points through the runtime (the library does not link the
+// driver library directly, so it also loads on machines without one).
+template <class F>
+F driver_fn(const char* name, int version) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &ptr, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(ptr);
+}
+
+}  // namespace
+
 unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static std::once_flag once;
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    std::call_once(once, [] {
+        get_current = driver_fn<GetCurrent>("cuCtxGetCurrent", 4000);
+        get_id = driver_fn<GetId>("cuCtxGetId", 12000);
+    });
+    if (!get_current || !get_id) return 0;
     CUcontext ctx = nullptr;
     unsigned long long id = 0;
-    if (cuCtxGetCurrent(&ctx) != CUDA_SUCCESS || !ctx) return 0;
-    if (cuCtxGetId(ctx, &id) != CUDA_SUCCESS) return 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
     return id;
 }
 

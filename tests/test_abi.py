@@ -224,6 +224,13 @@ def test_soft_cap_setters_reject_bad_arguments(lib):
     # (making a plan needs a device; the NaN / inf checks run in test_gpu_softcap.py)
 
 
+def test_kv_layout_setter_rejects_bad_arguments(lib):
+    assert lib.bsr_plan_set_kv_layout(None, 0) == sfa.SFA_ERR_INVALID_ARG
+    assert lib.bsr_plan_set_kv_layout(None, 1) == sfa.SFA_ERR_INVALID_ARG
+    # a plan with a layout value outside the enum: checked on the GPU machine
+    # (making a plan uploads its work list)
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(sfa, "LIB_PATH", str(tmp_path / "absent.so"))
     monkeypatch.setattr(sfa, "_lib", None)

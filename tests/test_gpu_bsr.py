@@ -246,3 +246,46 @@ def test_masked_plan_reuse():
         y, l = oracle.bsr(q, x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C, 0.125,
                           mask=x["mask"])
         compare(out.cpu(), lse.cpu(), y, l, "bf16")
+
+
+# ---------------------------------------------------------------------------
+# k / v in HND layout ("flashinfer.prefill.single_prefill_with_kv_cache",
+# kv_layout): the same problem as with NHD tensors, k and v permuted to
+# (num_kv_heads, N, head_dim); the oracle gets the NHD tensors.
+
+HND_SHAPES = [
+    # M, N, R, C, Hq, Hkv, d, dtype, mode
+    (256, 384, 64, 64, 8, 2, 128, "f16", "plain"),     # 128-key tensor-core kernel
+    (200, 256, 64, 128, 4, 4, 64, "bf16", "plain"),    # C = 2 x 64, ragged last row block
+    (256, 320, 64, 64, 16, 2, 128, "bf16", "causal"),  # causal mode, N > M
+    (130, 192, 32, 64, 16, 1, 128, "f16", "mask"),     # 64-key kernel, per-element mask
+    (97, 120, 16, 24, 6, 3, 192, "f16", "plain"),      # register-tiled kernel
+    (64, 96, 8, 32, 2, 1, 64, "bf16", "mask"),         # register-tiled kernel with a mask
+]
+
+
+@pytest.mark.parametrize("M,N,R,C,Hq,Hkv,d,dtype,mode", HND_SHAPES)
+def test_hnd_kv_layout(M, N, R, C, Hq, Hkv, d, dtype, mode):
+    case = synth.BsrCase("h", M=M, N=N, R=R, C=C, Hq=Hq, Hkv=Hkv, d=d, dtype=dtype, p=0.45,
+                         sm_scale=1 / math.sqrt(d), seed=91, mask_keep=0.5 if mode == "mask" else 0.0)
+    x = synth.make_bsr_inputs(case)
+    causal = mode == "causal"
+    plan = sfa.bsr_plan(x["indptr"], x["indices"], M, N, R, C, Hq, Hkv, d, sm_scale=case.sm_scale,
+                        dtype=dtype, causal=causal, mask=x["mask"], kv_layout="HND")
+    k_hnd = x["k"].permute(1, 0, 2).contiguous().cuda()
+    v_hnd = x["v"].permute(1, 0, 2).contiguous().cuda()
+    q = x["q"].cuda()
+    out = torch.empty_like(q)
+    lse = torch.empty((M, Hq), dtype=torch.float32, device="cuda")
+    sfa.bsr_run(plan, q, k_hnd, v_hnd, out, lse)
+    torch.cuda.synchronize()
+    y, l = oracle.bsr(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                      case.sm_scale, mask=x["mask"], causal=causal)
+    compare(out.cpu(), lse.cpu(), y, l, dtype)
+    # the same plan switched back to NHD reads the original tensors
+    sfa.bsr_plan_set_kv_layout(plan, "NHD")
+    out2 = torch.empty_like(q)
+    sfa.bsr_run(plan, q, x["k"].cuda(), x["v"].cuda(), out2, lse)
+    torch.cuda.synchronize()
+    compare(out2.cpu(), lse.cpu(), y, l, dtype)
+    assert sfa.load().bsr_plan_set_kv_layout(plan.handle, 2) == sfa.SFA_ERR_INVALID_ARG
