@@ -73,6 +73,11 @@ def load_library(path: str):
     lib.oracle_varbsr.restype = ci
     lib.oracle_varbsr_rows.argtypes = [vp] * 6 + [ci] * 8 + [cd, ci, vp, ctypes.c_int64, vp, vp]
     lib.oracle_varbsr_rows.restype = ci
+    lib.oracle_decode.argtypes = [vp, i64, ci, vp]
+    lib.oracle_decode.restype = None
+    lib.oracle_bsr_scaled.argtypes = ([vp] * 6 + [ci] * 8 + [cd, cd, ci, ci] + [vp] * 3 +
+                                      [vp, i64, vp, vp])
+    lib.oracle_bsr_scaled.restype = ci
     return lib
 
 
@@ -89,12 +94,34 @@ def threads() -> int:
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
 
+# element type codes of the C oracle
+DTYPE_CODES = {"f16": 0, "bf16": 1, "e4m3": 2, "e5m2": 3}
+
+
 def _dtype_of(t: torch.Tensor) -> int:
     if t.dtype == torch.float16:
         return 0
     if t.dtype == torch.bfloat16:
         return 1
     raise TypeError(f"oracle takes fp16/bf16 tensors, got {t.dtype}")
+
+
+def _any_dtype_of(t: torch.Tensor) -> int:
+    """Element type code of a 16-bit or 8-bit floating-point tensor."""
+    fp8 = {getattr(torch, "float8_e4m3fn", None): 2, getattr(torch, "float8_e5m2", None): 3}
+    if t.dtype in fp8 and t.dtype is not None:
+        return fp8[t.dtype]
+    return _dtype_of(t)
+
+
+def decode(codes, dtype: str) -> np.ndarray:
+    """float64 values the oracle reads for uint8 (E4M3 / E5M2) or uint16
+    (f16 / bf16) codes."""
+    code = DTYPE_CODES[dtype]
+    arr = np.ascontiguousarray(codes, dtype=np.uint8 if code >= 2 else np.uint16)
+    out = np.empty(arr.size)
+    _load().oracle_decode(arr.ctypes.data, arr.size, code, out.ctypes.data)
+    return out.reshape(arr.shape)
 
 
 def _ptr(t: torch.Tensor) -> int:
@@ -216,6 +243,48 @@ def bsr(q, k, v, indptr, indices, M, N, R, C, scale, mask=None, packed_mask=None
     return y, lse
 
 
+def bsr_scaled(q, k, v, indptr, indices, M, N, R, C, scale, scale_q=None, scale_k=None,
+               scale_v=None, rows=None, mask=None, packed_mask=None, causal=False, softcap=0.0):
+    """Block-sparse attention (NHD) on q and k / v of any of fp16, bf16,
+    float8_e4m3fn, float8_e5m2 (q may differ from k / v), with run()'s
+    per-head dequantisation scales (scale_q [Hq], scale_k / scale_v [Hkv];
+    None = 1.0).  rows None: (y (M, Hq, d), lse (M, Hq)); rows (n, 2) of
+    (query row, qo head): (y (n, d), lse (n))."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    if _any_dtype_of(k) != _any_dtype_of(v):
+        raise TypeError("k and v must share an element type")
+    indptr = indptr.to(torch.int32).contiguous()
+    indices = indices.to(torch.int32).contiguous()
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+
+    def scales(x, n):
+        if x is None:
+            return None
+        a = np.ascontiguousarray(np.asarray(x, dtype=np.float64).reshape(-1))
+        if a.size != n:
+            raise ValueError("a scale per head expected")
+        return a
+    sq, sk, sv = scales(scale_q, Hq), scales(scale_k, Hkv), scales(scale_v, Hkv)
+    if rows is None:
+        r_ptr, n = None, M * Hq
+        y, lse = np.empty((M, Hq, d)), np.empty((M, Hq))
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        r_ptr, n = rows.ctypes.data, rows.shape[0]
+        y, lse = np.empty((n, d)), np.empty(n)
+    ind_ptr = _ptr(indices) if indices.numel() else 0
+    keep, pm_ptr = _mask_args(mask, packed_mask)
+    rc = _load().oracle_bsr_scaled(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(indptr), ind_ptr, pm_ptr, int(bool(causal)), M, N, R, C,
+        Hq, Hkv, d, float(scale), float(softcap), _any_dtype_of(q), _any_dtype_of(k),
+        None if sq is None else sq.ctypes.data, None if sk is None else sk.ctypes.data,
+        None if sv is None else sv.ctypes.data, r_ptr, n, y.ctypes.data, lse.ctypes.data)
+    _check(rc, "oracle_bsr_scaled")
+    del keep
+    return y, lse
+
+
 def bsr_rows(q, k, v, indptr, indices, M, N, R, C, scale, rows, mask=None, packed_mask=None,
              causal=False, softcap=0.0):
     """Selected rows: rows is (n, 2) of (query row i, qo head h)."""
@@ -289,7 +358,7 @@ def varbsr_rows(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, rows
 # values: an element also passes the MARE test when |actual - golden| <= cap
 # (1e-2 fp16, 4e-2 bf16).
 
-THRESHOLD = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}
+THRESHOLD = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7, "e4m3": 2.0 ** -3, "e5m2": 2.0 ** -2}
 ABS_CAP = {"f16": 1e-2, "bf16": 4e-2}
 
 

@@ -48,6 +48,14 @@
  *     cap > 0 a logit x becomes cap * tanh(x / cap).  The page does not say
  *     whether x includes sm_scale; read as the scaled logit sm_scale * q.k
  *     (the softmax input), so the LSE is over the capped logits.
+ *   FP8 -- BlockSparseAttentionWrapper plan() `q_data_type` / `kv_data_type`
+ *     and run() `scale_q` [num_qo_heads], `scale_k`, `scale_v`
+ *     [num_kv_heads] ("per-head quantisation scales, for FP8"; 1.0 when not
+ *     given); the formats are the two the operator page's precision table
+ *     names, E4M3 and E5M2.  Read as dequantisation: the value an element
+ *     stands for is its decoded code times its head's scale, and attention
+ *     runs on those values (q of qo head h times scale_q[h], k and v of kv
+ *     head g times scale_k[g] and scale_v[g]).
  *
  * Return codes: 0 ok, -1 bad argument, -2 an index outside [0, S2) (the
  * operator spec makes in-range indices a precondition).
@@ -81,6 +89,48 @@ static double oracle_bf16(uint16_t h) {
 
 static double oracle_load(const uint16_t* p, int64_t i, int dtype) {
     return dtype == 1 ? oracle_bf16(p[i]) : oracle_f16(p[i]);
+}
+
+/* The 8-bit floating-point formats, decoded exactly:
+ *   E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; no infinities, the
+ *         all-ones exponent with mantissa 7 is NaN (largest finite 448);
+ *         exponent 0 is subnormal, m/8 * 2^-6.
+ *   E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits with IEEE rules
+ *         (exponent 31: infinity for mantissa 0, else NaN; largest finite
+ *         57344); exponent 0 is subnormal, m/4 * 2^-14. */
+static double oracle_e4m3(uint8_t c) {
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);               /* (m / 8) 2^-6 */
+    else v = ldexp((double)(8 + m), e - 10);            /* (1 + m / 8) 2^(e - 7) */
+    return sign ? -v : v;
+}
+
+static double oracle_e5m2(uint8_t c) {
+    const int sign = c >> 7, e = (c >> 2) & 31, m = c & 3;
+    double v;
+    if (e == 31) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m, -16);         /* (m / 4) 2^-14 */
+    else v = ldexp((double)(4 + m), e - 17);            /* (1 + m / 4) 2^(e - 15) */
+    return sign ? -v : v;
+}
+
+/* Element i of a tensor of element type `dtype`: 0 f16, 1 bf16, 2 E4M3,
+ * 3 E5M2. */
+static double oracle_elem(const void* p, int64_t i, int dtype) {
+    switch (dtype) {
+        case 0: return oracle_f16(((const uint16_t*)p)[i]);
+        case 1: return oracle_bf16(((const uint16_t*)p)[i]);
+        case 2: return oracle_e4m3(((const uint8_t*)p)[i]);
+        default: return oracle_e5m2(((const uint8_t*)p)[i]);
+    }
+}
+
+/* Decoded values of `n` codes of `dtype` (the pins read the decoders through
+ * this). */
+void oracle_decode(const void* codes, int64_t n, int dtype, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_elem(codes, i, dtype);
 }
 
 typedef struct {
@@ -252,11 +302,15 @@ int oracle_sfa_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, int
  * lse: (M, Hq). */
 
 typedef struct {
-    int M, N, R, C, Hq, Hkv, d, dtype;
+    int M, N, R, C, Hq, Hkv, d;
+    int q_dtype, kv_dtype;        /* element types of q and of k / v (oracle_elem codes) */
     double scale;
     const uint8_t* packed_mask;   /* NULL: every stored block is full */
     int causal;                   /* used only without a mask */
     double softcap;               /* > 0: logits become softcap * tanh(logit / softcap) */
+    const double* scale_q;        /* [Hq] or NULL (1.0): dequantisation scale of q */
+    const double* scale_k;        /* [Hkv] or NULL */
+    const double* scale_v;        /* [Hkv] or NULL */
 } oracle_bsr_shape;
 
 /* plan()'s logits_soft_cap ("flashinfer.sparse", both wrappers): a logit x
@@ -268,7 +322,8 @@ static int oracle_bsr_check(const oracle_bsr_shape* s, const int32_t* indptr,
     if (s->M < 1 || s->N < 1 || s->R < 1 || s->C < 1 || s->Hq < 1 || s->Hkv < 1 || s->d < 1)
         return ORACLE_BAD_ARG;
     if (s->N % s->C != 0 || s->Hq % s->Hkv != 0) return ORACLE_BAD_ARG;
-    if (s->dtype != 0 && s->dtype != 1) return ORACLE_BAD_ARG;
+    if (s->q_dtype < 0 || s->q_dtype > 3 || s->kv_dtype < 0 || s->kv_dtype > 3)
+        return ORACLE_BAD_ARG;
     const int MB = (s->M + s->R - 1) / s->R, NB = s->N / s->C;
     if (indptr[0] != 0) return ORACLE_BAD_ARG;
     for (int i = 0; i < MB; ++i) {
@@ -281,8 +336,8 @@ static int oracle_bsr_check(const oracle_bsr_shape* s, const int32_t* indptr,
 
 /* One output row (query row i, qo head h).  `allowed` is caller scratch of N
  * bytes, `scores` of N doubles. */
-static void oracle_bsr_row(const oracle_bsr_shape* s, const uint16_t* q, const uint16_t* k,
-                           const uint16_t* v, const int32_t* indptr, const int32_t* indices,
+static void oracle_bsr_row(const oracle_bsr_shape* s, const void* q, const void* k,
+                           const void* v, const int32_t* indptr, const int32_t* indices,
                            int i, int h, unsigned char* allowed, double* scores, double* y_row,
                            double* lse_row) {
     const int kvh = h / (s->Hq / s->Hkv);
@@ -303,6 +358,10 @@ static void oracle_bsr_row(const oracle_bsr_shape* s, const uint16_t* q, const u
         for (int j = 0; j < s->N; ++j)
             if ((int64_t)j > (int64_t)i + (s->N - s->M)) allowed[j] = 0;
 
+    /* dequantisation scales of this row's qo head and kv head */
+    const double sq = s->scale_q ? s->scale_q[h] : 1.0;
+    const double sk = s->scale_k ? s->scale_k[kvh] : 1.0;
+    const double sv = s->scale_v ? s->scale_v[kvh] : 1.0;
     const int64_t qo = ((int64_t)i * s->Hq + h) * s->d;
     double mx = -INFINITY;
     for (int j = 0; j < s->N; ++j) {
@@ -310,7 +369,8 @@ static void oracle_bsr_row(const oracle_bsr_shape* s, const uint16_t* q, const u
         const int64_t ko = ((int64_t)j * s->Hkv + kvh) * s->d;
         double dot = 0.0;
         for (int e = 0; e < s->d; ++e)
-            dot += oracle_load(q, qo + e, s->dtype) * oracle_load(k, ko + e, s->dtype);
+            dot += (sq * oracle_elem(q, qo + e, s->q_dtype)) *
+                   (sk * oracle_elem(k, ko + e, s->kv_dtype));
         scores[j] = oracle_soft_cap(dot * s->scale, s->softcap);
         if (scores[j] > mx) mx = scores[j];
     }
@@ -329,7 +389,7 @@ static void oracle_bsr_row(const oracle_bsr_shape* s, const uint16_t* q, const u
         if (!allowed[j]) continue;
         const double w = scores[j] / sum;
         const int64_t vo = ((int64_t)j * s->Hkv + kvh) * s->d;
-        for (int e = 0; e < s->d; ++e) y_row[e] += w * oracle_load(v, vo + e, s->dtype);
+        for (int e = 0; e < s->d; ++e) y_row[e] += w * (sv * oracle_elem(v, vo + e, s->kv_dtype));
     }
     if (lse_row) *lse_row = mx + log(sum);
 }
@@ -338,7 +398,8 @@ int oracle_bsr_cap(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
                    const int32_t* indices, const uint8_t* packed_mask, int causal, int M, int N,
                    int R, int C, int Hq, int Hkv, int d, double scale, double softcap, int dtype,
                    double* y, double* lse) {
-    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale, packed_mask, causal, softcap};
+    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, dtype, scale, packed_mask, causal,
+                          softcap, NULL, NULL, NULL};
     int rc = oracle_bsr_check(&s, indptr, indices);
     if (rc) return rc;
     const int64_t rows = (int64_t)M * Hq;
@@ -385,7 +446,8 @@ int oracle_bsr_rows_cap(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         int causal, int M, int N, int R, int C, int Hq, int Hkv, int d,
                         double scale, double softcap, int dtype, const int64_t* rows,
                         int64_t nrows, double* y_rows, double* lse_rows) {
-    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, scale, packed_mask, causal, softcap};
+    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, dtype, dtype, scale, packed_mask, causal,
+                          softcap, NULL, NULL, NULL};
     int rc = oracle_bsr_check(&s, indptr, indices);
     if (rc) return rc;
     int err = ORACLE_OK;
@@ -425,6 +487,44 @@ int oracle_bsr_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                     int64_t nrows, double* y_rows, double* lse_rows) {
     return oracle_bsr_rows_ex(q, k, v, indptr, indices, NULL, 0, M, N, R, C, Hq, Hkv, d, scale,
                               dtype, rows, nrows, y_rows, lse_rows);
+}
+
+/* Block-sparse attention with element types of their own for q and k / v
+ * (any of f16, bf16, E4M3, E5M2) and run()'s per-head dequantisation scales
+ * (each NULL = 1.0).  rows = NULL: every (i, h) row in order, y (M, Hq, d);
+ * else rows[2r], rows[2r+1] = (query row i, qo head h), y (nrows, d). */
+int oracle_bsr_scaled(const void* q, const void* k, const void* v, const int32_t* indptr,
+                      const int32_t* indices, const uint8_t* packed_mask, int causal, int M, int N,
+                      int R, int C, int Hq, int Hkv, int d, double scale, double softcap,
+                      int q_dtype, int kv_dtype, const double* scale_q, const double* scale_k,
+                      const double* scale_v, const int64_t* rows, int64_t nrows, double* y,
+                      double* lse) {
+    oracle_bsr_shape s = {M, N, R, C, Hq, Hkv, d, q_dtype, kv_dtype, scale, packed_mask, causal,
+                          softcap, scale_q, scale_k, scale_v};
+    int rc = oracle_bsr_check(&s, indptr, indices);
+    if (rc) return rc;
+    const int64_t n = rows ? nrows : (int64_t)M * Hq;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        unsigned char* allowed = (unsigned char*)malloc((size_t)N);
+        double* scores = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n; ++r) {
+            const int i = rows ? (int)rows[2 * r] : (int)(r / Hq);
+            const int h = rows ? (int)rows[2 * r + 1] : (int)(r % Hq);
+            if (!allowed || !scores || i < 0 || i >= M || h < 0 || h >= Hq) {
+#pragma omp atomic write
+                err = ORACLE_BAD_ARG;
+                continue;
+            }
+            oracle_bsr_row(&s, q, k, v, indptr, indices, i, h, allowed, scores, y + r * d,
+                           lse ? lse + r : NULL);
+        }
+        free(allowed);
+        free(scores);
+    }
+    return err;
 }
 
 /* ---------------------------------------------------------------------- */

@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_bsr_mask as mpins
+from tests import test_oracle_fp8 as fpins
 from tests import test_oracle_pins as pins
 from tests import test_oracle_softcap as cpins
 from tests import test_oracle_varbsr as vpins
@@ -25,8 +26,8 @@ MUTANTS = [
     ("softmax_unnormalised", "weights[i] /= sum;", "weights[i] /= 1.0;"),
     ("lse_base2", "weights[i] /= sum;\n    if (lse_row) *lse_row = mx + log(sum);",
      "weights[i] /= sum;\n    if (lse_row) *lse_row = mx + log2(sum);"),
-    ("bsr_lse_base2", "y_row[e] += w * oracle_load(v, vo + e, s->dtype);\n    }\n    if (lse_row) *lse_row = mx + log(sum);",
-     "y_row[e] += w * oracle_load(v, vo + e, s->dtype);\n    }\n    if (lse_row) *lse_row = mx + log2(sum);"),
+    ("bsr_lse_base2", "y_row[e] += w * (sv * oracle_elem(v, vo + e, s->kv_dtype));\n    }\n    if (lse_row) *lse_row = mx + log(sum);",
+     "y_row[e] += w * (sv * oracle_elem(v, vo + e, s->kv_dtype));\n    }\n    if (lse_row) *lse_row = mx + log2(sum);"),
     ("varbsr_lse_base2", "* d + e, s->dtype);\n    }\n    if (lse_row) *lse_row = mx + log(sum);",
      "* d + e, s->dtype);\n    }\n    if (lse_row) *lse_row = mx + log2(sum);"),
     ("bnsd_index_as_bsnd", ": (((int64_t)b * s->N2 + n2) * s->S1 + s1) * s->topK;",
@@ -48,8 +49,8 @@ MUTANTS = [
      "if ((int64_t)j > (int64_t)i) allowed[j] = 0;"),
     ("bsr_causal_with_mask", "if (!s->packed_mask && s->causal)", "if (s->causal)"),
     ("bsr_row_block_reversed", "const int br = i / s->R;", "const int br = (s->M - 1 - i) / s->R;"),
-    ("bsr_scale_dropped", "oracle_load(k, ko + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot * s->scale,",
-     "oracle_load(k, ko + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot,"),
+    ("bsr_scale_dropped", "(sk * oracle_elem(k, ko + e, s->kv_dtype));\n        scores[j] = oracle_soft_cap(dot * s->scale,",
+     "(sk * oracle_elem(k, ko + e, s->kv_dtype));\n        scores[j] = oracle_soft_cap(dot,"),
     ("varbsr_scale_dropped", "* d + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot * s->scale,",
      "* d + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot,"),
     ("varbsr_kv_head_map", "i = (int)(r % s->M), g = h / G;", "i = (int)(r % s->M), g = h % s->Hkv;"),
@@ -65,10 +66,30 @@ MUTANTS = [
      "* d + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot, s->softcap) * s->scale;"),
     ("softcap_no_multiplier", "return cap > 0.0 ? cap * tanh(x / cap) : x;",
      "return cap > 0.0 ? tanh(x / cap) : x;"),
-    ("softcap_ignored_in_bsr", "oracle_load(k, ko + e, s->dtype);\n        scores[j] = oracle_soft_cap(dot * s->scale, s->softcap);",
-     "oracle_load(k, ko + e, s->dtype);\n        scores[j] = dot * s->scale;"),
+    ("softcap_ignored_in_bsr", "(sk * oracle_elem(k, ko + e, s->kv_dtype));\n        scores[j] = oracle_soft_cap(dot * s->scale, s->softcap);",
+     "(sk * oracle_elem(k, ko + e, s->kv_dtype));\n        scores[j] = dot * s->scale;"),
     ("bf16_as_f16", "return dtype == 1 ? oracle_bf16(p[i]) : oracle_f16(p[i]);",
      "return oracle_f16(p[i]);"),
+    # FP8 formats and per-head scales
+    ("e4m3_exponent_bias", "else v = ldexp((double)(8 + m), e - 10);",
+     "else v = ldexp((double)(8 + m), e - 11);"),
+    ("e4m3_subnormal_as_normal", "if (e == 0) v = ldexp((double)m, -9);",
+     "if (e == 0) v = ldexp((double)(8 + m), -10);"),
+    ("e4m3_no_nan", "if (e == 15 && m == 7) return NAN;", "if (e == 16) return NAN;"),
+    ("e5m2_mantissa_width", "else v = ldexp((double)(4 + m), e - 17);",
+     "else v = ldexp((double)(8 + m), e - 18);"),
+    ("e5m2_read_as_e4m3", "default: return oracle_e5m2(((const uint8_t*)p)[i]);",
+     "default: return oracle_e4m3(((const uint8_t*)p)[i]);"),
+    ("scale_q_by_kv_head", "const double sq = s->scale_q ? s->scale_q[h] : 1.0;",
+     "const double sq = s->scale_q ? s->scale_q[kvh] : 1.0;"),
+    ("scale_k_by_qo_head", "const double sk = s->scale_k ? s->scale_k[kvh] : 1.0;",
+     "const double sk = s->scale_k ? s->scale_k[h % s->Hkv] : 1.0;"),
+    ("scale_v_dropped", "y_row[e] += w * (sv * oracle_elem(v, vo + e, s->kv_dtype));",
+     "y_row[e] += w * oracle_elem(v, vo + e, s->kv_dtype);"),
+    ("scale_v_as_scale_k", "const double sv = s->scale_v ? s->scale_v[kvh] : 1.0;",
+     "const double sv = s->scale_k ? s->scale_k[kvh] : 1.0;"),
+    ("q_read_with_kv_type", "dot += (sq * oracle_elem(q, qo + e, s->q_dtype)) *",
+     "dot += (sq * oracle_elem(q, qo + e, s->kv_dtype)) *"),
 ]
 
 
@@ -102,6 +123,15 @@ def all_pins():
     out += [cpins.test_large_cap_is_no_cap, cpins.test_tiny_cap_gives_mean_of_allowed_values,
             lambda: cpins.test_bsr_matches_dense_brute_force("plain", 0.7),
             lambda: cpins.test_varbsr_matches_dense_brute_force(False)]
+    # FP8 decoding and scale pins
+    out += [fpins.test_e4m3_decode_matches_torch, fpins.test_e5m2_decode_matches_torch,
+            fpins.test_fp8_closed_forms, fpins.test_e5m2_is_the_high_byte_of_f16,
+            fpins.test_fp8_equals_the_16bit_run_on_the_same_values,
+            fpins.test_scale_v_scales_the_output_only, fpins.test_scale_k_is_a_per_group_sm_scale,
+            fpins.test_scale_q_is_a_per_head_sm_scale]
+    for kv in ("e4m3", "e5m2"):
+        out.append(lambda t=kv: fpins.test_matches_dense_brute_force(t, "f16"))
+        out.append(lambda t=kv: fpins.test_matches_dense_brute_force(t, t))
     return out
 
 
