@@ -50,7 +50,7 @@ METRIC = "sparse-attn effective TFLOP/s & gathered-KV GB/s, fraction of GB300 ro
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 HEADLINE = "sparse_prefill"
 SUB_WORKLOADS = ("gqa_decode", "mla_decode", "mla_mtp", "call_example", "bsr", "bsr_causal",
-                 "bsr_mask", "varbsr")
+                 "bsr_mask", "bsr_fp8", "varbsr")
 ALL_WORKLOADS = sorted(synth.SFA_WORKLOADS) + sorted(synth.BSR_WORKLOADS) + \
     sorted(synth.VARBSR_WORKLOADS)
 
@@ -250,6 +250,7 @@ MAIN_KERNEL = {
     "bsr": "bsr_tc_wide_kernel (one launch per bsr_run)",
     "bsr_causal": "bsr_tc_wide_kernel, causal mode (one launch per bsr_run)",
     "bsr_mask": "bsr_tc_kernel, per-element mask (one launch per bsr_run)",
+    "bsr_fp8": "bsr_tc_wide_kernel, E4M3 instantiation (one launch per bsr_run_scaled)",
     "varbsr": "bsr_tc_wide_kernel, variable mode (one launch per varbsr_run)",
 }
 
@@ -515,8 +516,18 @@ def run_bsr(name, args, world, rank, cpu_target_s):
         lse_shape = (case.M, case.Hq)
         shape_cfg = {"layout": "NHD", "R": case.R, "C": case.C, "nnz_blocks": counts["nnz"],
                      "element_mask_keep": case.mask_keep or None}
+        if case.fp8:
+            # q / k / v in E4M3 with per-head scales, fp16 out
+            sfa.bsr_plan_set_data_types(plan, case.fp8, case.fp8, case.dtype)
+            scales = [x[n].cuda() for n in ("scale_q", "scale_k", "scale_v")]
+
+            def run(pl, q_, k_, v_, out_, lse_, stream_):
+                sfa.bsr_run_scaled(pl, q_, k_, v_, *scales, out=out_, lse=lse_, stream=stream_)
+            shape_cfg["fp8"] = {"q_k_v": case.fp8, "out": case.dtype,
+                                "scales": "per head, max |x| / 448"}
     q, k, v = x["q"].cuda(), x["k"].cuda(), x["v"].cuda()
-    out = torch.empty_like(q)
+    out_dtype = {"f16": torch.float16, "bf16": torch.bfloat16}[case.dtype]
+    out = torch.empty(q.shape, dtype=out_dtype, device="cuda")
     lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
 
     def call(qq):
@@ -536,7 +547,7 @@ def run_bsr(name, args, world, rank, cpu_target_s):
         # K/V resident (the KV cache); q in from pinned host memory, out and
         # lse back, every step
         hq = x["q"].pin_memory()
-        hout = torch.empty_like(hq).pin_memory()
+        hout = torch.empty(hq.shape, dtype=out_dtype).pin_memory()
         hlse = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
         dq = torch.empty_like(q)
 
@@ -555,20 +566,27 @@ def run_bsr(name, args, world, rank, cpu_target_s):
     peaks, peak_src = load_peaks()
     tflops = counts["flops"] / (ms * 1e-3) / 1e12
     prof = committed_profile(name)
+    fp8 = getattr(case, "fp8", "")
+    # a contraction's own dtype: 8-bit MMAs run at twice the 16-bit rate
+    # (nominal 4.5 vs 2.25 PFLOP/s dense)
+    peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    peak_src_txt = (f"{peak_src} bf16_tflops x 2 (nominal fp8 / bf16 dense ratio 4.5 / 2.25); "
+                    "burst: the kernel is timed alone" if fp8 else
+                    f"{peak_src} bf16_tflops (burst: the kernel is timed alone; the fp16 dense "
+                    "rate is the bf16 rate)")
     cfg = {"workload": case.name, "M": case.M, "N": case.N, **shape_cfg, "Hq": case.Hq,
            "Hkv": case.Hkv, "d": case.d, "p": case.p, "causal": case.causal,
            "l2": "q, out (268 MiB) stream through; K/V (67 MiB) L2-resident by design",
            "launch": mode,
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
     rec = {"workload": name, "value": whole_job_rate(counts["flops"], ms, world) / 1e12,
-           "unit": "TFLOP/s", "ms_per_step": ms, "us_per_call": ms * 1e3, "dtype": case.dtype,
-           "config": cfg, "tflops": world * tflops,
-           "tensor_frac": tflops / peaks["bf16_tflops"],
-           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
-                        "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+           "unit": "TFLOP/s", "ms_per_step": ms, "us_per_call": ms * 1e3,
+           "dtype": fp8 or case.dtype, "config": cfg, "tflops": world * tflops,
+           "tensor_frac": tflops / peak,
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
+                        "unit": "TFLOP/s", "frac": tflops / peak,
                         "traffic": None if prof is None else prof["dram"],
-                        "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed "
-                                       "alone; the fp16 dense rate is the bf16 rate)",
+                        "peak_source": peak_src_txt,
                         "algorithmic": "useful FLOPs (4 * d per allowed row, column, qo head)",
                         "kernel": MAIN_KERNEL[name] + "; CUDA events on its stream"},
            "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
@@ -595,9 +613,15 @@ def bsr_cpu_baseline(case, x, counts, variable, target_s):
                                x["block_col_sz"], case.sm_scale, flat, causal=case.causal)
         else:
             pairs = np.stack([np.repeat(qrows, case.Hq), np.tile(heads, len(qrows))], axis=1)
-            oracle.bsr_rows(x["q"], x["k"], x["v"], x["indptr"], x["indices"], case.M, case.N,
-                            case.R, case.C, case.sm_scale, pairs, mask=x["mask"],
-                            causal=case.causal)
+            if getattr(case, "fp8", ""):
+                oracle.bsr_scaled(x["q"], x["k"], x["v"], x["indptr"], x["indices"], case.M,
+                                  case.N, case.R, case.C, case.sm_scale,
+                                  scale_q=x["scale_q"].numpy(), scale_k=x["scale_k"].numpy(),
+                                  scale_v=x["scale_v"].numpy(), rows=pairs, causal=case.causal)
+            else:
+                oracle.bsr_rows(x["q"], x["k"], x["v"], x["indptr"], x["indices"], case.M,
+                                case.N, case.R, case.C, case.sm_scale, pairs, mask=x["mask"],
+                                causal=case.causal)
 
     t0 = time.perf_counter()
     run_rows(np.array([case.M // 2], dtype=np.int64))

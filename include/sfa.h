@@ -53,8 +53,16 @@ typedef enum {
  * All row-major and contiguous, except v in key-prefix mode (below). */
 typedef enum { SFA_LAYOUT_BSND = 0, SFA_LAYOUT_BNSD = 1 } sfa_layout;
 
-/* q, k, v and out share one element type (§3 数据类型). */
-typedef enum { SFA_DTYPE_F16 = 0, SFA_DTYPE_BF16 = 1 } sfa_dtype;
+/* Element types.  The top-K entry points take F16 or BF16, shared by q, k,
+ * v and out (§3 数据类型).  E4M3 / E5M2 are the two 8-bit floating-point
+ * formats of the operator page's precision table (§4 精度要求), accepted by
+ * bsr_plan_set_data_types only. */
+typedef enum {
+    SFA_DTYPE_F16 = 0,
+    SFA_DTYPE_BF16 = 1,
+    SFA_DTYPE_E4M3 = 2,   /* 1 sign, 4 exponent (bias 7), 3 mantissa bits; max 448 */
+    SFA_DTYPE_E5M2 = 3    /* 1 sign, 5 exponent (bias 15), 2 mantissa bits; max 57344 */
+} sfa_dtype;
 
 /*
  * sfa_run -- top-K sparse flash attention.
@@ -287,7 +295,8 @@ typedef enum { SFA_KV_LAYOUT_NHD = 0, SFA_KV_LAYOUT_HND = 1 } sfa_kv_layout;
 sfa_status bsr_plan_set_kv_layout(bsr_plan_t plan, sfa_kv_layout kv_layout);
 
 /*
- * bsr_run -- block-sparse attention with a plan.
+ * bsr_run -- block-sparse attention with a plan (bsr_run_scaled without
+ * scales).
  *   q    device (M, num_qo_heads, head_dim), NHD, dtype.
  *   k, v device (N, num_kv_heads, head_dim), NHD, dtype, or
  *        (num_kv_heads, N, head_dim) after bsr_plan_set_kv_layout(HND).
@@ -310,6 +319,44 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
  * Errors: SFA_ERR_INVALID_ARG (NULL plan, non-finite cap).
  */
 sfa_status bsr_plan_set_logits_soft_cap(bsr_plan_t plan, float logits_soft_cap);
+
+/*
+ * bsr_plan_set_data_types -- plan()'s q_data_type, kv_data_type and
+ * o_data_type ("flashinfer.sparse", BlockSparseAttentionWrapper.plan();
+ * kv_data_type defaults to q_data_type, o_data_type to half).  bsr_plan's
+ * `dtype` sets all three; this changes them for every later run.
+ * Combinations of this build:
+ *   - q = k / v = out = the plan's dtype (F16 or BF16), as after bsr_plan;
+ *   - q = k / v in {E4M3, E5M2} with out in {F16, BF16} (FP8 attention; the
+ *     per-head scales of bsr_run_scaled apply), for plans of the tensor-core
+ *     path with head_dim 128 and no per-element mask, without a soft cap.
+ * Host only.  Errors: SFA_ERR_INVALID_ARG (NULL plan, a value outside
+ * sfa_dtype), SFA_ERR_UNSUPPORTED (any other combination or plan).
+ */
+sfa_status bsr_plan_set_data_types(bsr_plan_t plan, sfa_dtype q_dtype, sfa_dtype kv_dtype,
+                                   sfa_dtype o_dtype);
+
+/*
+ * bsr_run_scaled -- run() with its per-head scales ("flashinfer.sparse",
+ * BlockSparseAttentionWrapper.run(): scale_q [num_qo_heads], scale_k and
+ * scale_v [num_kv_heads], "for FP8 quantisation", 1.0 when not given).
+ * They are read as dequantisation scales: element codes times their head's
+ * scale are the values attention runs on, i.e. the scores of qo head h (kv
+ * head g) are sm_scale * scale_q[h] * scale_k[g] * q.k and its output is
+ * scale_v[g] * sum_j softmax_j * v_j; lse is over those scores.
+ *   q, k, v   device, the plan's q / kv data types (bsr_run's shapes and
+ *             layouts; 8-bit codes for E4M3 / E5M2).
+ *   scale_q, scale_k, scale_v  device float32 arrays, 4-byte aligned, or
+ *             NULL (= 1.0 for every head).  Each scale must be positive and
+ *             finite; other values give unspecified numbers (never a fault).
+ *   out, lse  device, out of the plan's o_data_type; lse float32 or NULL.
+ * On a plan whose data types are 16-bit, every scale must be NULL
+ * (SFA_ERR_UNSUPPORTED otherwise) and this is bsr_run.  An FP8 plan with a
+ * soft cap set returns SFA_ERR_UNSUPPORTED.  Other errors as bsr_run.
+ */
+sfa_status bsr_run_scaled(bsr_plan_t plan, const void* q, const void* k, const void* v,
+                          const float* scale_q, const float* scale_k, const float* scale_v,
+                          void* out, float* lse, sfa_stream_t stream);
 
 /* Frees the plan's host state.  Safe on NULL.  Does not touch the
  * caller's workspaces. */

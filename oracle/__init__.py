@@ -359,7 +359,7 @@ def varbsr_rows(q, k, v, block_mask_map, block_row_sz, block_col_sz, scale, rows
 # (1e-2 fp16, 4e-2 bf16).
 
 THRESHOLD = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7, "e4m3": 2.0 ** -3, "e5m2": 2.0 ** -2}
-ABS_CAP = {"f16": 1e-2, "bf16": 4e-2}
+ABS_CAP = {"f16": 1e-2, "bf16": 4e-2, "e4m3": 4e-2, "e5m2": 4e-2}
 
 
 def round_to(x, dtype: str) -> np.ndarray:
@@ -368,14 +368,18 @@ def round_to(x, dtype: str) -> np.ndarray:
     return t.to({"f16": torch.float16, "bf16": torch.bfloat16}[dtype]).to(torch.float64).numpy()
 
 
-def precision_report(actual, golden, dtype: str, round_golden: bool = True) -> dict:
+def precision_report(actual, golden, dtype: str, round_golden: bool = True,
+                     out_dtype: str | None = None) -> dict:
     """MERE / MARE of `actual` against `golden`.  The golden of the operator
     spec returns its output in the input dtype, so by default the float64
-    oracle values are rounded to `dtype` before comparing."""
+    oracle values are rounded to `dtype` before comparing.  For the 8-bit
+    formats (thresholds 2^-3 E4M3, 2^-2 E5M2) the output is 16-bit:
+    `out_dtype` names it, the golden is rounded to it, and the near-zero cap
+    is bf16's (the 8-bit paths' P carries about bf16's precision)."""
     a = np.asarray(actual, dtype=np.float64).ravel()
     g = np.asarray(golden, dtype=np.float64).ravel()
     if round_golden:
-        g = round_to(g, dtype)
+        g = round_to(g, out_dtype or dtype)
     if a.shape != g.shape:
         raise ValueError("shape mismatch")
     thr = THRESHOLD[dtype]

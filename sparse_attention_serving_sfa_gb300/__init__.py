@@ -26,7 +26,7 @@ SFA_ERR_DEVICE_TIMEOUT = 6
 
 LAYOUTS = {"BSND": 0, "BNSD": 1}
 KV_LAYOUTS = {"NHD": 0, "HND": 1}
-DTYPES = {"f16": 0, "bf16": 1}
+DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2, "e5m2": 3}
 
 # Every entry point of include/sfa.h.
 EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
@@ -34,7 +34,8 @@ EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
            "bsr_plan_destroy", "bsr_plan_masked", "bsr_plan_masked_int_workspace_size",
            "varbsr_plan", "varbsr_plan_int_workspace_size", "varbsr_plan_dims", "varbsr_run",
            "varbsr_plan_destroy", "bsr_plan_set_logits_soft_cap",
-           "varbsr_plan_set_logits_soft_cap", "bsr_plan_set_kv_layout")
+           "varbsr_plan_set_logits_soft_cap", "bsr_plan_set_kv_layout",
+           "bsr_plan_set_data_types", "bsr_run_scaled")
 
 
 class SfaError(RuntimeError):
@@ -114,6 +115,10 @@ def load():
             lib.varbsr_plan_set_logits_soft_cap.restype = ci
             lib.bsr_plan_set_kv_layout.argtypes = [vp, ci]
             lib.bsr_plan_set_kv_layout.restype = ci
+            lib.bsr_plan_set_data_types.argtypes = [vp, ci, ci, ci]
+            lib.bsr_plan_set_data_types.restype = ci
+            lib.bsr_run_scaled.argtypes = [vp] * 10
+            lib.bsr_run_scaled.restype = ci
             _lib = lib
     return _lib
 
@@ -306,6 +311,22 @@ def bsr_plan_set_logits_soft_cap(plan: BsrPlan, logits_soft_cap: float):
 def bsr_run(plan: BsrPlan, q, k, v, out, lse=None, stream=None):
     _check(load().bsr_run(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                           _stream(stream)), "bsr_run")
+
+
+def bsr_plan_set_data_types(plan: BsrPlan, q_dtype, kv_dtype, o_dtype):
+    """plan()'s q / kv / o data types: "f16", "bf16", "e4m3", "e5m2"."""
+    _check(load().bsr_plan_set_data_types(plan.handle, _enum(q_dtype, DTYPES),
+                                          _enum(kv_dtype, DTYPES), _enum(o_dtype, DTYPES)),
+           "bsr_plan_set_data_types")
+
+
+def bsr_run_scaled(plan: BsrPlan, q, k, v, scale_q=None, scale_k=None, scale_v=None, out=None,
+                   lse=None, stream=None):
+    """run() with per-head float32 device scales (None = 1.0).  FP8 tensors
+    may be torch float8 or uint8 tensors holding the codes."""
+    _check(load().bsr_run_scaled(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(scale_q),
+                                 _ptr(scale_k), _ptr(scale_v), _ptr(out), _ptr(lse),
+                                 _stream(stream)), "bsr_run_scaled")
 
 
 def bsr_plan_destroy(plan: BsrPlan):

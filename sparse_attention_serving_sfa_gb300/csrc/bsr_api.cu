@@ -24,6 +24,8 @@ struct bsr_plan_s {
     int mask_mode;                  // 0 none, 1 causal, 2 per-element bits
     float softcap_log2 = 0.f;       // logits_soft_cap * log2(e); 0 = none
     int kv_layout = SFA_KV_LAYOUT_NHD;
+    // plan()'s q_data_type / kv_data_type / o_data_type (all `dtype` unless set)
+    sfa_dtype q_dtype, kv_dtype, o_dtype;
     const int32_t* d_indptr;
     const int32_t* d_indices;
     const void* d_work;             // BsrTile list (generic) or 4-int items (tensor cores)
@@ -177,6 +179,7 @@ sfa_status bsr_plan_masked(const int32_t* indptr_host, const int32_t* indices_ho
     plan->M = M; plan->N = N; plan->R = R; plan->C = C;
     plan->Hq = num_qo_heads; plan->Hkv = num_kv_heads; plan->d = head_dim;
     plan->dtype = dtype;
+    plan->q_dtype = plan->kv_dtype = plan->o_dtype = dtype;
     plan->scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)head_dim);
     plan->MB = MB; plan->NB = NB; plan->nnz = f_nnz; plan->ntiles = ntiles;
     plan->tc = tc;
@@ -231,12 +234,20 @@ sfa_status bsr_plan_masked(const int32_t* indptr_host, const int32_t* indices_ho
     return SFA_OK;
 }
 
-sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v, void* out,
-                   float* lse, sfa_stream_t stream) {
+sfa_status bsr_run_scaled(bsr_plan_t plan, const void* q, const void* k, const void* v,
+                          const float* scale_q, const float* scale_k, const float* scale_v,
+                          void* out, float* lse, sfa_stream_t stream) {
     if (!plan || !q || !k || !v || !out) return SFA_ERR_INVALID_ARG;
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
     if (!a16(q) || !a16(k) || !a16(v) || !a16(out)) return SFA_ERR_INVALID_ARG;
-    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SFA_ERR_INVALID_ARG;
+    if ((lse && !a4(lse)) || (scale_q && !a4(scale_q)) || (scale_k && !a4(scale_k)) ||
+        (scale_v && !a4(scale_v)))
+        return SFA_ERR_INVALID_ARG;
+    const bool f8 = plan->kv_dtype == SFA_DTYPE_E4M3 || plan->kv_dtype == SFA_DTYPE_E5M2;
+    // per-head scales are the FP8 path's (run(): "for FP8 quantisation")
+    if (!f8 && (scale_q || scale_k || scale_v)) return SFA_ERR_UNSUPPORTED;
+    if (f8 && plan->softcap_log2 > 0.f) return SFA_ERR_UNSUPPORTED;
     sfa::BsrParams p{};
     p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse;
     p.indptr = plan->d_indptr;
@@ -250,9 +261,18 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
     p.mask = plan->d_mask;
     p.softcap_log2 = plan->softcap_log2;
     p.kv_hnd = plan->kv_layout == SFA_KV_LAYOUT_HND ? 1 : 0;
+    p.f8 = !f8 ? 0 : (plan->kv_dtype == SFA_DTYPE_E4M3 ? 1 : 2);
+    p.scale_q = scale_q;
+    p.scale_k = scale_k;
+    p.scale_v = scale_v;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
-    if (plan->tc) {
+    if (f8) {
+        int* ew = sfa::device_error_word();
+        if (!ew) return SFA_ERR_CUDA;
+        // the 128-key tensor-core kernel's FP8 instantiations; `dtype` = out's
+        err = sfa::launch_bsr_tc_wide(p, plan->d_work, plan->ntiles, ew, plan->o_dtype, s);
+    } else if (plan->tc) {
         int* ew = sfa::device_error_word();
         if (!ew) return SFA_ERR_CUDA;
         // per-element mask: 64-key blocks (measured faster); otherwise 128-key steps
@@ -263,6 +283,32 @@ sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v,
         err = sfa::launch_bsr_generic(p, plan->dtype, s);
     }
     return err == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+sfa_status bsr_run(bsr_plan_t plan, const void* q, const void* k, const void* v, void* out,
+                   float* lse, sfa_stream_t stream) {
+    return bsr_run_scaled(plan, q, k, v, nullptr, nullptr, nullptr, out, lse, stream);
+}
+
+sfa_status bsr_plan_set_data_types(bsr_plan_t plan, sfa_dtype q_dtype, sfa_dtype kv_dtype,
+                                   sfa_dtype o_dtype) {
+    auto known = [](int t) { return t >= SFA_DTYPE_F16 && t <= SFA_DTYPE_E5M2; };
+    if (!plan || !known(q_dtype) || !known(kv_dtype) || !known(o_dtype))
+        return SFA_ERR_INVALID_ARG;
+    const bool wide16 = o_dtype == SFA_DTYPE_F16 || o_dtype == SFA_DTYPE_BF16;
+    if (q_dtype == kv_dtype && kv_dtype == o_dtype && wide16) {
+        if (o_dtype != plan->dtype) return SFA_ERR_UNSUPPORTED;   // the plan's own kernels
+    } else {
+        // FP8: q and k / v of one 8-bit format, 16-bit out, on the 128-key
+        // tensor-core kernel (head_dim 128, plain or causal blocks)
+        const bool f8 = kv_dtype == SFA_DTYPE_E4M3 || kv_dtype == SFA_DTYPE_E5M2;
+        if (!f8 || q_dtype != kv_dtype || !wide16) return SFA_ERR_UNSUPPORTED;
+        if (!plan->tc || plan->d != 128 || plan->mask_mode == 2) return SFA_ERR_UNSUPPORTED;
+    }
+    plan->q_dtype = q_dtype;
+    plan->kv_dtype = kv_dtype;
+    plan->o_dtype = o_dtype;
+    return SFA_OK;
 }
 
 sfa_status bsr_plan_set_logits_soft_cap(bsr_plan_t plan, float logits_soft_cap) {

@@ -456,6 +456,34 @@ bool make_map_hnd(CUtensorMap* map, const void* base, bool bf16, int dim, int ro
     return r == CUDA_SUCCESS;
 }
 
+// 8-bit elements: 3-D maps as above, box 128 elements (128 bytes) wide.
+bool make_map8(CUtensorMap* map, const void* base, int dim, int heads, int rows, int hb, int rb) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)rows};
+    const cuuint64_t gstride[2] = {(cuuint64_t)dim, (cuuint64_t)dim * heads};
+    const cuuint32_t box[3] = {128, (cuuint32_t)hb, (cuuint32_t)rb};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstride,
+                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_map8_hnd(CUtensorMap* map, const void* base, int dim, int rows, int heads, int rb,
+                   int hb) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)rows, (cuuint64_t)heads};
+    const cuuint64_t gstride[2] = {(cuuint64_t)dim, (cuuint64_t)dim * rows};
+    const cuuint32_t box[3] = {128, (cuuint32_t)rb, (cuuint32_t)hb};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstride,
+                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 template <class E, int D, bool CAP>

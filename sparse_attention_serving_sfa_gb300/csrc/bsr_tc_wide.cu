@@ -25,6 +25,16 @@
 //     high part plus the 16-bit rounding of the remainder, stored over S,
 //     keys 64..127 first (still in registers from the max pass).
 // TMEM per tile: S / P in columns [0, 128), O in [128, 128 + D).
+//
+// FP8 instantiations (F8 = 1: E4M3, 2: E5M2; plan() q_data_type /
+// kv_data_type, run() scale_q / scale_k / scale_v of "flashinfer.sparse"):
+// q, k and v hold 8-bit codes, both contractions run as
+// tcgen05.mma.kind::f8f6f4 (32 keys or dims per instruction), the
+// dequantisation scales scale_q[h] * scale_k[g] multiply each row's scores and
+// scale_v[g] its output.  P = exp2(s - m + 8) (kept below the format's largest
+// value by rescaling O whenever the running max grows by more than 0.5) goes
+// to the tensor core in V's format as a high part plus the rounding of the
+// remainder, four keys per TMEM column; out is fp16 or bf16.
 #include <cudaTypedefs.h>
 
 #include <type_traits>
@@ -48,10 +58,11 @@ constexpr int kTileCols = 256;      // TMEM columns per M-tile
 constexpr int kOCol = 128;          // O after the 128 S / P columns
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
-template <int D>
+template <int D, int EB>                                  // EB: bytes per element
 struct WideSmem {
-    static constexpr int panels = D / 64;
-    static constexpr int qTile = kTileM * D * 2;          // panels x 128 rows x 128 B
+    static constexpr int rowBytes = D * EB;
+    static constexpr int panels = rowBytes / 128;
+    static constexpr int qTile = kTileM * rowBytes;       // panels x 128 rows x 128 B
     static constexpr int kPanel = kStep * 128;            // 128 keys x 128 B
     static constexpr int kvHalf = kBlk * 128;             // one block's rows of a panel
     static constexpr int kvTile = panels * kPanel;        // K (or V) of one step
@@ -100,11 +111,28 @@ struct WideParams {
     int causal;             // mode 3: bottom-right causal on top of the windows
     float capl2, inv_capl2; // logits soft cap in log2 units (CAP instantiations)
     int kv_hnd;             // modes 0 / 1: K / V maps over (Hkv, N, d)
+    // FP8 instantiations: per-head dequantisation scales (NULL = 1)
+    const float* scale_q;   // [Hq]
+    const float* scale_k;   // [Hkv]
+    const float* scale_v;   // [Hkv]
 };
 
 // Keys j <= lim allowed among the 64 of a block (lim relative to its first key).
 __device__ __forceinline__ uint64_t causal_bits64(int64_t lim) {
     return lim < 0 ? 0ull : (lim >= 63 ? ~0ull : ((2ull << lim) - 1ull));
+}
+
+// 16 columns from the even (ODD = 0) or odd (ODD = 1) entries of r[0..32).
+template <int ODD>
+__device__ __forceinline__ void tmem_st16_strided(uint32_t taddr, const uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0 + ODD]), "r"(r[2 + ODD]), "r"(r[4 + ODD]), "r"(r[6 + ODD]), "r"(r[8 + ODD]),
+        "r"(r[10 + ODD]), "r"(r[12 + ODD]), "r"(r[14 + ODD]), "r"(r[16 + ODD]), "r"(r[18 + ODD]),
+        "r"(r[20 + ODD]), "r"(r[22 + ODD]), "r"(r[24 + ODD]), "r"(r[26 + ODD]), "r"(r[28 + ODD]),
+        "r"(r[30 + ODD])
+        : "memory");
 }
 
 // 32 columns from the even (ODD = 0) or odd (ODD = 1) entries of r[64].
@@ -134,14 +162,35 @@ struct WideSchedule {
     static constexpr bool tile_skip = MODE != 0;
 };
 
-template <class E, int D, int MODE, bool CAP>
+template <class E, int D, int MODE, bool CAP, int F8>
 __global__ void __launch_bounds__(kThreads, 1)
 bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const WideParams p) {
-    using L = WideSmem<D>;
+    // E: element type of q / k / v / out, or of out alone with F8
+    constexpr int EB = F8 ? 1 : 2;
+    static_assert(!F8 || D == 128, "8-bit rows of 128 bytes");
+    using L = WideSmem<D, EB>;
     constexpr bool kBf16 = std::is_same<E, BF16>::value;
-    constexpr uint32_t kIdescQK = idesc_f16(kTileM, kStep, kBf16, false, false);
-    constexpr uint32_t kIdescPV = idesc_f16(kTileM, D, kBf16, false, true);
+    constexpr bool kE5 = F8 == 2;
+    constexpr uint32_t kIdescQK = F8 ? idesc_f8(kTileM, kStep, kE5, false, false)
+                                     : idesc_f16(kTileM, kStep, kBf16, false, false);
+    constexpr uint32_t kIdescPV = F8 ? idesc_f8(kTileM, D, kE5, false, true)
+                                     : idesc_f16(kTileM, D, kBf16, false, true);
+    constexpr int KK = 32 / EB;              // keys (or dims) per MMA instruction
+    constexpr int KQ = kBlk / KK;            // instructions per 64-key half
+    constexpr int PC = 16 * EB;              // P columns of one part (high or low) of a half
+    constexpr int kCol0 = 128 / EB;          // TMA coordinate step between 128-byte panels
+    // log2 of the factor P carries (8-bit P is kept in the format's normal range)
+    constexpr float kPShift = F8 ? 8.f : 0.f;
+    constexpr float kThresh = F8 ? 0.5f : kRescaleThreshold;
+    auto mma_ss = [](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (F8) tc_mma_f8(d, a, b, id, acc);
+        else tc_mma_f16(d, a, b, id, acc);
+    };
+    auto mma_ts = [](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (F8) tc_mma_f8_ts(d, a, b, id, acc);
+        else tc_mma_f16_ts(d, a, b, id, acc);
+    };
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -200,11 +249,11 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             for (int t = 0; t < ntl; ++t)
                 for (int pn = 0; pn < L::panels; ++pn) {
                     if constexpr (MODE == 3)
-                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
-                                    item.row0 + t * p.TR, item.kvh * p.G, bar(B_Q));
+                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq,
+                                    pn * kCol0, item.row0 + t * p.TR, item.kvh * p.G, bar(B_Q));
                     else
-                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq, pn * 64,
-                                    item.kvh * p.G, item.row0 + t * p.TR, bar(B_Q));
+                        tma_load_3d(sbase + L::q + t * L::qTile + pn * (kTileM * 128), &mq,
+                                    pn * kCol0, item.kvh * p.G, item.row0 + t * p.TR, bar(B_Q));
                 }
             // step st: blocks 2 st and 2 st + 1; a missing second block reads
             // rows N.. (all outside the tensor: zeros, full byte count)
@@ -219,11 +268,11 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                         const uint32_t kd = dst + pn * L::kPanel + h * L::kvHalf;
                         const uint32_t vd = kd + L::kvTile;
                         if (MODE == 3 || p.kv_hnd) {
-                            tma_load_3d(kd, &mk, pn * 64, col, item.kvh, bar(B_KV_FULL + s));
-                            tma_load_3d(vd, &mv, pn * 64, col, item.kvh, bar(B_KV_FULL + s));
+                            tma_load_3d(kd, &mk, pn * kCol0, col, item.kvh, bar(B_KV_FULL + s));
+                            tma_load_3d(vd, &mv, pn * kCol0, col, item.kvh, bar(B_KV_FULL + s));
                         } else {
-                            tma_load_3d(kd, &mk, pn * 64, item.kvh, col, bar(B_KV_FULL + s));
-                            tma_load_3d(vd, &mv, pn * 64, item.kvh, col, bar(B_KV_FULL + s));
+                            tma_load_3d(kd, &mk, pn * kCol0, item.kvh, col, bar(B_KV_FULL + s));
+                            tma_load_3d(vd, &mv, pn * kCol0, item.kvh, col, bar(B_KV_FULL + s));
                         }
                     }
                 }
@@ -240,13 +289,14 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 const uint32_t kbase = sbase + L::kv + s * 2 * L::kvTile;
                 // S_t = Q_t K^T, 128 keys
                 for (int t = 0; t < ntl; ++t) {
+                    // K steps of 32 bytes: 16 dims (16-bit) or 32 dims (8-bit)
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
+                    for (int kk = 0; kk < L::rowBytes / 32; ++kk) {
                         const uint32_t off = (kk & 3) * 32;
                         const uint64_t ad = sdesc_sw128(
                             sbase + L::q + t * L::qTile + (kk >> 2) * (kTileM * 128) + off, 16, 1024);
                         const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * L::kPanel + off, 16, 1024);
-                        tc_mma_f16(tmem + t * kTileCols, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                        mma_ss(tmem + t * kTileCols, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(bar(B_S_FULL + t));
                 }
@@ -258,8 +308,8 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     load_step(st + 1);
                     loaded = st + 1;
                 }
-                // O_t += P_t V over keys 64 h .. 64 h + 63: P from TMEM (16 keys
-                // = 8 columns per MMA; high parts at 64 h, remainders at 64 h + 32).
+                // O_t += P_t V over keys 64 h .. 64 h + 63: P from TMEM (KK keys
+                // = 8 columns per MMA; high parts at 64 h, remainders at 64 h + PC).
                 // The softmax writes keys 64..127 first, so their P.V runs while
                 // it works on keys 0..63; a step with one block has no P.V for
                 // the second half.
@@ -267,13 +317,12 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 auto pv_half = [&](int t, int h, bool first) {
                     for (int part = 0; part < 2; ++part)
 #pragma unroll
-                        for (int kq = 0; kq < 4; ++kq) {
-                            const int kk = 4 * h + kq;
-                            const uint32_t a = tmem + t * kTileCols + 64 * h + 32 * part + 8 * kq;
-                            const uint64_t bd =
-                                sdesc_sw128(kbase + L::kvTile + kk * 16 * 128, L::kPanel, 1024);
+                        for (int kq = 0; kq < KQ; ++kq) {
+                            const uint32_t a = tmem + t * kTileCols + 64 * h + PC * part + 8 * kq;
+                            const uint64_t bd = sdesc_sw128(
+                                kbase + L::kvTile + (64 * h + KK * kq) * 128, L::kPanel, 1024);
                             const uint32_t acc = (first && part == 0 && kq == 0) ? 0u : 1u;
-                            tc_mma_f16_ts(tmem + t * kTileCols + kOCol, a, bd, kIdescPV, acc);
+                            mma_ts(tmem + t * kTileCols + kOCol, a, bd, kIdescPV, acc);
                         }
                 };
                 if constexpr (WideSchedule<MODE>::split_p) {
@@ -301,13 +350,13 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                         tc_fence_after();
                         for (int part = 0; part < 2; ++part)
 #pragma unroll
-                            for (int kk = 0; kk < kStep / 16; ++kk) {
-                                const uint32_t a = tmem + t * kTileCols + 64 * (kk >> 2) + 32 * part +
-                                                   8 * (kk & 3);
+                            for (int kk = 0; kk < kStep / KK; ++kk) {
+                                const uint32_t a = tmem + t * kTileCols + 64 * (kk / KQ) + PC * part +
+                                                   8 * (kk % KQ);
                                 const uint64_t bd =
-                                    sdesc_sw128(kbase + L::kvTile + kk * 16 * 128, L::kPanel, 1024);
+                                    sdesc_sw128(kbase + L::kvTile + kk * KK * 128, L::kPanel, 1024);
                                 const uint32_t acc = (st > 0 || part > 0 || kk > 0) ? 1u : 0u;
-                                tc_mma_f16_ts(tmem + t * kTileCols + kOCol, a, bd, kIdescPV, acc);
+                                mma_ts(tmem + t * kTileCols + kOCol, a, bd, kIdescPV, acc);
                             }
                         if (st == ns - 1) tc_commit(bar(B_O_DONE + t));
                     }
@@ -340,6 +389,13 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         };
         auto my_h = [&]() { return MODE == 3 ? item.kvh * p.G + r / p.TR : item.kvh * p.G + r % p.G; };
         auto my_valid = [&]() { return my_i() < row_end && r / p.G < p.TR; };
+        // multiplier of this row's raw scores (log2 units): the softmax scale,
+        // times the row's dequantisation scales in the FP8 instantiations
+        float rs = p.scale_log2;
+        if constexpr (F8 != 0) {
+            if (p.scale_q) rs *= p.scale_q[my_h()];
+            if (p.scale_k) rs *= p.scale_k[item.kvh];
+        }
         // allowed keys of block b for this row (bit j = key j of the block)
         auto allowed = [&](int b) -> uint64_t {
             if constexpr (MODE == 1) {
@@ -367,10 +423,38 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         // half's S columns; returns the half's sum of P
         auto make_p = [&](int h, uint64_t am) -> float {
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (F8 != 0) {
+                // keys 4k .. 4k + 3 -> high parts in sv[2k], remainders in
+                // sv[2k + 1] (entries already read), four 8-bit P per word
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    float pv[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float u = __uint_as_float(sv[4 * k + j]) * rs;
+                        if constexpr (CAP) u = soft_cap_log2(u, p.capl2, p.inv_capl2);
+                        float pp = fast_exp2(u - m_used + kPShift);
+                        if constexpr (MODE != 0)
+                            if (!((am >> (4 * k + j)) & 1ull)) pp = 0.f;
+                        pv[j] = pp;
+                    }
+                    ls[k & 3] += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+                    const uint32_t h01 = f8_pack2<kE5>(pv[0], pv[1]);
+                    const uint32_t h23 = f8_pack2<kE5>(pv[2], pv[3]);
+                    const float2 b01 = f8_unpack2<kE5>(h01), b23 = f8_unpack2<kE5>(h23);
+                    const uint32_t l01 = f8_pack2<kE5>(pv[0] - b01.x, pv[1] - b01.y);
+                    const uint32_t l23 = f8_pack2<kE5>(pv[2] - b23.x, pv[3] - b23.y);
+                    sv[2 * k] = h01 | (h23 << 16);
+                    sv[2 * k + 1] = l01 | (l23 << 16);
+                }
+                tmem_st16_strided<0>(lane_base + 64 * h, sv);
+                tmem_st16_strided<1>(lane_base + 64 * h + 16, sv);
+                return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            }
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                float u0 = __uint_as_float(sv[2 * k]) * p.scale_log2;
-                float u1 = __uint_as_float(sv[2 * k + 1]) * p.scale_log2;
+                float u0 = __uint_as_float(sv[2 * k]) * rs;
+                float u1 = __uint_as_float(sv[2 * k + 1]) * rs;
                 if constexpr (CAP) {
                     u0 = soft_cap_log2(u0, p.capl2, p.inv_capl2);
                     u1 = soft_cap_log2(u1, p.capl2, p.inv_capl2);
@@ -419,12 +503,12 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
             }
             // the scale is positive and rounding monotonic: max of scaled = scaled max
-            float bmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            float bmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * rs;
             // the soft cap is increasing too: capped max = max of capped
             if constexpr (CAP)
                 if (bmax != -INFINITY) bmax = soft_cap_log2(bmax, p.capl2, p.inv_capl2);
             const float m_new = fmaxf(m_used, bmax);
-            const bool need = m_new > m_used + kRescaleThreshold;
+            const bool need = m_new > m_used + kThresh;
             // P.V of step st - 1 ran on the tensor core before this step's
             // Q.K^T, whose completion this thread waited for: O is settled
             if (st > 0 && __any_sync(0xffffffffu, need)) {
@@ -478,7 +562,10 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc_fence_after();
         }
         const bool empty = !(l > 0.f);
-        const float inv = empty ? 0.f : 1.f / l;
+        float vscale = 1.f;
+        if constexpr (F8 != 0)
+            if (p.scale_v) vscale = p.scale_v[item.kvh];
+        const float inv = empty ? 0.f : vscale / l;
         using T = typename E::T;
         const int64_t orow_idx = MODE == 3 ? (int64_t)h * p.M + i : (int64_t)i * p.Hq + h;
         T* orow = static_cast<T*>(p.out) + orow_idx * D;
@@ -502,7 +589,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
         }
         if (valid_row && p.lse)
-            p.lse[orow_idx] = empty ? -INFINITY : (m_used + __log2f(l)) * kLn2;
+            p.lse[orow_idx] = empty ? -INFINITY : (m_used + __log2f(l) - kPShift) * kLn2;
     }
     tc_fence_before();
     __syncthreads();
@@ -512,12 +599,21 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     }
 }
 
-template <class E, int D, int MODE, bool CAP>
+template <class E, int D, int MODE, bool CAP, int F8>
 cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems, cudaStream_t stream) {
-    using L = WideSmem<D>;
+    using L = WideSmem<D, F8 ? 1 : 2>;
     const bool bf16 = std::is_same<E, BF16>::value;
     CUtensorMap mq, mk, mv;
-    if (MODE == 3) {
+    if (F8 != 0) {
+        // 8-bit rows of 128 bytes: q NHD, k / v NHD or HND
+        if (MODE == 3 || !make_map8(&mq, bp.q, D, bp.Hq, bp.M, wp.G, wp.TR))
+            return cudaErrorInvalidValue;
+        if (bp.kv_hnd ? (!make_map8_hnd(&mk, bp.k, D, bp.N, bp.Hkv, kBlk, 1) ||
+                         !make_map8_hnd(&mv, bp.v, D, bp.N, bp.Hkv, kBlk, 1))
+                      : (!make_map8(&mk, bp.k, D, bp.Hkv, bp.N, 1, kBlk) ||
+                         !make_map8(&mv, bp.v, D, bp.Hkv, bp.N, 1, kBlk)))
+            return cudaErrorInvalidValue;
+    } else if (MODE == 3) {
         if (!make_map_hnd(&mq, bp.q, bf16, D, bp.M, bp.Hq, wp.TR, wp.G) ||
             !make_map_hnd(&mk, bp.k, bf16, D, bp.N, bp.Hkv, kBlk, 1) ||
             !make_map_hnd(&mv, bp.v, bf16, D, bp.N, bp.Hkv, kBlk, 1))
@@ -530,7 +626,7 @@ cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems,
                             !make_map(&mv, bp.v, bf16, D, bp.Hkv, bp.N, 1, kBlk))) {
         return cudaErrorInvalidValue;
     }
-    auto kern = bsr_tc_wide_kernel<E, D, MODE, CAP>;
+    auto kern = bsr_tc_wide_kernel<E, D, MODE, CAP, F8>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
     if (err != cudaSuccess) return err;
     kern<<<nitems, kThreads, L::alloc, stream>>>(mq, mk, mv, wp);
@@ -556,6 +652,9 @@ cudaError_t launch_bsr_tc_wide(const BsrParams& bp, const void* items, int nitem
     wp.C = bp.mask_mode == 3 ? kBlk : bp.C;
     wp.causal = bp.causal;
     wp.kv_hnd = bp.mask_mode == 3 ? 1 : bp.kv_hnd;
+    wp.scale_q = bp.scale_q;
+    wp.scale_k = bp.scale_k;
+    wp.scale_v = bp.scale_v;
     wp.Hq = bp.Hq;
     wp.G = bp.Hq / bp.Hkv;
     wp.TR = kTileM / wp.G;
@@ -564,14 +663,30 @@ cudaError_t launch_bsr_tc_wide(const BsrParams& bp, const void* items, int nitem
     wp.capl2 = cap ? bp.softcap_log2 : 0.f;
     wp.inv_capl2 = cap ? 1.f / bp.softcap_log2 : 0.f;
     const bool bf16 = dtype == SFA_DTYPE_BF16;
+    if (bp.f8) {
+        // FP8 q / k / v (head_dim 128, plain or causal blocks, no soft cap);
+        // `dtype` is the output's
+        if (bp.d != 128 || cap || (bp.mask_mode != 0 && bp.mask_mode != 1))
+            return cudaErrorInvalidValue;
+#define SFA_BSR_WIDE_F8(MODE_, F8_)                                                              \
+    if (bp.mask_mode == MODE_ && bp.f8 == F8_)                                                   \
+        return bf16 ? launch_wide_t<BF16, 128, MODE_, false, F8_>(bp, wp, nitems, stream)       \
+                    : launch_wide_t<F16, 128, MODE_, false, F8_>(bp, wp, nitems, stream);
+        SFA_BSR_WIDE_F8(0, 1)
+        SFA_BSR_WIDE_F8(0, 2)
+        SFA_BSR_WIDE_F8(1, 1)
+        SFA_BSR_WIDE_F8(1, 2)
+#undef SFA_BSR_WIDE_F8
+        return cudaErrorInvalidValue;
+    }
 #define SFA_BSR_WIDE_MODE_CAP(MODE_, CAP_)                                                       \
     if (bp.mask_mode == MODE_ && cap == CAP_) {                                                  \
         if (bp.d == 128)                                                                         \
-            return bf16 ? launch_wide_t<BF16, 128, MODE_, CAP_>(bp, wp, nitems, stream)          \
-                        : launch_wide_t<F16, 128, MODE_, CAP_>(bp, wp, nitems, stream);          \
+            return bf16 ? launch_wide_t<BF16, 128, MODE_, CAP_, 0>(bp, wp, nitems, stream)          \
+                        : launch_wide_t<F16, 128, MODE_, CAP_, 0>(bp, wp, nitems, stream);          \
         if (bp.d == 64)                                                                          \
-            return bf16 ? launch_wide_t<BF16, 64, MODE_, CAP_>(bp, wp, nitems, stream)           \
-                        : launch_wide_t<F16, 64, MODE_, CAP_>(bp, wp, nitems, stream);           \
+            return bf16 ? launch_wide_t<BF16, 64, MODE_, CAP_, 0>(bp, wp, nitems, stream)           \
+                        : launch_wide_t<F16, 64, MODE_, CAP_, 0>(bp, wp, nitems, stream);           \
     }
 #define SFA_BSR_WIDE_MODE(MODE_) SFA_BSR_WIDE_MODE_CAP(MODE_, false) SFA_BSR_WIDE_MODE_CAP(MODE_, true)
     SFA_BSR_WIDE_MODE(0)

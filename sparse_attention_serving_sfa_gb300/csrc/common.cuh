@@ -44,6 +44,32 @@ struct BF16 {
     }
 };
 
+// 8-bit floating point (E4M3 when E5 is false, else E5M2), two elements at
+// a time: the first in the low byte.  Packing rounds to nearest even and
+// saturates to the largest finite value; unpacking is exact (every E4M3 and
+// E5M2 value is an fp16 value).
+template <bool E5>
+__device__ __forceinline__ uint32_t f8_pack2(float first, float second) {
+    uint16_t r;
+    if constexpr (E5)
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
+    else
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
+    return r;
+}
+
+template <bool E5>
+__device__ __forceinline__ float2 f8_unpack2(uint32_t two) {
+    const uint16_t in = (uint16_t)two;
+    uint32_t h2;
+    if constexpr (E5)
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(in));
+    else
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    __half2 h = *reinterpret_cast<__half2*>(&h2);
+    return __half22float2(h);
+}
+
 // ---------------------------------------------------------------------------
 // Asynchronous global -> shared copies (16 bytes per thread, L2 only).
 

@@ -114,6 +114,12 @@ struct BsrParams {
     // 1: k and v are (Hkv, N, d) (HND) instead of (N, Hkv, d) (NHD); modes
     // 0-2 only (mode 3 is HND throughout)
     int kv_hnd;
+    // 8-bit q / k / v: 0 no (16-bit), 1 E4M3, 2 E5M2 (the launch's dtype is
+    // then the output's); per-head dequantisation scales, NULL = 1
+    int f8;
+    const float* scale_q;   // [Hq]
+    const float* scale_k;   // [Hkv]
+    const float* scale_v;   // [Hkv]
 };
 
 cudaError_t launch_bsr_generic(const BsrParams& p, sfa_dtype dtype, cudaStream_t stream);
@@ -140,6 +146,10 @@ bool make_map(CUtensorMap* map, const void* base, bool bf16, int dim, int heads,
               int rb);
 bool make_map_hnd(CUtensorMap* map, const void* base, bool bf16, int dim, int rows, int heads,
                   int rb, int hb);
+// The same over 8-bit elements, box 128 elements (128 bytes) wide.
+bool make_map8(CUtensorMap* map, const void* base, int dim, int heads, int rows, int hb, int rb);
+bool make_map8_hnd(CUtensorMap* map, const void* base, int dim, int rows, int heads, int rb,
+                   int hb);
 
 // Launches `kern` with programmatic dependent launch allowed: the grid may be
 // scheduled while the previous kernel in the stream finishes; the kernel must

@@ -58,6 +58,15 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a
            ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4 with 8-bit A and B
+// (fp32 accumulate): the same fields as kind::f16, A / B formats 0 = E4M3,
+// 1 = E5M2; one instruction covers K = 32 elements (32 bytes).
+__host__ __device__ constexpr uint32_t idesc_f8(int M, int N, bool e5m2, bool a_mn, bool b_mn) {
+    return (1u << 4) | ((e5m2 ? 1u : 0u) << 7) | ((e5m2 ? 1u : 0u) << 10) |
+           ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
 // ---------------------------------------------------------------------------
 // Tensor memory
 
@@ -146,6 +155,27 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
     asm volatile(
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D(tmem) (+)= A(smem desc) * B(smem desc) with 8-bit A and B (K = 32).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Same with A (M rows x 32 8-bit K elements) read from tensor memory: lane m
+// holds row m, four K elements per 32-bit column (8 columns per K step).
+__device__ __forceinline__ void tc_mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

@@ -68,6 +68,33 @@ def normal(seed: int, stream: int, shape, dtype: str) -> torch.Tensor:
     return torch.from_numpy(buf).reshape(shape).to(_TORCH_DTYPE[dtype])
 
 
+def normal_f32(seed: int, stream: int, shape) -> torch.Tensor:
+    """N(0,1) float32 samples of `shape` (not rounded)."""
+    n = int(np.prod(shape))
+    buf = np.empty(n, dtype=np.float32)
+    if n:
+        _load().syn_normal_f32(seed, stream, n, buf.ctypes.data)
+    return torch.from_numpy(buf).reshape(shape)
+
+
+FP8_TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
+
+
+def quantize_per_head(x: torch.Tensor, fmt: str, head_axis: int):
+    """FP8 codes of float32 `x` with one scale per index of `head_axis`:
+    scale = max |x| over the head / the format's largest finite value, codes
+    = x / scale converted (nearest) by torch.  Returns (float8 tensor, float32
+    scales)."""
+    dims = [a for a in range(x.dim()) if a != head_axis]
+    amax = x.abs().amax(dim=dims).clamp_min(1e-12)
+    scale = (amax / FP8_MAX[fmt]).to(torch.float32)
+    shape = [1] * x.dim()
+    shape[head_axis] = -1
+    codes = (x / scale.view(shape)).to(FP8_TORCH[fmt])
+    return codes, scale
+
+
 def index_uniform(seed: int, rows: int, rng: int, topk: int, sorted_: bool) -> np.ndarray:
     """rows x topk distinct draws from [0, rng), random order or ascending."""
     out = np.empty((rows, topk), dtype=np.int32)
@@ -153,6 +180,7 @@ class BsrCase:
     seed: int = 1238
     causal: bool = False            # bottom-right causal (only without a mask)
     mask_keep: float = 0.0          # > 0: per-element block mask, each element kept with this p
+    fp8: str = ""                   # "e4m3" / "e5m2": q, k, v in that format (dtype = out's)
 
     @property
     def MB(self) -> int:
@@ -190,7 +218,11 @@ CALL_EXAMPLE = SfaCase("call_example", B=2, S1=1024, S2=8192, N1=32, N2=8, Dk=12
 SFA_WORKLOADS = {c.name: c for c in (TINY, GQA_DECODE, MLA_DECODE, MLA_MTP, PREFILL, CALL_EXAMPLE)}
 BSR_CAUSAL = BSR.replace(name="bsr_causal", causal=True)
 BSR_MASK = BSR.replace(name="bsr_mask", mask_keep=0.5)
-BSR_WORKLOADS = {c.name: c for c in (BSR, BSR_CAUSAL, BSR_MASK)}
+# The block-sparse workload with q, k, v in E4M3 and per-head scales
+# (BlockSparseAttentionWrapper plan() kv_data_type, run() scale_q / k / v),
+# fp16 out.
+BSR_FP8 = BSR.replace(name="bsr_fp8", fp8="e4m3")
+BSR_WORKLOADS = {c.name: c for c in (BSR, BSR_CAUSAL, BSR_MASK, BSR_FP8)}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -260,14 +292,23 @@ def bsr_mask(seed: int, nnz: int, R: int, C: int, keep: float) -> np.ndarray:
 
 def make_bsr_inputs(case: BsrCase) -> dict:
     """CPU tensors q (M,Hq,d), k/v (N,Hkv,d) in NHD order, int32 indptr/indices,
-    and (mask_keep > 0) the (nnz, R, C) bool mask."""
+    and (mask_keep > 0) the (nnz, R, C) bool mask.  With case.fp8, q / k / v
+    are float8 codes of the same normals quantised per head, and scale_q
+    (Hq) / scale_k / scale_v (Hkv) float32 hold their scales."""
     c = case
-    q = normal(c.seed, 0, (c.M, c.Hq, c.d), c.dtype)
-    k = normal(c.seed, 1, (c.N, c.Hkv, c.d), c.dtype)
-    v = normal(c.seed, 2, (c.N, c.Hkv, c.d), c.dtype)
     indptr, indices = bsr_pattern(c.seed + 1, c.MB, c.NB, c.p)
+    if c.fp8:
+        q, sq = quantize_per_head(normal_f32(c.seed, 0, (c.M, c.Hq, c.d)), c.fp8, 1)
+        k, sk = quantize_per_head(normal_f32(c.seed, 1, (c.N, c.Hkv, c.d)), c.fp8, 1)
+        v, sv = quantize_per_head(normal_f32(c.seed, 2, (c.N, c.Hkv, c.d)), c.fp8, 1)
+        scales = {"scale_q": sq, "scale_k": sk, "scale_v": sv}
+    else:
+        q = normal(c.seed, 0, (c.M, c.Hq, c.d), c.dtype)
+        k = normal(c.seed, 1, (c.N, c.Hkv, c.d), c.dtype)
+        v = normal(c.seed, 2, (c.N, c.Hkv, c.d), c.dtype)
+        scales = {"scale_q": None, "scale_k": None, "scale_v": None}
     out = {"q": q, "k": k, "v": v, "indptr": torch.from_numpy(indptr),
-           "indices": torch.from_numpy(indices.copy()), "mask": None}
+           "indices": torch.from_numpy(indices.copy()), "mask": None, **scales}
     if c.mask_keep > 0:
         out["mask"] = bsr_mask(c.seed + 2, int(indptr[-1]), c.R, c.C, c.mask_keep)
     return out
