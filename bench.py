@@ -67,6 +67,8 @@ def parse(argv=None):
                          "list (auto = all with the default headline, none otherwise)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-probe", action="store_true",
+                    help="skip the gather-only probe of the top-K workloads")
     ap.add_argument("--eager", action="store_true",
                     help="time eager calls instead of a captured CUDA graph")
     ap.add_argument("--replicas", type=int, default=0,
@@ -386,6 +388,10 @@ def run_sfa(name, args, world, rank, cpu_target_s):
                                      world)
     clocks = sampler.stop()
 
+    probe = None
+    if not args.no_probe:
+        probe = gather_probe(case, replicas, reps, args, world, counts, ms)
+
     e2e = None
     if not args.no_e2e:
         # the KV cache stays resident (as in serving); q and the indices come
@@ -433,6 +439,7 @@ def run_sfa(name, args, world, rank, cpu_target_s):
            "tensor_frac": tflops / peaks["bf16_tflops"],
            "roofline_time_frac": max(t_hbm, t_tc) / (ms * 1e-3),
            "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+           "gather_probe": probe,
            "work": {"flops": counts["flops"], "gathered_bytes": counts["gathered_bytes"],
                     "unmasked_slots": counts["unmasked_slots"]}}
     if rank == 0 and not args.no_cpu_baseline:
@@ -440,6 +447,43 @@ def run_sfa(name, args, world, rank, cpu_target_s):
     del replicas, out, lse, ws
     torch.cuda.empty_cache()
     return rec
+
+
+def gather_probe(case, replicas, reps, args, world, counts, kernel_ms):
+    """The call's K/V row gather alone (sfa_gather_probe: no arithmetic),
+    timed like the call on the same replicas: the gather ceiling of the
+    workload.  When no two index lists share a KV head's rows (S1 = 1), the
+    same byte count read as rows 0 .. topK - 1 of every list (sequential
+    rows) is timed too."""
+    import sparse_attention_serving_sfa_gb300 as sfa
+    peaks, _ = load_peaks()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    sink = torch.empty(2 * sms * 4 + 64, dtype=torch.uint8, device="cuda")
+
+    def timed(idx_of):
+        def step(i):
+            d = replicas[i % reps]
+            sfa.sfa_gather_probe(d["k"], d["v"], idx_of(d), case.B, case.S1, case.S2, case.N2,
+                                 case.Dk, case.Dv, case.topK, case.layout, sink,
+                                 torch.cuda.current_stream())
+        for i in range(max(args.warmup, 3)):
+            step(i)
+        torch.cuda.synchronize()
+        ms, _, _ = device_time(step, args.steps, args.eager, world)
+        gbs = counts["gathered_bytes"] / (ms * 1e-3) / 1e9
+        return {"ms_per_step": ms, "gbs": gbs, "frac_of_copy_peak": gbs / peaks["hbm_gbs"]}
+
+    out = {"what": "sfa_gather_probe: the same K/V rows read with coalesced 16-byte loads, no "
+                   "arithmetic",
+           "random_rows": timed(lambda d: d["idx"])}
+    # the kernel's gather rate as a fraction of the probe's (1.0 = the
+    # attention kernel is as fast as reading its rows alone)
+    out["kernel_frac_of_probe_rate"] = out["random_rows"]["ms_per_step"] / kernel_ms
+    if case.S1 == 1:
+        seq = torch.arange(case.topK, dtype=torch.int32, device="cuda").expand(
+            replicas[0]["idx"].shape).contiguous()
+        out["sequential_rows"] = timed(lambda d: seq)
+    return out
 
 
 def sfa_cpu_baseline(case, host, counts, target_s=10.0):
@@ -663,7 +707,7 @@ def run_ours(args, rank, world, local):
            "dtype": head["dtype"], "data": "synthetic (seeded generator, shapes of the workload)",
            "config": head["config"]}
     for key in ("us_per_call", "gathered_gbs", "tflops", "tensor_frac", "roofline_time_frac",
-                "roofline", "e2e", "gpu_launches", "cpu_baseline", "work"):
+                "roofline", "e2e", "gpu_launches", "cpu_baseline", "gather_probe", "work"):
         if key in head:
             res[key] = head[key]
     res["gpu_launches"] = head["gpu_launches"]

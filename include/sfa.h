@@ -158,6 +158,25 @@ const char* sfa_status_string(sfa_status status);
  * counterpart). */
 uint64_t sfa_kernel_launches(void);
 
+/*
+ * sfa_gather_probe -- measurement probe (no paper counterpart): reads every
+ * K row, and every V row unless v == k (the prefix view), that sfa_run with
+ * the same k, v, sparse_idx, sizes and layout gathers ("SparseFlashAttention
+ * 算子 API 描述", §2 具体子步骤, the sparse gather step), and does nothing
+ * else.  Its duration is the floor for any kernel that must fetch those
+ * bytes: the gather ceiling the attention kernels are measured against.
+ *   sink        device buffer of at least 2 * SM count * 4 bytes; it may
+ *               receive one word per CTA (a fold of the data read).
+ * The rows are read with 16-byte loads, the lanes of a warp covering a row's
+ * pieces (coalesced), many rows in flight per lane.
+ * Arguments otherwise as sfa_run (16-bit elements); out-of-range indices are
+ * skipped.  Errors: SFA_ERR_INVALID_ARG, SFA_ERR_WORKSPACE (sink too small),
+ * SFA_ERR_UNSUPPORTED (K + V bytes per slot above 1536), SFA_ERR_CUDA.
+ */
+sfa_status sfa_gather_probe(const void* k, const void* v, const int32_t* sparse_idx, int B,
+                            int S1, int S2, int N2, int Dk, int Dv, int topK, sfa_layout layout,
+                            void* sink, size_t sink_bytes, sfa_stream_t stream);
+
 /* Size of the device scratch array behind sfa_run_noalloc (8 MiB). */
 #define SFA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -35,7 +35,7 @@ EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
            "varbsr_plan", "varbsr_plan_int_workspace_size", "varbsr_plan_dims", "varbsr_run",
            "varbsr_plan_destroy", "bsr_plan_set_logits_soft_cap",
            "varbsr_plan_set_logits_soft_cap", "bsr_plan_set_kv_layout",
-           "bsr_plan_set_data_types", "bsr_run_scaled")
+           "bsr_plan_set_data_types", "bsr_run_scaled", "sfa_gather_probe")
 
 
 class SfaError(RuntimeError):
@@ -119,6 +119,8 @@ def load():
             lib.bsr_plan_set_data_types.restype = ci
             lib.bsr_run_scaled.argtypes = [vp] * 10
             lib.bsr_run_scaled.restype = ci
+            lib.sfa_gather_probe.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, sz, vp]
+            lib.sfa_gather_probe.restype = ci
             _lib = lib
     return _lib
 
@@ -198,6 +200,15 @@ def sfa_run_noalloc(q, k, v, sparse_idx, B, S1, S2, N1, N2, Dk, Dv, topK, scale,
 
 
 SFA_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def sfa_gather_probe(k, v, sparse_idx, B, S1, S2, N2, Dk, Dv, topK, layout, sink, stream=None):
+    """Forwards to sfa_gather_probe() (measurement only): the call's K/V row
+    gather alone.  sink: a device tensor of >= 2 * SM count * 4 bytes."""
+    _check(load().sfa_gather_probe(_ptr(k), _ptr(v), _ptr(sparse_idx), B, S1, S2, N2, Dk, Dv,
+                                   topK, _enum(layout, LAYOUTS), _ptr(sink),
+                                   sink.numel() * sink.element_size(), _stream(stream)),
+           "sfa_gather_probe")
 
 
 def sfa_workspace_size(B, S1, N1, N2, Dk, Dv, topK, num_splits=0) -> int:

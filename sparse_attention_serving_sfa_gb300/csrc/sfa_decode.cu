@@ -11,7 +11,8 @@
 //     (index list, 64-slot chunk) pairs, split into equal contiguous ranges
 //     (stream-K): every SM streams the same number of bytes, no tail waves;
 //   - two producer warps gather each chunk's K rows (and V rows, unless V is
-//     the key prefix view) plus the group's q rows with 16-byte cp.async, half
+//     the key prefix view), plus the group's q rows at the first chunk of an
+//     index list, with 16-byte cp.async, half
 //     a warp per 256-byte row (coalesced), into padded rows of a ring of
 //     shared-memory stages; completion is tracked by mbarriers
 //     (cp.async.mbarrier.arrive), indices are prefetched three chunks ahead,
@@ -273,8 +274,10 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
                         cp_async_16_zfill(st + L::kTile + j * L::vs + pc * 16, vrow + pc * 8, ok ? 16 : 0);
                 }
             }
-            // the group's q rows: piece e of G * Dk / 8
-            {
+            // the group's q rows (piece e of G * Dk / 8), only into the stage
+            // of an index list's first chunk in this range: the consumers
+            // read q from that stage alone
+            if (k.cc == 0 || c == c_begin) {
                 const T* qg = static_cast<const T*>(p.q) + uc.b * p.q_sb + uc.s1 * p.q_ss;
                 for (int e = pw * 32 + lane; e < G * (DK / 8); e += kProdThreads) {
                     const int h = e / (DK / 8), pc = e % (DK / 8);

@@ -231,6 +231,18 @@ def test_kv_layout_setter_rejects_bad_arguments(lib):
     # (making a plan uploads its work list)
 
 
+def test_gather_probe_rejects_bad_arguments(lib):
+    # host-side checks only (null pointers, sizes, alignment): no GPU needed
+    assert lib.sfa_gather_probe(None, FAKE, FAKE, 1, 1, 8, 1, 64, 64, 4, 0, FAKE, 4096,
+                                None) == sfa.SFA_ERR_INVALID_ARG
+    assert lib.sfa_gather_probe(FAKE, FAKE, FAKE, 1, 1, 8, 1, 64, 64, 9, 0, FAKE, 4096,
+                                None) == sfa.SFA_ERR_INVALID_ARG     # topK > S2
+    assert lib.sfa_gather_probe(FAKE, FAKE, FAKE, 1, 1, 8, 1, 64, 128, 4, 0, FAKE, 4096,
+                                None) == sfa.SFA_ERR_INVALID_ARG     # Dv > Dk
+    assert lib.sfa_gather_probe(FAKE, FAKE, FAKE + 8, 1, 1, 8, 1, 64, 64, 4, 0, FAKE, 4096,
+                                None) == sfa.SFA_ERR_INVALID_ARG     # unaligned indices
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(sfa, "LIB_PATH", str(tmp_path / "absent.so"))
     monkeypatch.setattr(sfa, "_lib", None)
