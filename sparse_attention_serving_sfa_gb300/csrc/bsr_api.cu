@@ -185,8 +185,8 @@ sfa_status bsr_plan_masked(const int32_t* indptr_host, const int32_t* indices_ho
     plan->tc = tc;
     plan->mask_mode = mask_mode;
 
-    // Work list, heaviest block rows first: generic row tiles of <= 64 rows
-    // (the kernel's grid.y spans the qo heads), or tensor-core items of
+    // Work list: generic row tiles of <= 64 rows (the kernel's grid.y spans
+    // the qo heads), heaviest block rows first, or tensor-core items of
     // (block row, first row, kv head).
     std::vector<sfa::BsrTile> tiles;
     tiles.reserve((size_t)ntiles);
@@ -201,7 +201,12 @@ sfa_status bsr_plan_masked(const int32_t* indptr_host, const int32_t* indices_ho
             }
         }
     }
+    // tensor-core items go kv head by kv head (the third int), so that the
+    // CTAs resident at one time share one head's K / V (a few MB, kept in L2
+    // while q and out stream through), heaviest block rows first within a
+    // head
     std::stable_sort(tiles.begin(), tiles.end(), [&](const sfa::BsrTile& a, const sfa::BsrTile& b) {
+        if (tc && a.nrows != b.nrows) return a.nrows < b.nrows;
         return (f_indptr[a.rb + 1] - f_indptr[a.rb]) > (f_indptr[b.rb + 1] - f_indptr[b.rb]);
     });
 

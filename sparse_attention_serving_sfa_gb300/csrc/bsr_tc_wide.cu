@@ -449,8 +449,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 }
                 tmem_st16_strided<0>(lane_base + 64 * h, sv);
                 tmem_st16_strided<1>(lane_base + 64 * h + 16, sv);
-                return (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            }
+            } else {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
                 float u0 = __uint_as_float(sv[2 * k]) * rs;
@@ -474,6 +473,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             tmem_st32_strided<0>(lane_base + 64 * h, sv);
             tmem_st32_strided<1>(lane_base + 64 * h + 32, sv);
+            }
             return (ls[0] + ls[1]) + (ls[2] + ls[3]);
         };
         // a second tile without rows of this item has no work

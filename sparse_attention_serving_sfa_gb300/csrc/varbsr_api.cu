@@ -135,7 +135,9 @@ sfa_status build(const uint8_t* mm, const int32_t* rs, const int32_t* cs, int MB
             r0 += s;
         }
     }
-    // heaviest items first
+    // kv head by kv head (CTAs resident at one time share one head's K / V,
+    // kept in L2 while q and out stream through), heaviest items first within
+    // a head
     const size_t ni = out.items.size() / 4;
     std::vector<int> order(ni);
     for (size_t i = 0; i < ni; ++i) order[i] = (int)i;
@@ -143,7 +145,11 @@ sfa_status build(const uint8_t* mm, const int32_t* rs, const int32_t* cs, int MB
         const int l = out.items[4 * (size_t)i];
         return out.lists[l + 1] - out.lists[l];
     };
-    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return weight(a) > weight(b); });
+    auto head = [&](int i) { return out.items[4 * (size_t)i + 2]; };
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        if (head(a) != head(b)) return head(a) < head(b);
+        return weight(a) > weight(b);
+    });
     std::vector<int32_t> sorted(out.items.size());
     for (size_t i = 0; i < ni; ++i)
         std::copy(out.items.begin() + 4 * (size_t)order[i], out.items.begin() + 4 * (size_t)order[i] + 4,
