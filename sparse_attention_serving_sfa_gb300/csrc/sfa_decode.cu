@@ -576,6 +576,15 @@ cudaError_t run_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaStrea
     int64_t ctas = p.num_ctas > 0 ? p.num_ctas : (int64_t)num_sms * occ;
     // many index lists per CTA: whole lists per range balance well enough
     s.aligned = (s.units >= 8 * ctas || s.units > kMaxCounters) ? 1 : 0;
+    // fewer lists than resident CTAs: split every list into the same number
+    // of segments (ctas = lists x segments), so that each range lies inside
+    // one list -- a range that crosses into the next list pays a merge in
+    // mid-range (measured on GQA decode, 128 lists of 16 chunks: 256 CTAs
+    // 18.6 us against 20.4 us for the 304 resident ones)
+    if (!s.aligned && p.num_ctas == 0) {
+        const int64_t seg = ctas / s.units;
+        if (seg >= 2) ctas = s.units * (seg < s.cpu ? seg : s.cpu);
+    }
     if (ctas > (s.aligned ? s.units : s.total)) ctas = s.aligned ? s.units : s.total;
     s.ctas = (int)ctas;
     if (s.aligned) {

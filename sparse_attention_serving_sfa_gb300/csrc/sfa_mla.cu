@@ -785,6 +785,14 @@ cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaSt
     s.total = s.units * s.cpu;
     int64_t clusters = resident;
     if (p.num_ctas > 0) clusters = (p.num_ctas + 1) / 2;    // tuning / tests
+    // fewer units than resident clusters: split every unit into the same
+    // number of segments, so that each cluster's range lies inside one unit
+    // (MLA decode, 32 units of 32 chunks: 64 clusters 70.5 us against 77.2 us
+    // for the 76 resident ones)
+    if (p.num_ctas == 0) {
+        const int64_t seg = clusters / s.units;
+        if (seg >= 2) clusters = s.units * (seg < s.cpu ? seg : s.cpu);
+    }
     if (clusters > s.total) clusters = s.total;
     if (clusters < 1) clusters = 1;
     // keep the number of clusters sharing one unit within kMaxSeg: a unit of
