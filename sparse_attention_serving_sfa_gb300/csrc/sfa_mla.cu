@@ -8,37 +8,33 @@
 // chunks.
 //
 // O for 128 heads x 512 dims (fp32) fills all 512 columns of one SM's tensor
-// memory, so a unit (one index list and its 128 heads) is computed by a 2-CTA
-// cluster that splits the head dimensions:
-//   CTA r owns K/Q dims [256 r, 256 r + 256) (nope) and [512 + 32 r, 544 + 32 r)
-//   (rope), and V / O dims [256 r, 256 r + 256) -- the first 256 of its K dims.
-// Per 64-slot chunk, each CTA gathers only its 576 bytes of every selected K
-// row (no duplicated gather) and computes a partial S_r = Q_r K_r^T; the two
-// partials are exchanged with one bulk shared-memory copy into the peer CTA,
-// so both CTAs hold the same S = S_0 + S_1, run the same online softmax and
-// compute O_r += P V_r for their half of Dv (P as a 16-bit high part plus
-// remainder, ~fp32 accurate).
+// memory, so a unit (one index list and its 128 heads) is computed by a pair
+// of CTAs that split the output dims: CTA r owns O dims [256 r, 256 r + 256).
+// Each CTA of the pair gathers the whole selected K rows (1152 bytes; the
+// second read of a row comes from L2), computes the full S = Q K^T over all
+// 576 dims itself and runs its own online softmax -- the two CTAs never
+// exchange data, so neither waits for the other -- then O_r += P V_r for its
+// half of Dv (P as a 16-bit high part plus remainder, ~fp32 accurate).  The
+// pair is launched as a 2-CTA cluster only so that both halves of a unit run
+// at the same time and share the row reads in L2.
 //
-// Tensor memory holds O, three S/P buffers (a chunk's scores, then its
-// probabilities written over them as the A operand of P.V) and half of the
-// unit's Q nope dims (the other half and the rope dims are read from shared
-// memory; an MMA's A operand costs the same from either).  With three buffers
-// QK runs up to two chunks ahead of P.V, so a chunk's scores are ready when
-// the softmax wants to send them, and P(i + 1) can be written while P.V(i)
-// runs.
+// Tensor memory (512 columns): Q dims [0, 256) as the A operand of Q.K^T in
+// [0, 128) | two S/P buffers [128, 192), [192, 256) (a chunk's scores, then
+// its probabilities written over them as the A operand of P.V) | O [256, 512).
+// Shared memory: two stages of a chunk's K rows (9 panels of 64 dims, 128-byte
+// swizzle, 72 KB each) and Q dims [256, 576) (5 panels, 80 KB).
 //
-// TMEM (512 columns): Q nope dims [0, 128) in [0, 64) | S/P buffers
-// [64, 128), [128, 192), [192, 256) | O [256, 512).
-//
-// Roles per CTA (13 warps): 8 softmax warps (two warpgroups, thread = head =
-// TMEM lane; warpgroup w takes slots [32 w, 32 w + 32) of a chunk and O dims
-// [128 w, 128 w + 128) of the CTA's half), 1 MMA warp (Q TMA, tcgen05.mma
-// issue from an event loop), 4 producer warps (cp.async gather, index
-// prefetch, L2 prefetch of later chunks, visibility masks).  The softmax sends
-// chunk i + 1's partial scores before computing chunk i's probabilities when
-// they are ready, so the copy overlaps that work.  Work is stream-K over
-// (unit, chunk) pairs per cluster; the parts of a unit split over clusters are
-// written as fp32 partials and merged by a second kernel.
+// Roles per CTA (9 warps): 4 softmax warps (one warpgroup, thread = head =
+// TMEM lane, all 64 slots of a chunk), 1 MMA warp (Q TMA, tcgen05.mma issue
+// from an event loop: Q.K^T of chunk i + 1 as soon as its rows have landed,
+// P.V of chunk i as soon as its P is written), 4 producer warps (cp.async
+// gather of whole rows, index prefetch, L2 prefetch two chunks ahead,
+// visibility masks).  Work is stream-K over (unit, chunk) pairs per pair of
+// CTAs; the parts of a unit split over pairs are written as fp32 partials and
+// merged by a second kernel.  (An earlier design split the K dims over the
+// pair and exchanged partial scores through distributed shared memory every
+// chunk: per-chunk timelines showed the pair running in lockstep through that
+// exchange, ~5,100 cycles per chunk for ~1,900 cycles of tensor work.)
 #include <cudaTypedefs.h>
 
 #include <limits.h>
@@ -57,53 +53,52 @@ namespace {
 constexpr int kChunk = 64;
 constexpr int kHeads = 128;               // the MMA M dimension
 constexpr int kDk = 576, kDv = 512;
-constexpr int kHalfDv = 256;              // nope dims (and V / O dims) per CTA
-constexpr int kStages = 3;
-constexpr int kBufs = 3;                  // S/P buffers in tensor memory: QK runs up to 2 chunks ahead
-constexpr int kSoftThreads = 256;
-constexpr int kMmaWarp = 8;
-constexpr int kProdWarp0 = 9;
+constexpr int kHalfDv = 256;              // V / O dims per CTA
+constexpr int kStages = 2;
+constexpr int kBufs = 2;                  // S/P buffers in tensor memory
+constexpr int kSoftThreads = 128;
+constexpr int kMmaWarp = 4;
+constexpr int kProdWarp0 = 5;
 constexpr int kProdThreads = 128;
 constexpr int kThreads = kSoftThreads + 32 + kProdThreads;
 constexpr int kTmemCols = 512;
-constexpr int kQnCol = 0, kSCol = 64, kOCol = 256;   // Q nope dims [0, 128) | 3 S/P buffers | O
+constexpr int kQtDims = 256;              // Q dims held in tensor memory
+constexpr int kQtCol = 0, kSCol = 128, kOCol = 256;
+constexpr int kPanels = kDk / 64;         // 9 panels of 64 dims per K row
+constexpr int kQsPanels = (kDk - kQtDims) / 64;   // 5 Q panels in shared memory
+constexpr int kPieces = kDk / 8;          // 16-byte pieces per K row
 constexpr int kLookahead = 6;
-constexpr int kPrefetch = 3;              // chunks ahead that the producers pull into L2
+constexpr int kPrefetch = 2;              // chunks ahead that the producers pull into L2
 constexpr int kNoSlot = INT_MIN;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kMaxSeg = 8;                // clusters sharing one unit
-constexpr uint32_t kXBytes = kHeads * kChunk * 4;
+constexpr int kMaxSeg = 8;                // pairs sharing one unit
 
 struct MlaSmem {
-    static constexpr int nopePanel = kChunk * 128;          // 64 rows x 128 B (64 dims), 128B swizzle
-    static constexpr int ropePanel = kChunk * 64;           // 64 rows x 64 B (32 dims), 64B swizzle
-    static constexpr int kvStage = 4 * nopePanel + ropePanel;   // 36 KB
+    static constexpr int panel = kChunk * 128;              // 64 rows x 128 B (64 dims)
+    static constexpr int kvStage = kPanels * panel;         // 72 KB: a chunk's K rows
+    static constexpr int qpanel = kHeads * 128;             // 128 heads x 128 B
     static constexpr int kv = 0;
-    static constexpr int stg = kv + kStages * kvStage;      // own partial S (send), 32 KB
-    static constexpr int x = stg + kXBytes;                 // peer partial S (receive), 32 KB
-    static constexpr int qn = x + kXBytes;                  // Q nope dims [128, 256): 2 panels x 128 rows x 128 B
-    static constexpr int qr = qn + 2 * kHeads * 128;        // Q rope: 128 rows x 64 B, 64B swizzle
-    static constexpr int red = qr + kHeads * 64;            // [2][128] row max per warpgroup
-    static constexpr int red2 = red + 2 * kHeads * 4;       // [2][128] row sum per warpgroup
-    static constexpr int bars = red2 + 2 * kHeads * 4;
-    static constexpr int meta = bars + 24 * 8;              // [stage][4] uint16 visibility masks
-    static constexpr int misc = meta + kStages * 8;         // tmem base, abort flag, early-send flag
+    static constexpr int qs = kv + kStages * kvStage;       // Q dims [256, 576)
+    static constexpr int bars = qs + kQsPanels * qpanel;
+    static constexpr int meta = bars + 16 * 8;              // [stage][4] uint16 visibility masks
+    static constexpr int misc = meta + kStages * 8;         // tmem base, abort flag
     static constexpr int total = misc + 16;
     static constexpr int alloc = total + 1024;
 };
-static_assert(MlaSmem::kvStage % 1024 == 0 && MlaSmem::qn % 1024 == 0 && MlaSmem::qr % 1024 == 0,
+static_assert(MlaSmem::alloc <= 232448, "dynamic shared memory per block");
+static_assert(MlaSmem::kvStage % 1024 == 0 && MlaSmem::qs % 1024 == 0 && MlaSmem::qpanel % 1024 == 0,
               "swizzle atoms must stay aligned");
 
 enum {
-    B_QR_FULL = 0, B_Q_FREE = 1, B_Q_READY = 2, B_KV_FULL = 3, B_KV_FREE = 6, B_S_FULL = 9,
-    B_P_FULL = 12, B_O_DONE = 15, B_UNIT_DONE = 18, B_X_FULL = 19, B_X_EMPTY = 20, B_DRAIN = 21
+    B_Q_FULL = 0, B_Q_FREE = 1, B_Q_READY = 2, B_KV_FULL = 3, B_KV_FREE = 5, B_S_FULL = 7,
+    B_P_FULL = 9, B_O_DONE = 11, B_UNIT_DONE = 13, B_DRAIN = 14
 };
 
 struct MlaSched {
     int64_t total;      // chunks over all units
     int64_t units;
     int cpu;            // chunks per unit
-    int clusters;
+    int clusters;       // CTA pairs
     int seg_max;
     int q_head_inner;   // q tensor map dims are {d, head, s1, b} (else {d, s1, head, b})
 };
@@ -128,8 +123,7 @@ __device__ __forceinline__ UCoord ucoord(int64_t u, const SfaParams& p) {
 
 template <class E>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mqr,
-               const SfaParams p, const MlaSched sch) {
+sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const MlaSched sch) {
     using T = typename E::T;
     using L = MlaSmem;
     constexpr bool kBf16 = std::is_same<E, BF16>::value;
@@ -141,7 +135,7 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+    const uint32_t rank = cluster_ctarank();
     const int64_t cl = blockIdx.x >> 1;
     const int c_begin = (int)mla_range_begin(cl, sch), c_end = (int)mla_range_begin(cl + 1, sch);
     const int n = c_end - c_begin;
@@ -150,10 +144,11 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(bar(B_QR_FULL), 1);
+        mbar_init(bar(B_Q_FULL), 1);
         mbar_init(bar(B_Q_FREE), 1);
         mbar_init(bar(B_Q_READY), kSoftThreads);
         mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_UNIT_DONE), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_KV_FULL + s), kProdThreads + kProdThreads / 32);
             mbar_init(bar(B_KV_FREE + s), 1);
@@ -163,9 +158,6 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             mbar_init(bar(B_P_FULL + b), kSoftThreads);
             mbar_init(bar(B_O_DONE + b), 1);
         }
-        mbar_init(bar(B_UNIT_DONE), 1);
-        mbar_init(bar(B_X_FULL), 1);      // own arrive.expect_tx + the peer's bulk copy bytes
-        mbar_init(bar(B_X_EMPTY), 1);     // the peer has read what this CTA sent it
         fence_barrier_init();
     }
     // launched with programmatic dependent launch: nothing above touches
@@ -175,7 +167,7 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     grid_launch_dependents();
     if (warp == kMmaWarp) tmem_alloc(sbase + L::misc, kTmemCols);
     tc_fence_before();
-    cluster_sync();      // both CTAs' barriers exist before any remote access
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::misc);
 
@@ -184,10 +176,10 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 
     if (warp >= kProdWarp0) {
         // ============================ producers ============================
-        // Warp pw gathers slots 16 pw .. 16 pw + 15 of every chunk: per slot
-        // one 512-byte nope run (lane = 16-byte piece), then the 64-byte rope
-        // runs of its 16 rows, 8 rows per instruction.  Lane l holds the index
-        // of slot 16 pw + l % 16.  Unit coordinates advance incrementally.
+        // Warp pw gathers slots 16 pw .. 16 pw + 15 of every chunk, one whole
+        // row (72 16-byte pieces: lane = piece, three instructions) at a time,
+        // piece c of panel q at row * 128 + ((c ^ row % 8) << 4) of the
+        // panel.  Lane l holds the index of slot 16 pw + l % 16.
         const int pw = warp - kProdWarp0;
         const int sl = lane & 15;
         struct Cursor {
@@ -251,37 +243,31 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             const bool vis = in_range && !(p.causal && myid > diag);
             const int myrow = in_range ? myid : -1;
             unsigned char* st = smem + L::kv + s * L::kvStage;
-            // nope dims [256 rank, +256): panel = lane / 8, 16-byte chunk lane % 8
-            const T* nope = k.kg + (int)rank * kHalfDv + 8 * lane;
-            const int pn = lane >> 3, c = lane & 7;
-#pragma unroll 8
+#pragma unroll 4
             for (int r = 0; r < 16; ++r) {
                 const int id = __shfl_sync(0xffffffffu, myrow, r);
                 const int row = 16 * pw + r;
-                cp_async_16_zfill(st + pn * L::nopePanel + row * 128 + ((c ^ (row & 7)) << 4),
-                                  nope + (id >= 0 ? (int64_t)id * p.k_ss : 0), id >= 0 ? 16 : 0);
-            }
-            // rope dims [512 + 32 rank, +32): 64-byte rows, chunk c at c ^ ((row / 2) % 4)
-            const T* rope = k.kg + 512 + 32 * (int)rank + 8 * (lane & 3);
+                const T* src = k.kg + (id >= 0 ? (int64_t)id * p.k_ss : 0);
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int r = 8 * t + (lane >> 2);
-                const int id = __shfl_sync(0xffffffffu, myrow, r);
-                const int row = 16 * pw + r;
-                cp_async_16_zfill(st + 4 * L::nopePanel + row * 64 + (((lane & 3) ^ ((row >> 1) & 3)) << 4),
-                                  rope + (id >= 0 ? (int64_t)id * p.k_ss : 0), id >= 0 ? 16 : 0);
+                for (int t = 0; t < 3; ++t) {
+                    const int pc = lane + 32 * t;
+                    if (pc < kPieces) {
+                        const int q = pc >> 3, c = pc & 7;
+                        cp_async_16_zfill(st + q * L::panel + row * 128 + ((c ^ (row & 7)) << 4),
+                                          src + 8 * pc, id >= 0 ? 16 : 0);
+                    }
+                }
             }
             cp_async_mbar_arrive(bar(B_KV_FULL + s));
             // rows of chunk i + kPrefetch into L2 ahead of their stage being
-            // free: lane l takes slot l % 16, lines l / 16, 2 + l / 16 of its
-            // nope run and (lanes < 16) its rope line
+            // free: lane l takes slot l % 16 and 5 (l < 16) or 4 of its nine
+            // 128-byte lines
             if (i + kPrefetch < n) {
                 const int pid = ring[kPrefetch - 1];
                 if (pid >= 0 && pid < p.S2) {
                     const char* rowp = reinterpret_cast<const char*>(pk.kg + (int64_t)pid * p.k_ss);
-                    prefetch_l2(rowp + 512 * (int)rank + 128 * (lane >> 4));
-                    prefetch_l2(rowp + 512 * (int)rank + 256 + 128 * (lane >> 4));
-                    if (lane < 16) prefetch_l2(rowp + 1024 + 64 * (int)rank);
+                    const int l0 = (lane >> 4) * 5, l1 = (lane >> 4) ? 9 : 5;
+                    for (int line = l0; line < l1; ++line) prefetch_l2(rowp + 128 * line);
                 }
                 advance(pk);
             }
@@ -296,55 +282,46 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         cp_async_wait<0>();
     } else if (warp == kMmaWarp) {
         // ============================ MMA issue ============================
-        // QK(j) may be issued once PV(j - 3) is (its S/P buffer j % 3 is then
-        // free in pipe order): QK(i + 1) is required before P(i) can exist,
-        // QK(i + 2) goes in when its rows have landed; PV(i) as soon as P(i)
-        // is there.  An event loop, so that a later chunk's gather never
-        // holds up a ready PV.
+        // Q.K^T(j) needs its rows and S buffer j % 2, free once P.V(j - 2) is
+        // issued (tensor-core order); P.V(i) needs P(i).  An event loop, so
+        // that a ready P.V never waits behind a later chunk's gather.
         if (lane == 0 && n > 0) {
             tma_prefetch_map(&mq);
-            tma_prefetch_map(&mqr);
             uint32_t qfree_phase = 0, q_phase = 0;
             bool ok = true;
-            // the unit's Q rope panel (TMA) and its Q nope half (written to
-            // tensor memory by the softmax threads)
+            // the unit's Q dims [256, 576) by TMA, and its dims [0, 256)
+            // written to tensor memory by the softmax threads
             auto unit_q = [&](int u) {
                 const UCoord uc = ucoord(u, p);
-                mbar_arrive_expect_tx(bar(B_QR_FULL), kHeads * 64 + 2 * kHeads * 128);
+                mbar_arrive_expect_tx(bar(B_Q_FULL), kQsPanels * L::qpanel);
                 const int c1 = sch.q_head_inner ? uc.n2 * kHeads : uc.s1;
                 const int c2 = sch.q_head_inner ? uc.s1 : uc.n2 * kHeads;
-                tma_load_4d(sbase + L::qr, &mqr, 512 + 32 * (int)rank, c1, c2, uc.b, bar(B_QR_FULL));
-                for (int pn = 0; pn < 2; ++pn)
-                    tma_load_4d(sbase + L::qn + pn * (kHeads * 128), &mq, (int)rank * kHalfDv + 128 + 64 * pn,
-                                c1, c2, uc.b, bar(B_QR_FULL));
-                ok = ok && mbar_wait(bar(B_QR_FULL), q_phase, p.err_word, abort_flag);
+                for (int pn = 0; pn < kQsPanels; ++pn)
+                    tma_load_4d(sbase + L::qs + pn * L::qpanel, &mq, kQtDims + 64 * pn, c1, c2, uc.b,
+                                bar(B_Q_FULL));
+                ok = ok && mbar_wait(bar(B_Q_FULL), q_phase, p.err_word, abort_flag);
                 ok = ok && mbar_wait(bar(B_Q_READY), q_phase, p.err_word, abort_flag);
                 q_phase ^= 1;
                 tc_fence_after();
             };
             auto qk = [&](int j) {
                 const int s = j % kStages;
-                ok = ok && mbar_wait(bar(B_KV_FULL + s), (j / kStages) & 1, p.err_word, abort_flag);
                 fence_proxy_async_smem();     // cp.async (generic proxy) data -> tensor core
                 tc_fence_after();
                 const uint32_t kb = sbase + L::kv + s * L::kvStage;
                 const uint32_t d = tmem + kSCol + 64 * (j % kBufs);
-                // nope dims [0, 128): A from tensor memory; [128, 256): A from shared memory
+                // dims [0, 256): A from tensor memory; [256, 576): A from shared memory
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * L::nopePanel + (kk & 3) * 32, 16, 1024);
-                    tc_mma_f16_ts(d, tmem + kQnCol + 8 * kk, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < kQtDims / 16; ++kk) {
+                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * L::panel + (kk & 3) * 32, 16, 1024);
+                    tc_mma_f16_ts(d, tmem + kQtCol + 8 * kk, bd, kIdescQK, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
-                for (int kk = 8; kk < 16; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sbase + L::qn + ((kk - 8) >> 2) * (kHeads * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * L::nopePanel + (kk & 3) * 32, 16, 1024);
-                    tc_mma_f16(d, ad, bd, kIdescQK, 1u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const uint64_t ad = sdesc_sw64(sbase + L::qr + kk * 32, 512);
-                    const uint64_t bd = sdesc_sw64(kb + 4 * L::nopePanel + kk * 32, 512);
+                for (int kk = kQtDims / 16; kk < kDk / 16; ++kk) {
+                    const int qk_ = kk - kQtDims / 16;
+                    const uint64_t ad =
+                        sdesc_sw128(sbase + L::qs + (qk_ >> 2) * L::qpanel + (qk_ & 3) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * L::panel + (kk & 3) * 32, 16, 1024);
                     tc_mma_f16(d, ad, bd, kIdescQK, 1u);
                 }
                 tc_commit(bar(B_S_FULL + j % kBufs));
@@ -355,11 +332,16 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             int next_qk = 0;
             uint64_t idle_since = 0;
             for (int i = 0; i < n && ok;) {
-                if (next_qk < unit_end && next_qk <= i + 1) {
+                // Q.K^T of the next chunk: required before anything else when
+                // it is chunk i itself; one chunk ahead when its rows are in
+                if (next_qk < unit_end && next_qk <= i) {
+                    ok = mbar_wait(bar(B_KV_FULL + next_qk % kStages), (next_qk / kStages) & 1, p.err_word,
+                                   abort_flag);
+                    if (!ok) break;
                     qk(next_qk++);
                     continue;
                 }
-                if (next_qk < unit_end && next_qk == i + 2 &&
+                if (next_qk < unit_end && next_qk == i + 1 &&
                     mbar_try_wait(bar(B_KV_FULL + next_qk % kStages), (next_qk / kStages) & 1)) {
                     qk(next_qk++);
                     continue;
@@ -384,14 +366,16 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 idle_since = 0;
                 const int s = i % kStages;
                 tc_fence_after();
-                const uint32_t kb = sbase + L::kv + s * L::kvStage;
+                // O_r += P V_r: V_r = dims [256 r, 256 r + 256) of the chunk's
+                // rows (panels 4 r .. 4 r + 3), an MN-major operand
+                const uint32_t vb = sbase + L::kv + s * L::kvStage + 4 * (int)rank * L::panel;
                 const uint32_t pa = tmem + kSCol + 64 * (i % kBufs);
                 const bool first = (i == 0) || (c_begin + i) % cpu == 0;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kChunk / 16; ++kk) {
-                        const uint64_t bd = sdesc_sw128(kb + kk * 16 * 128, L::nopePanel, 1024);
+                        const uint64_t bd = sdesc_sw128(vb + kk * 16 * 128, L::panel, 1024);
                         const uint32_t acc = (first && part == 0 && kk == 0) ? 0u : 1u;
                         tc_mma_f16_ts(tmem + kOCol, pa + 32 * part + 8 * kk, bd, kIdescPV, acc);
                     }
@@ -401,8 +385,8 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 if (i == unit_end) {
                     tc_commit(bar(B_UNIT_DONE));   // the unit's O is final
                     if (i < n) {
-                        // the rope panel and Q columns are rewritten once
-                        // every MMA of the unit is done
+                        // the Q panels and Q columns are rewritten once every
+                        // MMA of the unit is done
                         tc_commit(bar(B_Q_FREE));
                         ok = ok && mbar_wait(bar(B_Q_FREE), qfree_phase, p.err_word, abort_flag);
                         qfree_phase ^= 1;
@@ -421,63 +405,30 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         }
     } else {
         // ============================ softmax ============================
-        const int w = tid >> 7;                              // warpgroup: slot / dim half
-        const int r = tid & (kHeads - 1);                    // head row = TMEM lane
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        const uint32_t x_peer = map_peer(sbase + L::x, peer);
-        const uint32_t xfull_peer = map_peer(bar(B_X_FULL), peer);
-        const uint32_t xempty_peer = map_peer(bar(B_X_EMPTY), peer);
-        float* red = reinterpret_cast<float*>(smem + L::red);
-        float* red2 = reinterpret_cast<float*>(smem + L::red2);
-        volatile int* early_flag = reinterpret_cast<volatile int*>(smem + L::misc + 8);
-        // Q nope dims [256 rank + 64 w, +64) of head r into TMEM columns
-        // [32 w, 32 w + 32): two 16-bit dims per column (dims [128, 256) of
-        // the CTA's half come by TMA into shared memory)
-        auto load_qn = [&](int u) {
+        const int r = tid;                                   // head row = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        // Q dims [0, 256) of head r into TMEM columns [0, 128): two 16-bit
+        // dims per column (dims [256, 576) come by TMA into shared memory)
+        auto load_q = [&](int u) {
             const UCoord uc = ucoord(u, p);
             const uint4* src = reinterpret_cast<const uint4*>(
                 static_cast<const T*>(p.q) + uc.b * p.q_sb + uc.s1 * p.q_ss +
-                (int64_t)(uc.n2 * kHeads + r) * p.q_sh + (int)rank * kHalfDv + 64 * w);
-            uint32_t v[32];
+                (int64_t)(uc.n2 * kHeads + r) * p.q_sh);
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t v[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 x = __ldg(src + j);
-                v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 x = __ldg(src + 8 * cb + j);
+                    v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+                }
+                tmem_st32(lane_base + kQtCol + 32 * cb, v);
             }
-            tmem_st32(lane_base + kQnCol + 32 * w, v);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(B_Q_READY));
         };
-        // send(j): this CTA's partial scores of chunk j to the peer (one bulk
-        // copy from the staging buffer into the peer's receive buffer); sv
-        // keeps them for the sum
-        uint32_t sv[32];
-        auto send = [&](int j) {
-            mbar_wait(bar(B_S_FULL + j % kBufs), (j / kBufs) & 1, p.err_word, abort_flag);
-            tc_fence_after();
-            tmem_ld32(lane_base + kSCol + 64 * (j % kBufs) + 32 * w, sv);
-            tmem_wait_ld();
-            // the staging buffer is free once the peer has read the last copy
-            if (tid == 0 && j > 0)
-                mbar_wait_cluster(bar(B_X_EMPTY), (j - 1) & 1, p.err_word, abort_flag);
-            named_sync(1, kSoftThreads);
-            unsigned char* stg = smem + L::stg + r * 256;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<uint4*>(stg + (((8 * w + q) ^ (r & 15)) << 4)) =
-                    make_uint4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
-            fence_proxy_async_smem();         // generic writes -> bulk copy engine
-            named_sync(1, kSoftThreads);
-            if (tid == 0) {
-                mbar_arrive_expect_tx(bar(B_X_FULL), kXBytes);
-                bulk_s2cluster(x_peer, sbase + L::stg, kXBytes, xfull_peer);
-            }
-        };
-        if (n > 0) {
-            load_qn(unit_of(c_begin));
-            send(0);
-        }
+        if (n > 0) load_q(unit_of(c_begin));
         float m_used = -INFINITY, l = 0.f;
         bool first_of_unit = true;
         uint32_t unit_phase = 0;
@@ -485,97 +436,76 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             const int c = c_begin + i;
             const int u = unit_of(c);
             const bool last_of_unit = (i + 1 == n) || unit_of(c + 1) != u;
-            // ---- receive the peer's partial scores of chunk i ----
+            // the chunk's visibility masks, then its scores
             mbar_wait(bar(B_KV_FULL + i % kStages), (i / kStages) & 1, p.err_word, abort_flag);
-            mbar_wait(bar(B_X_FULL), i & 1, p.err_word, abort_flag);
-            const uint2 vis = reinterpret_cast<const uint2*>(smem + L::meta)[i % kStages];
-            const uint32_t vw = w ? vis.y : vis.x;
-            const unsigned char* xr = smem + L::x + r * 256;
-            float s[32];
-            float bmax = -INFINITY;
+            const uint2 vm = reinterpret_cast<const uint2*>(smem + L::meta)[i % kStages];
+            const uint64_t vis = ((uint64_t)vm.y << 32) | vm.x;   // bit j = slot j visible
+            mbar_wait(bar(B_S_FULL + i % kBufs), (i / kBufs) & 1, p.err_word, abort_flag);
+            tc_fence_after();
+            uint32_t sv[64];
+            const uint32_t sp = kSCol + 64 * (i % kBufs);
+            tmem_ld32(lane_base + sp, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tmem_ld32(lane_base + sp + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            tmem_wait_ld();
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint4 o = *reinterpret_cast<const uint4*>(xr + (((8 * w + q) ^ (r & 15)) << 4));
-                const float ov[4] = {__uint_as_float(o.x), __uint_as_float(o.y), __uint_as_float(o.z),
-                                     __uint_as_float(o.w)};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int jj = 4 * q + e;
-                    // both CTAs add the two partials in the same (commutative) way
-                    const float v = __uint_as_float(sv[jj]) + ov[e];
-                    s[jj] = ((vw >> jj) & 1u) ? v * p.scale_log2 : -INFINITY;
-                    bmax = fmaxf(bmax, s[jj]);
-                }
+            for (int j = 0; j < 64; ++j) {
+                const float v = ((vis >> j) & 1ull) ? __uint_as_float(sv[j]) * p.scale_log2 : -INFINITY;
+                sv[j] = __float_as_uint(v);
+                mx4[j & 3] = fmaxf(mx4[j & 3], v);
             }
-            red[w * kHeads + r] = bmax;
-            // send chunk i + 1 before this chunk's softmax when its scores are
-            // already computed (the copy then overlaps the work below), else
-            // after P(i) is out; a new unit's first chunk waits for that unit's
-            // Q, written in the epilogue
-            if (tid == 0)
-                *early_flag = !last_of_unit && mbar_try_wait(bar(B_S_FULL + (i + 1) % kBufs), ((i + 1) / kBufs) & 1);
-            named_sync(1, kSoftThreads);      // X read by every thread, row maxima posted
-            if (tid == 0) mbar_arrive_remote(xempty_peer);
-            bmax = fmaxf(red[r], red[kHeads + r]);
-            const bool early = *early_flag != 0;
-            if (early) send(i + 1);
+            const float bmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             // ---- online softmax over the chunk (mask shared by all heads) ----
             const float m_new = fmaxf(m_used, bmax);
             const bool need = m_new > m_used + kRescaleThreshold;
             const float f = need ? fast_exp2(m_used - m_new) : 1.f;   // 0 while m_used is -inf
             if (need) m_used = m_new;
-            uint32_t hw[16], lw[16];
-            float lsum = 0.f;
+            uint32_t hw[32], lw[32];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float a = s[2 * e], b = s[2 * e + 1];
+            for (int e = 0; e < 32; ++e) {
+                const float a = __uint_as_float(sv[2 * e]), b = __uint_as_float(sv[2 * e + 1]);
                 const float p0 = (a == -INFINITY) ? 0.f : fast_exp2(a - m_used);
                 const float p1 = (b == -INFINITY) ? 0.f : fast_exp2(b - m_used);
-                lsum += p0 + p1;
+                ls[e & 3] += p0 + p1;
                 hw[e] = E::pack2(p0, p1);
                 const float2 h = E::unpack2(hw[e]);
                 lw[e] = E::pack2(p0 - h.x, p1 - h.y);
             }
-            l = l * f + lsum;                 // this warpgroup's share of the row sum
+            l = l * f + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
             if (!first_of_unit && __any_sync(0xffffffffu, need)) {
                 // O is rescaled once P.V of the previous chunk is done: its
-                // buffer's barrier, whose previous use (chunk i - 4) is done
-                // and whose next (chunk i + 2) cannot be, so the phase is
+                // buffer's barrier, whose previous use (chunk i - 3) is done
+                // (this chunk's Q.K^T followed it in tensor-core order) and
+                // whose next (chunk i + 1) cannot be, so the phase is
                 // unambiguous.
                 const int pb = (i - 1) % kBufs;
                 mbar_wait(bar(B_O_DONE + pb), ((i - 1) / kBufs) & 1, p.err_word, abort_flag);
                 tc_fence_after();
 #pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
+                for (int cb = 0; cb < kHalfDv / 32; ++cb) {
                     uint32_t ov[32];
-                    tmem_ld32(lane_base + kOCol + 128 * w + 32 * cb, ov);
+                    tmem_ld32(lane_base + kOCol + 32 * cb, ov);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
-                    tmem_st32(lane_base + kOCol + 128 * w + 32 * cb, ov);
+                    tmem_st32(lane_base + kOCol + 32 * cb, ov);
                 }
             }
             // P over the S columns of its chunk: high parts in [sp, sp + 32),
             // remainders in [sp + 32, sp + 64); slot j -> column j / 2
-            const uint32_t sp = kSCol + 64 * (i % kBufs);
-            tmem_st16(lane_base + sp + 16 * w, hw);
-            tmem_st16(lane_base + sp + 32 + 16 * w, lw);
+            tmem_st32(lane_base + sp, hw);
+            tmem_st32(lane_base + sp + 32, lw);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(B_P_FULL + i % kBufs));
             first_of_unit = false;
-            if (!last_of_unit) {
-                if (!early) send(i + 1);
-                continue;
-            }
+            if (!last_of_unit) continue;
 
-            // ---- epilogue of unit u: dims [256 rank + 128 w, +128) ----
+            // ---- epilogue of unit u: this CTA's dims [256 rank, +256) ----
             mbar_wait(bar(B_UNIT_DONE), unit_phase, p.err_word, abort_flag);
             unit_phase ^= 1;
             tc_fence_after();
-            red2[w * kHeads + r] = l;
-            named_sync(1, kSoftThreads);
-            const float lt = red2[r] + red2[kHeads + r];
             const int64_t first = (int64_t)u * cpu, lastc = first + cpu - 1;
             const int64_t c_lo = mla_cluster_of(first, sch), c_hi = mla_cluster_of(lastc, sch);
             const bool split = c_hi > c_lo;
@@ -583,15 +513,15 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             const int n1 = uc.n2 * kHeads + r;
             const int64_t row = (int64_t)u * kHeads + r;
             const int64_t slot = row * sch.seg_max + (cl - c_lo);
-            const bool empty = !(lt > 0.f);
-            const float inv = empty ? 0.f : 1.f / lt;
-            const int d0 = (int)rank * kHalfDv + 128 * w;
+            const bool empty = !(l > 0.f);
+            const float inv = empty ? 0.f : 1.f / l;
+            const int d0 = (int)rank * kHalfDv;
             T* orow = static_cast<T*>(p.out) + uc.b * p.o_sb + n1 * p.o_sh + uc.s1 * p.o_ss + d0;
             float* wo = split ? p.ws_o + slot * kDv + d0 : nullptr;
 #pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = 0; cb < kHalfDv / 32; ++cb) {
                 uint32_t ov[32];
-                tmem_ld32(lane_base + kOCol + 128 * w + 32 * cb, ov);
+                tmem_ld32(lane_base + kOCol + 32 * cb, ov);
                 tmem_wait_ld();
                 if (!split) {
 #pragma unroll
@@ -612,31 +542,25 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 }
             }
             if (!split) {
-                if (rank == 0 && w == 0 && p.lse)
+                if (rank == 0 && p.lse)
                     p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] =
-                        empty ? -INFINITY : (m_used + __log2f(lt)) * kLn2;
-            } else if (w == 0) {
-                // (m, l) of this part; both CTAs of the cluster write the same values
+                        empty ? -INFINITY : (m_used + __log2f(l)) * kLn2;
+            } else {
+                // (m, l) of this part; both CTAs of the pair compute the same values
                 p.ws_ml[slot * 2] = m_used;
-                p.ws_ml[slot * 2 + 1] = lt;
+                p.ws_ml[slot * 2 + 1] = l;
             }
             m_used = -INFINITY;
             l = 0.f;
             first_of_unit = true;
             // tensor memory's Q columns are free (every MMA of the unit is
-            // done): the next unit's Q, then its first chunk's exchange
-            if (i + 1 < n) {
-                load_qn(u + 1);
-                send(i + 1);
-            }
+            // done): the next unit's Q
+            if (i + 1 < n) load_q(u + 1);
         }
-        // the last copy sent to the peer has landed before this CTA can leave
-        if (tid == 0 && n > 0)
-            mbar_wait_cluster(bar(B_X_EMPTY), (n - 1) & 1, p.err_word, nullptr, 100000000ull);
     }
     __syncwarp();
     tc_fence_before();
-    cluster_sync();      // the peer no longer writes into this CTA's shared memory
+    __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -775,11 +699,9 @@ cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaSt
     if (resident < 1) return cudaErrorInvalidConfiguration;
     MlaSched s;
     s.q_head_inner = p.q_sh <= p.q_ss ? 1 : 0;
-    CUtensorMap mq, mqr;
+    CUtensorMap mq;
     const bool bf16 = std::is_same<E, BF16>::value;
-    if (!make_q_map(&mq, p, bf16, s.q_head_inner != 0, 64) ||
-        !make_q_map(&mqr, p, bf16, s.q_head_inner != 0, 32))
-        return cudaErrorInvalidValue;
+    if (!make_q_map(&mq, p, bf16, s.q_head_inner != 0, 64)) return cudaErrorInvalidValue;
     s.cpu = (p.topK + kChunk - 1) / kChunk;
     s.units = (int64_t)p.B * p.N2 * p.S1;
     s.total = s.units * s.cpu;
@@ -816,7 +738,7 @@ cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaSt
         p.ws_ml = p.ws_o + rows * s.seg_max * kDv;
     }
     cudaError_t err = launch_pdl(sfa_mla_kernel<E>, dim3((unsigned)(2 * s.clusters)), dim3(kThreads),
-                                 (size_t)MlaSmem::alloc, stream, mq, mqr, p, s);
+                                 (size_t)MlaSmem::alloc, stream, mq, p, s);
     count_launches(1);
     if (err != cudaSuccess || s.seg_max == 1) return err;
     // merge of split units; launched early (programmatic dependent launch),
