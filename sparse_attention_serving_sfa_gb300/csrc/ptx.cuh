@@ -126,6 +126,12 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster
 // scope: this thread's earlier shared::cluster accesses are ordered before a
 // thread that then waits on the barrier with cluster-scope acquire).

@@ -33,9 +33,16 @@
 //     otherwise its partial (O, running max, sum) goes to the workspace and
 //     the last CTA to finish the list (a per-list arrival counter in the
 //     workspace head, reset by that CTA) merges the L2-resident partials and
-//     writes the output -- one launch, no separate combine kernel.
+//     writes the output -- one launch, no separate combine kernel;
+//   - with fewer index lists than resident CTAs, every list is split into
+//     the same number (2..8) of segments and a list's segments run as one
+//     thread-block cluster: each CTA leaves its partial in its own shared
+//     memory and the cluster's first CTA merges them over distributed shared
+//     memory (two cluster barriers instead of a fence, an atomic and a round
+//     trip through L2).
 #include <limits.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -55,6 +62,7 @@ constexpr int kNoSlot = INT_MIN;              // marks a slot past topK
 constexpr int kRowPad = 16;                   // bytes of padding per smem row
 constexpr int kHeads = 8;                     // G <= 8: the N = 8 side of the MMAs
 constexpr int kLookahead = 8;                 // chunks of indices prefetched
+constexpr int kMaxCluster = 8;                // portable cluster size
 
 // Chunk ranges of the persistent CTAs.  Stream-K: equal contiguous ranges of
 // the flat chunk sequence (an index list may be split across CTAs, which then
@@ -67,13 +75,23 @@ struct DecodeSched {
     int ctas;        // grid size
     int seg_max;     // most CTAs sharing one index list
     int aligned;     // 1: ranges hold whole index lists
+    int cluster;     // >= 2: list u is split into `cluster` segments, run by the
+                     // thread-block cluster u (CTAs cluster * u + rank)
 };
 
 __host__ __device__ inline int64_t range_begin(int64_t c, const DecodeSched& s) {
+    if (s.cluster > 1) {
+        const int64_t u = c / s.cluster, j = c - u * s.cluster;
+        return u * s.cpu + (j * s.cpu) / s.cluster;
+    }
     return s.aligned ? (c * s.units / s.ctas) * s.cpu : c * s.total / s.ctas;
 }
 // CTA whose range holds chunk x.
 __host__ __device__ inline int64_t cta_of(int64_t x, const DecodeSched& s) {
+    if (s.cluster > 1) {
+        const int64_t u = x / s.cpu, j = x - u * s.cpu;
+        return u * s.cluster + ((j + 1) * s.cluster - 1) / s.cpu;
+    }
     return s.aligned ? ((x / s.cpu + 1) * s.ctas - 1) / s.units : ((x + 1) * s.ctas - 1) / s.total;
 }
 
@@ -178,6 +196,7 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
     constexpr int KT = DK / 16;      // k-steps of Q.K^T
     constexpr int NT = DV / 8;       // n-tiles of P.V
     static_assert(KT % 2 == 0 && NT % 2 == 0, "head dims must be multiples of 32 and 16");
+    static_assert(kHeads * DV * 4 + kHeads * 8 <= L::stage, "a cluster merge partial fits a stage");
 
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t smem_base = smem_u32(smem);
@@ -295,6 +314,13 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
         }
         // no copy may still be in flight when the warp leaves
         cp_async_wait<0>();
+        if (sch.cluster > 1) {
+            // the consumers' two cluster barriers of the merge count every
+            // thread of the cluster that has not exited: take part in both
+            __syncwarp();
+            cluster_sync();
+            cluster_sync();
+        }
         return;
     }
 
@@ -333,9 +359,6 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
             for (int e = 0; e < 4; ++e)
                 obuf[(warp * kHeads + hc + (e & 1)) * DV + 16 * mt + rq + 8 * (e >> 1)] = o[mt][e];
         named_sync(1, kConsThreads);
-        const int64_t first = u * sch.cpu, last = first + sch.cpu - 1;
-        const int64_t c_lo = cta_of(first, sch), c_hi = cta_of(last, sch);
-        const int nseg = (int)(c_hi - c_lo + 1);
         const UnitCoord uc = unit_coord(u, p);
         auto write_out = [&](int g, int d2, float M, float Ls, float ax, float ay) {
             const int n1 = uc.n2 * G + g;
@@ -347,6 +370,71 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
                 p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] =
                     empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
         };
+        if (sch.cluster > 1) {
+            // This CTA's state of the list (over its 4 warps) goes to its own
+            // stage area, idle now: every chunk of the range is consumed and
+            // no copy is in flight.  [G][DV] O, then [G] (max, sum).
+            float* part_o = reinterpret_cast<float*>(smem);
+            float2* part_ml = reinterpret_cast<float2*>(smem + kHeads * DV * 4);
+            for (int e = tid; e < G * (DV / 2); e += kConsThreads) {
+                const int g = e / (DV / 2), d2 = e % (DV / 2);
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsWarps; ++w) M = fmaxf(M, ml_buf[w * kHeads + g].x);
+                float Ls = 0.f, ax = 0.f, ay = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsWarps; ++w) {
+                    const float2 ml = ml_buf[w * kHeads + g];
+                    const float f = rescale_factor(ml.x, M);
+                    const float2 ov = *reinterpret_cast<const float2*>(obuf + (w * kHeads + g) * DV + 2 * d2);
+                    Ls += f * ml.y;
+                    ax += f * ov.x;
+                    ay += f * ov.y;
+                }
+                reinterpret_cast<float2*>(part_o + g * DV)[d2] = make_float2(ax, ay);
+                if (d2 == 0) part_ml[g] = make_float2(M, Ls);
+            }
+            // every CTA's partial is visible to the whole cluster ...
+            cluster_sync();
+            if (cluster_ctarank() == 0) {
+                // ... and the first CTA merges them, reading the others'
+                // shared memory (all loads issued before any use)
+                const int ncl = sch.cluster;
+                for (int e = tid; e < G * (DV / 2); e += kConsThreads) {
+                    const int g = e / (DV / 2), d2 = e % (DV / 2);
+                    const uint32_t a_ml = smem_u32(part_ml + g);
+                    const uint32_t a_o = smem_u32(part_o + g * DV + 2 * d2);
+                    float2 mv[kMaxCluster], ov[kMaxCluster];
+#pragma unroll
+                    for (int r = 0; r < kMaxCluster; ++r) {
+                        mv[r] = make_float2(-INFINITY, 0.f);
+                        ov[r] = make_float2(0.f, 0.f);
+                        if (r < ncl) {
+                            mv[r] = ld_cluster_f2(map_peer(a_ml, (uint32_t)r));
+                            ov[r] = ld_cluster_f2(map_peer(a_o, (uint32_t)r));
+                        }
+                    }
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, mv[r].x);
+                    float Ls = 0.f, ax = 0.f, ay = 0.f;
+#pragma unroll
+                    for (int r = 0; r < kMaxCluster; ++r) {
+                        const float f = rescale_factor(mv[r].x, M);
+                        Ls += f * mv[r].y;
+                        ax += f * ov[r].x;
+                        ay += f * ov[r].y;
+                    }
+                    write_out(g, d2, M, Ls, ax, ay);
+                }
+            }
+            // no CTA leaves while the first one may still read its memory
+            cluster_sync();
+            return;
+        }
+        const int64_t first = u * sch.cpu, last = first + sch.cpu - 1;
+        const int64_t c_lo = cta_of(first, sch), c_hi = cta_of(last, sch);
+        const int nseg = (int)(c_hi - c_lo + 1);
         for (int e = tid; e < G * (DV / 2); e += kConsThreads) {
             const int g = e / (DV / 2), d2 = e % (DV / 2);
             float M = -INFINITY;
@@ -545,7 +633,27 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    if (cur >= 0) flush(cur);
+    if (cur >= 0) {
+        flush(cur);
+    } else if (sch.cluster > 1) {
+        cluster_sync();     // (an empty range: every segment holds a chunk)
+        cluster_sync();
+    }
+}
+
+// Resident clusters of `cluster` CTAs of `kern` on the current device, asked
+// once per (kernel, device, cluster size).
+template <class K>
+int resident_clusters(K kern, int smem, int cluster) {
+    static std::atomic<int> known[kMaxDevices][kMaxCluster + 1];   // count + 1; 0: not asked
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int n = known[dev][cluster].load(std::memory_order_relaxed);
+    if (n == 0) {
+        n = max_active_clusters(kern, kThreads, smem, cluster) + 1;
+        known[dev][cluster].store(n, std::memory_order_relaxed);
+    }
+    return n - 1;
 }
 
 // Deepest ring that fits in shared memory next to the merge buffers, for
@@ -580,14 +688,22 @@ cudaError_t run_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaStrea
     // of segments (ctas = lists x segments), so that each range lies inside
     // one list -- a range that crosses into the next list pays a merge in
     // mid-range (measured on GQA decode, 128 lists of 16 chunks: 256 CTAs
-    // 18.6 us against 20.4 us for the 304 resident ones)
+    // 18.6 us against 20.4 us for the 304 resident ones).  With 2..8
+    // segments, and room for all the clusters at once, a list's segments run
+    // as one cluster and merge in distributed shared memory.
+    s.cluster = 0;
     if (!s.aligned && p.num_ctas == 0) {
         const int64_t seg = ctas / s.units;
-        if (seg >= 2) ctas = s.units * (seg < s.cpu ? seg : s.cpu);
+        if (seg >= 2) {
+            const int64_t nseg = seg < s.cpu ? seg : s.cpu;
+            ctas = s.units * nseg;
+            if (nseg <= kMaxCluster && resident_clusters(kern, L::total, (int)nseg) >= s.units)
+                s.cluster = (int)nseg;
+        }
     }
     if (ctas > (s.aligned ? s.units : s.total)) ctas = s.aligned ? s.units : s.total;
     s.ctas = (int)ctas;
-    if (s.aligned) {
+    if (s.aligned || s.cluster > 1) {
         s.seg_max = 1;
     } else {
         const int64_t lmin = s.total / s.ctas;             // shortest range
@@ -602,7 +718,7 @@ cudaError_t run_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaStrea
         p.ws_o = static_cast<float*>(ws);
         p.ws_ml = p.ws_o + rows * s.seg_max * p.Dv;
     }
-    err = launch_pdl(kern, dim3(s.ctas), dim3(kThreads), L::total, stream, p, s);
+    err = launch_pdl_clustered(kern, dim3(s.ctas), dim3(kThreads), L::total, stream, s.cluster, p, s);
     count_launches(1);
     return err;
 }

@@ -277,6 +277,33 @@ def test_decode_stream_k_partitions(B, S1, N2, topK, S2):
     run_and_check(case)
 
 
+@pytest.mark.parametrize("seg,topK,mix", [(2, 1024, False), (3, 1000, True), (5, 1000, False),
+                                          (7, 700, True), (8, 450, False), (8, 300, True)])
+def test_decode_cluster_merge(seg, topK, mix):
+    """Fewer index lists than resident CTAs (two per SM at these dims): each
+    list is cut into `seg` segments that run as one thread-block cluster and
+    merge through distributed shared memory -- ragged segments where the chunk
+    count is no multiple of seg, fewer segments than asked where a list holds
+    fewer chunks (topK = 300: 5 chunks), and, with `mix`, slots and whole
+    lists masked by the causal rule (empty partials in the merge).  The same
+    shape with the grid size forced takes the merge through the workspace;
+    both must match the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N2, S1 = 2, 2
+    B = max(1, (2 * sms) // seg // (N2 * S1))
+    kw = dict(index_kind="causal_mix", masked_frac=0.3, full_masked_rows=1) if mix else {}
+    case = small(B=B, S1=S1, N1=4 * N2, N2=N2, Dk=128, Dv=128, topK=topK, S2=topK + 300,
+                 causal=True, layout="BSND", dtype="bf16", seed=900 + seg, **kw)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    for opts in ({}, {"num_ctas": B * S1 * N2 * seg}):
+        out, lse = T.run_gpu(case, dev, **opts)
+        T.check_full(case, d, out, lse)
+        if mix:
+            assert torch.all(out[0, 0] == 0) and torch.all(torch.isneginf(lse[0, 0]))
+    assert sfa.sfa_get_last_error() == sfa.SFA_OK
+
+
 def test_workspace_shared_across_shapes():
     """Calls of different shapes and paths share the library-owned workspace:
     split partials of the generic path must never land in the arrival
