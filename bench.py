@@ -460,12 +460,17 @@ def gather_probe(case, replicas, reps, args, world, counts, kernel_ms):
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     sink = torch.empty(2 * sms * 4 + 64, dtype=torch.uint8, device="cuda")
 
-    def timed(idx_of):
+    def timed(idx_of, tma=False):
         def step(i):
             d = replicas[i % reps]
-            sfa.sfa_gather_probe(d["k"], d["v"], idx_of(d), case.B, case.S1, case.S2, case.N2,
-                                 case.Dk, case.Dv, case.topK, case.layout, sink,
-                                 torch.cuda.current_stream())
+            if tma:
+                sfa.sfa_gather_probe_tma(d["k"], d["v"], idx_of(d), case.B, case.S1, case.S2,
+                                         case.N2, case.Dk, case.Dv, case.topK, case.layout,
+                                         torch.cuda.current_stream())
+            else:
+                sfa.sfa_gather_probe(d["k"], d["v"], idx_of(d), case.B, case.S1, case.S2, case.N2,
+                                     case.Dk, case.Dv, case.topK, case.layout, sink,
+                                     torch.cuda.current_stream())
         for i in range(max(args.warmup, 3)):
             step(i)
         torch.cuda.synchronize()
@@ -476,6 +481,8 @@ def gather_probe(case, replicas, reps, args, world, counts, kernel_ms):
     out = {"what": "sfa_gather_probe: the same K/V rows read with coalesced 16-byte loads, no "
                    "arithmetic",
            "random_rows": timed(lambda d: d["idx"])}
+    # the same rows by TMA row gathers (tile::gather4), one CTA per SM
+    out["random_rows_tma_gather4"] = timed(lambda d: d["idx"], tma=True)
     # the kernel's gather rate as a fraction of the probe's (1.0 = the
     # attention kernel is as fast as reading its rows alone)
     out["kernel_frac_of_probe_rate"] = out["random_rows"]["ms_per_step"] / kernel_ms

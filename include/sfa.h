@@ -177,6 +177,21 @@ sfa_status sfa_gather_probe(const void* k, const void* v, const int32_t* sparse_
                             int S1, int S2, int N2, int Dk, int Dv, int topK, sfa_layout layout,
                             void* sink, size_t sink_bytes, sfa_stream_t stream);
 
+/*
+ * sfa_gather_probe_tma -- the same measurement probe with the rows moved by
+ * TMA row gathers (cp.async.bulk.tensor tile::gather4: four rows of a 2-D
+ * tensor map per copy, one copy per column box of up to 256 elements) into a
+ * ring of shared-memory stages, one CTA per SM; nothing reads the rows.
+ * k and v must be contiguous ([B][S2][N2][D] for BSND, [B][N2][S2][D] for
+ * BNSD), or v == k (the prefix view: K rows only).  Arguments otherwise as
+ * sfa_gather_probe, without the sink.  Errors: SFA_ERR_INVALID_ARG,
+ * SFA_ERR_UNSUPPORTED (B * S2 * N2 >= 2^31 rows, or rows too long for two
+ * 64-row stages), SFA_ERR_CUDA.
+ */
+sfa_status sfa_gather_probe_tma(const void* k, const void* v, const int32_t* sparse_idx, int B,
+                                int S1, int S2, int N2, int Dk, int Dv, int topK,
+                                sfa_layout layout, sfa_stream_t stream);
+
 /* Size of the device scratch array behind sfa_run_noalloc (8 MiB). */
 #define SFA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -35,7 +35,8 @@ EXPORTS = ("sfa_run", "sfa_run_ex", "sfa_workspace_size", "sfa_get_last_error",
            "varbsr_plan", "varbsr_plan_int_workspace_size", "varbsr_plan_dims", "varbsr_run",
            "varbsr_plan_destroy", "bsr_plan_set_logits_soft_cap",
            "varbsr_plan_set_logits_soft_cap", "bsr_plan_set_kv_layout",
-           "bsr_plan_set_data_types", "bsr_run_scaled", "sfa_gather_probe")
+           "bsr_plan_set_data_types", "bsr_run_scaled", "sfa_gather_probe",
+           "sfa_gather_probe_tma")
 
 
 class SfaError(RuntimeError):
@@ -121,6 +122,8 @@ def load():
             lib.bsr_run_scaled.restype = ci
             lib.sfa_gather_probe.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, sz, vp]
             lib.sfa_gather_probe.restype = ci
+            lib.sfa_gather_probe_tma.argtypes = [vp, vp, vp] + [ci] * 8 + [vp]
+            lib.sfa_gather_probe_tma.restype = ci
             _lib = lib
     return _lib
 
@@ -209,6 +212,14 @@ def sfa_gather_probe(k, v, sparse_idx, B, S1, S2, N2, Dk, Dv, topK, layout, sink
                                    topK, _enum(layout, LAYOUTS), _ptr(sink),
                                    sink.numel() * sink.element_size(), _stream(stream)),
            "sfa_gather_probe")
+
+
+def sfa_gather_probe_tma(k, v, sparse_idx, B, S1, S2, N2, Dk, Dv, topK, layout, stream=None):
+    """Forwards to sfa_gather_probe_tma() (measurement only): the same rows
+    moved by TMA row gathers (k, v contiguous, or v is k)."""
+    _check(load().sfa_gather_probe_tma(_ptr(k), _ptr(v), _ptr(sparse_idx), B, S1, S2, N2, Dk, Dv,
+                                       topK, _enum(layout, LAYOUTS), _stream(stream)),
+           "sfa_gather_probe_tma")
 
 
 def sfa_workspace_size(B, S1, N1, N2, Dk, Dv, topK, num_splits=0) -> int:

@@ -405,8 +405,7 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 
 // ---- host: tensor maps (shared with the 128-key kernel) ------------------
 
-namespace {
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     std::call_once(once, [] {
@@ -420,6 +419,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
 }  // namespace
 
 // 3-D map over a [rows][heads][dim] tensor: box = 64 dims x hb heads x rb rows,
@@ -480,6 +481,24 @@ bool make_map8_hnd(CUtensorMap* map, const void* base, int dim, int rows, int he
     const cuuint32_t estride[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstride,
                     box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 2-D map over `rows` rows of `width` 16-bit elements, `row_stride`
+// elements apart: box = box_w elements x 1 row, no swizzle (the row-gather
+// form: each tile::gather4 copy moves four such boxes of four rows).
+bool make_rows_map(CUtensorMap* map, const void* base, bool bf16, int width, int64_t rows,
+                   int64_t row_stride, int box_w) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t gdim[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)row_stride * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_w, 1};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void*>(base), gdim, gstride, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -146,6 +147,12 @@ bool make_map(CUtensorMap* map, const void* base, bool bf16, int dim, int heads,
               int rb);
 bool make_map_hnd(CUtensorMap* map, const void* base, bool bf16, int dim, int rows, int heads,
                   int rb, int hb);
+// 2-D map over `rows` rows of `width` 16-bit elements, row_stride elements
+// apart; box = box_w elements x 1 row, no swizzle (tile::gather4 copies).
+bool make_rows_map(CUtensorMap* map, const void* base, bool bf16, int width, int64_t rows,
+                   int64_t row_stride, int box_w);
+// The driver's cuTensorMapEncodeTiled (nullptr if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // The same over 8-bit elements, box 128 elements (128 bytes) wide.
 bool make_map8(CUtensorMap* map, const void* base, int dim, int heads, int rows, int hb, int rb);
 bool make_map8_hnd(CUtensorMap* map, const void* base, int dim, int rows, int heads, int rb,

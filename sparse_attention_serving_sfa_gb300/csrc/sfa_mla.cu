@@ -632,19 +632,7 @@ __global__ void __launch_bounds__(512) sfa_mla_combine(const SfaParams p, const 
         p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] = empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                            &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
 
 // 4-D maps of q ordered by stride: {d, head, s1, b} when heads are adjacent
 // (BSND), else {d, s1, head, b}.  Box = `box_d` dims x 128 heads: 64 dims with

@@ -243,6 +243,19 @@ def test_gather_probe_rejects_bad_arguments(lib):
                                 None) == sfa.SFA_ERR_INVALID_ARG     # unaligned indices
 
 
+def test_tma_gather_probe_rejects_bad_arguments(lib):
+    assert lib.sfa_gather_probe_tma(None, FAKE, FAKE, 1, 1, 8, 1, 64, 64, 4, 0,
+                                    None) == sfa.SFA_ERR_INVALID_ARG
+    assert lib.sfa_gather_probe_tma(FAKE, FAKE, FAKE, 1, 1, 8, 1, 64, 64, 9, 0,
+                                    None) == sfa.SFA_ERR_INVALID_ARG     # topK > S2
+    assert lib.sfa_gather_probe_tma(FAKE, FAKE, FAKE, 1, 1, 8, 1, 96, 64, 4, 0,
+                                    None) == sfa.SFA_ERR_INVALID_ARG     # Dk % 64
+    assert lib.sfa_gather_probe_tma(FAKE, FAKE, FAKE, 1, 1, 8, 1, 64, 64, 4, 2,
+                                    None) == sfa.SFA_ERR_INVALID_ARG     # layout
+    assert lib.sfa_gather_probe_tma(FAKE, FAKE, FAKE, 1 << 16, 1, 1 << 14, 8, 64, 64, 4, 0,
+                                    None) == sfa.SFA_ERR_UNSUPPORTED     # 2^33 rows
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(sfa, "LIB_PATH", str(tmp_path / "absent.so"))
     monkeypatch.setattr(sfa, "_lib", None)
