@@ -127,9 +127,11 @@ typedef struct {
     /* Number of topK splits of the generic path; 0 = chosen from the SM
      * count. */
     int num_splits;
-    /* Launch tuning of the small-group path (G <= 8): persistent CTAs per SM
-     * (1 = deep shared-memory ring, 2 = two CTAs with shallow rings) and the
-     * total number of CTAs (chunk ranges).  0 = automatic. */
+    /* Launch tuning of the small-group paths.  ctas_per_sm (G <= 8):
+     * persistent CTAs per SM of the warp-MMA kernel (1 = deep shared-memory
+     * ring, 2 = two CTAs with shallow rings).  num_ctas: the total number of
+     * CTAs (chunk or index-list ranges) of that kernel, or of the tensor-core
+     * kernel for many index lists of 9 to 16 heads.  0 = automatic. */
     int ctas_per_sm;
     int num_ctas;
 } sfa_options;

@@ -42,6 +42,13 @@ Plan choose_plan(const SfaParams& p, sfa_dtype, int num_sms, int forced_splits) 
         pl.extra_ws_bytes = mla_ws_bytes(p);
         return pl;
     }
+    if (forced_splits <= 0 && group_tc_supported(p, num_sms)) {
+        // whole index lists per CTA: no splits, no workspace
+        pl.kind = PATH_GROUP_TC;
+        pl.splits = 1;
+        pl.slots_per_split = p.topK;
+        return pl;
+    }
     if (decode_supported(p)) {
         // persistent stream-K kernel: its own schedule, partials in extra_ws
         pl.kind = PATH_DECODE;
@@ -73,6 +80,7 @@ cudaError_t run_plan(const Plan& plan, SfaParams& p, sfa_dtype dtype, void* extr
         return launch_sfa_mla(p, dtype, num_sms, extra_ws, plan.extra_ws_bytes, stream);
     if (plan.kind == PATH_DECODE)
         return launch_sfa_decode(p, dtype, num_sms, extra_ws, plan.extra_ws_bytes, stream);
+    if (plan.kind == PATH_GROUP_TC) return launch_sfa_group_tc(p, dtype, num_sms, stream);
     cudaError_t err = launch_sfa_generic(p, dtype, stream);
     if (err != cudaSuccess) return err;
     if (p.splits > 1) err = launch_sfa_combine(p, dtype, stream);

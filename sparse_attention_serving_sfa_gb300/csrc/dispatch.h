@@ -9,6 +9,7 @@ enum PathKind {
     PATH_GENERIC = 0,  // warp-FMA kernel, any supported shape
     PATH_DECODE = 1,   // small-group persistent gather kernel (sfa_decode.cu)
     PATH_MLA = 2,      // 128-head MLA tensor-core kernel (sfa_mla.cu)
+    PATH_GROUP_TC = 3, // many index lists, 8 < G <= 16, Dv = 128: tensor cores (sfa_group_tc.cu)
 };
 
 struct Plan {

@@ -70,6 +70,13 @@ size_t decode_ws_bytes(const SfaParams& p);
 cudaError_t launch_sfa_decode(const SfaParams& p, sfa_dtype dtype, int num_sms, void* ws,
                               size_t ws_bytes, cudaStream_t stream);
 
+// Small-group tensor-core path (8 < G <= 16, Dv == 128, Dk in {128, 192,
+// 256}, at least four index lists per CTA of a one-per-SM grid): slots on the
+// MMA M side, whole lists per CTA, no workspace.
+bool group_tc_supported(const SfaParams& p, int num_sms);
+cudaError_t launch_sfa_group_tc(const SfaParams& p, sfa_dtype dtype, int num_sms,
+                                cudaStream_t stream);
+
 // MLA path (G == 128 query heads per index list, Dk == 576, Dv == 512, value
 // = key prefix): 2-CTA cluster tensor-core kernel, stream-K over chunks with
 // an in-kernel merge of split units.  mla_ws_bytes bounds its workspace.

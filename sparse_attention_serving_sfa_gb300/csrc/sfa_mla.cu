@@ -341,12 +341,14 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
                     qk(next_qk++);
                     continue;
                 }
-                if (next_qk < unit_end && next_qk == i + 1 &&
-                    mbar_try_wait(bar(B_KV_FULL + next_qk % kStages), (next_qk / kStages) & 1)) {
-                    qk(next_qk++);
-                    continue;
-                }
-                if (!mbar_try_wait(bar(B_P_FULL + i % kBufs), (i / kBufs) & 1)) {
+                // P.V of chunk i as soon as its P is written (it frees the
+                // stage); until then Q.K^T of the next chunk if its rows are in
+                if (!mbar_test_wait(bar(B_P_FULL + i % kBufs), (i / kBufs) & 1)) {
+                    if (next_qk < unit_end && next_qk == i + 1 &&
+                        mbar_test_wait(bar(B_KV_FULL + next_qk % kStages), (next_qk / kStages) & 1)) {
+                        qk(next_qk++);
+                        continue;
+                    }
                     // nothing to issue yet: poll, with the same bound as the waits
                     if (*abort_flag) {
                         ok = false;

@@ -318,6 +318,93 @@ def test_workspace_shared_across_shapes():
 
 
 # ---------------------------------------------------------------------------
+# many index lists (at least four per CTA) of small groups: 9 to 16 query
+# heads per list (Dv = 128, Dk in {128, 192, 256}) take the tensor-core kernel
+# (slots on the MMA's M side in 128-slot chunks, whole lists per CTA), up to 8
+# the warp-MMA kernel's whole-list schedule.  num_ctas shrinks the grid so
+# that small shapes take these schedules.
+
+def tc_case(**kw):
+    base = dict(name="tc", B=2, S1=24, S2=600, N1=24, N2=2, Dk=128, Dv=128, topK=300,
+                dtype="bf16", layout="BSND", causal=True, scale=0.09, seed=5151)
+    base.update(kw)
+    return synth.SfaCase(**base)
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 8, 9, 12, 16])
+@pytest.mark.parametrize("Dk,prefix", [(128, False), (128, True), (192, True), (256, False),
+                                       (256, True)])
+def test_group_tc_shapes(G, Dk, prefix):
+    case = tc_case(N1=2 * G, Dk=Dk, value_is_key_prefix=prefix, dtype="f16" if G % 2 else "bf16",
+                   seed=5200 + G)
+    run_and_check(case, num_ctas=8)
+
+
+@pytest.mark.parametrize("topK,S2", [(1, 30), (100, 300), (128, 128), (129, 400), (255, 256),
+                                     (640, 2000)])
+def test_group_tc_ragged_topk(topK, S2):
+    """Partial last chunks (slots past topK zero-filled and masked), a single
+    slot, exactly one chunk, and topK = S2."""
+    run_and_check(tc_case(topK=topK, S2=S2, N1=32, N2=2, seed=5300 + topK), num_ctas=6)
+
+
+@pytest.mark.parametrize("layout", ["BSND", "BNSD"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_group_tc_layouts_dtypes(layout, dtype, causal):
+    run_and_check(tc_case(layout=layout, dtype=dtype, causal=causal, S1=40, S2=200, topK=170),
+                  num_ctas=10)
+
+
+@pytest.mark.parametrize("num_ctas", [1, 3, 7, 0])
+def test_group_tc_grid_sizes(num_ctas):
+    """Ranges of whole index lists: one CTA for everything, ragged ranges
+    (lists % CTAs != 0), and the default one-per-SM grid (640 lists)."""
+    case = tc_case(B=4, S1=80, N1=20, N2=2, topK=200, S2=500, seed=5400 + num_ctas)
+    run_and_check(case, num_ctas=num_ctas)
+
+
+def test_group_tc_masked_rows_and_rescale():
+    """Whole lists above the causal diagonal (+0 rows, lse = -inf) and a large
+    scale: scores grow across chunks by far more than the lazy-rescale
+    threshold, so O is rescaled many times."""
+    case = tc_case(S1=40, S2=700, topK=600, N1=32, N2=2, index_kind="causal_mix",
+                   masked_frac=0.3, full_masked_rows=5, scale=1.5)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    out, lse = T.run_gpu(case, dev, num_ctas=8)
+    T.check_full(case, d, out, lse)
+    assert torch.all(out[0, :5] == 0) and torch.all(torch.isneginf(lse[0, :5]))
+
+
+def test_group_tc_out_of_range_indices():
+    case = tc_case(topK=200, S2=400, S1=20)
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    bad = dev["idx"].clone()
+    bad[1, 3, 1, 5:9] = torch.tensor([-1, 400, 1 << 30, -(1 << 30)], dtype=torch.int32)
+    out, lse = T.run_gpu(case, dict(dev, idx=bad), validate_indices=True, num_ctas=5)
+    assert sfa.sfa_get_last_error() == sfa.SFA_ERR_INDEX_RANGE
+    # the bad slots of list (b 1, s1 3, n2 1) act as masked: the same as slots
+    # whose index lies above that list's causal diagonal (s1 + S2 - S1 = 383)
+    d2 = dict(d)
+    d2["idx"] = d["idx"].clone()
+    d2["idx"][1, 3, 1, 5:9] = 399
+    T.check_full(case, d2, out, lse)
+
+
+def test_group_tc_and_cuda_core_kernels_agree_with_oracle():
+    """The same many-list shape of 16 heads per list on the tensor-core kernel
+    and on the CUDA-core kernel (a forced split count selects the latter)."""
+    case = tc_case(S1=40, N1=64, N2=4, topK=256, S2=512, dtype="f16")
+    d = synth.make_sfa_inputs(case)
+    dev = T.to_dev(d)
+    for opts in ({"num_ctas": 8}, {"num_splits": 2}):
+        out, lse = T.run_gpu(case, dev, **opts)
+        T.check_full(case, d, out, lse)
+
+
+# ---------------------------------------------------------------------------
 # MLA tensor-core path (128 heads per index list, Dk = 576, Dv = 512, value =
 # key prefix): 2-CTA clusters, stream-K with in-kernel merge
 
