@@ -122,36 +122,6 @@ __device__ __forceinline__ uint64_t causal_bits64(int64_t lim) {
     return lim < 0 ? 0ull : (lim >= 63 ? ~0ull : ((2ull << lim) - 1ull));
 }
 
-// 16 columns from the even (ODD = 0) or odd (ODD = 1) entries of r[0..32).
-template <int ODD>
-__device__ __forceinline__ void tmem_st16_strided(uint32_t taddr, const uint32_t (&r)[64]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0 + ODD]), "r"(r[2 + ODD]), "r"(r[4 + ODD]), "r"(r[6 + ODD]), "r"(r[8 + ODD]),
-        "r"(r[10 + ODD]), "r"(r[12 + ODD]), "r"(r[14 + ODD]), "r"(r[16 + ODD]), "r"(r[18 + ODD]),
-        "r"(r[20 + ODD]), "r"(r[22 + ODD]), "r"(r[24 + ODD]), "r"(r[26 + ODD]), "r"(r[28 + ODD]),
-        "r"(r[30 + ODD])
-        : "memory");
-}
-
-// 32 columns from the even (ODD = 0) or odd (ODD = 1) entries of r[64].
-template <int ODD>
-__device__ __forceinline__ void tmem_st32_strided(uint32_t taddr, const uint32_t (&r)[64]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0 + ODD]), "r"(r[2 + ODD]), "r"(r[4 + ODD]), "r"(r[6 + ODD]), "r"(r[8 + ODD]),
-        "r"(r[10 + ODD]), "r"(r[12 + ODD]), "r"(r[14 + ODD]), "r"(r[16 + ODD]), "r"(r[18 + ODD]),
-        "r"(r[20 + ODD]), "r"(r[22 + ODD]), "r"(r[24 + ODD]), "r"(r[26 + ODD]), "r"(r[28 + ODD]),
-        "r"(r[30 + ODD]), "r"(r[32 + ODD]), "r"(r[34 + ODD]), "r"(r[36 + ODD]), "r"(r[38 + ODD]),
-        "r"(r[40 + ODD]), "r"(r[42 + ODD]), "r"(r[44 + ODD]), "r"(r[46 + ODD]), "r"(r[48 + ODD]),
-        "r"(r[50 + ODD]), "r"(r[52 + ODD]), "r"(r[54 + ODD]), "r"(r[56 + ODD]), "r"(r[58 + ODD]),
-        "r"(r[60 + ODD]), "r"(r[62 + ODD])
-        : "memory");
-}
-
 // Per mode (measured): the causal and variable modes hand P to the tensor
 // core in two halves and skip a second M-tile that has no rows of the item
 // (row blocks of any size); plain blocks do neither (both measured slower

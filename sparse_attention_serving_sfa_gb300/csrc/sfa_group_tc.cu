@@ -126,16 +126,6 @@ __device__ __forceinline__ UnitCoord unit_coord(int64_t u, const SfaParams& p) {
     return c;
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
@@ -289,6 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1) sfa_group_tc_kernel(const SfaPara
         int ring[kLookahead];
 #pragma unroll
         for (int r = 0; r < kLookahead; ++r) ring[r] = fetch();
+        // stage s's visibility mask and arrivals: every producer thread
+        // arrives, lane 0 after writing its warp's mask
+        auto release = [&](int s, uint32_t m) {
+            if (lane == 0) reinterpret_cast<uint32_t*>(smem + L::meta)[4 * s + pw] = m;
+            __syncwarp();
+            mbar_arrive(bar(B_KV_FULL + s));
+            if (lane == 0) mbar_arrive(bar(B_KV_FULL + s));
+        };
+        uint32_t prev_mask = 0;
+        int released = -1;                  // last chunk whose copies were issued
         for (int i = 0; i < n; ++i) {
             const int s = i % NS;
             if (!mbar_wait(bar(B_KV_FREE + s), ((i / NS) & 1) ^ 1, p.err_word, abort_flag)) break;
@@ -336,13 +336,26 @@ __global__ void __launch_bounds__(kThreads, 1) sfa_group_tc_kernel(const SfaPara
                                 qg + (int64_t)(uc.n2 * G + h) * p.q_sh + 8 * pc);
                 }
             }
-            cp_async_mbar_arrive(bar(B_KV_FULL + s));
+            cp_async_commit();
+            // The tensor core reads the rows (async proxy): a stage is
+            // released once its copies have landed and the thread that made
+            // them has fenced them -- one chunk late, so that two chunks'
+            // copies stay in flight.
             const uint32_t mask = __ballot_sync(0xffffffffu, vis);
-            if (lane == 0) {
-                reinterpret_cast<uint32_t*>(smem + L::meta)[4 * s + pw] = mask;
-                mbar_arrive(bar(B_KV_FULL + s));
+            if (i > 0) {
+                cp_async_wait<1>();
+                fence_proxy_async_smem();
+                release((i - 1) % NS, prev_mask);
             }
+            prev_mask = mask;
             advance(k);
+            released = i;
+        }
+        if (released >= 0) {
+            // the last chunk issued
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            release(released % NS, prev_mask);
         }
         // no copy may still be in flight when the warp leaves
         cp_async_wait<0>();
@@ -352,7 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1) sfa_group_tc_kernel(const SfaPara
             bool ok = true;
             auto qk = [&](int j) {
                 const int s = j % NS;
-                fence_proxy_async_smem();     // cp.async (generic proxy) data -> tensor core
                 tc_fence_after();
                 const uint32_t st = sbase + s * L::stage;
                 const uint32_t d = tmem + TM::sBuf * (j & 1);
@@ -459,11 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1) sfa_group_tc_kernel(const SfaPara
             uint32_t sv[KP * kN];
             {
                 const uint32_t sa = lane_base + TM::sBuf * b;
-                tmem_ld32(sa, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                if constexpr (KP == 3) tmem_ld16(sa + 32, *reinterpret_cast<uint32_t(*)[16]>(&sv[32]));
-                if constexpr (KP == 4) tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                if constexpr (KP == 2) tmem_ld32_sync(sa, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                if constexpr (KP == 3) tmem_ld48_sync(sa, *reinterpret_cast<uint32_t(*)[48]>(&sv[0]));
+                if constexpr (KP == 4) tmem_ld64_sync(sa, *reinterpret_cast<uint32_t(*)[64]>(&sv[0]));
             }
-            tmem_wait_ld();
             float x[GP], cm[GP];
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
@@ -504,8 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfa_group_tc_kernel(const SfaPara
                 for (int a = 0; a < 2; ++a) {
                     uint32_t ov[32];
                     const uint32_t oa = lane_base + (a ? TM::o1 : TM::o0);
-                    tmem_ld32(oa, ov);
-                    tmem_wait_ld();
+                    tmem_ld32_sync(oa, ov);
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
                         ov[c] = __float_as_uint(__uint_as_float(ov[c]) * ((c & 15) < GP ? f[(c & 15) % GP] : 1.f));
@@ -544,9 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1) sfa_group_tc_kernel(const SfaPara
             const float wl = warp_reduce_scatter<GP, false>(ls, lane);
             if ((lane & (32 / GP - 1)) == 0) redl[warp * kN + my_head] = wl;
             uint32_t ov[32], ow[32];
-            tmem_ld32(lane_base + TM::o0, ov);
-            tmem_ld32(lane_base + TM::o1, ow);
-            tmem_wait_ld();
+            tmem_ld32_sync(lane_base + TM::o0, ov);
+            tmem_ld32_sync(lane_base + TM::o1, ow);
             tc_fence_before();
             named_sync(1, kSoftThreads);
             const int64_t u = cg / cpu;
