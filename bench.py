@@ -302,22 +302,84 @@ def device_time(step, steps, eager, world):
     return ms, int(launches), mode
 
 
-def e2e_time(step_host, n, warm, world):
-    """Event-timed eager calls of step_host(i), each copying its inputs in from
-    pinned host memory and its outputs back."""
+E2E_SCHEDULE = ("every step copies its inputs in from pinned host memory and its outputs back; "
+                "two device buffer sets, copies on two copy streams overlapping the neighbouring "
+                "steps' calls")
+
+
+def e2e_time(h2d, compute, d2h, n, warm, world, eager=False):
+    """Event-timed end-to-end steps through the public API, run as a serving
+    loop runs them: two sets of device buffers; step i's inputs copy in from
+    pinned host memory on a copy stream while step i - 1 computes, its call
+    runs once they have landed, and its outputs copy back to pinned host
+    memory on a second copy stream while step i + 1 computes.  The timed
+    region holds every step's copies in and out and ends when the last
+    step's outputs are on the host.  h2d(i, b), compute(i, b) and d2h(i, b)
+    issue step i's work on buffer set b on the current stream.  As for the
+    device time, the n steps are captured once into a CUDA graph (copies,
+    calls and the streams' event edges) and replayed, unless `eager` or the
+    capture fails.  Returns (ms per step, how the steps were launched)."""
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(2)]   # inputs of set b landed
+    done = [torch.cuda.Event() for _ in range(2)]    # the call on set b finished
+    back = [torch.cuda.Event() for _ in range(2)]    # outputs of set b on the host
+
+    def run(m):
+        cs = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(cs)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        with torch.cuda.stream(s_in):
+            h2d(0, 0)
+            ready[0].record(s_in)
+        for i in range(m):
+            b = i & 1
+            if i + 1 < m:
+                if i >= 1:
+                    s_in.wait_event(done[b ^ 1])      # step i - 1 has read set b ^ 1
+                with torch.cuda.stream(s_in):
+                    h2d(i + 1, b ^ 1)
+                    ready[b ^ 1].record(s_in)
+            cs.wait_event(ready[b])
+            if i >= 2:
+                cs.wait_event(back[b])                # step i - 2's outputs are out
+            compute(i, b)
+            done[b].record(cs)
+            s_out.wait_event(done[b])
+            with torch.cuda.stream(s_out):
+                d2h(i, b)
+                back[b].record(s_out)
+        for b in range(min(m, 2)):
+            cs.wait_event(back[b])
+
     stream = torch.cuda.current_stream()
-    for i in range(warm):
-        step_host(i)
+    run(warm)
     torch.cuda.synchronize()
+    graph, mode = None, "eager"
+    if not eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+                run(n)
+            graph.replay()           # one untimed replay
+            torch.cuda.synchronize()
+            mode = f"CUDA graph of the {n} steps (copies and calls), replayed once"
+        except Exception as e:  # noqa: BLE001 - fall back to eager steps
+            graph = None
+            mode = f"eager (graph capture failed: {type(e).__name__})"
+            torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     ev0.record(stream)
-    for i in range(n):
-        step_host(i)
+    if graph is not None:
+        graph.replay()
+    else:
+        run(n)
     ev1.record(stream)
     torch.cuda.synchronize()
-    return max_over_ranks(ev0.elapsed_time(ev1) / n, world, "cuda")
+    return max_over_ranks(ev0.elapsed_time(ev1) / n, world, "cuda"), mode
 
 
 def nbytes(t):
@@ -371,10 +433,11 @@ def run_sfa(name, args, world, rank, cpu_target_s):
                                       case.topK)
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
 
-    def call(d, q=None, idx=None):
+    def call(d, q=None, idx=None, o=None, l=None):
         sfa.sfa_run_ex(d["q"] if q is None else q, d["k"], d["v"], d["idx"] if idx is None else idx,
                        case.B, case.S1, case.S2, case.N1, case.N2, case.Dk, case.Dv, case.topK,
-                       case.scale, case.layout, case.causal, case.dtype, out, lse,
+                       case.scale, case.layout, case.causal, case.dtype,
+                       out if o is None else o, lse if l is None else l,
                        torch.cuda.current_stream(), workspace=ws, value_is_key_prefix=prefix)
 
     for i in range(max(args.warmup, 3) + reps):
@@ -399,19 +462,26 @@ def run_sfa(name, args, world, rank, cpu_target_s):
         hq, hidx = host["q"].pin_memory(), host["idx"].pin_memory()
         hout = torch.empty(out_shape, dtype=tdt).pin_memory()
         hlse = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
-        dq, didx = torch.empty_like(replicas[0]["q"]), torch.empty_like(replicas[0]["idx"])
+        sets = [{"q": torch.empty_like(replicas[0]["q"]), "idx": torch.empty_like(replicas[0]["idx"]),
+                 "out": torch.empty_like(out), "lse": torch.empty_like(lse)} for _ in range(2)]
 
-        def step_host(i):
-            dq.copy_(hq, non_blocking=True)
-            didx.copy_(hidx, non_blocking=True)
-            call(replicas[i % reps], q=dq, idx=didx)
-            hout.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
+        def h2d(i, b):
+            sets[b]["q"].copy_(hq, non_blocking=True)
+            sets[b]["idx"].copy_(hidx, non_blocking=True)
+
+        def compute(i, b):
+            t = sets[b]
+            call(replicas[i % reps], q=t["q"], idx=t["idx"], o=t["out"], l=t["lse"])
+
+        def d2h(i, b):
+            hout.copy_(sets[b]["out"], non_blocking=True)
+            hlse.copy_(sets[b]["lse"], non_blocking=True)
 
         n_e2e = max(min(args.steps, 50), 5)
-        e_ms = e2e_time(step_host, n_e2e, min(reps, 3), world)
+        e_ms, e_mode = e2e_time(h2d, compute, d2h, n_e2e, min(reps, 3), world, args.eager)
         e2e = {"value": whole_job_rate(counts["gathered_bytes"], e_ms, world) / 1e9,
-               "unit": "GB/s", "ms_per_step": e_ms, "steps": n_e2e,
+               "unit": "GB/s", "ms_per_step": e_ms, "steps": n_e2e, "schedule": E2E_SCHEDULE,
+               "launch": e_mode,
                "h2d_bytes_per_step": nbytes(hq) + nbytes(hidx),
                "d2h_bytes_per_step": nbytes(hout) + nbytes(hlse)}
 
@@ -581,8 +651,9 @@ def run_bsr(name, args, world, rank, cpu_target_s):
     out = torch.empty(q.shape, dtype=out_dtype, device="cuda")
     lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
 
-    def call(qq):
-        run(plan, qq, k, v, out, lse, torch.cuda.current_stream())
+    def call(qq, o=None, l=None):
+        run(plan, qq, k, v, out if o is None else o, lse if l is None else l,
+            torch.cuda.current_stream())
 
     for _ in range(max(args.warmup, 3)):
         call(q)
@@ -600,18 +671,24 @@ def run_bsr(name, args, world, rank, cpu_target_s):
         hq = x["q"].pin_memory()
         hout = torch.empty(hq.shape, dtype=out_dtype).pin_memory()
         hlse = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
-        dq = torch.empty_like(q)
+        sets = [{"q": torch.empty_like(q), "out": torch.empty_like(out), "lse": torch.empty_like(lse)}
+                for _ in range(2)]
 
-        def step_host(i):
-            dq.copy_(hq, non_blocking=True)
-            call(dq)
-            hout.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
+        def h2d(i, b):
+            sets[b]["q"].copy_(hq, non_blocking=True)
+
+        def compute(i, b):
+            call(sets[b]["q"], o=sets[b]["out"], l=sets[b]["lse"])
+
+        def d2h(i, b):
+            hout.copy_(sets[b]["out"], non_blocking=True)
+            hlse.copy_(sets[b]["lse"], non_blocking=True)
 
         n_e2e = max(min(args.steps, 20), 5)
-        e_ms = e2e_time(step_host, n_e2e, 2, world)
+        e_ms, e_mode = e2e_time(h2d, compute, d2h, n_e2e, 2, world, args.eager)
         e2e = {"value": whole_job_rate(counts["flops"], e_ms, world) / 1e12, "unit": "TFLOP/s",
-               "ms_per_step": e_ms, "steps": n_e2e, "h2d_bytes_per_step": nbytes(hq),
+               "ms_per_step": e_ms, "steps": n_e2e, "schedule": E2E_SCHEDULE, "launch": e_mode,
+               "h2d_bytes_per_step": nbytes(hq),
                "d2h_bytes_per_step": nbytes(hout) + nbytes(hlse)}
 
     peaks, peak_src = load_peaks()
