@@ -1,6 +1,6 @@
 // C ABI of the variable block-sparse path ("flashinfer.sparse",
 // VariableBlockSparseAttentionWrapper): plan() turns each kv head's block
-// mask map and block sizes into key tile lists and a work list, uploads them
+// mask map and block sizes into key window lists and a work list, uploads them
 // into the caller's int workspace; run() launches the tensor-core BSR kernel
 // in its variable mode with that plan.
 #include <math.h>
@@ -28,14 +28,15 @@ struct varbsr_plan_s {
 
 namespace {
 
-constexpr int kTileKeys = 64;
+constexpr int kTileKeys = 64;   // keys of a window (two 32-key halves)
+constexpr int kHalfKeys = 32;
 
 size_t round4(size_t n) { return (n + 3) & ~size_t(3); }
 
 struct Built {
     int M = 0, N = 0;
     std::vector<int32_t> lists;     // nlists + 1 offsets into tiles
-    std::vector<int32_t> tiles;     // 4 ints each: key0, mask lo, mask hi, 0
+    std::vector<int32_t> tiles;     // 4 ints each: key0, mask of half 0, mask of half 1, key1
     std::vector<int32_t> items;     // 4 ints each: list, row0, kv head, row end
 };
 
@@ -49,20 +50,36 @@ sfa_status check_args(const uint8_t* mm, const int32_t* rs, const int32_t* cs, i
     return SFA_OK;
 }
 
-// Key tiles of one (kv head, row block): the allowed key columns (set blocks,
-// and with causal only keys <= limit) covered greedily by 64-key windows, each
-// starting at the first allowed key not yet covered -- the fewest windows that
-// cover the set.
+// Key windows of one (kv head, row block): the allowed key columns (set
+// blocks, and with causal only keys <= limit) covered greedily by 32-key
+// halves, each starting at the first allowed key not yet covered (the fewest
+// halves that cover the set), paired in order into 64-key windows: {first
+// key of half 0, mask of half 0, mask of half 1, first key of half 1}, bit j
+// of a half's mask = its key j allowed.  An odd last half is paired with an
+// empty one at key n_keys (rows past the end of the keys: read as zeros,
+// all masked).
 void tile_row_block(const uint8_t* mrow, const int32_t* cs, int NB, int64_t limit,
-                    std::vector<int32_t>& tiles) {
+                    int64_t n_keys, std::vector<int32_t>& tiles) {
     int64_t key0 = -1;
-    uint64_t bits = 0;
+    uint32_t bits = 0;
+    int64_t pend_key = -1;              // a finished half waiting for its pair
+    uint32_t pend_bits = 0;
+    auto emit_half = [&](int64_t k, uint32_t m) {
+        if (pend_key < 0) {
+            pend_key = k;
+            pend_bits = m;
+            return;
+        }
+        tiles.push_back((int32_t)pend_key);
+        tiles.push_back((int32_t)pend_bits);
+        tiles.push_back((int32_t)m);
+        tiles.push_back((int32_t)k);
+        pend_key = -1;
+    };
     auto flush = [&] {
-        if (key0 < 0) return;
-        tiles.push_back((int32_t)key0);
-        tiles.push_back((int32_t)(uint32_t)bits);
-        tiles.push_back((int32_t)(uint32_t)(bits >> 32));
-        tiles.push_back(0);
+        if (key0 >= 0) emit_half(key0, bits);
+        key0 = -1;
+        bits = 0;
     };
     int64_t c0 = 0;
     for (int cb = 0; cb < NB; ++cb) {
@@ -71,18 +88,18 @@ void tile_row_block(const uint8_t* mrow, const int32_t* cs, int NB, int64_t limi
         c0 += cs[cb];
         if (!mrow[cb]) continue;
         while (a < b) {
-            if (key0 < 0 || a >= key0 + kTileKeys) {
+            if (key0 < 0 || a >= key0 + kHalfKeys) {
                 flush();
                 key0 = a;
-                bits = 0;
             }
-            const int64_t e = std::min(b, key0 + kTileKeys);
+            const int64_t e = std::min(b, key0 + kHalfKeys);
             const int o0 = (int)(a - key0), n = (int)(e - a);
-            bits |= (n == 64 ? ~0ull : ((1ull << n) - 1ull)) << o0;
+            bits |= (n == 32 ? ~0u : ((1u << n) - 1u)) << o0;
             a = e;
         }
     }
     flush();
+    if (pend_key >= 0) emit_half(n_keys, 0u);
 }
 
 sfa_status build(const uint8_t* mm, const int32_t* rs, const int32_t* cs, int MB, int NB, int Hq,
@@ -121,7 +138,7 @@ sfa_status build(const uint8_t* mm, const int32_t* rs, const int32_t* cs, int MB
             const int list = (int)out.lists.size() - 1;
             if (s > 0) {
                 const int64_t limit = causal ? r0 + s - 1 + (N - M) : N - 1;
-                tile_row_block(mm + ((int64_t)g * MB + rb) * NB, cs + (int64_t)g * NB, NB, limit,
+                tile_row_block(mm + ((int64_t)g * MB + rb) * NB, cs + (int64_t)g * NB, NB, limit, N,
                                out.tiles);
                 for (int x = 0; x < s; x += rows_per) {
                     out.items.push_back(list);

@@ -265,9 +265,9 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 def _varbsr_expected_bytes(mm, rs, cs, Hq, Hkv, causal):
     """Workspace bytes from an independent count: per (kv head, row block) the
-    fewest 64-key windows covering the allowed keys (greedy from the first
-    uncovered key), and ceil(rows / (2 * 128 / G)) work items per non-empty
-    row block."""
+    fewest 32-key halves covering the allowed keys (greedy from the first
+    uncovered key), two to a window (an odd last half padded), and
+    ceil(rows / (2 * 128 / G)) work items per non-empty row block."""
     Hkv_, MB, NB = mm.shape
     M, N = int(rs[0].sum()), int(cs[0].sum())
     rows_per = 2 * (128 // (Hq // Hkv))
@@ -283,13 +283,14 @@ def _varbsr_expected_bytes(mm, rs, cs, Hq, Hkv, causal):
                     keys[cstart[cb]:cstart[cb + 1]] = True
                 if causal:
                     keys[max(0, r0 + s - 1 + N - M + 1):] = False
-                j = 0
+                j = halves = 0
                 while j < N:
                     if keys[j]:
-                        ntiles += 1
-                        j += 64
+                        halves += 1
+                        j += 32
                     else:
                         j += 1
+                ntiles += -(-halves // 2)
                 nitems += -(-s // rows_per)
             r0 += s
     nlists = Hkv_ * MB

@@ -119,14 +119,18 @@ def test_plan_tiles_cover_exactly_the_allowed_keys(causal):
             lst = g * c.MB + rb
             prev_end = -1
             for t in tiles[lists[lst]:lists[lst + 1]]:
-                key0 = int(t[0])
-                bits = (int(np.uint32(t[2])) << 32) | int(np.uint32(t[1]))
-                assert key0 >= prev_end and bits & 1       # disjoint, starts on an allowed key
-                for j in range(64):
-                    if (bits >> j) & 1:
-                        assert key0 + j < c.N
-                        got[key0 + j] = True
-                prev_end = key0 + 64
+                # two 32-key halves: (start, mask) = (t[0], t[1]) and (t[3], t[2]);
+                # an odd last half is paired with an empty one at key N
+                for start, mask in ((int(t[0]), int(np.uint32(t[1]))), (int(t[3]), int(np.uint32(t[2])))):
+                    if mask == 0:
+                        assert start == c.N                    # the padding half
+                        continue
+                    assert start >= prev_end and mask & 1      # disjoint, starts on an allowed key
+                    for j in range(32):
+                        if (mask >> j) & 1:
+                            assert start + j < c.N
+                            got[start + j] = True
+                    prev_end = start + 32
             if s > 0:
                 assert np.array_equal(got, want), (g, rb)
             else:
