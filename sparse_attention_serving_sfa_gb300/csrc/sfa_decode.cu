@@ -12,9 +12,9 @@
 //     (stream-K): every SM streams the same number of bytes, no tail waves;
 //   - two producer warps gather each chunk's K rows (and V rows, unless V is
 //     the key prefix view), plus the group's q rows at the first chunk of an
-//     index list, with 16-byte cp.async, half
-//     a warp per 256-byte row (coalesced), into padded rows of a ring of
-//     shared-memory stages; completion is tracked by mbarriers
+//     index list, with 16-byte cp.async, eight lanes per row and four rows
+//     per step (coalesced), into padded rows of a ring of shared-memory
+//     stages; completion is tracked by mbarriers
 //     (cp.async.mbarrier.arrive), indices are prefetched three chunks ahead,
 //     slots past topK or with an out-of-range index are zero-filled and
 //     masked.  (Per-row bulk TMA copies were measured at ~85 cycles per
@@ -233,11 +233,12 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
 
     if (warp >= kConsWarps) {
         // ======================= producer warps =======================
-        // warp pw gathers slots 32 pw .. 32 pw + 31 of every chunk; half a
-        // warp copies one row (16 lanes x 16 bytes per 256 bytes).
+        // warp pw gathers slots 32 pw .. 32 pw + 31 of every chunk, four rows
+        // per step: lane l copies 16-byte pieces l % 8, l % 8 + 8, ... of
+        // row l / 8 of the step (every lane busy whatever the row length).
         const int pw = warp - kConsWarps;
         const int cpu = sch.cpu;
-        const int half = lane >> 4, hl = lane & 15;
+        const int quarter = lane >> 3, ql = lane & 7;
         Cursor fk = cursor_at(c_begin, cpu, p);     // index prefetch cursor
         int64_t fc = c_begin;
         auto fetch = [&]() {
@@ -277,19 +278,19 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
             const T* vg = static_cast<const T*>(p.v) + uc.b * p.v_sb + uc.n2 * p.v_sh;
             unsigned char* st = smem + s * L::stage;
 #pragma unroll 4
-            for (int r = 0; r < 32; r += 2) {
-                const int src_lane = r + half;
+            for (int r = 0; r < 32; r += 4) {
+                const int src_lane = r + quarter;
                 const int id = __shfl_sync(0xffffffffu, myid, src_lane);
                 const bool ok = id >= 0 && id < p.S2;
                 const int j = 32 * pw + src_lane;
                 const T* krow = kg + (ok ? (int64_t)id * p.k_ss : 0);
 #pragma unroll
-                for (int pc = hl; pc < DK / 8; pc += 16)
+                for (int pc = ql; pc < DK / 8; pc += 8)
                     cp_async_16_zfill(st + j * L::ks + pc * 16, krow + pc * 8, ok ? 16 : 0);
                 if constexpr (!VK) {
                     const T* vrow = vg + (ok ? (int64_t)id * p.v_ss : 0);
 #pragma unroll
-                    for (int pc = hl; pc < DV / 8; pc += 16)
+                    for (int pc = ql; pc < DV / 8; pc += 8)
                         cp_async_16_zfill(st + L::kTile + j * L::vs + pc * 16, vrow + pc * 8, ok ? 16 : 0);
                 }
             }
