@@ -53,6 +53,18 @@ constexpr int kStep = 2 * kBlk;     // keys per step
 constexpr int kStages = 2;
 constexpr int kSoftWarps = 8;
 constexpr int kThreads = kSoftWarps * 32 + 32;
+// The variable mode's block: two softmax warpgroups and a control warpgroup
+// (one working warp) that gives registers back, so that a softmax thread
+// holds a whole 128-key step of scores and reads them from tensor memory in
+// one round trip: launched with kRegsLaunch registers a thread, then control
+// kRegsControl, softmax kRegsSoftmax.  (Measured on the other modes it ran
+// 3-8% slower than one 64-key half at a time with kThreads threads.)
+constexpr int kThreadsSplit = kSoftWarps * 32 + 128;
+constexpr int kRegsLaunch = 168, kRegsControl = 80, kRegsSoftmax = 208;
+static_assert(kRegsSoftmax * kSoftWarps * 32 + kRegsControl * 128 <= kRegsLaunch * kThreadsSplit,
+              "the register split fits what the block was launched with");
+static_assert(2 * 32 * kRegsSoftmax + 32 * kRegsControl <= 16384,
+              "the register split fits each SM sub-partition (two softmax warps and one control warp)");
 constexpr int kTmemCols = 512;
 constexpr int kTileCols = 256;      // TMEM columns per M-tile
 constexpr int kOCol = 128;          // O after the 128 S / P columns
@@ -135,10 +147,12 @@ template <int MODE>
 struct WideSchedule {
     static constexpr bool split_p = MODE != 0;
     static constexpr bool tile_skip = MODE != 0;
+    static constexpr bool split_regs = MODE == 3;
+    static constexpr int threads = split_regs ? kThreadsSplit : kThreads;
 };
 
 template <class E, int D, int MODE, bool CAP, int F8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(WideSchedule<MODE>::threads, 1)
 bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const WideParams p) {
     // E: element type of q / k / v / out, or of out alone with F8
@@ -214,9 +228,11 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::tmem_slot);
 
-    if (warp == kSoftWarps) {
+    constexpr bool kSplitRegs = WideSchedule<MODE>::split_regs;
+    if (warp >= kSoftWarps) {
+        if constexpr (kSplitRegs) regs_release<kRegsControl>();
         // ============================ control ============================
-        if (lane == 0 && ns > 0) {
+        if (warp == kSoftWarps && lane == 0 && ns > 0) {
             tma_prefetch_map(&mq);
             tma_prefetch_map(&mk);
             tma_prefetch_map(&mv);
@@ -368,12 +384,14 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
         }
     } else {
+        if constexpr (kSplitRegs) regs_acquire<kRegsSoftmax>();
         // ============================ softmax ============================
         const int t = warp >> 2, wq = warp & 3;
         const int r = wq * 32 + lane;                       // row of the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16) + t * kTileCols;
         float m_used = -INFINITY, l = 0.f;
-        uint32_t sv[64];
+        // a step's 128 scores (keys 0..63 then 64..127), or one 64-key half at a time
+        uint32_t sv[kSplitRegs ? 128 : 64];
         // query row / qo head of this thread's tile row
         // (recomputed where used, so the plain mode keeps no registers for them)
         auto my_i = [&]() {
@@ -410,24 +428,25 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             if (nb > 0) am_next[0] = allowed(0);
             if (nb > 1) am_next[1] = allowed(1);
         }
-        auto apply_mask = [&](uint64_t am) {
+        auto apply_mask = [&](int h, uint64_t am) {
 #pragma unroll
             for (int j = 0; j < 64; ++j)
-                if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
+                if (!((am >> j) & 1ull)) sv[(kSplitRegs ? 64 * h : 0) + j] = __float_as_uint(-INFINITY);
         };
         // P of one 64-key half from the scores in sv, written over that
         // half's S columns; returns the half's sum of P
         auto make_p = [&](int h, uint64_t am) -> float {
+            uint32_t (&w)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sv[kSplitRegs ? 64 * h : 0]);
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (F8 != 0) {
-                // keys 4k .. 4k + 3 -> high parts in sv[2k], remainders in
-                // sv[2k + 1] (entries already read), four 8-bit P per word
+                // keys 4k .. 4k + 3 -> high parts in w[2k], remainders in
+                // w[2k + 1] (entries already read), four 8-bit P per word
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     float pv[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        float u = __uint_as_float(sv[4 * k + j]) * rs;
+                        float u = __uint_as_float(w[4 * k + j]) * rs;
                         if constexpr (CAP) u = soft_cap_log2(u, p.capl2, p.inv_capl2);
                         float pp = fast_exp2(u - m_used + kPShift);
                         if constexpr (MODE != 0)
@@ -440,16 +459,16 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     const float2 b01 = f8_unpack2<kE5>(h01), b23 = f8_unpack2<kE5>(h23);
                     const uint32_t l01 = f8_pack2<kE5>(pv[0] - b01.x, pv[1] - b01.y);
                     const uint32_t l23 = f8_pack2<kE5>(pv[2] - b23.x, pv[3] - b23.y);
-                    sv[2 * k] = h01 | (h23 << 16);
-                    sv[2 * k + 1] = l01 | (l23 << 16);
+                    w[2 * k] = h01 | (h23 << 16);
+                    w[2 * k + 1] = l01 | (l23 << 16);
                 }
-                tmem_st16_strided<0>(lane_base + 64 * h, sv);
-                tmem_st16_strided<1>(lane_base + 64 * h + 16, sv);
+                tmem_st16_strided<0>(lane_base + 64 * h, w);
+                tmem_st16_strided<1>(lane_base + 64 * h + 16, w);
             } else {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                float u0 = __uint_as_float(sv[2 * k]) * rs;
-                float u1 = __uint_as_float(sv[2 * k + 1]) * rs;
+                float u0 = __uint_as_float(w[2 * k]) * rs;
+                float u1 = __uint_as_float(w[2 * k + 1]) * rs;
                 if constexpr (CAP) {
                     u0 = soft_cap_log2(u0, p.capl2, p.inv_capl2);
                     u1 = soft_cap_log2(u1, p.capl2, p.inv_capl2);
@@ -464,11 +483,11 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 ls[k & 3] += p0 + p1;
                 const uint32_t hw = E::pack2(p0, p1);
                 const float2 hf = E::unpack2(hw);
-                sv[2 * k] = hw;
-                sv[2 * k + 1] = E::pack2(p0 - hf.x, p1 - hf.y);
+                w[2 * k] = hw;
+                w[2 * k + 1] = E::pack2(p0 - hf.x, p1 - hf.y);
             }
-            tmem_st32_strided<0>(lane_base + 64 * h, sv);
-            tmem_st32_strided<1>(lane_base + 64 * h + 32, sv);
+            tmem_st32_strided<0>(lane_base + 64 * h, w);
+            tmem_st32_strided<1>(lane_base + 64 * h + 32, w);
             }
             return (ls[0] + ls[1]) + (ls[2] + ls[3]);
         };
@@ -484,19 +503,38 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 if (2 * st + 3 < nb) am_next[1] = allowed(2 * st + 3);
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-            tmem_wait_ld();
-            if constexpr (MODE != 0) apply_mask(am0);
-#pragma unroll
-            for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
-            if (two) {
-                tmem_ld32(lane_base + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                tmem_ld32(lane_base + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                tmem_wait_ld();
-                if constexpr (MODE != 0) apply_mask(am1);
+            if constexpr (kSplitRegs) {
+                // the step's scores in one round trip (one block: its 64 only)
+                if (two) {
+                    tmem_ld128_sync(lane_base, *reinterpret_cast<uint32_t(*)[128]>(&sv[0]));
+                } else {
+                    tmem_ld64_sync(lane_base, *reinterpret_cast<uint32_t(*)[64]>(&sv[0]));
+                }
+                if constexpr (MODE != 0) apply_mask(0, am0);
 #pragma unroll
                 for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
+                if (two) {
+                    if constexpr (MODE != 0) apply_mask(1, am1);
+#pragma unroll
+                    for (int j = 64; j < 64 * (kSplitRegs ? 2 : 1); ++j)
+                        mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
+                }
+            } else {
+                // keys 0..63, then 64..127 (kept in sv for their P)
+                tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                tmem_wait_ld();
+                if constexpr (MODE != 0) apply_mask(0, am0);
+#pragma unroll
+                for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
+                if (two) {
+                    tmem_ld32(lane_base + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                    tmem_ld32(lane_base + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                    tmem_wait_ld();
+                    if constexpr (MODE != 0) apply_mask(1, am1);
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[j]));
+                }
             }
             // the scale is positive and rounding monotonic: max of scaled = scaled max
             float bmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * rs;
@@ -509,11 +547,15 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             // Q.K^T, whose completion this thread waited for: O is settled
             if (st > 0 && __any_sync(0xffffffffu, need)) {
                 const float f = need ? fast_exp2(m_used - m_new) : 1.f;
-#pragma unroll
+#pragma unroll (kSplitRegs ? 1 : D / 32)
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
-                    tmem_ld32(lane_base + kOCol + 32 * c, ov);
-                    tmem_wait_ld();
+                    if constexpr (kSplitRegs) {
+                        tmem_ld32_sync(lane_base + kOCol + 32 * c, ov);
+                    } else {
+                        tmem_ld32(lane_base + kOCol + 32 * c, ov);
+                        tmem_wait_ld();
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
                     tmem_st32(lane_base + kOCol + 32 * c, ov);
@@ -522,15 +564,18 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             if (need) m_used = m_new;
             if (two) {
-                l += make_p(1, am1);               // keys 64..127 are in sv
+                l += make_p(1, am1);               // keys 64..127
                 if constexpr (WideSchedule<MODE>::split_p) {
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(bar(B_P_HALF + t));
                 }
-                tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                tmem_wait_ld();
+                // keys 0..63: still in sv, or read again
+                if constexpr (!kSplitRegs) {
+                    tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                    tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                    tmem_wait_ld();
+                }
                 l += make_p(0, am0);
             } else if constexpr (WideSchedule<MODE>::split_p) {
                 // one block: no P.V for the second half (its barrier still
@@ -569,8 +614,12 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
             if (ns_t > 0) {
-                tmem_ld32(lane_base + kOCol + 32 * c, ov);
-                tmem_wait_ld();
+                if constexpr (kSplitRegs) {
+                    tmem_ld32_sync(lane_base + kOCol + 32 * c, ov);
+                } else {
+                    tmem_ld32(lane_base + kOCol + 32 * c, ov);
+                    tmem_wait_ld();
+                }
             }
             if (valid_row) {
 #pragma unroll
@@ -626,7 +675,20 @@ cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems,
     auto kern = bsr_tc_wide_kernel<E, D, MODE, CAP, F8>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
     if (err != cudaSuccess) return err;
-    kern<<<nitems, kThreads, L::alloc, stream>>>(mq, mk, mv, wp);
+    if constexpr (WideSchedule<MODE>::split_regs) {
+        // the register split assumes the block is launched with kRegsLaunch
+        // registers a thread: with fewer, the softmax warps' request could
+        // not be met (checked once per instantiation)
+        static int regs_ok = -1;
+        if (regs_ok < 0) {
+            cudaFuncAttributes fa;
+            err = cudaFuncGetAttributes(&fa, kern);
+            if (err != cudaSuccess) return err;
+            regs_ok = fa.numRegs == kRegsLaunch ? 1 : 0;
+        }
+        if (!regs_ok) return cudaErrorInvalidConfiguration;
+    }
+    kern<<<nitems, WideSchedule<MODE>::threads, L::alloc, stream>>>(mq, mk, mv, wp);
     count_launches(1);
     return cudaGetLastError();
 }

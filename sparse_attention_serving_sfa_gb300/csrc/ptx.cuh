@@ -205,6 +205,18 @@ __device__ __forceinline__ void cluster_sync() {
                      : "memory");
 }
 
+// Register reallocation between warpgroups (all warps of the warpgroup
+// execute it): give registers back to the CTA's pool, or take them from it
+// (blocks until enough have been given back).
+template <uint32_t N>
+__device__ __forceinline__ void regs_release() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_acquire() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Programmatic dependent launch: wait for the primary grid's memory.
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
