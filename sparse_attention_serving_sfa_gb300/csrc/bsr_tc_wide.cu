@@ -7,8 +7,8 @@
 // which serves plan()'s per-element block mask), for plain blocks (mode 0),
 // bottom-right causal (mode 1) and VariableBlockSparseAttentionWrapper's
 // variable blocks over HND tensors (mode 3: per (kv head, row block) a list
-// of 64-key windows, each two 32-key halves at their own start keys with a
-// 32-bit mask of allowed keys each).  Each step takes two 64-key blocks (or windows), so the per-step
+// of 64-key windows, each four 16-key quarters at their own start keys and a
+// 64-bit mask of allowed keys).  Each step takes two 64-key blocks (or windows), so the per-step
 // round trip (Q.K^T -> softmax -> P.V and the barriers between them) is paid
 // once per 128 keys:
 //   - control warp (one thread): TMA loads of the two Q tiles and of two
@@ -104,13 +104,14 @@ struct WideItem {
     int rb, row0, kvh, pad;
 };
 
-// Mode 3 key window: two 32-key halves, keys [key0, key0 + 32) and [key1,
-// key1 + 32); bit j of lo = key0 + j allowed, bit j of hi = key1 + j allowed.
-struct WideWindow {
-    int key0;
+// Mode 3 key window: four 16-key quarters, keys [key[q], key[q] + 16) in
+// rows 16 q .. 16 q + 15 of the 64-key block; bit j of the mask (hi:lo) =
+// row j allowed.
+struct alignas(8) WideWindow {
+    int key[4];
     unsigned lo, hi;
-    int key1;
 };
+constexpr int kQuarter = kBlk / 4;
 
 struct WideParams {
     void* out;
@@ -134,9 +135,9 @@ struct WideParams {
 __device__ __forceinline__ uint64_t causal_bits64(int64_t lim) {
     return lim < 0 ? 0ull : (lim >= 63 ? ~0ull : ((2ull << lim) - 1ull));
 }
-// The same among the 32 keys of a half window.
-__device__ __forceinline__ uint32_t causal_bits32(int64_t lim) {
-    return lim < 0 ? 0u : (lim >= 31 ? ~0u : ((2u << lim) - 1u));
+// The same among the 16 keys of a quarter window.
+__device__ __forceinline__ uint32_t causal_bits16(int64_t lim) {
+    return lim < 0 ? 0u : (lim >= 15 ? 0xffffu : ((2u << lim) - 1u));
 }
 
 // Per mode (measured): the causal and variable modes hand P to the tensor
@@ -201,7 +202,7 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     const WideWindow* wins = reinterpret_cast<const WideWindow*>(p.indices);
     // first key of 64-key block b
     auto block_key0 = [&](int b) -> int {
-        if constexpr (MODE == 3) return wins[blk0 + b].key0;
+        if constexpr (MODE == 3) return wins[blk0 + b].key[0];
         return p.indices[blk0 + b / sub] * p.C + (b % sub) * kBlk;
     };
 
@@ -255,19 +256,21 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 for (int h = 0; h < 2; ++h) {
                     const int b = 2 * st + h;
                     if constexpr (MODE == 3) {
-                        // a window's two 32-key halves, 32-row boxes: rows
-                        // [key0, +32) then [key1, +32) (a missing window: rows
+                        // a window's four 16-key quarters, 16-row boxes at
+                        // rows key[q] .. key[q] + 15 (a missing window: rows
                         // past the end, zeros)
-                        const WideWindow w = b < nb ? wins[blk0 + b] : WideWindow{p.N, 0u, 0u, p.N};
+                        const WideWindow w =
+                            b < nb ? wins[blk0 + b] : WideWindow{{p.N, p.N, p.N, p.N}, 0u, 0u};
                         for (int pn = 0; pn < L::panels; ++pn) {
                             const uint32_t kd = dst + pn * L::kPanel + h * L::kvHalf;
                             const uint32_t vd = kd + L::kvTile;
-                            tma_load_3d(kd, &mk, pn * kCol0, w.key0, item.kvh, bar(B_KV_FULL + s));
-                            tma_load_3d(vd, &mv, pn * kCol0, w.key0, item.kvh, bar(B_KV_FULL + s));
-                            tma_load_3d(kd + (kBlk / 2) * 128, &mk, pn * kCol0, w.key1, item.kvh,
-                                        bar(B_KV_FULL + s));
-                            tma_load_3d(vd + (kBlk / 2) * 128, &mv, pn * kCol0, w.key1, item.kvh,
-                                        bar(B_KV_FULL + s));
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                tma_load_3d(kd + q * kQuarter * 128, &mk, pn * kCol0, w.key[q], item.kvh,
+                                            bar(B_KV_FULL + s));
+                                tma_load_3d(vd + q * kQuarter * 128, &mv, pn * kCol0, w.key[q], item.kvh,
+                                            bar(B_KV_FULL + s));
+                            }
                         }
                         continue;
                     }
@@ -412,13 +415,15 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 return causal_bits64((int64_t)my_i() + (p.N - p.M) - block_key0(b));
             } else if constexpr (MODE == 3) {
                 const WideWindow w = wins[blk0 + b];
-                uint32_t lo = w.lo, hi = w.hi;
+                uint64_t m = ((uint64_t)w.hi << 32) | w.lo;
                 if (p.causal) {
                     const int64_t lim = (int64_t)my_i() + (p.N - p.M);
-                    lo &= causal_bits32(lim - w.key0);
-                    hi &= causal_bits32(lim - w.key1);
+                    uint64_t c = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) c |= (uint64_t)causal_bits16(lim - w.key[q]) << (16 * q);
+                    m &= c;
                 }
-                return ((uint64_t)hi << 32) | lo;
+                return m;
             }
             return ~0ull;
         };
@@ -659,10 +664,10 @@ cudaError_t launch_wide_t(const BsrParams& bp, const WideParams& wp, int nitems,
                          !make_map8(&mv, bp.v, D, bp.Hkv, bp.N, 1, kBlk)))
             return cudaErrorInvalidValue;
     } else if (MODE == 3) {
-        // key windows come as two halves of kBlk / 2 rows each
+        // key windows come as four quarters of kQuarter rows each
         if (!make_map_hnd(&mq, bp.q, bf16, D, bp.M, bp.Hq, wp.TR, wp.G) ||
-            !make_map_hnd(&mk, bp.k, bf16, D, bp.N, bp.Hkv, kBlk / 2, 1) ||
-            !make_map_hnd(&mv, bp.v, bf16, D, bp.N, bp.Hkv, kBlk / 2, 1))
+            !make_map_hnd(&mk, bp.k, bf16, D, bp.N, bp.Hkv, kQuarter, 1) ||
+            !make_map_hnd(&mv, bp.v, bf16, D, bp.N, bp.Hkv, kQuarter, 1))
             return cudaErrorInvalidValue;
     } else if (!make_map(&mq, bp.q, bf16, D, bp.Hq, bp.M, wp.G, wp.TR)) {
         return cudaErrorInvalidValue;

@@ -28,15 +28,16 @@ struct varbsr_plan_s {
 
 namespace {
 
-constexpr int kTileKeys = 64;   // keys of a window (two 32-key halves)
-constexpr int kHalfKeys = 32;
+constexpr int kTileKeys = 64;   // keys of a window (four 16-key quarters)
+constexpr int kQuarterKeys = 16;
+constexpr int kWindowInts = 6;  // first key of each quarter, then the 64-bit mask (low word first)
 
 size_t round4(size_t n) { return (n + 3) & ~size_t(3); }
 
 struct Built {
     int M = 0, N = 0;
     std::vector<int32_t> lists;     // nlists + 1 offsets into tiles
-    std::vector<int32_t> tiles;     // 4 ints each: key0, mask of half 0, mask of half 1, key1
+    std::vector<int32_t> tiles;     // kWindowInts ints per key window
     std::vector<int32_t> items;     // 4 ints each: list, row0, kv head, row end
 };
 
@@ -51,33 +52,32 @@ sfa_status check_args(const uint8_t* mm, const int32_t* rs, const int32_t* cs, i
 }
 
 // Key windows of one (kv head, row block): the allowed key columns (set
-// blocks, and with causal only keys <= limit) covered greedily by 32-key
-// halves, each starting at the first allowed key not yet covered (the fewest
-// halves that cover the set), paired in order into 64-key windows: {first
-// key of half 0, mask of half 0, mask of half 1, first key of half 1}, bit j
-// of a half's mask = its key j allowed.  An odd last half is paired with an
-// empty one at key n_keys (rows past the end of the keys: read as zeros,
-// all masked).
+// blocks, and with causal only keys <= limit) covered greedily by 16-key
+// quarters, each starting at the first allowed key not yet covered (the
+// fewest quarters that cover the set), four in order to a 64-key window:
+// {first key of quarters 0..3, mask low word, mask high word}, bit 16 q + j of
+// the mask = key j of quarter q allowed.  A last window with fewer than four
+// quarters is completed with empty ones at key n_keys (rows past the end of
+// the keys: read as zeros, all masked).
 void tile_row_block(const uint8_t* mrow, const int32_t* cs, int NB, int64_t limit,
                     int64_t n_keys, std::vector<int32_t>& tiles) {
-    int64_t key0 = -1;
+    int64_t key0 = -1;                  // the quarter being filled
     uint32_t bits = 0;
-    int64_t pend_key = -1;              // a finished half waiting for its pair
-    uint32_t pend_bits = 0;
-    auto emit_half = [&](int64_t k, uint32_t m) {
-        if (pend_key < 0) {
-            pend_key = k;
-            pend_bits = m;
-            return;
-        }
-        tiles.push_back((int32_t)pend_key);
-        tiles.push_back((int32_t)pend_bits);
-        tiles.push_back((int32_t)m);
-        tiles.push_back((int32_t)k);
-        pend_key = -1;
+    int64_t wkey[4] = {0, 0, 0, 0};     // the window being filled
+    uint64_t wmask = 0;
+    int nq = 0;
+    auto emit_quarter = [&](int64_t k, uint32_t m) {
+        wkey[nq] = k;
+        wmask |= (uint64_t)m << (16 * nq);
+        if (++nq < 4) return;
+        for (int q = 0; q < 4; ++q) tiles.push_back((int32_t)wkey[q]);
+        tiles.push_back((int32_t)(uint32_t)wmask);
+        tiles.push_back((int32_t)(uint32_t)(wmask >> 32));
+        nq = 0;
+        wmask = 0;
     };
     auto flush = [&] {
-        if (key0 >= 0) emit_half(key0, bits);
+        if (key0 >= 0) emit_quarter(key0, bits);
         key0 = -1;
         bits = 0;
     };
@@ -88,18 +88,19 @@ void tile_row_block(const uint8_t* mrow, const int32_t* cs, int NB, int64_t limi
         c0 += cs[cb];
         if (!mrow[cb]) continue;
         while (a < b) {
-            if (key0 < 0 || a >= key0 + kHalfKeys) {
+            if (key0 < 0 || a >= key0 + kQuarterKeys) {
                 flush();
                 key0 = a;
             }
-            const int64_t e = std::min(b, key0 + kHalfKeys);
+            const int64_t e = std::min(b, key0 + kQuarterKeys);
             const int o0 = (int)(a - key0), n = (int)(e - a);
-            bits |= (n == 32 ? ~0u : ((1u << n) - 1u)) << o0;
+            bits |= ((1u << n) - 1u) << o0;         // n <= 16
             a = e;
         }
     }
     flush();
-    if (pend_key >= 0) emit_half(n_keys, 0u);
+    const int pad = nq > 0 ? 4 - nq : 0;
+    for (int i = 0; i < pad; ++i) emit_quarter(n_keys, 0u);
 }
 
 sfa_status build(const uint8_t* mm, const int32_t* rs, const int32_t* cs, int MB, int NB, int Hq,
@@ -147,8 +148,8 @@ sfa_status build(const uint8_t* mm, const int32_t* rs, const int32_t* cs, int MB
                     out.items.push_back((int32_t)(r0 + s));
                 }
             }
-            if (out.tiles.size() / 4 > (size_t)INT32_MAX) return SFA_ERR_UNSUPPORTED;
-            out.lists.push_back((int32_t)(out.tiles.size() / 4));
+            if (out.tiles.size() / kWindowInts > (size_t)INT32_MAX) return SFA_ERR_UNSUPPORTED;
+            out.lists.push_back((int32_t)(out.tiles.size() / kWindowInts));
             r0 += s;
         }
     }
@@ -176,7 +177,8 @@ sfa_status build(const uint8_t* mm, const int32_t* rs, const int32_t* cs, int MB
 }
 
 size_t ws_bytes(const Built& b) {
-    return 4 * (round4(b.lists.size()) + b.tiles.size() + b.items.size());
+    // lists, windows and items each start on a 16-byte boundary
+    return 4 * (round4(b.lists.size()) + round4(b.tiles.size()) + b.items.size());
 }
 
 }  // namespace
@@ -241,17 +243,17 @@ sfa_status varbsr_plan(const uint8_t* block_mask_map_host, const int32_t* block_
     plan->scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)head_dim);
     plan->causal = causal ? 1 : 0;
     plan->nlists = (int)b.lists.size() - 1;
-    plan->ntiles = (int)(b.tiles.size() / 4);
+    plan->ntiles = (int)(b.tiles.size() / kWindowInts);
     plan->nitems = (int)(b.items.size() / 4);
-    const size_t n_lists = round4(b.lists.size());
+    const size_t n_lists = round4(b.lists.size()), n_tiles = round4(b.tiles.size());
     plan->staging.assign(need / 4, 0);
     std::copy(b.lists.begin(), b.lists.end(), plan->staging.begin());
     std::copy(b.tiles.begin(), b.tiles.end(), plan->staging.begin() + n_lists);
-    std::copy(b.items.begin(), b.items.end(), plan->staging.begin() + n_lists + b.tiles.size());
+    std::copy(b.items.begin(), b.items.end(), plan->staging.begin() + n_lists + n_tiles);
     int32_t* base = static_cast<int32_t*>(int_ws);
     plan->d_lists = base;
     plan->d_tiles = base + n_lists;
-    plan->d_items = base + n_lists + b.tiles.size();
+    plan->d_items = base + n_lists + n_tiles;
     cudaError_t err = cudaMemcpyAsync(int_ws, plan->staging.data(), need, cudaMemcpyHostToDevice,
                                       reinterpret_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) {

@@ -179,14 +179,16 @@ def _varbsr_example():
 
 def test_varbsr_int_workspace_size(lib):
     mm, rs, cs = _varbsr_example()
-    # 3 lists (offsets 4 ints) + 3 key tiles x 4 ints + 3 items x 4 ints
-    assert sfa.varbsr_plan_int_workspace_size(mm, rs, cs, 1, 1, 128) == 4 * (4 + 12 + 12)
+    # 3 lists (offsets: 4 ints) + 3 key windows x 6 ints (rounded up to 20)
+    # + 3 items x 4 ints
+    assert sfa.varbsr_plan_int_workspace_size(mm, rs, cs, 1, 1, 128) == 4 * (4 + 20 + 12)
     # causal (qo_len == kv_len == 6): row block 0 (row 0) sees no allowed key
-    # (its set block holds keys 4, 5), so one tile fewer
-    assert sfa.varbsr_plan_int_workspace_size(mm, rs, cs, 1, 1, 128, causal=True) == 4 * (4 + 8 + 12)
-    # a 64-key window per tile: one set block of 130 keys needs 3 tiles
+    # (its set block holds keys 4, 5), so one window fewer
+    assert sfa.varbsr_plan_int_workspace_size(mm, rs, cs, 1, 1, 128, causal=True) == 4 * (4 + 12 + 12)
+    # four 16-key quarters per window: one set block of 130 keys needs 9
+    # quarters, 3 windows (18 ints, rounded up to 20)
     n = sfa.varbsr_plan_int_workspace_size(np.ones((1, 1, 1), np.uint8), [[10]], [[130]], 4, 1, 64)
-    assert n == 4 * (4 + 12 + 4)
+    assert n == 4 * (4 + 20 + 4)
 
 
 @pytest.mark.parametrize("rs,cs,Hq,Hkv,d,status", [
@@ -265,9 +267,10 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 def _varbsr_expected_bytes(mm, rs, cs, Hq, Hkv, causal):
     """Workspace bytes from an independent count: per (kv head, row block) the
-    fewest 32-key halves covering the allowed keys (greedy from the first
-    uncovered key), two to a window (an odd last half padded), and
-    ceil(rows / (2 * 128 / G)) work items per non-empty row block."""
+    fewest 16-key quarters covering the allowed keys (greedy from the first
+    uncovered key), four to a window of 6 ints (a last window padded), and
+    ceil(rows / (2 * 128 / G)) work items per non-empty row block; each part
+    starts on a 16-byte boundary."""
     Hkv_, MB, NB = mm.shape
     M, N = int(rs[0].sum()), int(cs[0].sum())
     rows_per = 2 * (128 // (Hq // Hkv))
@@ -283,18 +286,18 @@ def _varbsr_expected_bytes(mm, rs, cs, Hq, Hkv, causal):
                     keys[cstart[cb]:cstart[cb + 1]] = True
                 if causal:
                     keys[max(0, r0 + s - 1 + N - M + 1):] = False
-                j = halves = 0
+                j = quarters = 0
                 while j < N:
                     if keys[j]:
-                        halves += 1
-                        j += 32
+                        quarters += 1
+                        j += 16
                     else:
                         j += 1
-                ntiles += -(-halves // 2)
+                ntiles += -(-quarters // 4)
                 nitems += -(-s // rows_per)
             r0 += s
     nlists = Hkv_ * MB
-    return 4 * (((nlists + 1 + 3) // 4) * 4 + 4 * ntiles + 4 * nitems)
+    return 4 * (((nlists + 1 + 3) // 4) * 4 + (6 * ntiles + 3) // 4 * 4 + 4 * nitems)
 
 
 @pytest.mark.parametrize("seed,causal,Hq,Hkv", [(1, False, 8, 2), (2, True, 8, 2),

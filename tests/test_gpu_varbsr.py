@@ -84,14 +84,15 @@ def test_shapes(M, N, MB, NB, Hq, Hkv, d, dtype, p, causal):
 
 
 def _plan_lists(plan, Hkv, MB):
-    """(lists, tiles (n, 4), items (m, 4)) read back from the plan's workspace."""
+    """(lists, windows (n, 6), items (m, 4)) read back from the plan's
+    workspace (each part starts on a 16-byte boundary)."""
     ws = plan.int_ws.cpu().view(torch.int32).numpy()
     nl = Hkv * MB
     lists = ws[: nl + 1]
     off = (nl + 1 + 3) // 4 * 4
     nt = int(lists[-1])
-    tiles = ws[off: off + 4 * nt].reshape(nt, 4)
-    return lists, tiles, ws[off + 4 * nt:]
+    tiles = ws[off: off + 6 * nt].reshape(nt, 6)
+    return lists, tiles, ws[off + (6 * nt + 3) // 4 * 4:]
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -119,18 +120,21 @@ def test_plan_tiles_cover_exactly_the_allowed_keys(causal):
             lst = g * c.MB + rb
             prev_end = -1
             for t in tiles[lists[lst]:lists[lst + 1]]:
-                # two 32-key halves: (start, mask) = (t[0], t[1]) and (t[3], t[2]);
-                # an odd last half is paired with an empty one at key N
-                for start, mask in ((int(t[0]), int(np.uint32(t[1]))), (int(t[3]), int(np.uint32(t[2])))):
+                # four 16-key quarters: starts t[0..3], mask t[5]:t[4] with
+                # bits 16 q .. 16 q + 15 for quarter q; a last window is
+                # completed with empty quarters at key N
+                m64 = int(np.uint32(t[4])) | (int(np.uint32(t[5])) << 32)
+                for q in range(4):
+                    start, mask = int(t[q]), (m64 >> (16 * q)) & 0xFFFF
                     if mask == 0:
-                        assert start == c.N                    # the padding half
+                        assert start == c.N                    # a padding quarter
                         continue
                     assert start >= prev_end and mask & 1      # disjoint, starts on an allowed key
-                    for j in range(32):
+                    for j in range(16):
                         if (mask >> j) & 1:
                             assert start + j < c.N
                             got[start + j] = True
-                    prev_end = start + 32
+                    prev_end = start + 16
             if s > 0:
                 assert np.array_equal(got, want), (g, rb)
             else:
