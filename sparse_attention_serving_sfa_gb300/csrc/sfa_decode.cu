@@ -658,10 +658,11 @@ int resident_clusters(K kern, int smem, int cluster) {
 }
 
 // Deepest ring that fits in shared memory next to the merge buffers, for
-// one or two CTAs per SM.
+// one or two CTAs per SM (228 KB of shared memory per SM, 1 KB of it
+// reserved per resident CTA).
 template <int DK, int DV, bool VK, int CPS>
 constexpr int stages_for() {
-    constexpr int budget = (CPS == 1 ? 220 : 110) * 1024;
+    constexpr int budget = (CPS == 1 ? 220 : 113) * 1024;
     constexpr int fixed = Smem<DK, DV, VK, 1>::total - Smem<DK, DV, VK, 1>::stage;
     constexpr int ns = (budget - fixed) / Smem<DK, DV, VK, 1>::stage;
     return ns > 6 ? 6 : (ns < 2 ? 2 : ns);
