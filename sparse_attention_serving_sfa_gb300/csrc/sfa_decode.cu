@@ -101,14 +101,16 @@ struct Smem {
     static constexpr int vs = VK ? ks : DV * 2 + kRowPad;
     static constexpr int kTile = kChunk * ks;
     static constexpr int vTile = VK ? 0 : kChunk * vs;
-    static constexpr int qTile = 16 * ks;                // 16 rows, rows >= G stay zero
+    static constexpr int qTile = kHeads * ks;            // 8 rows, rows >= G stay zero
     static constexpr int stage = kTile + vTile + qTile;
     static constexpr int meta = NS * stage;              // NS x int4 {-, mask lo, mask hi, -}
     static constexpr int bars = meta + NS * 16;          // full[NS], empty[NS]
     static constexpr int ml = bars + 2 * NS * 8;         // [4 warps][8 rows] float2 (m, l)
-    static constexpr int obuf = ml + kConsWarps * kHeads * 8;   // [4][8][DV] float
-    static constexpr int abort = obuf + kConsWarps * kHeads * DV * 4;
+    static constexpr int abort = ml + kConsWarps * kHeads * 8;
     static constexpr int total = abort + 16;
+    // the 4 warps' O states of a list ([4][8][DV] float) go to the K / V
+    // tiles of a stage the consumers hold (its q rows are left alone)
+    static constexpr int obufBytes = kConsWarps * kHeads * DV * 4;
 };
 
 struct UnitCoord {
@@ -196,7 +198,9 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
     constexpr int KT = DK / 16;      // k-steps of Q.K^T
     constexpr int NT = DV / 8;       // n-tiles of P.V
     static_assert(KT % 2 == 0 && NT % 2 == 0, "head dims must be multiples of 32 and 16");
-    static_assert(kHeads * DV * 4 + kHeads * 8 <= L::stage, "a cluster merge partial fits a stage");
+    static_assert(kHeads * DV * 4 + kHeads * 8 <= L::kTile + L::vTile, "a cluster merge partial fits a stage");
+    static_assert(L::obufBytes <= L::kTile + L::vTile, "the merge buffer fits a stage's K / V tiles");
+    static_assert(NS >= 2, "the cluster merge uses two stages");
 
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t smem_base = smem_u32(smem);
@@ -335,7 +339,6 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
     const int quad = lane & 3, rq = lane >> 2;
     const int hc = 2 * quad;
     float2* ml_buf = reinterpret_cast<float2*>(smem + L::ml);
-    float* obuf = reinterpret_cast<float*>(smem + L::obuf);
     constexpr int MT = DV / 16;          // m-tiles of O^T
 
     float o[MT][4];                      // O^T[16 mt + rq (+8)][hc (+1)]
@@ -344,8 +347,14 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
     int64_t cur = -1;
 
     // Merge of the 4 warps' states of index list `u`, then either the final
-    // output (this CTA holds all of the list's chunks) or a partial.
-    auto flush = [&](int64_t u) {
+    // output (this CTA holds all of the list's chunks) or a partial.  Called
+    // after the P.V of the list's last chunk in this range, whose stage `s`
+    // the consumers still hold: the warps' O states go to its K / V tiles
+    // (at the end of a clustered range, when every stage is idle, to stage 1:
+    // stage 0 takes the partial the cluster reads).
+    auto flush = [&](int64_t u, int s) {
+        float* obuf = reinterpret_cast<float*>(smem + (sch.cluster > 1 ? 1 : s) * L::stage);
+        named_sync(1, kConsThreads);        // every warp is done with the stage's rows
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             float l = l_part[e];
@@ -543,7 +552,6 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
             ((warp < 2 ? (uint32_t)meta.y : (uint32_t)meta.z) >> (16 * (warp & 1))) & 0xffffu;
 
         if (u != cur) {
-            if (cur >= 0) flush(cur);
             cur = u;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -631,12 +639,13 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
         for (int mt = 0; mt < MT; ++mt) mma16816<E>(o[mt], va[mt], bh0, bh1);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) mma16816<E>(o[mt], va[mt], bl0, bl1);
+        // the list's last chunk in this range: merge and write (or publish)
+        // before the stage is released
+        if (c + 1 == c_end || k.cc + 1 == sch.cpu) flush(cur, s);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    if (cur >= 0) {
-        flush(cur);
-    } else if (sch.cluster > 1) {
+    if (cur < 0 && sch.cluster > 1) {
         cluster_sync();     // (an empty range: every segment holds a chunk)
         cluster_sync();
     }
