@@ -101,6 +101,8 @@ struct MlaSched {
     int clusters;       // CTA pairs
     int seg_max;
     int q_head_inner;   // q tensor map dims are {d, head, s1, b} (else {d, s1, head, b})
+    int quad;           // every unit is two ranges run by the two pairs of one 4-CTA
+                        // cluster, merged in distributed shared memory
 };
 
 __host__ __device__ inline int64_t mla_range_begin(int64_t c, const MlaSched& s) {
@@ -121,8 +123,10 @@ __device__ __forceinline__ UCoord ucoord(int64_t u, const SfaParams& p) {
     return c;
 }
 
+// Launched in clusters of 2 CTAs (a pair), or of 4 (two pairs holding the two
+// ranges of one unit) when sch.quad is set.
 template <class E>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const MlaSched sch) {
     using T = typename E::T;
     using L = MlaSmem;
@@ -135,7 +139,8 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = cluster_ctarank();
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t rank = crank & 1;                  // this CTA's half of the output dims
     const int64_t cl = blockIdx.x >> 1;
     const int c_begin = (int)mla_range_begin(cl, sch), c_end = (int)mla_range_begin(cl + 1, sch);
     const int n = c_end - c_begin;
@@ -511,6 +516,30 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             const int64_t first = (int64_t)u * cpu, lastc = first + cpu - 1;
             const int64_t c_lo = mla_cluster_of(first, sch), c_hi = mla_cluster_of(lastc, sch);
             const bool split = c_hi > c_lo;
+            if (sch.quad) {
+                // this range's O (float4 j of head r at [j][r]: consecutive
+                // heads, consecutive 16 bytes) and (m, l) stay in shared
+                // memory (the stages and Q panels are idle: the unit's MMAs
+                // are done and every copy has landed) for the cluster merge
+                // at the end of the kernel
+                float4* so = reinterpret_cast<float4*>(smem + L::kv);
+#pragma unroll 1
+                for (int cb = 0; cb < kHalfDv / 32; ++cb) {
+                    uint32_t ov[32];
+                    tmem_ld32(lane_base + kOCol + 32 * cb, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)
+                        so[(8 * cb + t) * kHeads + r] =
+                            make_float4(__uint_as_float(ov[4 * t]), __uint_as_float(ov[4 * t + 1]),
+                                        __uint_as_float(ov[4 * t + 2]), __uint_as_float(ov[4 * t + 3]));
+                }
+                reinterpret_cast<float2*>(smem + L::qs)[r] = make_float2(m_used, l);
+                m_used = -INFINITY;
+                l = 0.f;
+                first_of_unit = true;
+                continue;                                // a quad range holds one unit
+            }
             const UCoord uc = ucoord(u, p);
             const int n1 = uc.n2 * kHeads + r;
             const int64_t row = (int64_t)u * kHeads + r;
@@ -563,6 +592,42 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (sch.quad) {
+        // the cluster's first pair merges the second pair's state of the unit
+        // (same output half: CTA crank + 2), reading its shared memory
+        cluster_sync();
+        if (crank < 2 && tid < kSoftThreads && n > 0) {
+            const int h = tid;
+            const float2 a = reinterpret_cast<const float2*>(smem + L::qs)[h];
+            const float2 b = ld_cluster_f2(map_peer(smem_u32(smem + L::qs) + 8 * h, crank + 2));
+            const float M = fmaxf(a.x, b.x);
+            const float fa = rescale_factor(a.x, M), fb = rescale_factor(b.x, M);
+            const float Ls = fa * a.y + fb * b.y;
+            const bool empty = !(Ls > 0.f);
+            const float inv = empty ? 0.f : 1.f / Ls;
+            const UCoord uc = ucoord(unit_of(c_begin), p);
+            const int n1 = uc.n2 * kHeads + h;
+            T* orow = static_cast<T*>(p.out) + uc.b * p.o_sb + n1 * p.o_sh + uc.s1 * p.o_ss + (int)rank * kHalfDv;
+            const float4* so = reinterpret_cast<const float4*>(smem + L::kv);
+            const uint32_t peer_o = map_peer(smem_u32(smem + L::kv), crank + 2);
+#pragma unroll 4
+            for (int j = 0; j < kHalfDv / 4; j += 2) {
+                const float4 x0 = so[j * kHeads + h], x1 = so[(j + 1) * kHeads + h];
+                const float4 y0 = ld_cluster_f4(peer_o + 16u * (uint32_t)(j * kHeads + h));
+                const float4 y1 = ld_cluster_f4(peer_o + 16u * (uint32_t)((j + 1) * kHeads + h));
+                uint4 o;
+                o.x = empty ? 0u : E::pack2((fa * x0.x + fb * y0.x) * inv, (fa * x0.y + fb * y0.y) * inv);
+                o.y = empty ? 0u : E::pack2((fa * x0.z + fb * y0.z) * inv, (fa * x0.w + fb * y0.w) * inv);
+                o.z = empty ? 0u : E::pack2((fa * x1.x + fb * y1.x) * inv, (fa * x1.y + fb * y1.y) * inv);
+                o.w = empty ? 0u : E::pack2((fa * x1.z + fb * y1.z) * inv, (fa * x1.w + fb * y1.w) * inv);
+                *reinterpret_cast<uint4*>(orow + 4 * j) = o;
+            }
+            if (rank == 0 && p.lse)
+                p.lse[uc.b * p.l_sb + n1 * p.l_sh + uc.s1 * p.l_ss] = empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
+        }
+        // the second pair stays resident until the first has read it
+        cluster_sync();
+    }
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -668,19 +733,22 @@ int prepare_device(int num_sms) {
     if (cudaFuncSetAttribute(sfa_mla_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              MlaSmem::alloc) != cudaSuccess)
         return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(num_sms & ~1));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = MlaSmem::alloc;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sfa_mla_kernel<E>, &cfg) != cudaSuccess || n < 1) {
-        (void)cudaGetLastError();
-        n = num_sms / 2;
-    }
+    int n = max_active_clusters(sfa_mla_kernel<E>, kThreads, MlaSmem::alloc, 2);
+    if (n < 1) n = num_sms / 2;
     if (n > num_sms / 2) n = num_sms / 2;
     if (n < 1) n = 1;
     cache[dev] = n;
     return n;
+}
+
+// Clusters of two pairs (4 CTAs) of the MLA kernel resident at once (cached).
+template <class E>
+int quad_clusters() {
+    static int cache[64] = {0};      // count + 1; 0: not asked
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) cache[dev] = max_active_clusters(sfa_mla_kernel<E>, kThreads, MlaSmem::alloc, 4) + 1;
+    return cache[dev] - 1;
 }
 
 template <class E>
@@ -720,17 +788,23 @@ cudaError_t launch_t(SfaParams p, int num_sms, void* ws, size_t ws_bytes, cudaSt
         clusters = clusters * 3 / 4;
     }
     s.clusters = (int)clusters;
-    if (s.seg_max > 1) {
+    // every unit cut in two ranges (an even chunk count: range c is chunks
+    // [c cpu / 2, (c + 1) cpu / 2)), and room for all the 4-CTA clusters at
+    // once: the two pairs of a unit run as one cluster and merge in
+    // distributed shared memory, without partials or a merge kernel
+    s.quad = (p.num_ctas == 0 && clusters == 2 * s.units && s.cpu % 2 == 0 &&
+              quad_clusters<E>() >= s.units) ? 1 : 0;
+    if (s.seg_max > 1 && !s.quad) {
         const int64_t rows = s.units * kHeads;
         const size_t need = (size_t)rows * s.seg_max * ((size_t)kDv + 2) * sizeof(float);
         if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
         p.ws_o = static_cast<float*>(ws);
         p.ws_ml = p.ws_o + rows * s.seg_max * kDv;
     }
-    cudaError_t err = launch_pdl(sfa_mla_kernel<E>, dim3((unsigned)(2 * s.clusters)), dim3(kThreads),
-                                 (size_t)MlaSmem::alloc, stream, mq, p, s);
+    cudaError_t err = launch_pdl_clustered(sfa_mla_kernel<E>, dim3((unsigned)(2 * s.clusters)), dim3(kThreads),
+                                           (size_t)MlaSmem::alloc, stream, s.quad ? 4 : 2, mq, p, s);
     count_launches(1);
-    if (err != cudaSuccess || s.seg_max == 1) return err;
+    if (err != cudaSuccess || s.seg_max == 1 || s.quad) return err;
     // merge of split units; launched early (programmatic dependent launch),
     // it waits for the main kernel's results before reading them
     const int64_t rows = s.units * kHeads;
