@@ -246,7 +246,8 @@ MAIN_KERNEL = {
     "tiny": "generic top-K kernel",
     "gqa_decode": "sfa_decode_kernel (one launch per call; split index lists merged in-kernel)",
     "sparse_prefill": "sfa_decode_kernel (one launch per call; whole index lists per CTA)",
-    "mla_decode": "sfa_mla_kernel + sfa_mla_combine (two launches per call; time is the call's)",
+    "mla_decode": "sfa_mla_kernel (one launch per call: the two ranges of every index list run as "
+                  "one 4-CTA cluster and merge in distributed shared memory)",
     "mla_mtp": "sfa_mla_kernel + sfa_mla_combine (two launches per call; time is the call's)",
     "call_example": "sfa_decode_kernel (one launch per call; whole index lists per CTA)",
     "bsr": "bsr_tc_wide_kernel (one launch per bsr_run)",
@@ -433,12 +434,13 @@ def run_sfa(name, args, world, rank, cpu_target_s):
                                       case.topK)
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
 
-    def call(d, q=None, idx=None, o=None, l=None):
+    def call(d, q=None, idx=None, o=None, l=None, ready=False):
         sfa.sfa_run_ex(d["q"] if q is None else q, d["k"], d["v"], d["idx"] if idx is None else idx,
                        case.B, case.S1, case.S2, case.N1, case.N2, case.Dk, case.Dv, case.topK,
                        case.scale, case.layout, case.causal, case.dtype,
                        out if o is None else o, lse if l is None else l,
-                       torch.cuda.current_stream(), workspace=ws, value_is_key_prefix=prefix)
+                       torch.cuda.current_stream(), workspace=ws, value_is_key_prefix=prefix,
+                       inputs_ready=ready)
 
     for i in range(max(args.warmup, 3) + reps):
         call(replicas[i % reps])
@@ -450,6 +452,18 @@ def run_sfa(name, args, world, rank, cpu_target_s):
     ms, launches, mode = device_time(lambda i: call(replicas[i % reps]), args.steps, args.eager,
                                      world)
     clocks = sampler.stop()
+
+    # the same calls with sfa_options.inputs_ready (the inputs of every call
+    # exist before the previous call starts, as they do here): the
+    # small-group kernel then gathers while the previous call finishes
+    ready = None
+    if MAIN_KERNEL.get(name, "").startswith("sfa_decode_kernel"):
+        r_ms, _, r_mode = device_time(lambda i: call(replicas[i % reps], ready=True), args.steps,
+                                      args.eager, world)
+        ready = {"what": "sfa_options.inputs_ready = 1: a call waits for the previous one only "
+                         "before its first write", "us_per_call": r_ms * 1e3,
+                 "value": whole_job_rate(counts["gathered_bytes"], r_ms, world) / 1e9, "unit": "GB/s",
+                 "launch": r_mode}
 
     probe = None
     if not args.no_probe:
@@ -509,7 +523,7 @@ def run_sfa(name, args, world, rank, cpu_target_s):
            "tensor_frac": tflops / peaks["bf16_tflops"],
            "roofline_time_frac": max(t_hbm, t_tc) / (ms * 1e-3),
            "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-           "gather_probe": probe,
+           "gather_probe": probe, "with_inputs_ready": ready,
            "work": {"flops": counts["flops"], "gathered_bytes": counts["gathered_bytes"],
                     "unmasked_slots": counts["unmasked_slots"]}}
     if rank == 0 and not args.no_cpu_baseline:
@@ -791,7 +805,8 @@ def run_ours(args, rank, world, local):
            "dtype": head["dtype"], "data": "synthetic (seeded generator, shapes of the workload)",
            "config": head["config"]}
     for key in ("us_per_call", "gathered_gbs", "tflops", "tensor_frac", "roofline_time_frac",
-                "roofline", "e2e", "gpu_launches", "cpu_baseline", "gather_probe", "work"):
+                "roofline", "e2e", "gpu_launches", "cpu_baseline", "gather_probe",
+                "with_inputs_ready", "work"):
         if key in head:
             res[key] = head[key]
     res["gpu_launches"] = head["gpu_launches"]

@@ -49,7 +49,7 @@ class SfaOptions(ctypes.Structure):
     _fields_ = [("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("value_is_key_prefix", ctypes.c_int), ("validate_indices", ctypes.c_int),
                 ("num_splits", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("num_ctas", ctypes.c_int)]
+                ("num_ctas", ctypes.c_int), ("inputs_ready", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -172,13 +172,13 @@ def sfa_run(q, k, v, sparse_idx, B, S1, S2, N1, N2, Dk, Dv, topK, scale, layout,
 def sfa_run_ex(q, k, v, sparse_idx, B, S1, S2, N1, N2, Dk, Dv, topK, scale, layout, causal, dtype,
                out, lse=None, stream=None, workspace=None, workspace_bytes=0,
                value_is_key_prefix=False, validate_indices=False, num_splits=0,
-               ctas_per_sm=0, num_ctas=0, check=True) -> int:
+               ctas_per_sm=0, num_ctas=0, inputs_ready=False, check=True) -> int:
     """Forwards to sfa_run_ex() with an sfa_options built from the keywords."""
     if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
         workspace_bytes = workspace.numel() * workspace.element_size()
     opt = SfaOptions(_ptr(workspace), int(workspace_bytes), int(bool(value_is_key_prefix)),
                      int(bool(validate_indices)), int(num_splits), int(ctas_per_sm),
-                     int(num_ctas))
+                     int(num_ctas), int(bool(inputs_ready)))
     st = load().sfa_run_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(sparse_idx), B, S1, S2, N1, N2, Dk, Dv,
                            topK, float(scale), _enum(layout, LAYOUTS), int(bool(causal)),
                            _enum(dtype, DTYPES), _ptr(out), _ptr(lse), _stream(stream),

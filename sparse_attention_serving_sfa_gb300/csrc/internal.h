@@ -32,6 +32,7 @@ struct SfaParams {
     int B, S1, S2, N1, N2, G, Dk, Dv, topK;
     int causal, validate, splits, slots_per_split;
     int ctas_per_sm, num_ctas;   // launch tuning of the small-group path (0 = auto)
+    int inputs_ready;            // inputs not written by the preceding grid (sfa_options)
     float scale_log2;  // scale * log2(e)
     int64_t q_sb, q_ss, q_sh;
     int64_t k_sb, k_ss, k_sh;

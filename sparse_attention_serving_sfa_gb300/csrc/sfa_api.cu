@@ -251,6 +251,7 @@ sfa_status sfa_run_ex(const void* q, const void* k, const void* v, const int32_t
     p.validate = (opt && opt->validate_indices) ? 1 : 0;
     p.ctas_per_sm = opt ? opt->ctas_per_sm : 0;
     p.num_ctas = opt ? opt->num_ctas : 0;
+    p.inputs_ready = (opt && opt->inputs_ready) ? 1 : 0;
     p.err_word = device_error_word();  // index checks (if validating) and wait timeouts
     if (!p.err_word) return SFA_ERR_CUDA;
     p.scale_log2 = scale * kLog2e;

@@ -230,8 +230,12 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
     fence_proxy_async_smem();    // zero fill above precedes later bulk copies
     // launched with programmatic dependent launch: nothing above touches
     // global memory; wait here for the previous grid in the stream (its
-    // writes are then visible), and let the next one start launching
-    grid_dependency_wait();
+    // writes are then visible), and let the next one start launching.  When
+    // the caller states that the inputs were ready before that grid, the wait
+    // moves to the merge, before this kernel's first global write (out, lse,
+    // workspace); until then it only reads q, k, v and the indices (and may
+    // set bits of the error word, an atomic OR).
+    if (!p.inputs_ready) grid_dependency_wait();
     grid_launch_dependents();
     __syncthreads();
 
@@ -354,6 +358,7 @@ __global__ void __launch_bounds__(kThreads) sfa_decode_kernel(const SfaParams p,
     // stage 0 takes the partial the cluster reads).
     auto flush = [&](int64_t u, int s) {
         float* obuf = reinterpret_cast<float*>(smem + (sch.cluster > 1 ? 1 : s) * L::stage);
+        if (p.inputs_ready) grid_dependency_wait();   // (returns at once after the first time)
         named_sync(1, kConsThreads);        // every warp is done with the stage's rows
 #pragma unroll
         for (int e = 0; e < 2; ++e) {

@@ -277,6 +277,35 @@ def test_decode_stream_k_partitions(B, S1, N2, topK, S2):
     run_and_check(case)
 
 
+@pytest.mark.parametrize("schedule", ["cluster", "stream_k", "many_lists"])
+def test_inputs_ready_back_to_back(schedule):
+    """sfa_options.inputs_ready: four calls on different inputs issued back to
+    back on one stream with no synchronisation, so each call's gather may run
+    while the previous call is still writing; the four outputs must all equal
+    the oracle's.  Schedules: lists cut into segments merged in a cluster;
+    ranges that split lists, merged through the library workspace's counters
+    (which a call may touch only once the previous one is done); whole lists
+    per CTA."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if schedule == "many_lists":
+        case = small(B=4, S1=320, N1=8, N2=2, topK=100, S2=600, causal=True, seed=41)
+        opts = {}
+    else:
+        B = max(1, (2 * sms) // 2 // 4)
+        case = small(B=B, S1=2, N1=8, N2=2, topK=512, S2=900, causal=True, layout="BNSD", seed=42)
+        opts = {} if schedule == "cluster" else {"num_ctas": 7}
+    inputs = [synth.make_sfa_inputs(case.replace(seed=case.seed + t)) for t in range(4)]
+    devs = [T.to_dev(d) for d in inputs]
+    torch.cuda.synchronize()
+    results = [sfa.sparse_flash_attention(dv["q"], dv["k"], dv["v"], dv["idx"], case.scale,
+                                          case.layout, case.causal, return_lse=True,
+                                          inputs_ready=True, **opts) for dv in devs]
+    torch.cuda.synchronize()
+    for d, (out, lse) in zip(inputs, results):
+        T.check_full(case, d, out, lse)
+    assert sfa.sfa_get_last_error() == sfa.SFA_OK
+
+
 @pytest.mark.parametrize("seg,topK,mix", [(2, 1024, False), (3, 1000, True), (5, 1000, False),
                                           (7, 700, True), (8, 450, False), (8, 300, True)])
 def test_decode_cluster_merge(seg, topK, mix):
