@@ -455,9 +455,9 @@ def run_sfa(name, args, world, rank, cpu_target_s):
 
     # the same calls with sfa_options.inputs_ready (the inputs of every call
     # exist before the previous call starts, as they do here): the
-    # small-group kernel then gathers while the previous call finishes
+    # small-group and MLA kernels then gather while the previous call finishes
     ready = None
-    if MAIN_KERNEL.get(name, "").startswith("sfa_decode_kernel"):
+    if MAIN_KERNEL.get(name, "").startswith(("sfa_decode_kernel", "sfa_mla_kernel")):
         r_ms, _, r_mode = device_time(lambda i: call(replicas[i % reps], ready=True), args.steps,
                                       args.eager, world)
         ready = {"what": "sfa_options.inputs_ready = 1: a call waits for the previous one only "

@@ -136,11 +136,12 @@ typedef struct {
     int num_ctas;
     /* 1: the caller states that q, k, v and sparse_idx were not written by
      * the kernel that precedes this call in the stream (they were ready
-     * before it started), so the small-group kernel (G <= 8) may read them
-     * while that kernel is still running: it waits for the preceding grid
-     * (programmatic dependent launch) only before its first write of out,
-     * lse or the workspace, and a call's gather overlaps the previous call's
-     * tail.  Other paths ignore it.  0 = wait before the first read. */
+     * before it started), so the small-group kernel (G <= 8) and the MLA
+     * kernel (128 heads) may read them while that kernel is still running:
+     * they wait for the preceding grid (programmatic dependent launch) only
+     * before their first write of out, lse or the workspace, and a call's
+     * gather overlaps the previous call's tail.  Other paths ignore it.
+     * 0 = wait before the first read. */
     int inputs_ready;
 } sfa_options;
 

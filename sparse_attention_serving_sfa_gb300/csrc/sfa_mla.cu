@@ -167,8 +167,13 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
     }
     // launched with programmatic dependent launch: nothing above touches
     // global memory; wait here for the previous grid in the stream, and let
-    // the next one (the merge, or the next call) start launching
-    grid_dependency_wait();
+    // the next one (the merge, or the next call) start launching.  When the
+    // caller states that the inputs were ready before that grid, the softmax
+    // threads wait instead before their first write (a unit's epilogue);
+    // until then the kernel only reads q, k and the indices.  (A CTA of this
+    // kernel fills an SM's shared memory, so it starts only on an SM the
+    // previous grid has left, with its tensor memory released.)
+    if (!p.inputs_ready) grid_dependency_wait();
     grid_launch_dependents();
     if (warp == kMmaWarp) tmem_alloc(sbase + L::misc, kTmemCols);
     tc_fence_before();
@@ -510,6 +515,7 @@ sfa_mla_kernel(const __grid_constant__ CUtensorMap mq, const SfaParams p, const 
             if (!last_of_unit) continue;
 
             // ---- epilogue of unit u: this CTA's dims [256 rank, +256) ----
+            if (p.inputs_ready) grid_dependency_wait();   // (returns at once after the first time)
             mbar_wait(bar(B_UNIT_DONE), unit_phase, p.err_word, abort_flag);
             unit_phase ^= 1;
             tc_fence_after();

@@ -507,6 +507,30 @@ def test_mla_two_range_units_merge_in_cluster(B, S1, causal, dtype):
         assert torch.all(out[0, :2] == 0) and torch.all(torch.isneginf(lse[0, :2]))
 
 
+@pytest.mark.parametrize("schedule", ["cluster_merge", "merge_kernel", "whole_lists"])
+def test_mla_inputs_ready_back_to_back(schedule):
+    """sfa_options.inputs_ready on the MLA path: four calls on different inputs
+    issued back to back with no synchronisation (each may gather while the
+    previous call still runs); every output must equal the oracle's.
+    Schedules: two ranges per list merged in a 4-CTA cluster; ranges merged by
+    the merge kernel (forced CTA count); whole lists per pair."""
+    if schedule == "whole_lists":
+        case = mla(B=2, S1=24, S2=600, topK=64, causal=True, seed=31)   # 48 one-chunk lists
+        opts = {}
+    else:
+        case = mla(B=32, S1=1, S2=1024, topK=256, seed=32)
+        opts = {} if schedule == "cluster_merge" else {"num_ctas": 10}
+    inputs = [synth.make_sfa_inputs(case.replace(seed=case.seed + t)) for t in range(4)]
+    devs = [T.to_dev(d) for d in inputs]
+    torch.cuda.synchronize()
+    results = [sfa.sparse_flash_attention(dv["q"], dv["k"], dv["v"], dv["idx"], case.scale,
+                                          case.layout, case.causal, return_lse=True,
+                                          inputs_ready=True, **opts) for dv in devs]
+    torch.cuda.synchronize()
+    for d, (out, lse) in zip(inputs, results):
+        T.check_full(case, d, out, lse)
+
+
 def test_mla_out_of_range_indices_masked_and_reported():
     """Indices outside [0, S2) act as masked slots and set the error word."""
     case = mla(B=1, S1=2, topK=130, S2=400)
