@@ -433,7 +433,14 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             if (nb > 0) am_next[0] = allowed(0);
             if (nb > 1) am_next[1] = allowed(1);
         }
+        // Masked keys: their scores set to -inf before the max.  Without a
+        // soft cap or FP8 scales (the multiplier of the scores is then the
+        // positive softmax scale) that is the whole mask: exp2(-inf - m) = 0.
+        // The cap would map -inf to a finite value, and an FP8 scale may be
+        // 0, so those instantiations also zero P key by key.
+        constexpr bool kMaskOnce = MODE != 0 && !CAP && F8 == 0;
         auto apply_mask = [&](int h, uint64_t am) {
+            if (am == ~0ull) return;                     // a fully allowed block
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 if (!((am >> j) & 1ull)) sv[(kSplitRegs ? 64 * h : 0) + j] = __float_as_uint(-INFINITY);
@@ -470,6 +477,9 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 tmem_st16_strided<0>(lane_base + 64 * h, w);
                 tmem_st16_strided<1>(lane_base + 64 * h + 16, w);
             } else {
+            // (a row that has seen no allowed key has m = -inf and only -inf
+            // scores: subtracting 0 gives P = 0 instead of NaN)
+            const float m_sub = (kMaskOnce && m_used == -INFINITY) ? 0.f : m_used;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
                 float u0 = __uint_as_float(w[2 * k]) * rs;
@@ -478,9 +488,9 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     u0 = soft_cap_log2(u0, p.capl2, p.inv_capl2);
                     u1 = soft_cap_log2(u1, p.capl2, p.inv_capl2);
                 }
-                float p0 = fast_exp2(u0 - m_used);
-                float p1 = fast_exp2(u1 - m_used);
-                if constexpr (MODE != 0) {
+                float p0 = fast_exp2(u0 - m_sub);
+                float p1 = fast_exp2(u1 - m_sub);
+                if constexpr (MODE != 0 && !kMaskOnce) {
                     // masked keys give 0, also while the row has seen none (m = -inf)
                     if (!((am >> (2 * k)) & 1ull)) p0 = 0.f;
                     if (!((am >> (2 * k + 1)) & 1ull)) p1 = 0.f;
@@ -575,11 +585,12 @@ bsr_tc_wide_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     tc_fence_before();
                     mbar_arrive(bar(B_P_HALF + t));
                 }
-                // keys 0..63: still in sv, or read again
+                // keys 0..63: still in sv, or read again (and masked again)
                 if constexpr (!kSplitRegs) {
                     tmem_ld32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                     tmem_ld32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                     tmem_wait_ld();
+                    if constexpr (kMaskOnce) apply_mask(0, am0);
                 }
                 l += make_p(0, am0);
             } else if constexpr (WideSchedule<MODE>::split_p) {
