@@ -291,9 +291,14 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 const int i = item.row0 + t * p.TR + r / p.G;     // query row of this thread
                 if (i < row_end && r / p.G < p.TR) am = mask_bits64(mask_next);
             }
+            // masked keys: scores -inf before the max; without a soft cap
+            // (which would map -inf to a finite value) that is the whole
+            // mask, exp2(-inf - m) being 0
+            if (am != ~0ull) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-                if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
+                for (int j = 0; j < 64; ++j)
+                    if (!((am >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
+            }
             if (b + 1 < nb) mask_next = mask_word(b + 1);
             // block max in four independent chains, scaled once (the scale is
             // positive and rounding monotonic, so this equals the max of the
@@ -327,7 +332,10 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 }
             }
             if (need) m_used = m_new;
-            // P = exp2(s - m): high and low 16-bit parts, swizzled rows
+            // P = exp2(s - m): high and low 16-bit parts, swizzled rows (a row
+            // that has seen no allowed key has m = -inf and only -inf scores:
+            // subtracting 0 gives P = 0 instead of NaN)
+            const float m_sub = (!CAP && m_used == -INFINITY) ? 0.f : m_used;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};     // row sum in four chains
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
@@ -340,11 +348,14 @@ bsr_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                         u0 = soft_cap_log2(u0, p.capl2, p.inv_capl2);
                         u1 = soft_cap_log2(u1, p.capl2, p.inv_capl2);
                     }
-                    float p0 = fast_exp2(u0 - m_used);
-                    float p1 = fast_exp2(u1 - m_used);
-                    // masked keys give 0, also while the row has seen none (m = -inf)
-                    if (!((am >> (8 * c + 2 * e)) & 1ull)) p0 = 0.f;
-                    if (!((am >> (8 * c + 2 * e + 1)) & 1ull)) p1 = 0.f;
+                    float p0 = fast_exp2(u0 - m_sub);
+                    float p1 = fast_exp2(u1 - m_sub);
+                    if constexpr (CAP) {
+                        // capped masked keys give 0, also while the row has
+                        // seen none (m = -inf)
+                        if (!((am >> (8 * c + 2 * e)) & 1ull)) p0 = 0.f;
+                        if (!((am >> (8 * c + 2 * e + 1)) & 1ull)) p1 = 0.f;
+                    }
                     ls[e] += p0 + p1;
                     hw[e] = E::pack2(p0, p1);
                     const float2 h = E::unpack2(hw[e]);
