@@ -112,9 +112,10 @@ struct BsrParams {
     // key column j visible to row i iff j <= i + N - M), 2 per-element bits
     // (`mask`: element (r, c) of the k-th stored block is bit
     // (k * R + r) * C + c, most significant bit first within each byte),
-    // 3 variable blocks (HND tensors; `indptr` = key tile list offsets,
-    // `indices` = the key tiles, 4 ints each: start key, allowed-key mask
-    // low / high word, -; `causal` adds the bottom-right rule)
+    // 3 variable blocks (HND tensors; `indptr` = key window list offsets,
+    // `indices` = the key windows, 6 ints each: the first keys of four
+    // 16-key quarters, then the 64-bit allowed-key mask low / high word;
+    // `causal` adds the bottom-right rule)
     int mask_mode;
     const uint8_t* mask;
     int causal;

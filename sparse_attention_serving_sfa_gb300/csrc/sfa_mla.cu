@@ -15,8 +15,8 @@
 // 576 dims itself and runs its own online softmax -- the two CTAs never
 // exchange data, so neither waits for the other -- then O_r += P V_r for its
 // half of Dv (P as a 16-bit high part plus remainder, ~fp32 accurate).  The
-// pair is launched as a 2-CTA cluster only so that both halves of a unit run
-// at the same time and share the row reads in L2.
+// pair is launched as a cluster only so that both halves of a unit run at the
+// same time and share the row reads in L2.
 //
 // Tensor memory (512 columns): Q dims [0, 256) as the A operand of Q.K^T in
 // [0, 128) | two S/P buffers [128, 192), [192, 256) (a chunk's scores, then
@@ -30,8 +30,11 @@
 // P.V of chunk i as soon as its P is written), 4 producer warps (cp.async
 // gather of whole rows, index prefetch, L2 prefetch two chunks ahead,
 // visibility masks).  Work is stream-K over (unit, chunk) pairs per pair of
-// CTAs; the parts of a unit split over pairs are written as fp32 partials and
-// merged by a second kernel.  (An earlier design split the K dims over the
+// CTAs.  When every unit is cut into exactly two ranges, the two pairs of a
+// unit run as one 4-CTA cluster and the first merges the second's O and
+// (m, l) through distributed shared memory; otherwise the parts of a unit
+// split over pairs are written as fp32 partials and merged by a second
+// kernel.  (An earlier design split the K dims over the
 // pair and exchanged partial scores through distributed shared memory every
 // chunk: per-chunk timelines showed the pair running in lockstep through that
 // exchange, ~5,100 cycles per chunk for ~1,900 cycles of tensor work.)
