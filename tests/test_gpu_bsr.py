@@ -229,6 +229,50 @@ def test_mask_wins_over_causal_and_masked_rows_are_zero():
     assert torch.all(out[rows] == 0) and torch.all(torch.isneginf(lse[rows]))
 
 
+def test_causal_first_step_wholly_masked_for_top_rows():
+    """Bottom-right causal with kv_len - qo_len = 200 and each block row's
+    columns listed last to first: block row 0 keeps block 2 (keys 256..383,
+    seen by its rows 56..63) and processes it first, so its rows 0..55 see
+    nothing in their first step and their first allowed keys only in the
+    next (P must be 0, not NaN, while a row's running max is still -inf)."""
+    M, N, R, C, Hq, Hkv, d = 184, 384, 64, 128, 8, 2, 128
+    case = synth.BsrCase("r", M=M, N=N, R=R, C=C, Hq=Hq, Hkv=Hkv, d=d, dtype="f16", p=0.7,
+                         sm_scale=1 / math.sqrt(d), seed=84)
+    x = synth.make_bsr_inputs(case)
+    ip = x["indptr"].numpy()
+    ix = x["indices"].numpy().copy()
+    for rb in range(len(ip) - 1):
+        ix[ip[rb]:ip[rb + 1]] = ix[ip[rb]:ip[rb + 1]][::-1].copy()
+    assert 2 in ix[ip[0]:ip[1]] and ix[ip[0]] == max(ix[ip[0]:ip[1]])
+    ix_t = torch.from_numpy(ix)
+    out, lse = run_bsr_masked(x["q"], x["k"], x["v"], x["indptr"], ix_t, M, N, R, C,
+                              case.sm_scale, "f16", causal=True)
+    y, l = oracle.bsr(x["q"], x["k"], x["v"], x["indptr"], ix_t, M, N, R, C, case.sm_scale,
+                      causal=True)
+    compare(out, lse, y, l, "f16")
+
+
+def test_element_mask_first_blocks_hidden_from_top_rows():
+    """The per-element mask hides each block row's first two stored blocks
+    from its top half of rows, which then see their first allowed key only in
+    a later step (P = 0 while a row's max is -inf); rows left with nothing
+    are +0 with lse -inf."""
+    M, N, R, C, Hq, Hkv, d = 256, 512, 64, 64, 8, 2, 128
+    case = synth.BsrCase("f", M=M, N=N, R=R, C=C, Hq=Hq, Hkv=Hkv, d=d, dtype="bf16", p=0.5,
+                         sm_scale=1 / math.sqrt(d), seed=85, mask_keep=0.5)
+    x = synth.make_bsr_inputs(case)
+    mask = x["mask"].copy()
+    ip = x["indptr"].numpy()
+    for rb in range(len(ip) - 1):
+        for k in range(ip[rb], min(ip[rb] + 2, ip[rb + 1])):
+            mask[k, : R // 2, :] = False
+    out, lse = run_bsr_masked(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                              case.sm_scale, "bf16", mask=mask)
+    y, l = oracle.bsr(x["q"], x["k"], x["v"], x["indptr"], x["indices"], M, N, R, C,
+                      case.sm_scale, mask=mask)
+    compare(out, lse, y, l, "bf16")
+
+
 def test_masked_plan_reuse():
     """A masked plan stays valid for several runs on different inputs."""
     M, N, R, C, Hq, Hkv, d = 128, 192, 64, 64, 4, 1, 64
