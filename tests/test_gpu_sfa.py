@@ -485,9 +485,10 @@ def test_mla_cluster_schedules(num_ctas):
         T.check_full(case, d, out, lse)
 
 
-@pytest.mark.parametrize("B,S1,causal,dtype", [(32, 1, False, "bf16"), (1, 32, True, "bf16"),
-                                                (1, 32, True, "f16")])
-def test_mla_two_range_units_merge_in_cluster(B, S1, causal, dtype):
+@pytest.mark.parametrize("B,S1,causal,dtype,layout", [(32, 1, False, "bf16", "BSND"),
+                                                       (1, 32, True, "bf16", "BSND"),
+                                                       (1, 32, True, "f16", "BNSD")])
+def test_mla_two_range_units_merge_in_cluster(B, S1, causal, dtype, layout):
     """32 index lists of 128 heads with 4 chunks each: with 64-127 resident
     CTA pairs every list is cut into two ranges whose pairs run as one 4-CTA
     cluster and merge in distributed shared memory -- one kernel launch per
@@ -495,7 +496,7 @@ def test_mla_two_range_units_merge_in_cluster(B, S1, causal, dtype):
     row), and 32 causal query rows of one batch whose first two rows select
     only keys above the diagonal (+0, lse -inf after the merge)."""
     extra = dict(index_kind="causal_mix", masked_frac=0.1, full_masked_rows=2) if causal else {}
-    case = mla(B=B, S1=S1, S2=2048, topK=256, causal=causal, dtype=dtype, **extra)
+    case = mla(B=B, S1=S1, S2=2048, topK=256, causal=causal, dtype=dtype, layout=layout, **extra)
     d = synth.make_sfa_inputs(case)
     dev = T.to_dev(d)
     for _ in range(2):
@@ -504,7 +505,9 @@ def test_mla_two_range_units_merge_in_cluster(B, S1, causal, dtype):
         assert sfa.sfa_kernel_launches() - before == 1
         T.check_full(case, d, out, lse)
     if causal:
-        assert torch.all(out[0, :2] == 0) and torch.all(torch.isneginf(lse[0, :2]))
+        rows_out = out[0, :2] if layout == "BSND" else out[0, :, :2]
+        rows_lse = lse[0, :2] if layout == "BSND" else lse[0, :, :2]
+        assert torch.all(rows_out == 0) and torch.all(torch.isneginf(rows_lse))
 
 
 @pytest.mark.parametrize("schedule", ["cluster_merge", "merge_kernel", "whole_lists"])
