@@ -14,22 +14,24 @@
 //     the key prefix view), plus the group's q rows at the first chunk of an
 //     index list, with 16-byte cp.async, eight lanes per row and four rows
 //     per step (coalesced), into padded rows of a ring of shared-memory
-//     stages; completion is tracked by mbarriers
-//     (cp.async.mbarrier.arrive), indices are prefetched three chunks ahead,
-//     slots past topK or with an out-of-range index are zero-filled and
-//     masked.  (Per-row bulk TMA copies were measured at ~85 cycles per
+//     stages (as many as fit two CTAs per SM); completion is tracked by
+//     mbarriers (cp.async.mbarrier.arrive), indices are prefetched eight
+//     chunks ahead, slots past topK or with an out-of-range index are
+//     zero-filled and masked.  (Per-row bulk TMA copies were measured at ~85 cycles per
 //     256-byte row per SM -- about 0.9 TB/s over the GPU -- too slow for
 //     row gathers.)
 //   - four consumer warps each own 16 slots of every chunk and keep their own
-//     online-softmax state: the two small contractions Q.K^T ([16 x Dk] x
-//     [Dk x 16], query heads padded to 16 rows) and P.V ([16 x 16] x
-//     [16 x Dv]) run as warp-level mma.sync (bf16/fp16 in, fp32 accumulate),
-//     operands fetched with ldmatrix, P kept in registers between the two
+//     online-softmax state: the two small contractions, S^T = K Q^T
+//     ([16 slots x Dk] x [Dk x 8 heads], heads past G zero) and
+//     O^T += V^T P^T ([Dv x 16 slots] x [16 x 8]), run as warp-level mma.sync
+//     (bf16/fp16 in, fp32 accumulate), operands fetched with ldmatrix, P kept
+//     in registers between the two
 //     (as a 16-bit high part plus a 16-bit remainder, two MMAs);
 //     this keeps the instruction count per gathered byte low enough for the
 //     gather to set the pace;
 //   - at the end of an index list the four warps' states are merged through
-//     shared memory; a range that holds the whole list writes the output,
+//     the K / V tiles of the stage holding its last chunk (released after
+//     the merge); a range that holds the whole list writes the output,
 //     otherwise its partial (O, running max, sum) goes to the workspace and
 //     the last CTA to finish the list (a per-list arrival counter in the
 //     workspace head, reset by that CTA) merges the L2-resident partials and
